@@ -1,0 +1,354 @@
+"""ORACLE -- test infrastructure only (see the package docstring).
+
+Plain float64 statement of asynchronous MoE expert execution.  Citations name
+the page and the section they follow:
+
+* "SOSP'26 StreamEP" (marsggbo.github.io), section 3: tensors carry metadata
+  (RequestID, LayerID = layer / home rank / expert, tensor reference, top-k
+  weight); a Receptor puts each arriving token into a token pool and routes it
+  to the micro-queue of its target layer and task type; the scheduler picks a
+  non-empty queue; the executor gathers the scattered inputs into a contiguous
+  batch and runs the expert; results return to the home rank, where the top-k
+  merge buffers the first K-1 results and releases the token only when the
+  K-th lands; the merge is y = sum_j w_j E_j(x); the shared expert runs on the
+  home rank.
+* Same page, section 4: MTFS (most tokens first) picks the queue holding the
+  most tokens; the defragmenting score S(s) = Q(s) + sum_{j=1..W} delta^j
+  [Q(s_j) + H(s_j)] with its worked example (W=2, delta=0.5: 20 + 0.5*100 +
+  0.25*80 = 90 against an isolated queue of 60).
+* "CascadeEP: Asynchronous Expert Execution for MoE Prefill", abstract:
+  expert FFN starts before every replica's tokens are ready, and streamFFN
+  batches ready tokens to trade early start against FFN efficiency (read here
+  as a minimum batch per expert with a most-tokens-first fallback).
+* "asynchronous MoE serving" notes, "inferred obligations": accept exactly the
+  selected contributions once (no duplicate accumulation), publish readiness
+  only after the payload, and expect arrival-dependent addition order to break
+  bitwise equality unless the order is fixed -- hence the combine below sums
+  in ascending k order, whatever order the results arrived in.
+
+Readings where the pages are silent (the expert FFN form, the router rule,
+tie-breaks, wave timing) are stated at each function.
+"""
+from dataclasses import dataclass, field
+from itertools import combinations
+
+import numpy as np
+
+
+# ---------------------------------------------------------------- routing ----
+
+def route(logits, K):
+    """Top-K routing with renormalised softmax weights.
+
+    StreamEP section 3: each token selects the K experts with the highest
+    router scores (128 choose 4 for GPT-OSS-120B).  The router rule itself is
+    not on the pages; the reading used is: softmax over all E experts, keep the
+    K largest, renormalise their probabilities to sum to one.
+
+    The selection is decided on the logits exactly as given (softmax is
+    strictly increasing, so it selects the same set); equal logits go to the
+    lower expert index.  The k order of the result is descending score.
+
+    Returns idx [T, K] int64 and w [T, K] float64.
+    """
+    z = np.asarray(logits, dtype=np.float64)
+    T, E = z.shape
+    zmax = z.max(axis=1, keepdims=True)
+    p = np.exp(z - zmax)
+    p = p / p.sum(axis=1, keepdims=True)              # softmax over all E
+    idx = np.empty((T, K), dtype=np.int64)
+    w = np.empty((T, K), dtype=np.float64)
+    for t in range(T):
+        order = sorted(range(E), key=lambda e: (-z[t, e], e))
+        sel = order[:K]
+        idx[t] = sel
+        w[t] = p[t, sel] / p[t, sel].sum()             # renormalise over the top K
+    return idx, w
+
+
+def route_bruteforce(logits, K):
+    """Independent restatement for pinning ``route`` on small inputs.
+
+    Enumerates every K-subset, keeps the one with the largest logit sum (ties:
+    the lexicographically smallest subset), orders it by descending logit, and
+    computes the weights as a softmax restricted to the subset
+    exp(z_j - m) / sum_{i in S} exp(z_i - m).  That is algebraically the same
+    as "softmax then renormalise" because the full-softmax denominator cancels.
+    """
+    z = np.asarray(logits, dtype=np.float64)
+    T, E = z.shape
+    idx = np.empty((T, K), dtype=np.int64)
+    w = np.empty((T, K), dtype=np.float64)
+    for t in range(T):
+        best, best_sum = None, None
+        for S in combinations(range(E), K):
+            s = sum(z[t, e] for e in S)
+            if best is None or s > best_sum:
+                best, best_sum = S, s
+        S = sorted(best, key=lambda e: (-z[t, e], e))
+        m = max(z[t, e] for e in S)
+        num = np.array([np.exp(z[t, e] - m) for e in S])
+        idx[t] = S
+        w[t] = num / num.sum()
+    return idx, w
+
+
+# ------------------------------------------------------------ expert FFN ----
+
+def silu(a):
+    """silu(a) = a * sigmoid(a) = a / (1 + e^-a)."""
+    a = np.asarray(a, dtype=np.float64)
+    return a / (1.0 + np.exp(-a))
+
+
+def expert_ffn(X, W1, W3, W2):
+    """SwiGLU expert: E(x) = (silu(x W1) * (x W3)) W2.
+
+    The pages name no FFN form; the workload fixes SwiGLU with W1, W3 [H, I]
+    and W2 [I, H] and no bias.  X is [n, H]; result [n, H], float64.
+    """
+    X = np.asarray(X, dtype=np.float64)
+    g = X @ np.asarray(W1, dtype=np.float64)
+    u = X @ np.asarray(W3, dtype=np.float64)
+    return (silu(g) * u) @ np.asarray(W2, dtype=np.float64)
+
+
+def combine(contribs):
+    """Top-k merge, StreamEP section 3: y = sum_{j=1..K} w_j E_j(x).
+
+    ``contribs`` is the list of already-weighted results w_j E_j(x) indexed
+    by k; they are added in ascending k order (a fixed order, so the result
+    does not depend on which result arrived first)."""
+    y = np.zeros_like(np.asarray(contribs[0], dtype=np.float64))
+    for c in contribs:
+        y = y + c
+    return y
+
+
+def dense_moe(x, idx, w, experts, shared=None):
+    """Brute-force dense MoE for pinning: every token through every expert.
+
+    y_t = sum_e m_{t,e} w_{t,e} E_e(x_t) (+ E_shared(x_t)), with m the top-K
+    mask.  ``experts(e)`` returns (W1, W3, W2)."""
+    x = np.asarray(x, dtype=np.float64)
+    T = x.shape[0]
+    E = max(int(np.max(idx)) + 1, 1)
+    y = np.zeros_like(x)
+    for e in range(E):
+        out = expert_ffn(x, *experts(e))                # all tokens, masked below
+        for t in range(T):
+            hit = np.nonzero(idx[t] == e)[0]
+            if hit.size:
+                y[t] += w[t, hit[0]] * out[t]
+    if shared is not None:
+        y = y + expert_ffn(x, *shared)
+    return y
+
+
+# -------------------------------------------------------------- policies ----
+
+def mtfs_pick(depths, max_groups=0):
+    """MTFS, StreamEP section 4: the queue with the most tokens goes first.
+
+    Applied to the per-expert buckets of one layer's expert queue: non-empty
+    buckets ordered by depth, deepest first, equal depth -> lower expert id;
+    ``max_groups`` = 0 takes every non-empty bucket (one grouped step)."""
+    cand = [(-d, e) for e, d in enumerate(depths) if d > 0]
+    cand.sort()
+    picks = [e for _, e in cand]
+    return picks if max_groups <= 0 else picks[:max_groups]
+
+
+def threshold_pick(depths, min_batch, max_groups=0, fallback_groups=1):
+    """streamFFN reading (CascadeEP abstract): run an expert once it holds at
+    least ``min_batch`` ready tokens (deepest first); when none qualifies, fall
+    back to MTFS over the non-empty buckets, taking ``fallback_groups``."""
+    cand = [(-d, e) for e, d in enumerate(depths) if d >= min_batch]
+    cand.sort()
+    picks = [e for _, e in cand]
+    if picks:
+        return picks if max_groups <= 0 else picks[:max_groups]
+    return mtfs_pick(depths, fallback_groups)
+
+
+def defrag_score(q_now, lookahead, delta):
+    """Defragmenting score, StreamEP section 4:
+    S(s) = Q(s) + sum_{j=1..W} delta^j [Q(s_j) + H(s_j)].
+
+    ``lookahead`` lists (Q(s_j), H(s_j)) for j = 1..W along the execution chain
+    attention -> expert -> next attention."""
+    s = float(q_now)
+    for j, (q, h) in enumerate(lookahead, start=1):
+        s += (delta ** j) * (q + h)
+    return s
+
+
+# ----------------------------------------------------- asynchronous layer ----
+
+@dataclass
+class StepRecord:
+    step: int
+    picks: list                      # [(expert, count, sorted ((slot, k), ...))]
+    emitted: list                    # token slots whose combine completed this step
+
+
+@dataclass
+class _Slot:
+    mask: int = 0                    # which k have been delivered (bit k; bit K = shared)
+    results: dict = field(default_factory=dict)   # k -> weighted result (float64 [H])
+    landed: int = 0
+    combined: int = 0
+
+
+class AsyncMoEOracle:
+    """One MoE layer executed asynchronously, step by step.
+
+    Receptor (StreamEP section 3, steps 1-2): an arriving token is stored in
+    the token pool under its RequestID (its combine slot) and each of its
+    delivered (expert, k, weight) pairs is appended to that expert's bucket in
+    the layer's expert queue.  A token's first delivery also enqueues the
+    always-on shared expert (bucket E, weight 1) when the layer has one.
+
+    Step (sections 3-4): the policy picks buckets from their depths; each
+    picked bucket is drained whole, its tokens gathered into one contiguous
+    batch and run through the expert; every weighted result lands in the
+    (slot, k) entry of the top-k merge; a token is emitted once all of its K
+    (+1 shared) results have landed, as their sum in ascending k order.
+
+    ``experts(e)`` returns (W1, W3, W2) as float64 arrays, or ``None`` for
+    identity experts (E(x) = x).  ``compute`` restricts the float work to a
+    set of token slots (the bookkeeping always covers every token).
+    """
+
+    def __init__(self, num_experts, top_k, x, experts, has_shared=False, compute=None):
+        self.E, self.K = num_experts, top_k
+        self.x = np.asarray(x, dtype=np.float64)            # the token pool, by slot
+        self.T = self.x.shape[0]
+        self.experts = experts
+        self.has_shared = has_shared
+        self.nb = num_experts + (1 if has_shared else 0)
+        self.buckets = [[] for _ in range(self.nb)]
+        self.slots = [_Slot() for _ in range(self.T)]
+        self.weights = {}                                     # (slot, k) -> w
+        self.compute = None if compute is None else set(int(t) for t in compute)
+        self.y = {}
+        self.emit_step = {}
+        self.duplicates = 0
+        self.steps = []
+        self.nstep = 0
+
+    # Receptor ------------------------------------------------------------
+    def deliver(self, tokens, idx, w, rank=None):
+        """Deliver the pairs of ``tokens`` (all K, or those of rank (r, n))."""
+        for t in np.asarray(tokens, dtype=np.int64):
+            t = int(t)
+            s = self.slots[t]
+            for k in range(self.K):
+                e = int(idx[t, k])
+                if rank is not None and e % rank[1] != rank[0]:
+                    continue
+                if s.mask >> k & 1:                            # already accepted once
+                    self.duplicates += 1
+                    continue
+                s.mask |= 1 << k
+                self.weights[(t, k)] = float(w[t, k])
+                self.buckets[e].append((t, k))
+            if self.has_shared and not (s.mask >> self.K & 1):
+                s.mask |= 1 << self.K
+                self.weights[(t, self.K)] = 1.0
+                self.buckets[self.E].append((t, self.K))
+
+    def depths(self):
+        return [len(b) for b in self.buckets]
+
+    def snapshot(self):
+        """Queue contents: per bucket, the sorted multiset of (slot, k)."""
+        return [sorted(b) for b in self.buckets]
+
+    # Scheduler + executor -------------------------------------------------
+    def _expert_out(self, e, X):
+        if self.experts is None:
+            return X.copy()
+        return expert_ffn(X, *self.experts(e))
+
+    def step(self, policy):
+        """One scheduling step under ``policy`` (a callable depths -> picks)."""
+        self.nstep += 1
+        picks = policy(self.depths())
+        rec = StepRecord(step=self.nstep, picks=[], emitted=[])
+        need = self.K + (1 if self.has_shared else 0)
+        for e in picks:
+            batch = self.buckets[e]
+            self.buckets[e] = []
+            rec.picks.append((e, len(batch), tuple(sorted(batch))))
+            rows = [(t, k) for (t, k) in batch if self.compute is None or t in self.compute]
+            if rows:
+                X = self.x[[t for t, _ in rows]]               # gather: contiguous batch
+                out = self._expert_out(e, X)
+                for i, (t, k) in enumerate(rows):
+                    self.slots[t].results[k] = self.weights[(t, k)] * out[i]
+            for (t, k) in batch:                               # result lands in (t, k)
+                s = self.slots[t]
+                s.landed += 1
+                if s.landed == need:                           # the K-th result: release
+                    s.combined += 1
+                    self.emit_step[t] = self.nstep
+                    rec.emitted.append(t)
+                    if self.compute is None or t in self.compute:
+                        self.y[t] = combine([s.results[j] for j in sorted(s.results)])
+        rec.emitted.sort()
+        self.steps.append(rec)
+        return rec
+
+    def pending(self):
+        return sum(len(b) for b in self.buckets)
+
+
+def replay_layer(num_experts, top_k, x, idx, w, waves, policy, experts,
+                 has_shared=False, compute=None, max_steps=100000):
+    """Replay arrival waves against one asynchronous layer on a logical clock.
+
+    One tick per scheduling step; wave i is delivered (in wave order) before
+    the first step whose tick is >= its arrival tick; steps continue until
+    every delivered pair has been executed.  Arrival delays only shape the
+    batches, never the values."""
+    sim = AsyncMoEOracle(num_experts, top_k, x, experts, has_shared, compute)
+    order = sorted(range(len(waves)), key=lambda i: (waves[i].tick, i))
+    nxt = 0
+    tick = 0
+    while tick < max_steps:
+        tick += 1
+        while nxt < len(order) and waves[order[nxt]].tick <= tick:
+            wv = waves[order[nxt]]
+            sim.deliver(wv.tokens, idx, w, wv.rank)
+            nxt += 1
+        sim.step(policy)
+        if nxt == len(order) and sim.pending() == 0:
+            break
+    return sim
+
+
+def y_sample(tokens, x, idx, w, experts, shared=None):
+    """y for a few tokens straight from the merge formula (no queues)."""
+    out = {}
+    for t in tokens:
+        t = int(t)
+        xt = np.asarray(x[t], dtype=np.float64)[None, :]
+        contribs = [w[t, k] * expert_ffn(xt, *experts(int(idx[t, k])))[0] for k in range(idx.shape[1])]
+        if shared is not None:
+            contribs.append(expert_ffn(xt, *shared)[0])
+        out[t] = combine(contribs)
+    return out
+
+
+# --------------------------------------------------- attention stub (c5) ----
+
+def rmsnorm(x, eps=1e-6):
+    """RMSNorm without gain: x / sqrt(mean(x^2) + eps), per row."""
+    x = np.asarray(x, dtype=np.float64)
+    return x / np.sqrt(np.mean(x * x, axis=-1, keepdims=True) + eps)
+
+
+def attention_stub(x, P):
+    """Stand-in for the attention stage: RMSNorm(x) @ P."""
+    return rmsnorm(x) @ np.asarray(P, dtype=np.float64)

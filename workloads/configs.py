@@ -1,0 +1,106 @@
+"""Workload descriptions: shapes, distributions and arrival structure.
+
+The five named workloads follow the synthetic configurations the build is
+measured on (a tiny fp32 exactness case, a GPT-OSS-120B-shaped decode layer, a
+skewed prefill chunk with a straggler wave, a DeepSeek-style wide layer with a
+shared expert, and a streaming multi-layer decode).  The ``TEST_CONFIGS`` are
+smaller cases for element-by-element parity: they span several GEMM tiles in
+every dimension and leave ragged tails (H and 2I not multiples of 128, H and I
+not multiples of 64).
+"""
+from dataclasses import dataclass, replace
+
+
+@dataclass(frozen=True)
+class LayerSpec:
+    num_experts: int          # E routed experts
+    top_k: int                # K
+    hidden: int               # H
+    inter: int                # I (SwiGLU intermediate)
+    dtype: str                # "f32" | "bf16"
+    has_shared: bool = False  # one always-on shared expert, weight 1
+    shared_inter: int = 0     # its intermediate size (must equal `inter`)
+
+
+@dataclass(frozen=True)
+class WorkloadSpec:
+    name: str
+    layer: LayerSpec
+    tokens: int                       # T tokens (one per request slot)
+    router: str                       # "normal" | "uniform" | "zipf"
+    zipf_s: float = 1.2
+    waves: str = "even"               # "even" | "straggler" | "dirichlet" | "ep_rank"
+    num_waves: int = 4
+    arrival: str = "permute"          # "permute" | "exp" | "index"
+    straggler_frac: float = 0.30
+    dirichlet_alpha: float = 0.5
+    policy: str = "mtfs"              # "mtfs" | "threshold"
+    min_batch: int = 64
+    max_groups: int = 0               # 0 = all qualifying buckets
+    fallback_groups: int = 1
+    num_layers: int = 1
+    # streaming multi-layer decode (config "c5")
+    stream_steps: int = 0             # stop after this many combined token-layer steps
+    stream_ranks: int = 16
+    stream_sigma: float = 1.0
+    notes: str = ""
+
+
+GPT_OSS_LAYER = LayerSpec(num_experts=128, top_k=4, hidden=2880, inter=2880, dtype="bf16")
+
+CONFIGS = {
+    "c1": WorkloadSpec(
+        name="c1_tiny_fp32", layer=LayerSpec(8, 2, 64, 128, "f32"), tokens=32,
+        router="normal", waves="even", num_waves=4, arrival="permute", policy="mtfs",
+        notes="1 MoE layer, 8 experts, top-2, H=64, I=128, fp32, 32 tokens, 4 random-order waves"),
+    "c2": WorkloadSpec(
+        name="c2_gptoss_decode", layer=GPT_OSS_LAYER, tokens=256,
+        router="uniform", waves="even", num_waves=16, arrival="exp", policy="mtfs",
+        notes="128 experts top-4 H=I=2880 bf16, 256 decode tokens, 16 waves, exp delays, MTFS"),
+    "c3": WorkloadSpec(
+        name="c3_gptoss_prefill_zipf", layer=GPT_OSS_LAYER, tokens=4096,
+        router="zipf", zipf_s=1.2, waves="straggler", num_waves=16, arrival="exp",
+        straggler_frac=0.30, policy="mtfs",
+        notes="4096-token prefill chunk, Zipf(1.2) popularity, 15 waves + a 30% straggler last"),
+    "c4": WorkloadSpec(
+        name="c4_deepseek_wide_shared",
+        layer=LayerSpec(256, 8, 7168, 2048, "bf16", has_shared=True, shared_inter=2048),
+        tokens=2048, router="normal", waves="dirichlet", num_waves=8, arrival="index",
+        dirichlet_alpha=0.5, policy="threshold", min_batch=64, fallback_groups=1,
+        notes="256 routed + 1 shared expert, top-8, H=7168, I=2048, 2048 tokens, Dirichlet(0.5) waves"),
+    "c5": WorkloadSpec(
+        name="c5_streaming_4layer", layer=GPT_OSS_LAYER, tokens=512, router="uniform",
+        waves="stream", num_waves=16, arrival="lognormal", policy="mtfs", num_layers=4,
+        stream_steps=10000, stream_ranks=16, stream_sigma=1.0,
+        notes="4 layers of the c2 shape, 512 requests, RMSNorm+projection attention stub"),
+}
+
+# Smaller cases for element-by-element parity (several tiles + ragged tails).
+TEST_CONFIGS = {
+    # bf16, GEMM1 M = 2I = 416 (3 tiles + 32), K = H = 584 (9 k-blocks + 8);
+    # GEMM2 M = H = 584 (4 tiles + 72), K = I = 208 (3 k-blocks + 16).
+    "m1": WorkloadSpec(
+        name="m1_bf16_ragged", layer=LayerSpec(16, 4, 584, 208, "bf16"), tokens=200,
+        router="normal", waves="even", num_waves=5, arrival="exp", policy="mtfs"),
+    # bf16 with a shared expert and the threshold policy; one expert gets > 256 rows.
+    "m2": WorkloadSpec(
+        name="m2_bf16_shared_threshold",
+        layer=LayerSpec(24, 6, 320, 192, "bf16", has_shared=True, shared_inter=192),
+        tokens=600, router="zipf", zipf_s=1.2, waves="dirichlet", num_waves=6,
+        arrival="index", policy="threshold", min_batch=40, fallback_groups=1),
+    # fp32 with ragged shapes (SIMT path), pairs split across waves by EP rank.
+    "m3": WorkloadSpec(
+        name="m3_f32_ep_rank", layer=LayerSpec(12, 3, 136, 80, "f32"), tokens=96,
+        router="normal", waves="ep_rank", num_waves=4, arrival="permute", policy="mtfs"),
+    # bf16 decode-like: many experts, few tokens each.
+    "m4": WorkloadSpec(
+        name="m4_bf16_decode", layer=LayerSpec(64, 4, 1024, 512, "bf16"), tokens=64,
+        router="uniform", waves="even", num_waves=8, arrival="exp", policy="mtfs"),
+}
+
+
+def get_config(name, **overrides):
+    spec = CONFIGS.get(name) or TEST_CONFIGS.get(name)
+    if spec is None:
+        raise KeyError(name)
+    return replace(spec, **overrides) if overrides else spec
