@@ -1,0 +1,762 @@
+// C-ABI entry points and the queue-side kernels of the asynchronous MoE library:
+// weight packing, router, Receptor (enqueue), scheduler, collect.
+// The expert FFN kernels live in moe_ffn_simt.cu (fp32 / identity) and moe_ffn_tc.cu
+// (bf16 on tcgen05 tensor cores).
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <algorithm>
+#include <new>
+#include "moe_internal.cuh"
+
+using namespace moe;
+
+namespace {
+
+// ---------------------------------------------------------------- packing
+// out[e][orow(i)][c] = in[e][c][i] for a row-major [E][C][R] input: a batched transpose
+// into K-major rows.  `interleave` places source row i at packed row 32*(i/16) + i%16 +
+// 16*which (gate rows first, then up rows, in blocks of 16), so a 32-row slice of the
+// packed W13 holds gate and up of the same 16 features.
+template <typename T>
+__global__ void pack_transpose_kernel(const T* __restrict__ in, T* __restrict__ out, int C, int R,
+                                      int out_rows, int interleave, int which) {
+  __shared__ T tile[32][33];
+  const int e = blockIdx.z;
+  const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+  const T* src = in + (size_t)e * C * R;
+  T* dst = out + (size_t)e * out_rows * C;
+  for (int j = threadIdx.y; j < 32; j += blockDim.y) {
+    int c = c0 + j, r = r0 + threadIdx.x;
+    if (c < C && r < R) tile[j][threadIdx.x] = src[(size_t)c * R + r];
+  }
+  __syncthreads();
+  for (int j = threadIdx.y; j < 32; j += blockDim.y) {
+    int r = r0 + j, c = c0 + threadIdx.x;
+    if (r < R && c < C) {
+      int orow = interleave ? (32 * (r / 16) + (r % 16) + 16 * which) : r;
+      dst[(size_t)orow * C + c] = tile[threadIdx.x][j];
+    }
+  }
+}
+
+template <typename T>
+cudaError_t pack_one(const void* in, void* out, int nexp, int C, int R, int out_rows, int inter,
+                     int which, cudaStream_t s) {
+  dim3 grid((C + 31) / 32, (R + 31) / 32, nexp), block(32, 8);
+  pack_transpose_kernel<T><<<grid, block, 0, s>>>(static_cast<const T*>(in), static_cast<T*>(out),
+                                                   C, R, out_rows, inter, which);
+  return cudaGetLastError();
+}
+
+// ----------------------------------------------------------------- router
+// One warp per token.  Top-K by (logit desc, index asc), then w_k = exp(z_k - m) /
+// sum_j exp(z_j - m) over the selected set, m = the largest selected logit: this equals
+// softmax over all E renormalised over the top K, because the full denominator cancels.
+__global__ void route_kernel(const float* __restrict__ logits, int T, int E, int K,
+                             int32_t* __restrict__ idx, float* __restrict__ wout) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= T) return;
+  float v[32];
+  const int per = (E + 31) / 32;
+  for (int i = 0; i < 32; ++i) {
+    int e = lane + 32 * i;
+    v[i] = (i < per && e < E) ? logits[(size_t)t * E + e] : -INFINITY;
+  }
+  uint32_t taken = 0;
+  float selv[32];
+  int seli[32];
+  for (int k = 0; k < K; ++k) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+    for (int i = 0; i < per; ++i) {
+      int e = lane + 32 * i;
+      if (e < E && !(taken >> i & 1u)) {
+        if (bi == 0x7fffffff || v[i] > bv || (v[i] == bv && e < bi)) { bv = v[i]; bi = e; }
+      }
+    }
+    for (int off = 16; off > 0; off >>= 1) {
+      float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+      if (oi != 0x7fffffff && (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi))) { bv = ov; bi = oi; }
+    }
+    if ((bi & 31) == lane && bi != 0x7fffffff) taken |= 1u << (bi >> 5);
+    selv[k] = bv;
+    seli[k] = bi;
+  }
+  if (lane == 0) {
+    const float m = selv[0];
+    float den = 0.f;
+    for (int k = 0; k < K; ++k) den += expf(selv[k] - m);
+    for (int k = 0; k < K; ++k) {
+      idx[(size_t)t * K + k] = seli[k];
+      wout[(size_t)t * K + k] = expf(selv[k] - m) / den;
+    }
+  }
+}
+
+// --------------------------------------------------------------- Receptor
+// Pairs: one thread per (token, k) with k <= K (k == K is the shared expert).  Appends use
+// warp-aggregated atomics: lanes bound for the same bucket elect a leader that reserves all
+// of their positions with one atomicAdd on the bucket tail.
+// Token vectors: copied into pool[slot] with 16-byte vector loads/stores.
+template <typename T>
+__global__ void enqueue_kernel(LayerView L, Dims d, DevCounters* C, int n,
+                               const int32_t* __restrict__ rows, const int32_t* __restrict__ slots,
+                               const T* __restrict__ x, const int32_t* __restrict__ expert,
+                               const float* __restrict__ w, const uint32_t* __restrict__ kmask,
+                               const uint32_t* __restrict__ gens) {
+  const int lane = threadIdx.x & 31;
+  const long long total = (long long)n * d.KS;
+  const long long total_r = (total + 31) & ~31ll;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long base = (long long)blockIdx.x * blockDim.x + (threadIdx.x & ~31); base < total_r;
+       base += stride) {
+    const long long p = base + lane;
+    int key = -1 - lane;          // unique key for lanes with nothing to append
+    int slot = 0, k = 0;
+    if (p < total) {
+      const int i = (int)(p / d.KS);
+      k = (int)(p % d.KS);
+      const int row = rows ? rows[i] : i;
+      slot = slots ? slots[i] : row;
+      bool ok = true;
+      if (slot < 0 || slot >= d.S || row < 0) { set_error(C, MOE_ERR_INVALID); ok = false; }
+      if (ok && gens && L.gen[slot] != gens[i]) {
+        if (k == 0) { set_error(C, MOE_ERR_STALE); atomicAdd(&C->stale, 1ull); }
+        ok = false;
+      }
+      if (ok && k < d.K && kmask && !((kmask[i] >> k) & 1u)) ok = false;
+      int e = d.E;
+      if (ok && k < d.K) {
+        e = expert[(size_t)row * d.K + k];
+        if (e < 0 || e >= d.E) { set_error(C, MOE_ERR_INVALID); ok = false; }
+      }
+      if (ok) {
+        const uint32_t bit = 1u << k;
+        const uint32_t old = atomicOr(&L.enq_mask[slot], bit);
+        if (old & bit) {
+          if (k < d.K) { set_error(C, MOE_ERR_DUPLICATE); atomicAdd(&C->duplicates, 1ull); }
+          ok = false;            // shared expert: already enqueued by an earlier wave
+        } else {
+          if (old == 0u) atomicAdd(&C->open_tokens, 1);
+          L.wtab[(size_t)slot * d.KS + k] = (k < d.K) ? w[(size_t)row * d.K + k] : 1.0f;
+          key = e;
+        }
+      }
+    }
+    const uint32_t peers = __match_any_sync(0xffffffffu, key);
+    if (key >= 0) {
+      const int leader = __ffs(peers) - 1;
+      const uint32_t cnt = __popc(peers);
+      uint32_t pos0 = 0;
+      if (lane == leader) {
+        pos0 = atomicAdd(&L.tail[key], cnt);
+        atomicAdd(&C->pending_pairs, (int)cnt);
+      }
+      pos0 = __shfl_sync(peers, pos0, leader);
+      const uint32_t pos = pos0 + __popc(peers & ((1u << lane) - 1u));
+      if (pos - L.head[key] >= (uint32_t)d.cap) {
+        set_error(C, MOE_ERR_CAPACITY);
+      } else {
+        L.records[(size_t)key * d.cap + (pos % (uint32_t)d.cap)] = (slot << kKShift) | k;
+      }
+    }
+  }
+  // token vectors -> pool rows (16-byte chunks)
+  constexpr int V = 16 / sizeof(T);
+  const int chunks = d.H / V;
+  const long long total_c = (long long)n * chunks;
+  for (long long q = (long long)blockIdx.x * blockDim.x + threadIdx.x; q < total_c; q += stride) {
+    const int i = (int)(q / chunks), c = (int)(q % chunks);
+    const int row = rows ? rows[i] : i;
+    const int slot = slots ? slots[i] : row;
+    if (slot < 0 || slot >= d.S || row < 0) continue;
+    const int4 v = __ldg(reinterpret_cast<const int4*>(x + (size_t)row * d.H) + c);
+    reinterpret_cast<int4*>(static_cast<T*>(L.pool) + (size_t)slot * d.H)[c] = v;
+  }
+}
+
+// -------------------------------------------------------------- scheduler
+// One CTA.  Reads every bucket depth of the layer, applies the policy, drains the picked
+// buckets whole (head += depth) and writes the work list the FFN kernels consume.
+// MTFS (StreamEP section 4): deepest first, equal depth -> lower bucket id.  THRESHOLD
+// (streamFFN reading): buckets with depth >= min_batch, deepest first; if none, MTFS over
+// non-empty buckets limited to fallback_groups.
+__global__ void __launch_bounds__(1024) schedule_kernel(LayerView L, Dims d, StepPlan* P,
+                                                        DevCounters* C, moe_async_policy pol,
+                                                        TileGeom g, int layer, int trace_cap,
+                                                        int4* trace, long long weight_bytes_per_run) {
+  __shared__ int depth[kMaxBuckets];
+  __shared__ int order[kMaxBuckets];
+  __shared__ int n_elig, n_nonempty;
+  const int tid = threadIdx.x, nt = blockDim.x;
+  if (tid == 0) { n_elig = 0; n_nonempty = 0; }
+  __syncthreads();
+  for (int b = tid; b < d.NB; b += nt) {
+    const int dep = min((int)(L.tail[b] - L.head[b]), d.cap);
+    depth[b] = dep;
+    if (dep > 0) atomicAdd(&n_nonempty, 1);
+    if (dep > 0 && (pol.kind != MOE_POLICY_THRESHOLD || dep >= pol.min_batch)) atomicAdd(&n_elig, 1);
+  }
+  __syncthreads();
+  int minb = 1, G = pol.max_groups;
+  if (pol.kind == MOE_POLICY_THRESHOLD) {
+    if (n_elig > 0) minb = pol.min_batch > 1 ? pol.min_batch : 1;
+    else G = pol.fallback_groups > 0 ? pol.fallback_groups : 1;
+  }
+  const int ne = (pol.kind == MOE_POLICY_THRESHOLD && n_elig == 0) ? n_nonempty : n_elig;
+  // After an overflow or an out-of-range id the queues no longer describe valid pairs:
+  // stop executing (the sticky error is reported to the host).
+  const uint32_t err = *(volatile uint32_t*)&C->error;
+  const bool halted = err == MOE_ERR_CAPACITY || err == MOE_ERR_INVALID;
+  const int n = halted ? 0 : ((G > 0 && G < ne) ? G : ne);
+  for (int b = tid; b < d.NB; b += nt) {
+    const int db = depth[b];
+    if (db >= minb) {
+      int r = 0;
+      for (int c = 0; c < d.NB; ++c) {
+        const int dc = depth[c];
+        r += (dc >= minb) && (dc > db || (dc == db && c < b));
+      }
+      if (r < n) order[r] = b;
+    }
+  }
+  __syncthreads();
+  if (tid < 32) {
+    const int lane = tid;
+    int row_run = 0, t1_run = 0, t2_run = 0;
+    const int ft1 = (2 * d.I + g.bm1 - 1) / g.bm1;
+    const int ft2 = (d.H + g.bm2 - 1) / g.bm2;
+    for (int c0 = 0; c0 < n; c0 += 32) {
+      const int r = c0 + lane;
+      int b = 0, cnt = 0, t1 = 0, t2 = 0;
+      if (r < n) {
+        b = order[r];
+        cnt = depth[b];
+        t1 = ((cnt + g.bn1 - 1) / g.bn1) * ft1;
+        t2 = ((cnt + g.bn2 - 1) / g.bn2) * ft2;
+      }
+      int s_cnt = cnt, s_t1 = t1, s_t2 = t2;      // inclusive prefix sums within the chunk
+      for (int off = 1; off < 32; off <<= 1) {
+        int a = __shfl_up_sync(0xffffffffu, s_cnt, off);
+        int b1 = __shfl_up_sync(0xffffffffu, s_t1, off);
+        int b2 = __shfl_up_sync(0xffffffffu, s_t2, off);
+        if (lane >= off) { s_cnt += a; s_t1 += b1; s_t2 += b2; }
+      }
+      if (r < n) {
+        WorkItem it;
+        it.expert = b;
+        it.head = L.head[b];
+        it.count = cnt;
+        it.row_base = row_run + s_cnt - cnt;
+        it.t1_base = t1_run + s_t1 - t1;
+        it.t2_base = t2_run + s_t2 - t2;
+        P->items[r] = it;
+        L.head[b] = it.head + (uint32_t)cnt;
+        if (trace && trace_cap > 0) {
+          const int ti = atomicAdd(&C->trace_n, 1);
+          if (ti < trace_cap) trace[ti] = make_int4((int)C->steps + 1, layer, b, cnt);
+        }
+      }
+      row_run += __shfl_sync(0xffffffffu, s_cnt, 31);
+      t1_run += __shfl_sync(0xffffffffu, s_t1, 31);
+      t2_run += __shfl_sync(0xffffffffu, s_t2, 31);
+    }
+    if (lane == 0) {
+      P->layer = layer;
+      P->n_work = n;
+      P->n_tiles1 = t1_run;
+      P->n_tiles2 = t2_run;
+      P->rows = row_run;
+      C->steps += 1ull;
+      C->pairs_executed += (unsigned long long)row_run;
+      C->expert_runs += (unsigned long long)n;
+      C->weight_bytes += (unsigned long long)n * (unsigned long long)weight_bytes_per_run;
+      C->pending_pairs -= row_run;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- collect
+// Copy ready rows (in completion order) to the caller, then reclaim each slot: clear its
+// accepted mask and landing count and advance its generation, after the row was read.
+template <typename T>
+__global__ void collect_kernel(LayerView L, Dims d, int max_out, T* __restrict__ y_out,
+                               int32_t* __restrict__ slot_out, uint32_t* __restrict__ gen_out,
+                               const int32_t* __restrict__ n_io, int append) {
+  const uint32_t rh = L.ready_ht[0], rt = L.ready_ht[1];
+  const int base = append ? *n_io : 0;
+  const int n = max(0, min((int)(rt - rh), max_out - base));
+  constexpr int V = 16 / sizeof(T);
+  const int chunks = d.H / V;
+  for (int i = blockIdx.x; i < n; i += gridDim.x) {
+    const int slot = L.ready[(rh + (uint32_t)i) % (uint32_t)d.S];
+    const int4* src = reinterpret_cast<const int4*>(static_cast<const T*>(L.y) + (size_t)slot * d.H);
+    int4* dst = reinterpret_cast<int4*>(y_out + (size_t)(base + i) * d.H);
+    for (int c = threadIdx.x; c < chunks; c += blockDim.x) dst[c] = __ldcg(src + c);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      slot_out[base + i] = slot;
+      if (gen_out) gen_out[base + i] = L.gen[slot];
+      L.enq_mask[slot] = 0u;
+      L.done[slot] = 0u;
+      L.gen[slot] = L.gen[slot] + 1u;
+    }
+  }
+}
+
+__global__ void collect_finish_kernel(LayerView L, Dims d, DevCounters* C, int max_out,
+                                      int32_t* n_io, int append) {
+  const uint32_t rh = L.ready_ht[0], rt = L.ready_ht[1];
+  const int base = append ? *n_io : 0;
+  const int n = max(0, min((int)(rt - rh), max_out - base));
+  L.ready_ht[0] = rh + (uint32_t)n;
+  C->ready -= n;
+  *n_io = base + n;
+}
+
+// -------------------------------------------------------------- utilities
+
+bool valid_stream_layer(moe_async_t h, int layer) {
+  return h && layer >= 0 && layer < h->cfg.num_layers;
+}
+
+size_t elem_size(int dtype) { return dtype == MOE_BF16 ? 2 : 4; }
+
+void prof_free(moe_async_s* h);
+
+void free_handle(moe_async_s* h) {
+  if (!h) return;
+  prof_free(h);
+  if (h->tc_state) tc_teardown(h);
+  if (h->layers) {
+    for (int l = 0; l < h->cfg.num_layers; ++l) {
+      LayerView& L = h->layers[l];
+      void* ptrs[] = {L.pool, L.wtab, L.enq_mask, L.done, L.gen, L.slotbuf, L.y, L.records,
+                      L.head, L.tail, L.ready, L.ready_ht, const_cast<void*>(L.w13),
+                      const_cast<void*>(L.w2)};
+      for (void* p : ptrs) if (p) cudaFree(p);
+    }
+    delete[] h->layers;
+  }
+  if (h->plan) cudaFree(h->plan);
+  if (h->h) cudaFree(h->h);
+  if (h->counters) cudaFree(h->counters);
+  if (h->trace) cudaFree(h->trace);
+  if (h->host_counters) cudaFreeHost(h->host_counters);
+  delete h;
+}
+
+template <typename P>
+cudaError_t dalloc(P** p, size_t bytes) {
+  void* q = nullptr;
+  cudaError_t e = cudaMalloc(&q, bytes ? bytes : 16);
+  *p = static_cast<P*>(q);
+  return e;
+}
+
+moe_status read_counters(moe_async_t h, cudaStream_t s) {
+  MOE_CUDA_TRY(cudaMemcpyAsync(h->host_counters, h->counters, sizeof(DevCounters),
+                               cudaMemcpyDeviceToHost, s));
+  MOE_CUDA_TRY(cudaStreamSynchronize(s));
+  return MOE_OK;
+}
+
+struct ProfState {
+  static constexpr int kCap = 65536;
+  bool on = false;
+  int n = 0;
+  cudaEvent_t ev[2 * kCap];
+  int kind[kCap];
+  int created = 0;                 // events created so far (lazily)
+};
+
+void prof_free(moe_async_s* h) {
+  ProfState* p = static_cast<ProfState*>(h->prof);
+  if (!p) return;
+  for (int i = 0; i < p->created; ++i) cudaEventDestroy(p->ev[i]);
+  delete p;
+  h->prof = nullptr;
+}
+
+}  // namespace
+
+namespace moe {
+
+void prof_begin(moe_async_s* h, int kind, cudaStream_t s) {
+  h->launches += 1;
+  ProfState* p = static_cast<ProfState*>(h->prof);
+  if (!p || !p->on || p->n >= ProfState::kCap) return;
+  const int i = p->n;
+  while (p->created < 2 * i + 2) {
+    if (cudaEventCreate(&p->ev[p->created]) != cudaSuccess) { p->on = false; return; }
+    ++p->created;
+  }
+  p->kind[i] = kind;
+  cudaEventRecord(p->ev[2 * i], s);
+}
+
+void prof_end(moe_async_s* h, int kind, cudaStream_t s) {
+  (void)kind;
+  ProfState* p = static_cast<ProfState*>(h->prof);
+  if (!p || !p->on || p->n >= ProfState::kCap) return;
+  if (p->created < 2 * p->n + 2) return;
+  cudaEventRecord(p->ev[2 * p->n + 1], s);
+  p->n += 1;
+}
+
+}  // namespace moe
+
+// ====================================================================== C ABI
+
+extern "C" {
+
+const char* moe_async_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID: return "invalid argument";
+    case MOE_ERR_CAPACITY: return "capacity exceeded";
+    case MOE_ERR_DUPLICATE: return "duplicate pair";
+    case MOE_ERR_STALE: return "stale slot generation";
+    case MOE_ERR_TIMEOUT: return "timeout: tokens still open";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_UNSUPPORTED: return "unsupported configuration";
+  }
+  return "unknown status";
+}
+
+moe_status moe_async_create(const moe_async_config* cfg, const void* const* w1,
+                            const void* const* w3, const void* const* w2,
+                            const void* const* sw1, const void* const* sw3,
+                            const void* const* sw2, void* stream, moe_async_t* out) {
+  if (!cfg || !out) return MOE_ERR_INVALID;
+  const moe_async_config c = *cfg;
+  if (c.num_layers < 1 || c.num_experts < 1 || c.num_experts > kMaxExperts || c.top_k < 1 ||
+      c.top_k > c.num_experts || c.top_k + (c.has_shared ? 1 : 0) > 31 || c.hidden < 8 ||
+      c.hidden % 8 || c.inter < 16 || c.inter % 16 || c.max_slots < 1 ||
+      c.max_slots > (1 << 25) || c.bucket_capacity < 0 ||
+      (c.dtype != MOE_F32 && c.dtype != MOE_BF16) ||
+      (c.expert_kind != MOE_EXPERT_SWIGLU && c.expert_kind != MOE_EXPERT_IDENTITY) ||
+      c.trace_capacity < 0)
+    return MOE_ERR_INVALID;
+  const bool swiglu = c.expert_kind == MOE_EXPERT_SWIGLU;
+  if (swiglu && (!w1 || !w3 || !w2)) return MOE_ERR_INVALID;
+  if (swiglu && c.has_shared && (!sw1 || !sw3 || !sw2)) return MOE_ERR_INVALID;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  moe_async_s* h = new (std::nothrow) moe_async_s();
+  if (!h) return MOE_ERR_CUDA;
+  std::memset(static_cast<void*>(h), 0, sizeof(*h));
+  h->cfg = c;
+  Dims& d = h->dims;
+  d.E = c.num_experts;
+  d.K = c.top_k;
+  d.KS = c.top_k + (c.has_shared ? 1 : 0);
+  d.NB = c.num_experts + (c.has_shared ? 1 : 0);
+  d.H = c.hidden;
+  d.I = c.inter;
+  d.S = c.max_slots;
+  d.cap = c.bucket_capacity > 0 ? c.bucket_capacity : c.max_slots;
+  d.dtype = c.dtype;
+  d.has_shared = c.has_shared ? 1 : 0;
+  d.expert_kind = c.expert_kind;
+  if (cudaGetDevice(&h->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&h->num_sms, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess) {
+    free_handle(h);
+    return MOE_ERR_CUDA;
+  }
+  h->use_tc = false;
+  h->geom = h->use_tc ? tc_geom() : simt_geom();
+  if (!swiglu) h->geom = TileGeom{16, 2 * c.inter, 16, c.hidden};
+  h->parts_per_pair = (d.H + h->geom.bm2 - 1) / h->geom.bm2;
+
+  const size_t es = elem_size(c.dtype);
+  const size_t S = (size_t)d.S, H = (size_t)d.H, I = (size_t)d.I, KS = (size_t)d.KS;
+  h->layers = new (std::nothrow) LayerView[c.num_layers];
+  if (!h->layers) { free_handle(h); return MOE_ERR_CUDA; }
+  std::memset(static_cast<void*>(h->layers), 0, sizeof(LayerView) * c.num_layers);
+  bool ok = true;
+  for (int l = 0; l < c.num_layers && ok; ++l) {
+    LayerView& L = h->layers[l];
+    ok = ok && dalloc(&L.pool, S * H * es) == cudaSuccess;
+    ok = ok && dalloc(&L.wtab, S * KS * 4) == cudaSuccess;
+    ok = ok && dalloc(&L.enq_mask, S * 4) == cudaSuccess;
+    ok = ok && dalloc(&L.done, S * 4) == cudaSuccess;
+    ok = ok && dalloc(&L.gen, S * 4) == cudaSuccess;
+    ok = ok && dalloc(&L.slotbuf, S * KS * H * 4) == cudaSuccess;
+    ok = ok && dalloc(&L.y, S * H * es) == cudaSuccess;
+    ok = ok && dalloc(&L.records, (size_t)d.NB * d.cap * 4) == cudaSuccess;
+    ok = ok && dalloc(&L.head, (size_t)d.NB * 4) == cudaSuccess;
+    ok = ok && dalloc(&L.tail, (size_t)d.NB * 4) == cudaSuccess;
+    ok = ok && dalloc(&L.ready, S * 4) == cudaSuccess;
+    ok = ok && dalloc(&L.ready_ht, 2 * 4) == cudaSuccess;
+    if (ok && swiglu) {
+      void* p13 = nullptr;
+      void* p2 = nullptr;
+      ok = ok && dalloc(&p13, (size_t)d.NB * 2 * I * H * es) == cudaSuccess;
+      L.w13 = p13;
+      ok = ok && dalloc(&p2, (size_t)d.NB * H * I * es) == cudaSuccess;
+      L.w2 = p2;
+      h->packed_bytes += (int64_t)((size_t)d.NB * 3 * I * H * es);
+    }
+    if (ok) {
+      ok = cudaMemsetAsync(L.enq_mask, 0, S * 4, s) == cudaSuccess &&
+           cudaMemsetAsync(L.done, 0, S * 4, s) == cudaSuccess &&
+           cudaMemsetAsync(L.gen, 0, S * 4, s) == cudaSuccess &&
+           cudaMemsetAsync(L.head, 0, (size_t)d.NB * 4, s) == cudaSuccess &&
+           cudaMemsetAsync(L.tail, 0, (size_t)d.NB * 4, s) == cudaSuccess &&
+           cudaMemsetAsync(L.ready_ht, 0, 8, s) == cudaSuccess &&
+           cudaMemsetAsync(L.records, 0, (size_t)d.NB * d.cap * 4, s) == cudaSuccess &&
+           cudaMemsetAsync(L.slotbuf, 0, S * KS * H * 4, s) == cudaSuccess;
+    }
+    if (ok && swiglu) {
+      // W1 [E,H,I] -> packed rows 32*(i/16) + i%16 ; W3 -> same + 16 ; W2 [E,I,H] -> [E,H,I]
+      void* p13 = const_cast<void*>(L.w13);
+      void* p2 = const_cast<void*>(L.w2);
+      const int E = d.E, Hh = d.H, Ii = d.I;
+      auto pk = [&](const void* in, void* outp, int nexp, int C, int R, int orows, int il, int which) {
+        return c.dtype == MOE_BF16
+                   ? pack_one<__nv_bfloat16>(in, outp, nexp, C, R, orows, il, which, s)
+                   : pack_one<float>(in, outp, nexp, C, R, orows, il, which, s);
+      };
+      ok = ok && pk(w1[l], p13, E, Hh, Ii, 2 * Ii, 1, 0) == cudaSuccess;
+      ok = ok && pk(w3[l], p13, E, Hh, Ii, 2 * Ii, 1, 1) == cudaSuccess;
+      ok = ok && pk(w2[l], p2, E, Ii, Hh, Hh, 0, 0) == cudaSuccess;
+      if (ok && c.has_shared) {
+        char* s13 = static_cast<char*>(p13) + (size_t)E * 2 * I * H * es;
+        char* s2 = static_cast<char*>(p2) + (size_t)E * H * I * es;
+        ok = ok && pk(sw1[l], s13, 1, Hh, Ii, 2 * Ii, 1, 0) == cudaSuccess;
+        ok = ok && pk(sw3[l], s13, 1, Hh, Ii, 2 * Ii, 1, 1) == cudaSuccess;
+        ok = ok && pk(sw2[l], s2, 1, Ii, Hh, Hh, 0, 0) == cudaSuccess;
+      }
+    }
+  }
+  ok = ok && dalloc(&h->plan, sizeof(StepPlan)) == cudaSuccess;
+  ok = ok && dalloc(&h->h, S * KS * I * es) == cudaSuccess;
+  ok = ok && dalloc(&h->counters, sizeof(DevCounters)) == cudaSuccess;
+  ok = ok && cudaMemsetAsync(h->plan, 0, sizeof(StepPlan), s) == cudaSuccess;
+  ok = ok && cudaMemsetAsync(h->counters, 0, sizeof(DevCounters), s) == cudaSuccess;
+  if (ok && c.trace_capacity > 0) ok = dalloc(&h->trace, (size_t)c.trace_capacity * sizeof(int4)) == cudaSuccess;
+  if (ok) ok = cudaMallocHost(reinterpret_cast<void**>(&h->host_counters), sizeof(DevCounters)) == cudaSuccess;
+  if (!ok) { cudaStreamSynchronize(s); free_handle(h); return MOE_ERR_CUDA; }
+  if (h->use_tc) {
+    moe_status st = tc_setup(h);
+    if (st != MOE_OK) { cudaStreamSynchronize(s); free_handle(h); return st; }
+  }
+  if (cudaStreamSynchronize(s) != cudaSuccess) { free_handle(h); return MOE_ERR_CUDA; }
+  *out = h;
+  return MOE_OK;
+}
+
+moe_status moe_async_route(const float* d_logits, int32_t T, int32_t E, int32_t K, int32_t* d_idx,
+                           float* d_w, void* stream) {
+  if (T < 0 || E < 1 || E > kMaxExperts || K < 1 || K > E || K > 32) return MOE_ERR_INVALID;
+  if (T == 0) return MOE_OK;
+  if (!d_logits || !d_idx || !d_w) return MOE_ERR_INVALID;
+  const int wpb = 8;
+  route_kernel<<<(T + wpb - 1) / wpb, 32 * wpb, 0, static_cast<cudaStream_t>(stream)>>>(d_logits, T, E, K, d_idx, d_w);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status moe_async_enqueue(moe_async_t h, int32_t layer, int32_t n, const int32_t* d_rows,
+                             const int32_t* d_slot, const void* d_x, const int32_t* d_expert,
+                             const float* d_w, const uint32_t* d_kmask, const uint32_t* d_gen,
+                             void* stream) {
+  if (!valid_stream_layer(h, layer) || n < 0) return MOE_ERR_INVALID;
+  if (n == 0) return MOE_OK;
+  if (!d_x || !d_expert || !d_w) return MOE_ERR_INVALID;
+  if (reinterpret_cast<uintptr_t>(d_x) % 16) return MOE_ERR_INVALID;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const Dims& d = h->dims;
+  const long long work = std::max<long long>((long long)n * d.KS, (long long)n * d.H / 8);
+  int grid = (int)std::min<long long>((work + 255) / 256, (long long)h->num_sms * 8);
+  if (grid < 1) grid = 1;
+  prof_begin(h, MOE_KERNEL_ENQUEUE, s);
+  if (d.dtype == MOE_BF16)
+    enqueue_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(h->layers[layer], d, h->counters, n, d_rows, d_slot,
+        static_cast<const __nv_bfloat16*>(d_x), d_expert, d_w, d_kmask, d_gen);
+  else
+    enqueue_kernel<float><<<grid, 256, 0, s>>>(h->layers[layer], d, h->counters, n, d_rows, d_slot,
+        static_cast<const float*>(d_x), d_expert, d_w, d_kmask, d_gen);
+  prof_end(h, MOE_KERNEL_ENQUEUE, s);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status moe_async_schedule_step(moe_async_t h, int32_t layer, const moe_async_policy* policy,
+                                   void* stream) {
+  if (!valid_stream_layer(h, layer) || !policy) return MOE_ERR_INVALID;
+  if (policy->kind != MOE_POLICY_MTFS && policy->kind != MOE_POLICY_THRESHOLD) return MOE_ERR_INVALID;
+  if (policy->max_groups < 0 || policy->min_batch < 0 || policy->fallback_groups < 0) return MOE_ERR_INVALID;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const Dims& d = h->dims;
+  const long long wbytes = h->cfg.expert_kind == MOE_EXPERT_SWIGLU
+                               ? 3ll * d.H * d.I * (long long)elem_size(d.dtype) : 0ll;
+  prof_begin(h, MOE_KERNEL_SCHEDULE, s);
+  schedule_kernel<<<1, 1024, 0, s>>>(h->layers[layer], d, h->plan, h->counters, *policy, h->geom,
+                                     layer, h->cfg.trace_capacity, h->trace, wbytes);
+  prof_end(h, MOE_KERNEL_SCHEDULE, s);
+  if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  if (h->cfg.expert_kind == MOE_EXPERT_IDENTITY) return launch_identity(h, layer, s);
+  if (h->use_tc) return launch_ffn_tc(h, layer, s);
+  return launch_ffn_simt(h, layer, s);
+}
+
+moe_status moe_async_collect(moe_async_t h, int32_t layer, int32_t max_out, void* d_y_out,
+                             int32_t* d_slot_out, uint32_t* d_gen_out, int32_t* d_n_out,
+                             int32_t append, void* stream) {
+  if (!valid_stream_layer(h, layer) || max_out < 0 || !d_n_out) return MOE_ERR_INVALID;
+  if (max_out > 0 && (!d_y_out || !d_slot_out)) return MOE_ERR_INVALID;
+  if (reinterpret_cast<uintptr_t>(d_y_out) % 16) return MOE_ERR_INVALID;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const Dims& d = h->dims;
+  const int grid = std::max(1, std::min(max_out, h->num_sms * 4));
+  prof_begin(h, MOE_KERNEL_COLLECT, s);
+  if (max_out > 0) {
+    if (d.dtype == MOE_BF16)
+      collect_kernel<__nv_bfloat16><<<grid, 128, 0, s>>>(h->layers[layer], d, max_out,
+          static_cast<__nv_bfloat16*>(d_y_out), d_slot_out, d_gen_out, d_n_out, append);
+    else
+      collect_kernel<float><<<grid, 128, 0, s>>>(h->layers[layer], d, max_out,
+          static_cast<float*>(d_y_out), d_slot_out, d_gen_out, d_n_out, append);
+  }
+  collect_finish_kernel<<<1, 1, 0, s>>>(h->layers[layer], d, h->counters, max_out, d_n_out, append);
+  h->launches += max_out > 0 ? 1 : 0;
+  prof_end(h, MOE_KERNEL_COLLECT, s);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status moe_async_sync(moe_async_t h, void* stream) {
+  if (!h) return MOE_ERR_INVALID;
+  moe_status st = read_counters(h, static_cast<cudaStream_t>(stream));
+  if (st != MOE_OK) return st;
+  return static_cast<moe_status>(h->host_counters->error);
+}
+
+moe_status moe_async_wait(moe_async_t h, int32_t layer, const moe_async_policy* policy,
+                          int32_t max_steps, int32_t check_every, void* stream) {
+  if (!valid_stream_layer(h, layer) || !policy || max_steps < 0) return MOE_ERR_INVALID;
+  if (check_every < 1) check_every = 1;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int steps = 0;
+  for (;;) {
+    moe_status st = read_counters(h, s);
+    if (st != MOE_OK) return st;
+    if (h->host_counters->error) return static_cast<moe_status>(h->host_counters->error);
+    if (h->host_counters->open_tokens == 0) return MOE_OK;
+    if (steps >= max_steps) return MOE_ERR_TIMEOUT;
+    for (int i = 0; i < check_every && steps < max_steps; ++i, ++steps) {
+      st = moe_async_schedule_step(h, layer, policy, stream);
+      if (st != MOE_OK) return st;
+    }
+  }
+}
+
+moe_status moe_async_get_stats(moe_async_t h, void* stream, moe_async_stats* out) {
+  if (!h || !out) return MOE_ERR_INVALID;
+  moe_status st = read_counters(h, static_cast<cudaStream_t>(stream));
+  if (st != MOE_OK) return st;
+  const DevCounters& c = *h->host_counters;
+  out->steps = (int64_t)c.steps;
+  out->pairs_executed = (int64_t)c.pairs_executed;
+  out->expert_runs = (int64_t)c.expert_runs;
+  out->weight_bytes = (int64_t)c.weight_bytes;
+  out->tokens_combined = (int64_t)c.tokens_combined;
+  out->duplicates = (int64_t)c.duplicates;
+  out->stale = (int64_t)c.stale;
+  out->open_tokens = c.open_tokens;
+  out->pending_pairs = c.pending_pairs;
+  out->ready = c.ready;
+  out->error = (int32_t)c.error;
+  out->packed_weight_bytes = h->packed_bytes;
+  out->kernel_launches = h->launches;
+  return MOE_OK;
+}
+
+moe_status moe_async_profile(moe_async_t h, int32_t enable) {
+  if (!h) return MOE_ERR_INVALID;
+  ProfState* p = static_cast<ProfState*>(h->prof);
+  if (enable && !p) {
+    p = new (std::nothrow) ProfState();
+    if (!p) return MOE_ERR_CUDA;
+    h->prof = p;
+  }
+  if (p) p->on = enable != 0;
+  return MOE_OK;
+}
+
+moe_status moe_async_profile_read(moe_async_t h, void* stream, double* h_ms, int64_t* h_launches,
+                                  int32_t n_kinds) {
+  if (!h || n_kinds < 0 || (n_kinds > 0 && (!h_ms || !h_launches))) return MOE_ERR_INVALID;
+  MOE_CUDA_TRY(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
+  ProfState* p = static_cast<ProfState*>(h->prof);
+  if (!p) return MOE_OK;
+  for (int i = 0; i < p->n; ++i) {
+    const int k = p->kind[i];
+    if (k < 0 || k >= n_kinds) continue;
+    float ms = 0.f;
+    MOE_CUDA_TRY(cudaEventElapsedTime(&ms, p->ev[2 * i], p->ev[2 * i + 1]));
+    h_ms[k] += ms;
+    h_launches[k] += 1;
+  }
+  p->n = 0;
+  return MOE_OK;
+}
+
+moe_status moe_async_get_trace(moe_async_t h, void* stream, int32_t* h_buf, int32_t cap, int32_t* h_n) {
+  if (!h || !h_n || cap < 0 || (cap > 0 && !h_buf)) return MOE_ERR_INVALID;
+  moe_status st = read_counters(h, static_cast<cudaStream_t>(stream));
+  if (st != MOE_OK) return st;
+  int n = std::min(h->host_counters->trace_n, h->cfg.trace_capacity);
+  n = std::min(n, cap);
+  if (n > 0) MOE_CUDA_TRY(cudaMemcpy(h_buf, h->trace, (size_t)n * sizeof(int4), cudaMemcpyDeviceToHost));
+  *h_n = n;
+  return MOE_OK;
+}
+
+moe_status moe_async_snapshot(moe_async_t h, int32_t layer, void* stream, int32_t* h_depth,
+                              int32_t* h_records, int32_t cap, int32_t* h_n) {
+  if (!valid_stream_layer(h, layer) || !h_depth || !h_n || cap < 0 || (cap > 0 && !h_records))
+    return MOE_ERR_INVALID;
+  MOE_CUDA_TRY(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
+  const Dims& d = h->dims;
+  const LayerView& L = h->layers[layer];
+  uint32_t* head = static_cast<uint32_t*>(std::malloc((size_t)d.NB * 4));
+  uint32_t* tail = static_cast<uint32_t*>(std::malloc((size_t)d.NB * 4));
+  int32_t* recs = static_cast<int32_t*>(std::malloc((size_t)d.NB * d.cap * 4));
+  moe_status st = MOE_OK;
+  if (!head || !tail || !recs) st = MOE_ERR_CUDA;
+  if (st == MOE_OK && (cudaMemcpy(head, L.head, (size_t)d.NB * 4, cudaMemcpyDeviceToHost) != cudaSuccess ||
+                       cudaMemcpy(tail, L.tail, (size_t)d.NB * 4, cudaMemcpyDeviceToHost) != cudaSuccess ||
+                       cudaMemcpy(recs, L.records, (size_t)d.NB * d.cap * 4, cudaMemcpyDeviceToHost) != cudaSuccess))
+    st = MOE_ERR_CUDA;
+  int n = 0;
+  if (st == MOE_OK) {
+    for (int b = 0; b < d.NB; ++b) {
+      const uint32_t dep = tail[b] - head[b];
+      h_depth[b] = (int32_t)dep;
+      for (uint32_t j = 0; j < dep && j < (uint32_t)d.cap; ++j) {
+        if (n >= cap) { st = MOE_ERR_CAPACITY; break; }
+        const int32_t r = recs[(size_t)b * d.cap + ((head[b] + j) % (uint32_t)d.cap)];
+        h_records[2 * n] = r >> kKShift;
+        h_records[2 * n + 1] = r & kKMask;
+        ++n;
+      }
+    }
+  }
+  *h_n = n;
+  std::free(head);
+  std::free(tail);
+  std::free(recs);
+  return st;
+}
+
+moe_status moe_async_destroy(moe_async_t h, void* stream) {
+  if (!h) return MOE_ERR_INVALID;
+  cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  free_handle(h);
+  return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,228 @@
+/*
+ * moe_async.h -- C ABI of the asynchronous MoE expert-execution library (GB300, sm_103a).
+ *
+ * What the library computes.  One or more MoE layers executed asynchronously:
+ * routed token vectors arrive in waves tagged (RequestID, LayerID, expert,
+ * top-k weight) and are appended to per-expert micro-queues; a scheduling step
+ * picks ready queues (most-tokens-first or a minimum batch), gathers each
+ * picked queue's tokens into one contiguous batch, runs the expert SwiGLU FFN
+ * as a grouped GEMM, and scatters w * E(x) into per-(request, k) combine slots;
+ * a token's output y = sum_j w_j E_j(x) is released only once all K results
+ * (plus the shared expert's, if any) have landed.
+ *   - Metadata, token pool, micro-queues, scheduler, gather + top-k merge:
+ *     "SOSP'26 StreamEP" (marsggbo.github.io), sections 3 and 4.
+ *   - Minimum-batch streaming of ready tokens (streamFFN) and starting expert
+ *     work before every replica's tokens are ready: "CascadeEP: Asynchronous
+ *     Expert Execution for MoE Prefill under Attention Imbalance", abstract.
+ *   - Readiness published after the payload, exactly-once acceptance, reclaim
+ *     after the last read, generation-tagged slots: "asynchronous MoE serving"
+ *     notes, sections "recent work that narrows the proposals" (CascadeEP,
+ *     Appendix C) and "inferred obligations for a concrete protocol".
+ *
+ * Conventions for every call.
+ *   - Pointers named d_* are DEVICE pointers on the current CUDA device; h_*
+ *     are host pointers.  `stream` is a cudaStream_t passed as void* (NULL =
+ *     the legacy default stream).  Calls are stream-ordered and asynchronous
+ *     unless stated otherwise; a handle must be used from one stream at a time.
+ *   - Host-detectable errors (bad arguments) return immediately and launch
+ *     nothing.  Errors found on the device (duplicate pair, stale generation,
+ *     bucket overflow, out-of-range id) set a sticky device error word; it is
+ *     returned by the next synchronising call (moe_async_sync, _wait,
+ *     _get_stats) and stays set until moe_async_destroy.
+ *   - No call blocks without bound: moe_async_wait is limited by a step count.
+ *   - Thread safety: a handle is not thread-safe; distinct handles are.
+ */
+#ifndef MOE_ASYNC_H
+#define MOE_ASYNC_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct moe_async_s* moe_async_t;
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID = 1,      /* bad argument (host) or out-of-range id (device)          */
+  MOE_ERR_CAPACITY = 2,     /* a per-expert bucket or the ready ring overflowed          */
+  MOE_ERR_DUPLICATE = 3,    /* a (slot, k) pair was delivered twice; the copy is dropped */
+  MOE_ERR_STALE = 4,        /* a pair carried an out-of-date slot generation; dropped    */
+  MOE_ERR_TIMEOUT = 5,      /* moe_async_wait ran out of steps with tokens still open    */
+  MOE_ERR_CUDA = 6,         /* a CUDA runtime call failed                                */
+  MOE_ERR_UNSUPPORTED = 7   /* shape/dtype combination not supported by the kernels      */
+} moe_status;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+
+typedef enum {
+  MOE_POLICY_MTFS = 0,       /* most tokens first: deepest buckets first (StreamEP, section 4) */
+  MOE_POLICY_THRESHOLD = 1   /* buckets holding >= min_batch tokens; else MTFS fallback         */
+} moe_policy_kind;
+
+typedef enum {
+  MOE_EXPERT_SWIGLU = 0,     /* E(x) = (silu(x W1) * (x W3)) W2                               */
+  MOE_EXPERT_IDENTITY = 1    /* E(x) = x; exercises queues/readiness/combine without a GEMM    */
+} moe_expert_kind;
+
+typedef struct {
+  int32_t num_layers;       /* L >= 1                                                          */
+  int32_t num_experts;      /* E routed experts per layer, 1..1024                             */
+  int32_t top_k;            /* K, 1..30                                                        */
+  int32_t hidden;           /* H, multiple of 8                                                */
+  int32_t inter;            /* I, multiple of 16                                               */
+  int32_t dtype;            /* moe_dtype of x, weights and y (accumulation is always fp32)     */
+  int32_t has_shared;       /* 1: one always-on shared expert per layer, weight 1, I_s == I   */
+  int32_t max_slots;        /* combine slots (RequestIDs 0..max_slots-1) per layer             */
+  int32_t bucket_capacity;  /* pairs per expert bucket; 0 = max_slots (cannot overflow)        */
+  int32_t expert_kind;      /* moe_expert_kind                                                 */
+  int32_t trace_capacity;   /* >0: record up to this many (step, layer, expert, count) picks   */
+} moe_async_config;
+
+typedef struct {
+  int32_t kind;             /* moe_policy_kind                                                 */
+  int32_t max_groups;       /* at most this many buckets per step; 0 = no limit                */
+  int32_t min_batch;        /* THRESHOLD: minimum bucket depth to run                          */
+  int32_t fallback_groups;  /* THRESHOLD: buckets taken (deepest first) when none qualifies    */
+} moe_async_policy;
+
+typedef struct {
+  int64_t steps;            /* scheduling steps executed                                       */
+  int64_t pairs_executed;   /* routed (token, expert) pairs run through an expert              */
+  int64_t expert_runs;      /* sum over steps of the number of buckets picked                  */
+  int64_t weight_bytes;     /* expert weight bytes streamed, as scheduled (3*H*I*elem per run) */
+  int64_t tokens_combined;  /* tokens whose merge completed                                    */
+  int64_t duplicates;       /* pairs rejected as duplicates                                    */
+  int64_t stale;            /* pairs rejected for a stale generation                           */
+  int32_t open_tokens;      /* tokens with >= 1 accepted pair not yet combined (all layers)    */
+  int32_t pending_pairs;    /* accepted pairs not yet picked (all layers)                      */
+  int32_t ready;            /* combined tokens not yet collected (all layers)                  */
+  int32_t error;            /* sticky device error (moe_status)                                */
+  int64_t packed_weight_bytes; /* library-owned packed weight copy made at create              */
+  int64_t kernel_launches;  /* kernels this handle has launched since create                   */
+} moe_async_stats;
+
+/* Kernel kinds timed by moe_async_profile (index into the arrays of moe_async_profile_read). */
+typedef enum {
+  MOE_KERNEL_ENQUEUE = 0,    /* Receptor: pairs into buckets, token rows into the pool          */
+  MOE_KERNEL_SCHEDULE = 1,   /* device-side policy + work list                                  */
+  MOE_KERNEL_FFN1 = 2,       /* gather + GEMM1 (gate/up) + SwiGLU   (identity: scatter + merge) */
+  MOE_KERNEL_FFN2 = 3,       /* GEMM2 (down) + weighted scatter + readiness + merge             */
+  MOE_KERNEL_COLLECT = 4,    /* ready rows to the caller + slot reclaim                         */
+  MOE_KERNEL_KINDS = 5
+} moe_kernel_kind;
+
+/* Create a handle.  Weights are given per layer as arrays of L device pointers:
+ *   w1[l], w3[l] : [E, H, I] (expert e computes x @ W1[e]),  w2[l] : [E, I, H]
+ *   shared_w1[l], shared_w3[l] : [H, I], shared_w2[l] : [I, H]  (NULL arrays when has_shared = 0)
+ * all in cfg->dtype, row-major, contiguous.  The library packs them into its own K-major
+ * copy (gate/up rows interleaved) before returning (it synchronises `stream`), so the
+ * caller's weight buffers may be freed afterwards.  All state (token pool, buckets, combine
+ * slots, outputs, work lists) is allocated here; no later call allocates device memory.
+ * Returns MOE_ERR_INVALID / MOE_ERR_UNSUPPORTED for bad configs, MOE_ERR_CUDA on allocation
+ * failure (nothing leaks).  *out is set only on MOE_OK. */
+moe_status moe_async_create(const moe_async_config* cfg,
+                            const void* const* w1, const void* const* w3, const void* const* w2,
+                            const void* const* shared_w1, const void* const* shared_w3,
+                            const void* const* shared_w2,
+                            void* stream, moe_async_t* out);
+
+/* Router: top-K experts per token with renormalised softmax weights.
+ * StreamEP section 3 (each token selects its K highest-scoring experts); the rule is softmax
+ * over the E logits, keep the K largest, renormalise them to sum to one.  Equal logits go to
+ * the lower expert index; k = 0 is the highest score.
+ *   d_logits : [T, E] fp32      d_idx : [T, K] int32 (out)      d_w : [T, K] fp32 (out)
+ * Stateless (no handle).  1 <= K <= E <= 1024, K <= 32. */
+moe_status moe_async_route(const float* d_logits, int32_t T, int32_t E, int32_t K,
+                           int32_t* d_idx, float* d_w, void* stream);
+
+/* Receptor: deliver one wave of routed pairs into layer `layer`'s expert queue.
+ * StreamEP section 3, steps 1-2: each carried token is stored in the token pool under its
+ * combine slot, and each delivered (expert, k, w) pair is appended to that expert's bucket
+ * (warp-aggregated atomics).  A token's first accepted pair also enqueues the shared expert.
+ *   n        : tokens carried (0 is a no-op)
+ *   d_rows   : [n] row of d_x / d_expert / d_w for each carried token; NULL = rows 0..n-1
+ *   d_slot   : [n] combine slot (RequestID) per token, < max_slots; NULL = the row index
+ *   d_x      : [*, H] token vectors in cfg dtype (row-indexed)
+ *   d_expert : [*, K] int32 expert ids (row-indexed), 0 <= id < E
+ *   d_w      : [*, K] fp32 routing weights (row-indexed)
+ *   d_kmask  : [n] uint32, bit k set = pair k is delivered by this wave; NULL = all K
+ *   d_gen    : [n] uint32 expected slot generation; NULL = unchecked.  Mismatch -> the
+ *              token's pairs are dropped and MOE_ERR_STALE is latched.
+ * A pair already accepted for this slot generation is dropped and MOE_ERR_DUPLICATE latched.
+ * The caller's buffers may be reused once the stream reaches this point. */
+moe_status moe_async_enqueue(moe_async_t h, int32_t layer, int32_t n,
+                             const int32_t* d_rows, const int32_t* d_slot, const void* d_x,
+                             const int32_t* d_expert, const float* d_w,
+                             const uint32_t* d_kmask, const uint32_t* d_gen, void* stream);
+
+/* One scheduling step of layer `layer`, decided on the device from the bucket depths
+ * (no host synchronisation): the policy picks buckets, each picked bucket is drained whole,
+ * its tokens are gathered and run through the expert (grouped GEMM over all picks), the
+ * weighted results are written to their combine slots, and every token whose K (+shared)
+ * results are now complete is combined (y = sum in ascending k) and appended to the ready
+ * list.  A step with nothing to pick launches kernels that exit at once. */
+moe_status moe_async_schedule_step(moe_async_t h, int32_t layer, const moe_async_policy* policy,
+                                   void* stream);
+
+/* Collect ready tokens of layer `layer` in completion order:
+ *   d_y_out    : [max_out, H] cfg dtype     d_slot_out : [max_out] int32
+ *   d_gen_out  : [max_out] uint32 (generation the result belongs to; may be NULL)
+ *   d_n_out    : [1] int32 on the device
+ *   append = 0 : rows are written from index 0 and *d_n_out = number written (<= max_out)
+ *   append = 1 : rows are written from index *d_n_out (read on the device) and *d_n_out is
+ *                advanced by the number written (total <= max_out), so a caller can collect
+ *                after every step into one buffer without reading anything back
+ * Each collected slot is reclaimed (its generation advances) after its output row is copied,
+ * so it may carry a new request from then on. */
+moe_status moe_async_collect(moe_async_t h, int32_t layer, int32_t max_out, void* d_y_out,
+                             int32_t* d_slot_out, uint32_t* d_gen_out, int32_t* d_n_out,
+                             int32_t append, void* stream);
+
+/* Run scheduling steps of `layer` under `policy` until no token of the handle is open
+ * (accepted but not yet combined, in any layer), checking the device counters every `check_every` steps;
+ * at most max_steps steps.  Synchronises `stream`.  Returns MOE_ERR_TIMEOUT when tokens are
+ * still open after max_steps (e.g. a withheld pair), else the sticky device error. */
+moe_status moe_async_wait(moe_async_t h, int32_t layer, const moe_async_policy* policy,
+                          int32_t max_steps, int32_t check_every, void* stream);
+
+/* Synchronise `stream` and return the sticky device error (MOE_OK if none). */
+moe_status moe_async_sync(moe_async_t h, void* stream);
+
+/* Synchronise `stream` and copy the counters into *h_stats. */
+moe_status moe_async_get_stats(moe_async_t h, void* stream, moe_async_stats* h_stats);
+
+/* Synchronise and copy the pick trace: h_buf receives up to cap records of 4 int32
+ * (step, layer, expert, count) in step order, *h_n the number of records written. */
+moe_status moe_async_get_trace(moe_async_t h, void* stream, int32_t* h_buf, int32_t cap,
+                               int32_t* h_n);
+
+/* Synchronise and copy layer `layer`'s queue contents: h_depth[b] (b < E + has_shared) gets
+ * bucket b's depth, and h_records the pending records of every bucket in bucket order, each
+ * as (slot, k) int32 pairs (bucket-internal order is arrival order, which concurrent appends
+ * make nondeterministic).  cap = capacity of h_records in pairs; *h_n = pairs written. */
+moe_status moe_async_snapshot(moe_async_t h, int32_t layer, void* stream, int32_t* h_depth,
+                              int32_t* h_records, int32_t cap, int32_t* h_n);
+
+/* Per-kernel timing (tracing).  enable = 1 brackets every later kernel launch of the handle
+ * with a pair of CUDA events on its stream (up to 65536 launches are kept); enable = 0 stops.
+ * Host-side events only: no device memory is allocated. */
+moe_status moe_async_profile(moe_async_t h, int32_t enable);
+
+/* Synchronise `stream`, then for each kernel kind k < n_kinds add the summed event time of its
+ * recorded launches to h_ms[k] (milliseconds) and their number to h_launches[k]; the record
+ * is cleared afterwards. */
+moe_status moe_async_profile_read(moe_async_t h, void* stream, double* h_ms, int64_t* h_launches,
+                                  int32_t n_kinds);
+
+/* Free every device allocation of the handle.  Synchronises `stream` first. */
+moe_status moe_async_destroy(moe_async_t h, void* stream);
+
+/* Human-readable name of a status code (static string). */
+const char* moe_async_status_string(moe_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_ASYNC_H */

@@ -1,0 +1,279 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle, element by element.
+
+Indexing (routing ids, queue contents, pick traces, emission steps, slot maps) must match
+bit-exactly; float outputs within max|gpu - oracle| / max|oracle| <= 1e-5 (fp32) and
+<= 2e-2 (bf16 storage, fp32 accumulation).
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import moe_oracle as om
+from workloads import get_config, make_workload, make_logits, shuffled_waves, repartitioned_waves, Wave
+from tests.gpu_helpers import (TOL, rel_err, expert_getter, oracle_policy, gpu_layer, trace_steps,
+                               oracle_steps, by_token)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pkg():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__ as g
+    g.build()
+    import asynchronous_expert_execution_gb300 as p
+    return p
+
+
+# ---------------------------------------------------------------- routing
+
+@pytest.mark.parametrize("name", ["c1", "c2", "c3", "c4", "m2"])
+def test_route_parity(pkg, name):
+    spec = get_config(name)
+    z = make_logits(spec, seed=1)
+    idx, w = pkg.route(z.cuda(), spec.layer.top_k)
+    ri, rw = om.route(z.numpy(), spec.layer.top_k)
+    assert np.array_equal(idx.cpu().numpy(), ri)                 # bit-exact ids and k order
+    assert np.abs(w.cpu().numpy() - rw).max() <= 2e-6
+
+
+def test_route_ties_and_edges(pkg):
+    z = torch.tensor([[1.0, 3.0, 2.0, 3.0], [0.0, 0.0, 0.0, 0.0], [-1.0, 5.0, 5.0, 5.0]])
+    idx, w = pkg.route(z.cuda(), 2)
+    assert idx.cpu().tolist() == [[1, 3], [0, 1], [1, 2]]
+    assert np.allclose(w.cpu().numpy(), 0.5)
+    z = torch.randn(37, 1000)                                      # E not a multiple of 32
+    idx, w = pkg.route(z.cuda(), 32)
+    ri, rw = om.route(z.numpy(), 32)
+    assert np.array_equal(idx.cpu().numpy(), ri)
+    assert np.abs(w.cpu().numpy() - rw).max() <= 2e-6
+
+
+# ------------------------------------------------------ identity: exact merge
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("shared", [False, True])
+def test_identity_experts_bitexact(pkg, dtype, shared):
+    """E(x) = x, integer-valued x, power-of-two weights: y = (sum_j w_j) x exactly."""
+    from workloads import LayerSpec, WorkloadSpec
+    T, E, K, H = 300, 24, 4, 136
+    spec = WorkloadSpec(name="ident", layer=LayerSpec(E, K, H, 64, dtype, has_shared=shared, shared_inter=64),
+                        tokens=T, router="normal", waves="even", num_waves=6, arrival="exp", policy="mtfs")
+    wl = make_workload(spec, seed=3, weights=False)
+    rng = np.random.default_rng(5)
+    # |y| <= (K/2 + 1) * 8 on a 1/4 grid: exact in bf16 as well as fp32
+    xi = rng.integers(-8, 8, size=(T, H)).astype(np.float32)
+    x = torch.tensor(xi).to(wl.x.dtype)
+    idx = np.stack([rng.permutation(E)[:K] for _ in range(T)]).astype(np.int32)
+    wv = (rng.integers(1, 3, size=(T, K)) / 4.0).astype(np.float32)
+    res = gpu_layer(pkg, spec, wl, expert_kind="identity", x=x, idx=torch.tensor(idx), w=torch.tensor(wv))
+    assert res["status"] == 0 and res["drained"] >= 0
+    assert sorted(res["slots"].tolist()) == list(range(T))         # each token exactly once
+    sim = om.replay_layer(E, K, xi, idx, wv, wl.waves, om.mtfs_pick, None, has_shared=shared)
+    want = np.stack([sim.y[t] for t in range(T)])
+    got = by_token(res["slots"], res["y"], T, H)
+    assert np.array_equal(got, want)
+    assert np.array_equal(got, (wv.sum(1, dtype=np.float64) + (1.0 if shared else 0.0))[:, None] * xi)
+    assert trace_steps(res["trace"]) == oracle_steps(sim)
+    em = np.zeros(T, dtype=np.int64)
+    em[res["slots"]] = res["emit"]
+    assert all(em[t] == sim.emit_step[t] for t in range(T))
+
+
+# ------------------------------------------------------------- SwiGLU layers
+
+@pytest.mark.parametrize("name", ["c1", "m1", "m2", "m3", "m4"])
+def test_layer_parity(pkg, name):
+    spec = get_config(name)
+    L = spec.layer
+    wl = make_workload(spec, seed=0)
+    res = gpu_layer(pkg, spec, wl)
+    assert res["status"] == 0, res["status"]
+    assert res["drained"] >= 0
+    T = spec.tokens
+    ii, ww = om.route(wl.logits.numpy(), L.top_k)
+    assert np.array_equal(res["idx"], ii)
+    ex = expert_getter(wl.weights[0], L.num_experts)
+    sim = om.replay_layer(L.num_experts, L.top_k, wl.x.double().numpy(), ii, ww,
+                          wl.waves, oracle_policy(spec), ex, has_shared=L.has_shared)
+    assert sorted(res["slots"].tolist()) == list(range(T))
+    want = np.stack([sim.y[t] for t in range(T)])
+    got = by_token(res["slots"], res["y"], T, L.hidden)
+    err = rel_err(got, want)
+    assert err <= TOL[L.dtype], err
+    assert trace_steps(res["trace"]) == oracle_steps(sim)
+    em = np.zeros(T, dtype=np.int64)
+    em[res["slots"]] = res["emit"]
+    assert all(em[t] == sim.emit_step[t] for t in range(T))
+    st = res["stats"]
+    assert st["pairs_executed"] == T * (L.top_k + (1 if L.has_shared else 0))
+    assert st["tokens_combined"] == T and st["open_tokens"] == 0 and st["pending_pairs"] == 0
+    assert st["duplicates"] == 0 and st["error"] == 0
+
+
+def test_route_weights_into_oracle_tolerance(pkg):
+    """The oracle's own float64 weights (not the GPU's fp32 ones) also meet the bound."""
+    spec = get_config("m1")
+    L = spec.layer
+    wl = make_workload(spec, seed=2)
+    res = gpu_layer(pkg, spec, wl)
+    ii, ww = om.route(wl.logits.numpy(), L.top_k)
+    ref = om.dense_moe(wl.x.double().numpy(), ii, ww, expert_getter(wl.weights[0], L.num_experts))
+    assert rel_err(by_token(res["slots"], res["y"], spec.tokens, L.hidden), ref) <= TOL[L.dtype]
+
+
+def test_queue_snapshot_parity(pkg):
+    """Queue contents after delivering every wave (no step yet): per-expert multisets and
+    depths equal the oracle's, bit for bit."""
+    spec = get_config("m2")
+    L = spec.layer
+    wl = make_workload(spec, seed=0)
+    ws = [{k: v.cuda().contiguous() for k, v in wl.weights[0].items()}]
+    moe = pkg.MoEAsync(L.num_experts, L.top_k, L.hidden, L.inter, wl.x.dtype, spec.tokens, weights=ws,
+                       has_shared=True)
+    idx, w = pkg.route(wl.logits.cuda(), L.top_k)
+    x = wl.x.cuda()
+    for wv in wl.waves:
+        rows = torch.tensor(wv.tokens, dtype=torch.int32, device="cuda")
+        moe.enqueue(0, x, idx, w, rows=rows)
+    depths, recs = moe.snapshot(0)
+    sim = om.AsyncMoEOracle(L.num_experts, L.top_k, wl.x.double().numpy(), None, has_shared=True)
+    ii, ww = om.route(wl.logits.numpy(), L.top_k)
+    for wv in wl.waves:
+        sim.deliver(wv.tokens, ii, ww)
+    assert depths.tolist() == sim.depths()
+    assert recs == [list(b) for b in sim.snapshot()]
+    moe.close()
+
+
+@pytest.mark.parametrize("name", ["m1", "m2"])
+def test_arrival_order_and_partition_bitwise_invariance(pkg, name):
+    """Shuffled arrival ticks and different wave partitions give bitwise-identical y."""
+    spec = get_config(name)
+    wl = make_workload(spec, seed=1)
+    outs = []
+    variants = [wl.waves, shuffled_waves(wl.waves, 1), shuffled_waves(wl.waves, 2),
+                repartitioned_waves(spec.tokens, 3, 7), repartitioned_waves(spec.tokens, 9, 8)]
+    for wv in variants:
+        res = gpu_layer(pkg, spec, wl, waves=wv)
+        assert res["status"] == 0 and res["drained"] >= 0
+        outs.append(by_token(res["slots"], res["y"], spec.tokens, spec.layer.hidden))
+    for o in outs[1:]:
+        assert np.array_equal(o, outs[0])
+
+
+# ------------------------------------------------------ protocol / failures
+
+def _small(pkg, dtype="bf16", shared=False, cap=0, T=64, E=8, K=2, H=64, I=64):
+    from workloads import LayerSpec, WorkloadSpec
+    spec = WorkloadSpec(name="small", layer=LayerSpec(E, K, H, I, dtype, has_shared=shared, shared_inter=I),
+                        tokens=T, router="normal", waves="even", num_waves=2, arrival="index", policy="mtfs")
+    wl = make_workload(spec, seed=4)
+    ws = [{k: v.cuda().contiguous() for k, v in wl.weights[0].items()}]
+    moe = pkg.MoEAsync(E, K, H, I, wl.x.dtype, T, weights=ws, has_shared=shared, bucket_capacity=cap)
+    idx, w = pkg.route(wl.logits.cuda(), K)
+    return spec, wl, moe, wl.x.cuda(), idx, w
+
+
+def test_withheld_pair_times_out(pkg):
+    spec, wl, moe, x, idx, w = _small(pkg)
+    T = spec.tokens
+    kmask = torch.full((T,), 3, dtype=torch.int32, device="cuda")
+    kmask[5] = 1                                                   # token 5 withholds k = 1
+    moe.enqueue(0, x, idx, w, kmask=kmask)
+    st = moe.wait(0, pkg.Policy(), max_steps=6, check_every=2)
+    assert st == 5                                                  # MOE_ERR_TIMEOUT
+    y = torch.empty((T, spec.layer.hidden), dtype=x.dtype, device="cuda")
+    slots = torch.empty(T, dtype=torch.int32, device="cuda")
+    n = torch.zeros(1, dtype=torch.int32, device="cuda")
+    moe.collect(0, y, slots, n)
+    got = sorted(slots[: int(n.item())].cpu().tolist())
+    assert got == [t for t in range(T) if t != 5]                  # never emitted early
+    s = moe.stats()
+    assert s["open_tokens"] == 1 and s["error"] == 0
+    # the missing pair arrives late: the token completes
+    one = torch.tensor([5], dtype=torch.int32, device="cuda")
+    moe.enqueue(0, x, idx, w, rows=one, kmask=torch.tensor([2], dtype=torch.int32, device="cuda"))
+    assert moe.wait(0, pkg.Policy(), max_steps=4) == 0
+    moe.collect(0, y, slots, n)
+    assert int(n.item()) == 1 and int(slots[0].item()) == 5
+    moe.close()
+
+
+def test_duplicate_pair_rejected_once(pkg):
+    spec, wl, moe, x, idx, w = _small(pkg, shared=True)
+    T, H = spec.tokens, spec.layer.hidden
+    moe.enqueue(0, x, idx, w)
+    rows = torch.tensor([3, 7], dtype=torch.int32, device="cuda")
+    moe.enqueue(0, x, idx, w, rows=rows)                            # duplicates of tokens 3 and 7
+    for _ in range(2):
+        moe.schedule_step(0, pkg.Policy())
+    assert moe.sync() == 3                                          # MOE_ERR_DUPLICATE (sticky)
+    s = moe.stats()
+    assert s["duplicates"] == 2 * spec.layer.top_k
+    assert s["pairs_executed"] == T * (spec.layer.top_k + 1)       # nothing accumulated twice
+    y = torch.empty((T, H), dtype=x.dtype, device="cuda")
+    slots = torch.empty(T, dtype=torch.int32, device="cuda")
+    n = torch.zeros(1, dtype=torch.int32, device="cuda")
+    moe.collect(0, y, slots, n)
+    assert int(n.item()) == T
+    L = spec.layer
+    ii, ww = om.route(wl.logits.numpy(), L.top_k)
+    ref = om.dense_moe(wl.x.double().numpy(), ii, ww, expert_getter(wl.weights[0], L.num_experts),
+                       shared=expert_getter(wl.weights[0], L.num_experts)(L.num_experts))
+    got = by_token(slots.cpu().numpy(), y.float().cpu().numpy().astype(np.float64), T, H)
+    assert rel_err(got, ref) <= TOL["bf16"]
+    moe.close()
+
+
+def test_stale_generation_and_slot_reuse(pkg):
+    spec, wl, moe, x, idx, w = _small(pkg, dtype="f32")
+    T, H = spec.tokens, spec.layer.hidden
+    y = torch.empty((T, H), dtype=x.dtype, device="cuda")
+    slots = torch.empty(T, dtype=torch.int32, device="cuda")
+    gens = torch.empty(T, dtype=torch.int32, device="cuda")
+    n = torch.zeros(1, dtype=torch.int32, device="cuda")
+    g0 = torch.zeros(T, dtype=torch.int32, device="cuda")
+    moe.enqueue(0, x, idx, w, gen=g0)
+    assert moe.wait(0, pkg.Policy(), max_steps=4) == 0
+    moe.collect(0, y, slots, n, gen_out=gens)
+    assert int(n.item()) == T and gens.cpu().tolist() == [0] * T
+    first = by_token(slots.cpu().numpy(), y.cpu().numpy().astype(np.float64), T, H)
+    # second request generation on the same slots (gen 1): same values again
+    g1 = torch.ones(T, dtype=torch.int32, device="cuda")
+    moe.enqueue(0, x, idx, w, gen=g1)
+    assert moe.wait(0, pkg.Policy(), max_steps=4) == 0
+    moe.collect(0, y, slots, n, gen_out=gens)
+    assert gens.cpu().tolist() == [1] * T
+    assert np.array_equal(by_token(slots.cpu().numpy(), y.cpu().numpy().astype(np.float64), T, H), first)
+    # a late pair from generation 0 is stale now
+    rows = torch.tensor([2], dtype=torch.int32, device="cuda")
+    moe.enqueue(0, x, idx, w, rows=rows, gen=torch.zeros(1, dtype=torch.int32, device="cuda"))
+    assert moe.sync() == 4                                          # MOE_ERR_STALE
+    assert moe.stats()["stale"] == 1 and moe.stats()["open_tokens"] == 0
+    moe.close()
+
+
+def test_bucket_capacity_overflow_reported(pkg):
+    spec, wl, moe, x, idx, w = _small(pkg, cap=2, T=64, E=4, K=2)
+    moe.enqueue(0, x, idx, w)
+    assert moe.sync() == 2                                          # MOE_ERR_CAPACITY
+    moe.close()
+
+
+def test_empty_inputs(pkg):
+    spec, wl, moe, x, idx, w = _small(pkg)
+    moe.enqueue(0, x, idx, w, n=0)                                  # empty wave: no-op
+    moe.schedule_step(0, pkg.Policy())                              # nothing to pick
+    y = torch.empty((4, spec.layer.hidden), dtype=x.dtype, device="cuda")
+    slots = torch.empty(4, dtype=torch.int32, device="cuda")
+    n = torch.full((1,), 7, dtype=torch.int32, device="cuda")
+    moe.collect(0, y, slots, n)
+    assert int(n.item()) == 0
+    s = moe.stats()
+    assert s["steps"] == 1 and s["pairs_executed"] == 0 and s["error"] == 0
+    e0 = torch.empty(0, 4, device="cuda")
+    i0, w0 = pkg.route(e0, 2)
+    assert i0.shape == (0, 2)
+    moe.close()

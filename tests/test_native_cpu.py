@@ -1,0 +1,88 @@
+"""CPU-side checks of the C ABI: the library builds, loads, exports every declared
+symbol, and rejects bad arguments on the host before touching the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import __graft_entry__ as g
+    g.build()
+    from asynchronous_expert_execution_gb300 import _native as N
+    return N.load()
+
+
+def _declared():
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for f in os.listdir(inc):
+        if f.endswith(".h"):
+            src = open(os.path.join(inc, f)).read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names |= set(re.findall(r"\b(moe_\w+)\s*\(", src))
+    return names
+
+
+def test_every_declared_symbol_exported(lib):
+    from asynchronous_expert_execution_gb300 import _native as N
+    declared = _declared()
+    assert declared, "no declarations found"
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert declared == set(N.EXPORTS) | (declared - set(N.EXPORTS))
+    assert set(N.EXPORTS) <= declared
+
+
+def test_status_strings(lib):
+    for code in range(8):
+        assert lib.moe_async_status_string(code)
+
+
+def test_host_validation_without_gpu(lib):
+    from asynchronous_expert_execution_gb300 import _native as N
+    # router: bad sizes are rejected on the host
+    assert lib.moe_async_route(None, -1, 8, 2, None, None, None) == N.MOE_ERR_INVALID
+    assert lib.moe_async_route(None, 4, 8, 9, None, None, None) == N.MOE_ERR_INVALID
+    assert lib.moe_async_route(None, 4, 2000, 2, None, None, None) == N.MOE_ERR_INVALID
+    assert lib.moe_async_route(None, 0, 8, 2, None, None, None) == N.MOE_OK      # empty: no-op
+    # create: invalid configurations never reach CUDA
+    out = ctypes.c_void_p()
+    bad = [
+        dict(hidden=60),             # H not a multiple of 8
+        dict(inter=24),              # I not a multiple of 16
+        dict(top_k=0),
+        dict(top_k=9),               # K > E
+        dict(num_experts=2000),
+        dict(dtype=5),
+        dict(max_slots=0),
+    ]
+    for over in bad:
+        c = dict(num_layers=1, num_experts=8, top_k=2, hidden=64, inter=128, dtype=0, has_shared=0,
+                 max_slots=32, bucket_capacity=0, expert_kind=1, trace_capacity=0)
+        c.update(over)
+        cfg = N.Config(**c)
+        assert lib.moe_async_create(ctypes.byref(cfg), None, None, None, None, None, None, None,
+                                    ctypes.byref(out)) == N.MOE_ERR_INVALID, over
+    # SwiGLU without weights
+    cfg = N.Config(1, 8, 2, 64, 128, 0, 0, 32, 0, 0, 0)
+    assert lib.moe_async_create(ctypes.byref(cfg), None, None, None, None, None, None, None,
+                                ctypes.byref(out)) == N.MOE_ERR_INVALID
+    # calls on a null handle
+    pol = N.Policy(0, 0, 0, 1)
+    assert lib.moe_async_schedule_step(None, 0, ctypes.byref(pol), None) == N.MOE_ERR_INVALID
+    assert lib.moe_async_enqueue(None, 0, 1, None, None, None, None, None, None, None, None) == N.MOE_ERR_INVALID
+    assert lib.moe_async_destroy(None, None) == N.MOE_ERR_INVALID
+
+
+def test_product_path_has_no_oracle_import():
+    """The product package must not import the oracle (tests/bench/smoke only)."""
+    pkg = os.path.join(ROOT, "asynchronous_expert_execution_gb300")
+    for f in os.listdir(pkg):
+        if f.endswith(".py"):
+            src = open(os.path.join(pkg, f)).read()
+            assert not re.search(r"^\s*(from|import)\s+oracle\b", src, flags=re.M), f
