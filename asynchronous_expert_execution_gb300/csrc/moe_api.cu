@@ -467,7 +467,7 @@ moe_status moe_async_create(const moe_async_config* cfg, const void* const* w1,
     free_handle(h);
     return MOE_ERR_CUDA;
   }
-  h->use_tc = false;
+  h->use_tc = swiglu && c.dtype == MOE_BF16;
   h->geom = h->use_tc ? tc_geom() : simt_geom();
   if (!swiglu) h->geom = TileGeom{16, 2 * c.inter, 16, c.hidden};
   h->parts_per_pair = (d.H + h->geom.bm2 - 1) / h->geom.bm2;

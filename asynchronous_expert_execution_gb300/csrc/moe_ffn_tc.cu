@@ -1,11 +1,557 @@
-// Expert FFN for bf16 on the 5th-generation tensor cores (tcgen05 + TMEM, TMA-fed).
+// Expert FFN for bf16 on the 5th-generation tensor cores: tcgen05.mma with TMEM accumulators,
+// weights streamed by TMA, gathered token rows by cp.async.
+//
+// Swap-AB grouped GEMM.  Each tile computes D[128 x N] = A[128 x K] * B[N x K]^T where
+//   A = 128 rows of an expert's packed weights (K-major, 128B-swizzled, loaded by TMA), and
+//   B = N <= BN gathered token rows of the step's batch for that expert (K-major, 128B
+//       swizzle applied by the loader),
+// so a decode batch of a few tokens per expert still fills the 128-row MMA with weights and
+// the kernel streams each picked expert's weights once per token tile.
+//   GEMM1: A = W13 (gate/up rows interleaved in blocks of 16), K = H, B = pool rows of the
+//          tokens in the expert's bucket (the gather of StreamEP section 3, step 4, fused into
+//          the operand load); epilogue: h = silu(gate) * up, stored bf16.
+//   GEMM2: A = W2^T, K = I, B = the expert's h rows; epilogue: slotbuf[slot][k] = w * o
+//          (fp32), then readiness counting and the top-k merge y = sum_k (ascending k).
+//
+// Warp roles (256 threads, one persistent CTA per SM):
+//   warp 0  lane 0: TMA producer for A       warp 1: cp.async producer for B (gather)
+//   warp 2  lane 0: MMA issuer; warp 2 allocates / frees TMEM
+//   warps 4-7: epilogue (TMEM lanes 32*(warp-4) ..), double-buffered accumulators
+// Every wait is bounded in time; a timeout latches MOE_ERR_TIMEOUT, stops all roles, and the
+// CTA still frees its TMEM before exiting.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <new>
 #include "moe_internal.cuh"
 
 namespace moe {
+namespace {
 
-TileGeom tc_geom() { return simt_geom(); }
-moe_status tc_setup(moe_async_s*) { return MOE_OK; }
-void tc_teardown(moe_async_s*) {}
-moe_status launch_ffn_tc(moe_async_s* h, int layer, cudaStream_t s) { return launch_ffn_simt(h, layer, s); }
+constexpr int kBM = 128;              // MMA M (weight rows per tile)
+constexpr int kBK = 64;               // K per pipeline stage (one 128-byte swizzle atom)
+constexpr int kThreads = 256;
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // 2 s per wait
+
+// ------------------------------------------------------------------ PTX wrappers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait on a phase parity.  Returns false (and raises the CTA abort flag and the
+// sticky device error) when the phase does not complete within the limit, or when another
+// role already aborted.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          DevCounters* C) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (global_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      set_error(C, MOE_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint64_t* bar, int c0,
+                                            int c1, int c2, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+
+// 32 lanes x 16 consecutive fp32 columns of the accumulator; the wait is tied to the
+// registers so no use can be scheduled before it.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                 "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+                 "+r"(r[14]), "+r"(r[15])::"memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Named barrier over the 128 epilogue threads with an AND-reduction of a predicate, so a
+// decision taken after a bounded wait is uniform across the group.
+__device__ __forceinline__ bool epi_bar_and(bool pred) {
+  uint32_t out;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, 1, 128, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(out)
+      : "r"((uint32_t)pred)
+      : "memory");
+  return out != 0;
+}
+
+struct EpiBarrier {
+  __device__ __forceinline__ void operator()() const { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+};
+
+// tcgen05 shared-memory matrix descriptor: K-major operand, 128-byte swizzle, 8-row groups
+// 1024 bytes apart (SBO), descriptor version 1 (bit 46).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)(16u >> 4) << 16;
+  d |= (uint64_t)(1024u >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major, N and M encoded.
+__device__ __forceinline__ uint32_t idesc_bf16(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// ----------------------------------------------------------------- tile decoding
+
+struct Tile {
+  int expert;
+  uint32_t head;
+  int row_base;
+  int fti;      // feature (A-row) tile
+  int j0;       // first token of the tile within the item
+  int nj;       // valid tokens
+  int nmma;     // MMA N (multiple of 16, >= nj)
+};
+
+template <int BN>
+__device__ __forceinline__ Tile decode_tile(const StepPlan* P, int t, bool second) {
+  const WorkItem it = P->items[find_item(P, t, second)];
+  const int local = t - (second ? it.t2_base : it.t1_base);
+  const int ntt = (it.count + BN - 1) / BN;
+  Tile tl;
+  tl.expert = it.expert;
+  tl.head = it.head;
+  tl.row_base = it.row_base;
+  tl.fti = local / ntt;
+  tl.j0 = (local % ntt) * BN;
+  tl.nj = min(BN, it.count - tl.j0);
+  tl.nmma = min(BN, max(16, (tl.nj + 15) & ~15));
+  return tl;
+}
+
+template <int BN, int STAGES>
+struct SmemLayout {
+  static constexpr int kA = kBM * kBK * 2;                   // 16 KB
+  static constexpr int kB = BN * kBK * 2;
+  static constexpr int kOffA = 0;
+  static constexpr int kOffB = kOffA + STAGES * kA;
+  static constexpr int kOffBar = kOffB + STAGES * kB;
+  static constexpr int kNumBars = 2 * STAGES + 4;
+  static constexpr int kOffTmem = kOffBar + kNumBars * 8;
+  static constexpr int kOffAbort = kOffTmem + 4;
+  static constexpr int kOffRowPtr = (kOffAbort + 4 + 15) & ~15;
+  static constexpr int kOffSlot = kOffRowPtr + BN * 8;
+  static constexpr int kOffK = kOffSlot + BN * 4;
+  static constexpr int kOffFin = kOffK + BN * 4;
+  static constexpr int kOffW = kOffFin + BN * 4;
+  static constexpr int kBytes = kOffW + BN * 4;
+  static constexpr int kAlloc = kBytes + 1024;               // room to align the base to 1024
+};
+
+// ------------------------------------------------------------------ the kernel
+
+template <int BN, int STAGES, bool GEMM2>
+__global__ void __launch_bounds__(kThreads, 1)
+ffn_tc_kernel(const __grid_constant__ CUtensorMap tmA, LayerView L, Dims d, DevCounters* C,
+              const StepPlan* __restrict__ P, __nv_bfloat16* __restrict__ hbuf, int target) {
+  using SL = SmemLayout<BN, STAGES>;
+  constexpr int kLag = STAGES - 2;            // cp.async groups kept in flight by the B producer
+  constexpr uint32_t kTmemCols = 2 * BN;      // two accumulator buffers
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SL::kOffBar);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + STAGES;
+  uint64_t* tfull = bars + 2 * STAGES;
+  uint64_t* tempty = bars + 2 * STAGES + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SL::kOffTmem);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SL::kOffAbort);
+  const __nv_bfloat16** rowptr = reinterpret_cast<const __nv_bfloat16**>(smem + SL::kOffRowPtr);
+  int* slot_s = reinterpret_cast<int*>(smem + SL::kOffSlot);
+  int* k_s = reinterpret_cast<int*>(smem + SL::kOffK);
+  int* fin = reinterpret_cast<int*>(smem + SL::kOffFin);
+  float* w_s = reinterpret_cast<float*>(smem + SL::kOffW);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_tiles = GEMM2 ? P->n_tiles2 : P->n_tiles1;
+  const int Kdim = GEMM2 ? d.I : d.H;
+  const int nk = (Kdim + kBK - 1) / kBK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1 + 32);    // A producer's expect_tx arrive + 32 B-producer lanes
+      mbar_init(&empty[s], 1);        // tcgen05.commit
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);        // tcgen05.commit after the tile's last MMA
+      mbar_init(&tempty[b], 4);       // one arrive per epilogue warp
+    }
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------ A producer: TMA of weight tiles
+    if (lane == 0) {
+      const uint64_t pol = policy_evict_first();
+      uint32_t it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+        const Tile tl = decode_tile<BN>(P, t, GEMM2);
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1u;
+          if (!(ok = mbar_wait(&empty[s], ph ^ 1u, abort_flag, C))) break;
+          mbar_arrive_expect_tx(&full[s], SL::kA);
+          tma_load_3d(smem_u32(smem + SL::kOffA + s * SL::kA), &tmA, &full[s], kb * kBK, tl.fti * kBM,
+                      tl.expert, pol);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------ B producer: gathered rows via cp.async
+    const char* pool = static_cast<const char*>(L.pool);
+    uint32_t it = 0;
+    int issued = 0, signaled = 0;            // stages issued / signalled by this warp
+    bool ok = true;
+    for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+      const Tile tl = decode_tile<BN>(P, t, GEMM2);
+      __syncwarp();
+      for (int r = lane; r < tl.nmma; r += 32) {
+        const __nv_bfloat16* p = nullptr;
+        if (r < tl.nj) {
+          if (GEMM2) {
+            p = hbuf + (size_t)(tl.row_base + tl.j0 + r) * d.I;
+          } else {
+            const int rec = record_at(L, d, tl.expert, tl.head + tl.j0 + r);
+            p = reinterpret_cast<const __nv_bfloat16*>(pool) + (size_t)(rec >> kKShift) * d.H;
+          }
+        }
+        rowptr[r] = p;
+      }
+      __syncwarp();
+      for (int kb = 0; kb < nk; ++kb, ++it) {
+        const int s = it % STAGES;
+        const uint32_t ph = (it / STAGES) & 1u;
+        const bool w_ok = mbar_wait(&empty[s], ph ^ 1u, abort_flag, C);
+        if (!(ok = __all_sync(0xffffffffu, w_ok))) break;
+        const uint32_t bs = smem_u32(smem + SL::kOffB + s * SL::kB);
+        const int col0 = kb * kBK;
+        for (int q = lane; q < tl.nmma * 8; q += 32) {
+          const int r = q >> 3, c = q & 7;
+          const __nv_bfloat16* rp = rowptr[r];
+          const int col = col0 + c * 8;
+          const bool valid = rp != nullptr && col < Kdim;
+          const void* src = valid ? static_cast<const void*>(rp + col) : static_cast<const void*>(pool);
+          cp_async16(bs + r * 128 + ((c ^ (r & 7)) << 4), src, valid ? 16u : 0u);
+        }
+        cp_async_commit();
+        ++issued;
+        if (issued - signaled > kLag) {
+          cp_async_wait<kLag>();
+          fence_proxy_async();
+          mbar_arrive(&full[signaled % STAGES]);
+          ++signaled;
+        }
+      }
+    }
+    cp_async_wait<0>();
+    fence_proxy_async();
+    while (signaled < issued) {
+      mbar_arrive(&full[signaled % STAGES]);
+      ++signaled;
+    }
+  } else if (warp == 2) {
+    // ---------------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      uint32_t it = 0, tile_i = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x, ++tile_i) {
+        const Tile tl = decode_tile<BN>(P, t, GEMM2);
+        const int buf = tile_i & 1;
+        const uint32_t tph = (tile_i >> 1) & 1u;
+        if (!(ok = mbar_wait(&tempty[buf], tph ^ 1u, abort_flag, C))) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
+        const uint32_t idesc = idesc_bf16(kBM, tl.nmma);
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1u;
+          if (!(ok = mbar_wait(&full[s], ph, abort_flag, C))) break;
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(smem + SL::kOffA + s * SL::kA);
+          const uint32_t b0 = smem_u32(smem + SL::kOffB + s * SL::kB);
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k)
+            mma_bf16(d_tmem, sw128_desc(a0 + k * 32), sw128_desc(b0 + k * 32), idesc, (kb | k) != 0);
+          mma_commit(&empty[s]);
+        }
+        if (ok) mma_commit(&tfull[buf]);
+      }
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------------ epilogue
+    const int q = warp - 4;                       // TMEM lane quarter
+    const int et = threadIdx.x - 128;             // 0..127
+    uint32_t tile_i = 0;
+    for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++tile_i) {
+      const Tile tl = decode_tile<BN>(P, t, GEMM2);
+      const int buf = tile_i & 1;
+      const uint32_t tph = (tile_i >> 1) & 1u;
+      if (GEMM2) {
+        for (int j = et; j < tl.nj; j += 128) {
+          const int rec = record_at(L, d, tl.expert, tl.head + tl.j0 + j);
+          const int sl = rec >> kKShift, kk = rec & kKMask;
+          slot_s[j] = sl;
+          k_s[j] = kk;
+          w_s[j] = L.wtab[(size_t)sl * d.KS + kk];
+        }
+      }
+      const bool w_ok = mbar_wait(&tfull[buf], tph, abort_flag, C);
+      if (!epi_bar_and(w_ok)) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN);
+      if (!GEMM2) {
+        const int f = tl.fti * (kBM / 2) + 16 * q + (lane & 15);       // feature of this lane pair
+        const bool lo = lane < 16;
+        for (int c0 = 0; c0 < tl.nj; c0 += 16) {
+          float v[16];
+          tmem_ld16(tbase + c0, v);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float send = lo ? v[8 + j] : v[j];
+            const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
+            const int col = c0 + (lo ? j : 8 + j);
+            const float g = lo ? v[j] : recv;
+            const float u = lo ? recv : v[8 + j];
+            if (col < tl.nj && f < d.I)
+              hbuf[(size_t)(tl.row_base + tl.j0 + col) * d.I + f] = __float2bfloat16_rn(silu_f(g) * u);
+          }
+        }
+      } else {
+        const int f = tl.fti * kBM + 32 * q + lane;                     // output feature of H
+        for (int c0 = 0; c0 < tl.nj; c0 += 16) {
+          float v[16];
+          tmem_ld16(tbase + c0, v);
+          if (f < d.H) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int col = c0 + j;
+              if (col < tl.nj)
+                L.slotbuf[((size_t)slot_s[col] * d.KS + k_s[col]) * d.H + f] = w_s[col] * v[j];
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[buf]);
+      if (GEMM2) land_and_merge<__nv_bfloat16>(L, d, C, slot_s, tl.nj, target, et, 128, fin, EpiBarrier{});
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 2) {
+    __syncwarp();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------ host side
+
+struct TcState {
+  CUtensorMap map13[64];
+  CUtensorMap map2[64];
+};
+
+constexpr int kBN = 64;
+constexpr int kStages = 8;
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 3-D map over packed weights [NB][rows][K] (bf16, K contiguous), box 64 x 128 x 1, 128B swizzle,
+// zero fill outside the tensor (ragged K and ragged row tails).
+bool encode_weights(CUtensorMap* m, const void* base, int K, int rows, int nb) {
+  auto fn = get_encode();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)K, (cuuint64_t)rows, (cuuint64_t)nb};
+  cuuint64_t strides[2] = {(cuuint64_t)K * 2, (cuuint64_t)K * 2 * rows};
+  cuuint32_t box[3] = {kBK, kBM, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int BN, int STAGES, bool GEMM2>
+cudaError_t launch_one(moe_async_s* h, const CUtensorMap& map, int layer, cudaStream_t s) {
+  using SL = SmemLayout<BN, STAGES>;
+  auto kern = ffn_tc_kernel<BN, STAGES, GEMM2>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SL::kAlloc);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int target = h->dims.KS * h->parts_per_pair;
+  kern<<<h->num_sms, kThreads, SL::kAlloc, s>>>(map, h->layers[layer], h->dims, h->counters, h->plan,
+                                                static_cast<__nv_bfloat16*>(h->h), target);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+TileGeom tc_geom() { return TileGeom{kBN, kBM, kBN, kBM}; }
+
+moe_status tc_setup(moe_async_s* h) {
+  if (h->cfg.num_layers > 64) return MOE_ERR_UNSUPPORTED;
+  TcState* st = new (std::nothrow) TcState();
+  if (!st) return MOE_ERR_CUDA;
+  const Dims& d = h->dims;
+  for (int l = 0; l < h->cfg.num_layers; ++l) {
+    if (!encode_weights(&st->map13[l], h->layers[l].w13, d.H, 2 * d.I, d.NB) ||
+        !encode_weights(&st->map2[l], h->layers[l].w2, d.I, d.H, d.NB)) {
+      delete st;
+      return MOE_ERR_CUDA;
+    }
+  }
+  h->tc_state = st;
+  return MOE_OK;
+}
+
+void tc_teardown(moe_async_s* h) {
+  delete static_cast<TcState*>(h->tc_state);
+  h->tc_state = nullptr;
+}
+
+moe_status launch_ffn_tc(moe_async_s* h, int layer, cudaStream_t s) {
+  TcState* st = static_cast<TcState*>(h->tc_state);
+  if (!st) return MOE_ERR_INVALID;
+  prof_begin(h, MOE_KERNEL_FFN1, s);
+  cudaError_t e = launch_one<kBN, kStages, false>(h, st->map13[layer], layer, s);
+  prof_end(h, MOE_KERNEL_FFN1, s);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  prof_begin(h, MOE_KERNEL_FFN2, s);
+  e = launch_one<kBN, kStages, true>(h, st->map2[layer], layer, s);
+  prof_end(h, MOE_KERNEL_FFN2, s);
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
 
 }  // namespace moe

@@ -92,6 +92,11 @@ TEST_CONFIGS = {
     "m3": WorkloadSpec(
         name="m3_f32_ep_rank", layer=LayerSpec(12, 3, 136, 80, "f32"), tokens=96,
         router="normal", waves="ep_rank", num_waves=4, arrival="permute", policy="mtfs"),
+    # profiling-sized slice of the GPT-OSS layer: 32 experts of H = I = 2880 (1.6 GB of
+    # weights, well above L2), 64 decode tokens in 4 waves -- same kernels, same tile shapes.
+    "p1": WorkloadSpec(
+        name="p1_gptoss_slice", layer=GPT_OSS_LAYER.__class__(32, 4, 2880, 2880, "bf16"), tokens=64,
+        router="uniform", waves="even", num_waves=4, arrival="index", policy="mtfs"),
     # bf16 decode-like: many experts, few tokens each.
     "m4": WorkloadSpec(
         name="m4_bf16_decode", layer=LayerSpec(64, 4, 1024, 512, "bf16"), tokens=64,
