@@ -104,10 +104,14 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
-def source_hash():
+KERNEL_SOURCES = ("moe_ffn_tc.cu", "moe_internal.cuh")
+
+
+def source_hash(files=KERNEL_SOURCES):
+    """Hash of the sources the FFN kernels are built from (ncu counters go stale on change)."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "asynchronous_expert_execution_gb300", "csrc")
-    for f in sorted(os.listdir(d)):
+    for f in sorted(files):
         with open(os.path.join(d, f), "rb") as fh:
             h.update(f.encode() + fh.read())
     return h.hexdigest()[:16]
