@@ -219,6 +219,28 @@ moe_status moe_async_profile_read(moe_async_t h, void* stream, double* h_ms, int
 /* Free every device allocation of the handle.  Synchronises `stream` first. */
 moe_status moe_async_destroy(moe_async_t h, void* stream);
 
+/* One routed MoE layer forward that allocates no device memory.  The pages have no
+ * counterpart: this is for callers that cannot call cudaMalloc where they run the layer
+ * (a memory pool owns the device, an allocation-free runtime, a plugin that is handed only
+ * its input and output buffers).
+ *   y[t] = sum_{k=0..K-1, ascending} w[t,k] * E_{expert[t,k]}(x[t]),
+ *   E(x) = (silu(x W1) * (x W3)) W2, fp32 accumulation, no shared expert.
+ *   d_x [T,H], d_y [T,H] in dtype (moe_dtype); d_expert [T,K] int32 in [0,E) (other ids
+ *   contribute nothing); d_w [T,K] fp32; d_w1, d_w3 [E,H,I] and d_w2 [E,I,H] in dtype --
+ *   the caller's own weight layout, no packing.  All device pointers, all caller-owned.
+ * Scratch: a fixed 16 MiB array compiled into the library (held on every GPU that loads
+ * it, until the process exits) holds the T*K*I fp32 SwiGLU activations, so T*K*I*4 bytes
+ * may not exceed 16 MiB: larger calls return MOE_ERR_CAPACITY and launch nothing.  The
+ * first call on a device looks up the array's device address (no allocation); make that
+ * first call before any stream capture.  Every call shares the one array and each call
+ * overwrites every element it reads, so nothing has to be cleared, but calls whose kernels
+ * overlap on the GPU (different streams, or different host threads) race on it: order them.
+ * Calls no cudaMalloc/cudaFree.  Asynchronous on `stream`. */
+moe_status moe_async_forward_noalloc(int32_t T, int32_t E, int32_t K, int32_t H, int32_t I,
+                                     int32_t dtype, const void* d_x, const int32_t* d_expert,
+                                     const float* d_w, const void* d_w1, const void* d_w3,
+                                     const void* d_w2, void* d_y, void* stream);
+
 /* Human-readable name of a status code (static string). */
 const char* moe_async_status_string(moe_status s);
 
