@@ -352,3 +352,122 @@ def rmsnorm(x, eps=1e-6):
 def attention_stub(x, P):
     """Stand-in for the attention stage: RMSNorm(x) @ P."""
     return rmsnorm(x) @ np.asarray(P, dtype=np.float64)
+
+
+def layer_pick(att_depth, exp_depth, allow_attention=True):
+    """MTFS over the 2L micro-queues (StreamEP section 3: one attention queue and one expert
+    queue per layer; section 4: the queue holding the most tokens goes first).
+
+    Depths count tokens (requests) in both kinds of queue.  Equal depth -> lower layer;
+    within a layer the attention queue before the expert queue.  Returns (kind, layer)
+    with kind "att" / "exp", or None when every eligible queue is empty."""
+    cand = []
+    for l, d in enumerate(att_depth):
+        if allow_attention and d > 0:
+            cand.append((-d, l, 0))
+    for l, d in enumerate(exp_depth):
+        if d > 0:
+            cand.append((-d, l, 1))
+    if not cand:
+        return None
+    _, l, kind = min(cand)
+    return ("att" if kind == 0 else "exp", l)
+
+
+@dataclass
+class TickRecord:
+    tick: int
+    kind: str                        # "att", "exp" or "idle"
+    layer: int
+    count: int                       # requests served by the picked queue
+
+
+class StreamOracle:
+    """Streaming multi-layer decode on the 2L micro-queues, tick by tick.
+
+    StreamEP section 3: every request keeps its home (its state lives under its RequestID);
+    a layer's attention queue feeds the attention stage, whose output is routed (top-K) and
+    dispatched to that layer's expert queue; the merged result returns home and enters the
+    next layer's attention queue -- layers advance independently per request, no barrier.
+    Readings: the attention stage is the stub a = RMSNorm(x) P_l; x^(n+1) = MoE_l(a), layer
+    l = n mod L, no residual; router logits of (request, step) and dispatch delays are given
+    (value-independent routing); a dispatch made at tick t arrives at tick t + delay; one
+    queue is served per tick (layer_pick); an expert pick drains all of the layer's buckets;
+    once `stop` merges have completed (checked at the start of a tick) attention queues are
+    no longer served, in-flight work still finishes.
+
+    Per tick: deliver the arrivals due, pick a queue, serve it.  ``values`` = False keeps only
+    the integer bookkeeping; ``compute`` restricts the float chain to some requests.
+    """
+
+    def __init__(self, L, K, x0, proj, logits, delays, experts, stop, max_steps,
+                 values=True, compute=None):
+        self.L, self.K = L, K
+        self.R = len(x0)
+        self.x0 = np.asarray(x0, dtype=np.float64)
+        self.proj, self.logits, self.delays = proj, logits, np.asarray(delays)
+        self.experts = experts            # experts(layer, e) -> (W1, W3, W2)
+        self.stop, self.max_steps = stop, max_steps
+        self.values = values
+        self.compute = set(range(self.R)) if compute is None else set(int(r) for r in compute)
+        self.n = np.zeros(self.R, dtype=np.int64)
+        self.att = [set() for _ in range(L)]
+        self.att[0] = set(range(self.R))
+        self.transit = {}                 # r -> arrival tick
+        self.pending = [set() for _ in range(L)]   # requests whose pairs sit in layer l's queue
+        self.a = {}                       # r -> attention output for its current step
+        self.route = {}                   # r -> (idx, w) for its current step
+        self.x = {r: self.x0[r] for r in self.compute}
+        self.history = {r: [self.x0[r]] for r in self.compute}
+        self.done_tick = {}               # (r, n) -> tick at which step n completed
+        self.combined = 0
+        self.tick = 0
+        self.trace = []
+
+    def busy(self):
+        open_att = self.combined < self.stop and any(self.att)
+        return bool(self.transit) or any(self.pending) or open_att
+
+    def step(self):
+        self.tick += 1
+        for r in sorted(r for r, t in self.transit.items() if t == self.tick):
+            del self.transit[r]
+            self.pending[int(self.n[r]) % self.L].add(r)
+        pick = layer_pick([len(a) for a in self.att], [len(p) for p in self.pending],
+                          allow_attention=self.combined < self.stop)
+        if pick is None:
+            self.trace.append(TickRecord(self.tick, "idle", -1, 0))
+            return
+        kind, l = pick
+        if kind == "att":
+            batch = sorted(self.att[l])
+            self.att[l] = set()
+            for r in batch:
+                n = int(self.n[r])
+                idx, w = route(self.logits(r, n)[None, :], self.K)
+                self.route[r] = (idx[0], w[0])
+                if self.values and r in self.compute:
+                    self.a[r] = attention_stub(self.x[r][None, :], self.proj(l))[0]
+                self.transit[r] = self.tick + int(self.delays[r, n])
+        else:
+            batch = sorted(self.pending[l])
+            self.pending[l] = set()
+            for r in batch:
+                n = int(self.n[r])
+                if self.values and r in self.compute:
+                    idx, w = self.route[r]
+                    contribs = [w[k] * expert_ffn(self.a[r][None, :], *self.experts(l, int(idx[k])))[0]
+                                for k in range(self.K)]
+                    self.x[r] = combine(contribs)
+                    self.history[r].append(self.x[r])
+                self.n[r] = n + 1
+                self.done_tick[(r, n + 1)] = self.tick
+                self.combined += 1
+                if n + 1 < self.max_steps:
+                    self.att[(n + 1) % self.L].add(r)
+        self.trace.append(TickRecord(self.tick, kind, l, len(batch)))
+
+    def run(self, max_ticks=1000000):
+        while self.busy() and self.tick < max_ticks:
+            self.step()
+        return self

@@ -1,0 +1,142 @@
+"""Pins for the streaming multi-layer oracle (2L micro-queues, layer-level MTFS,
+dispatch delays, stop rule) against hand-derived traces, a scalar closed form and
+invariants."""
+import math
+
+import numpy as np
+
+from oracle import moe_oracle as om
+
+
+def _mk(R, L, E, K, H, delays, stop, max_steps, logits=None, experts=None, proj=None, x0=None, values=True):
+    rng = np.random.default_rng(0)
+    if logits is None:
+        tab = rng.uniform(size=(R, max_steps, E))
+        logits = lambda r, n: tab[r, n]
+    if x0 is None:
+        x0 = rng.standard_normal((R, H))
+    if proj is None:
+        Ps = [rng.standard_normal((H, H)) / math.sqrt(H) for _ in range(L)]
+        proj = lambda l: Ps[l]
+    if experts is None:
+        Ws = {(l, e): (rng.standard_normal((H, H)) / math.sqrt(H), rng.standard_normal((H, H)) / math.sqrt(H),
+                       rng.standard_normal((H, H)) / math.sqrt(H)) for l in range(L) for e in range(E)}
+        experts = lambda l, e: Ws[(l, e)]
+    return om.StreamOracle(L, K, x0, proj, logits, delays, experts, stop, max_steps, values=values)
+
+
+def pin_layer_pick():
+    assert om.layer_pick([3, 0], [2, 5]) == ("exp", 1)
+    assert om.layer_pick([5, 0], [2, 5]) == ("att", 0)      # tie: lower layer first
+    assert om.layer_pick([0, 5], [5, 0]) == ("exp", 0)
+    assert om.layer_pick([4, 0], [4, 0]) == ("att", 0)      # tie in a layer: attention first
+    assert om.layer_pick([4, 0], [1, 0], allow_attention=False) == ("exp", 0)
+    assert om.layer_pick([0, 0], [0, 0]) is None
+
+
+def test_layer_pick():
+    pin_layer_pick()
+
+
+def test_stream_trace_hand_equal_delays():
+    delays = np.ones((2, 8), dtype=np.int64)
+    s = _mk(R=2, L=2, E=2, K=1, H=3, delays=delays, stop=3, max_steps=8, values=False).run()
+    got = [(t.tick, t.kind, t.layer, t.count) for t in s.trace]
+    assert got == [(1, "att", 0, 2), (2, "exp", 0, 2), (3, "att", 1, 2), (4, "exp", 1, 2)]
+    assert s.n.tolist() == [2, 2] and s.combined == 4
+    assert s.done_tick == {(0, 1): 2, (1, 1): 2, (0, 2): 4, (1, 2): 4}
+
+
+def test_stream_trace_hand_jitter():
+    # request 1's first dispatch takes 3 ticks: the queues split and the layers interleave
+    delays = np.ones((2, 8), dtype=np.int64)
+    delays[1, 0] = 3
+    s = _mk(R=2, L=2, E=2, K=1, H=3, delays=delays, stop=4, max_steps=8, values=False).run()
+    got = [(t.tick, t.kind, t.layer, t.count) for t in s.trace]
+    # t1: att L0 {0,1} -> 0 arrives t2, 1 arrives t4
+    # t2: exp L0 {0} -> 0 to att L1            t3: att L1 {0} -> arrives t4
+    # t4: both arrive: exp L0 {1} vs exp L1 {0}: tie -> lower layer first
+    # t5: exp L1 {0} (depth 1) vs att L1 {1} (depth 1): same layer, attention first
+    # t6: exp L1 {0} -> 0 done twice (combined 3); t7: att L0 {0} vs ... see asserts
+    assert got[:6] == [(1, "att", 0, 2), (2, "exp", 0, 1), (3, "att", 1, 1), (4, "exp", 0, 1),
+                       (5, "att", 1, 1), (6, "exp", 1, 2)]
+    assert s.combined >= 4 and all(1 <= n <= 8 for n in s.n)
+
+
+def pin_stream_scalar_closed_form():
+    """H = I = 1, K = 1: x1 = w2 * silu(w1 * a) * (w3 * a) with a = p * x0 / sqrt(x0^2 + eps)."""
+    p, w1, w3, w2, x0, eps = 0.7, 1.3, -0.4, 2.1, 0.9, 1e-6
+    s = om.StreamOracle(1, 1, np.array([[x0]]), lambda l: np.array([[p]]), lambda r, n: np.array([0.0]),
+                        np.ones((1, 4), dtype=np.int64),
+                        lambda l, e: (np.array([[w1]]), np.array([[w3]]), np.array([[w2]])), stop=2,
+                        max_steps=4).run()
+    x = x0
+    for _ in range(2):
+        a = p * x / math.sqrt(x * x + eps)
+        g = w1 * a
+        x = w2 * (g / (1.0 + math.exp(-g))) * (w3 * a)
+    assert s.n.tolist() == [2]
+    assert abs(s.history[0][2][0] - x) < 1e-14
+
+
+def test_stream_scalar_closed_form():
+    pin_stream_scalar_closed_form()
+
+
+def test_stream_values_independent_of_delays():
+    R, L, E, K, H, M = 6, 2, 4, 2, 5, 6
+    rng = np.random.default_rng(3)
+    outs = []
+    for seed in range(3):
+        d = np.random.default_rng(seed).integers(1, 5, size=(R, M))
+        s = _mk(R, L, E, K, H, d, stop=20, max_steps=M)
+        s.run()
+        outs.append((s, d))
+    ref = outs[0][0]
+    for s, _ in outs[1:]:
+        for r in range(R):
+            m = min(len(s.history[r]), len(ref.history[r]))
+            for n in range(m):
+                assert np.array_equal(s.history[r][n], ref.history[r][n])
+
+
+def test_stream_conservation_and_stop():
+    R, L, M = 16, 4, 12
+    d = np.random.default_rng(5).integers(1, 6, size=(R, M))
+    s = _mk(R, L, 8, 2, 4, d, stop=70, max_steps=M, values=False).run()
+    assert s.combined == int(s.n.sum())
+    assert 70 <= s.combined < 70 + R
+    assert len(s.done_tick) == s.combined                  # every (r, n) completed once
+    for (r, n), t in s.done_tick.items():
+        if n > 1:
+            assert s.done_tick[(r, n - 1)] < t            # steps of a request in order
+    assert not s.transit and not any(s.pending)
+    # once `stop` merges are done at the start of a tick, no attention queue is served
+    done = 0
+    for t in s.trace:
+        if done >= 70:
+            assert t.kind != "att"
+        if t.kind == "exp":
+            done += t.count
+
+
+def test_stream_pins_catch_planted_mistakes(monkeypatch):
+    real = om.layer_pick
+    monkeypatch.setattr(om, "layer_pick", lambda a, e, allow_attention=True:
+                        real(e, a, allow_attention) and (("att" if real(e, a, allow_attention)[0] == "exp" else "exp"),
+                                                         real(e, a, allow_attention)[1]))
+    try:
+        pin_layer_pick()
+        caught = False
+    except AssertionError:
+        caught = True
+    assert caught
+    monkeypatch.setattr(om, "layer_pick", real)
+    real_rms = om.rmsnorm
+    monkeypatch.setattr(om, "rmsnorm", lambda x, eps=1e-6: np.asarray(x, float) / np.sqrt(np.mean(np.asarray(x, float) ** 2, -1, keepdims=True)))
+    try:
+        pin_stream_scalar_closed_form()
+        caught = False
+    except AssertionError:
+        caught = True
+    assert caught
