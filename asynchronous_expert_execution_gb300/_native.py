@@ -18,7 +18,8 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID", 2: "MOE_ERR_CAPACITY", 3: "MO
 EXPORTS = ("moe_async_create", "moe_async_route", "moe_async_enqueue", "moe_async_schedule_step",
            "moe_async_collect", "moe_async_wait", "moe_async_sync", "moe_async_get_stats",
            "moe_async_get_trace", "moe_async_snapshot", "moe_async_destroy",
-           "moe_async_status_string", "moe_async_profile", "moe_async_profile_read")
+           "moe_async_status_string", "moe_async_profile", "moe_async_profile_read",
+           "moe_async_stream_setup", "moe_async_stream_run", "moe_async_stream_trace")
 
 KERNEL_KINDS = ("enqueue", "schedule", "ffn1", "ffn2", "collect")
 
@@ -41,6 +42,10 @@ class Stats(ctypes.Structure):
                 ("pending_pairs", ctypes.c_int32), ("ready", ctypes.c_int32),
                 ("error", ctypes.c_int32), ("packed_weight_bytes", ctypes.c_int64),
                 ("kernel_launches", ctypes.c_int64)]
+
+
+class StreamConfig(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("num_requests", "max_steps", "stop_combines")]
 
 
 class MoEError(RuntimeError):
@@ -78,6 +83,9 @@ def load():
         "moe_async_profile": [P, I32],
         "moe_async_profile_read": [P, P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64), I32],
         "moe_async_status_string": [ctypes.c_int],
+        "moe_async_stream_setup": [P, ctypes.POINTER(StreamConfig), VPP, P, P, P, P, P, P],
+        "moe_async_stream_run": [P, I32, I32, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32), P],
+        "moe_async_stream_trace": [P, P, ctypes.POINTER(ctypes.c_int32), I32, ctypes.POINTER(ctypes.c_int32)],
     }
     for name, args in sig.items():
         f = getattr(lib, name)

@@ -141,6 +141,32 @@ class MoEAsync:
             o += depths[b]
         return depths, out
 
+    # -- streaming multi-layer decode (2L micro-queues) --------------------------
+    def stream_setup(self, proj, x0, logits, delays, max_steps, stop, history, done_tick, stream=None):
+        """proj: list of L [H, H] device tensors; x0 [R, H]; logits [R, M, E] fp32; delays
+        [R, M] int32; history [R, M+1, H] and done_tick [R, M+1] int32 are outputs."""
+        R = x0.shape[0]
+        arr = ctypes.c_void_p * len(proj)
+        self._stream_keep = (logits, delays, history, done_tick)
+        cfg = N.StreamConfig(R, max_steps, stop)
+        st = self.lib.moe_async_stream_setup(self.h, ctypes.byref(cfg), arr(*[p.data_ptr() for p in proj]),
+                                             _ptr(x0), _ptr(logits), _ptr(delays), _ptr(history),
+                                             _ptr(done_tick), _stream(stream))
+        N.check(st, "moe_async_stream_setup")
+
+    def stream_run(self, max_ticks=100000, check_every=16, stream=None):
+        """Run ticks until the stream is drained; returns (status, ticks, merges)."""
+        t, c = ctypes.c_int32(), ctypes.c_int32()
+        st = self.lib.moe_async_stream_run(self.h, max_ticks, check_every, ctypes.byref(t), ctypes.byref(c),
+                                           _stream(stream))
+        return st, t.value, c.value
+
+    def stream_trace(self, cap=1 << 18, stream=None):
+        buf = (ctypes.c_int32 * (4 * cap))()
+        n = ctypes.c_int32()
+        N.check(self.lib.moe_async_stream_trace(self.h, _stream(stream), buf, cap, ctypes.byref(n)), "stream_trace")
+        return np.frombuffer(buf, dtype=np.int32, count=4 * n.value).reshape(n.value, 4).copy()
+
     def profile(self, enable=True):
         """Bracket every later kernel launch with CUDA events (per-kernel timing)."""
         N.check(self.lib.moe_async_profile(self.h, int(enable)), "moe_async_profile")

@@ -49,51 +49,24 @@ cudaError_t pack_one(const void* in, void* out, int nexp, int C, int R, int out_
   return cudaGetLastError();
 }
 
+}  // namespace
+
+namespace moe {
+cudaError_t pack_transpose_bf16(const void* in, void* out, int C, int R, cudaStream_t s) {
+  return pack_one<__nv_bfloat16>(in, out, 1, C, R, R, 0, 0, s);
+}
+}  // namespace moe
+
+namespace {
+
 // ----------------------------------------------------------------- router
-// One warp per token.  Top-K by (logit desc, index asc), then w_k = exp(z_k - m) /
-// sum_j exp(z_j - m) over the selected set, m = the largest selected logit: this equals
-// softmax over all E renormalised over the top K, because the full denominator cancels.
+// One warp per token (warp_topk): top-K by (logit desc, index asc), renormalised softmax.
 __global__ void route_kernel(const float* __restrict__ logits, int T, int E, int K,
                              int32_t* __restrict__ idx, float* __restrict__ wout) {
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= T) return;
-  float v[32];
-  const int per = (E + 31) / 32;
-  for (int i = 0; i < 32; ++i) {
-    int e = lane + 32 * i;
-    v[i] = (i < per && e < E) ? logits[(size_t)t * E + e] : -INFINITY;
-  }
-  uint32_t taken = 0;
-  float selv[32];
-  int seli[32];
-  for (int k = 0; k < K; ++k) {
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
-    for (int i = 0; i < per; ++i) {
-      int e = lane + 32 * i;
-      if (e < E && !(taken >> i & 1u)) {
-        if (bi == 0x7fffffff || v[i] > bv || (v[i] == bv && e < bi)) { bv = v[i]; bi = e; }
-      }
-    }
-    for (int off = 16; off > 0; off >>= 1) {
-      float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-      int oi = __shfl_xor_sync(0xffffffffu, bi, off);
-      if (oi != 0x7fffffff && (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi))) { bv = ov; bi = oi; }
-    }
-    if ((bi & 31) == lane && bi != 0x7fffffff) taken |= 1u << (bi >> 5);
-    selv[k] = bv;
-    seli[k] = bi;
-  }
-  if (lane == 0) {
-    const float m = selv[0];
-    float den = 0.f;
-    for (int k = 0; k < K; ++k) den += expf(selv[k] - m);
-    for (int k = 0; k < K; ++k) {
-      idx[(size_t)t * K + k] = seli[k];
-      wout[(size_t)t * K + k] = expf(selv[k] - m) / den;
-    }
-  }
+  warp_topk(logits + (size_t)t * E, E, K, lane, idx + (size_t)t * K, wout + (size_t)t * K);
 }
 
 // --------------------------------------------------------------- Receptor
@@ -179,104 +152,12 @@ __global__ void enqueue_kernel(LayerView L, Dims d, DevCounters* C, int n,
 }
 
 // -------------------------------------------------------------- scheduler
-// One CTA.  Reads every bucket depth of the layer, applies the policy, drains the picked
-// buckets whole (head += depth) and writes the work list the FFN kernels consume.
-// MTFS (StreamEP section 4): deepest first, equal depth -> lower bucket id.  THRESHOLD
-// (streamFFN reading): buckets with depth >= min_batch, deepest first; if none, MTFS over
-// non-empty buckets limited to fallback_groups.
 __global__ void __launch_bounds__(1024) schedule_kernel(LayerView L, Dims d, StepPlan* P,
                                                         DevCounters* C, moe_async_policy pol,
                                                         TileGeom g, int layer, int trace_cap,
                                                         int4* trace, long long weight_bytes_per_run) {
-  __shared__ int depth[kMaxBuckets];
-  __shared__ int order[kMaxBuckets];
-  __shared__ int n_elig, n_nonempty;
-  const int tid = threadIdx.x, nt = blockDim.x;
-  if (tid == 0) { n_elig = 0; n_nonempty = 0; }
-  __syncthreads();
-  for (int b = tid; b < d.NB; b += nt) {
-    const int dep = min((int)(L.tail[b] - L.head[b]), d.cap);
-    depth[b] = dep;
-    if (dep > 0) atomicAdd(&n_nonempty, 1);
-    if (dep > 0 && (pol.kind != MOE_POLICY_THRESHOLD || dep >= pol.min_batch)) atomicAdd(&n_elig, 1);
-  }
-  __syncthreads();
-  int minb = 1, G = pol.max_groups;
-  if (pol.kind == MOE_POLICY_THRESHOLD) {
-    if (n_elig > 0) minb = pol.min_batch > 1 ? pol.min_batch : 1;
-    else G = pol.fallback_groups > 0 ? pol.fallback_groups : 1;
-  }
-  const int ne = (pol.kind == MOE_POLICY_THRESHOLD && n_elig == 0) ? n_nonempty : n_elig;
-  // After an overflow or an out-of-range id the queues no longer describe valid pairs:
-  // stop executing (the sticky error is reported to the host).
-  const uint32_t err = *(volatile uint32_t*)&C->error;
-  const bool halted = err == MOE_ERR_CAPACITY || err == MOE_ERR_INVALID;
-  const int n = halted ? 0 : ((G > 0 && G < ne) ? G : ne);
-  for (int b = tid; b < d.NB; b += nt) {
-    const int db = depth[b];
-    if (db >= minb) {
-      int r = 0;
-      for (int c = 0; c < d.NB; ++c) {
-        const int dc = depth[c];
-        r += (dc >= minb) && (dc > db || (dc == db && c < b));
-      }
-      if (r < n) order[r] = b;
-    }
-  }
-  __syncthreads();
-  if (tid < 32) {
-    const int lane = tid;
-    int row_run = 0, t1_run = 0, t2_run = 0;
-    const int ft1 = (2 * d.I + g.bm1 - 1) / g.bm1;
-    const int ft2 = (d.H + g.bm2 - 1) / g.bm2;
-    for (int c0 = 0; c0 < n; c0 += 32) {
-      const int r = c0 + lane;
-      int b = 0, cnt = 0, t1 = 0, t2 = 0;
-      if (r < n) {
-        b = order[r];
-        cnt = depth[b];
-        t1 = ((cnt + g.bn1 - 1) / g.bn1) * ft1;
-        t2 = ((cnt + g.bn2 - 1) / g.bn2) * ft2;
-      }
-      int s_cnt = cnt, s_t1 = t1, s_t2 = t2;      // inclusive prefix sums within the chunk
-      for (int off = 1; off < 32; off <<= 1) {
-        int a = __shfl_up_sync(0xffffffffu, s_cnt, off);
-        int b1 = __shfl_up_sync(0xffffffffu, s_t1, off);
-        int b2 = __shfl_up_sync(0xffffffffu, s_t2, off);
-        if (lane >= off) { s_cnt += a; s_t1 += b1; s_t2 += b2; }
-      }
-      if (r < n) {
-        WorkItem it;
-        it.expert = b;
-        it.head = L.head[b];
-        it.count = cnt;
-        it.row_base = row_run + s_cnt - cnt;
-        it.t1_base = t1_run + s_t1 - t1;
-        it.t2_base = t2_run + s_t2 - t2;
-        P->items[r] = it;
-        L.head[b] = it.head + (uint32_t)cnt;
-        if (trace && trace_cap > 0) {
-          const int ti = atomicAdd(&C->trace_n, 1);
-          if (ti < trace_cap) trace[ti] = make_int4((int)C->steps + 1, layer, b, cnt);
-        }
-      }
-      row_run += __shfl_sync(0xffffffffu, s_cnt, 31);
-      t1_run += __shfl_sync(0xffffffffu, s_t1, 31);
-      t2_run += __shfl_sync(0xffffffffu, s_t2, 31);
-    }
-    if (lane == 0) {
-      P->layer = layer;
-      P->n_work = n;
-      P->n_tiles1 = t1_run;
-      P->n_tiles2 = t2_run;
-      P->rows = row_run;
-      C->steps += 1ull;
-      C->pairs_executed += (unsigned long long)row_run;
-      C->expert_runs += (unsigned long long)n;
-      C->weight_bytes += (unsigned long long)n * (unsigned long long)weight_bytes_per_run;
-      C->pending_pairs -= row_run;
-    }
-  }
+  __shared__ PlanScratch sc;
+  plan_layer(L, d, P, C, pol, g, layer, trace_cap, trace, weight_bytes_per_run, (int)C->steps + 1, true, sc);
 }
 
 // ---------------------------------------------------------------- collect
@@ -330,6 +211,7 @@ void prof_free(moe_async_s* h);
 void free_handle(moe_async_s* h) {
   if (!h) return;
   prof_free(h);
+  if (h->stream_state) stream_teardown(h);
   if (h->tc_state) tc_teardown(h);
   if (h->layers) {
     for (int l = 0; l < h->cfg.num_layers; ++l) {

@@ -21,6 +21,7 @@
 // CTA still frees its TMEM before exiting.
 #include <cuda.h>
 #include <cudaTypedefs.h>
+#include <cstring>
 #include <new>
 #include "moe_internal.cuh"
 
@@ -198,6 +199,22 @@ __device__ __forceinline__ uint32_t idesc_bf16(int M, int N) {
 
 // ----------------------------------------------------------------- tile decoding
 
+enum : int { kModeGemm1 = 0, kModeGemm2 = 1, kModeAtt = 2 };
+
+// Everything a launch needs, for every layer: the layer a tile belongs to is read on the
+// device (the step plan, or the streaming runtime's pick), so one launch serves any layer.
+struct TcParams {
+  CUtensorMap mapA[kMaxLayers];     // GEMM1: packed W13, GEMM2: packed W2^T, ATT: packed P^T
+  LayerView views[kMaxLayers];
+  Dims d;
+  DevCounters* C;
+  const StepPlan* P;
+  __nv_bfloat16* hbuf;
+  int target;                       // landing target per token (GEMM2)
+  int stream_on;                    // GEMM2 merges feed the streaming runtime
+  StreamDev sd;
+};
+
 struct Tile {
   int expert;
   uint32_t head;
@@ -208,18 +225,29 @@ struct Tile {
   int nmma;     // MMA N (multiple of 16, >= nj)
 };
 
-template <int BN>
-__device__ __forceinline__ Tile decode_tile(const StepPlan* P, int t, bool second) {
-  const WorkItem it = P->items[find_item(P, t, second)];
-  const int local = t - (second ? it.t2_base : it.t1_base);
-  const int ntt = (it.count + BN - 1) / BN;
+template <int BN, int MODE>
+__device__ __forceinline__ Tile decode_tile(const TcParams& p, int t) {
   Tile tl;
-  tl.expert = it.expert;
-  tl.head = it.head;
-  tl.row_base = it.row_base;
+  int local, count;
+  if (MODE == kModeAtt) {
+    count = p.sd.ctl->att_count;
+    local = t;
+    tl.expert = 0;
+    tl.head = 0;
+    tl.row_base = 0;
+  } else {
+    const StepPlan* P = p.P;
+    const WorkItem it = P->items[find_item(P, t, MODE == kModeGemm2)];
+    local = t - (MODE == kModeGemm2 ? it.t2_base : it.t1_base);
+    count = it.count;
+    tl.expert = it.expert;
+    tl.head = it.head;
+    tl.row_base = it.row_base;
+  }
+  const int ntt = (count + BN - 1) / BN;
   tl.fti = local / ntt;
   tl.j0 = (local % ntt) * BN;
-  tl.nj = min(BN, it.count - tl.j0);
+  tl.nj = min(BN, count - tl.j0);
   tl.nmma = min(BN, max(16, (tl.nj + 15) & ~15));
   return tl;
 }
@@ -245,10 +273,8 @@ struct SmemLayout {
 
 // ------------------------------------------------------------------ the kernel
 
-template <int BN, int STAGES, bool GEMM2>
-__global__ void __launch_bounds__(kThreads, 1)
-ffn_tc_kernel(const __grid_constant__ CUtensorMap tmA, LayerView L, Dims d, DevCounters* C,
-              const StepPlan* __restrict__ P, __nv_bfloat16* __restrict__ hbuf, int target) {
+template <int BN, int STAGES, int MODE>
+__global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_constant__ TcParams p) {
   using SL = SmemLayout<BN, STAGES>;
   constexpr int kLag = STAGES - 2;            // cp.async groups kept in flight by the B producer
   constexpr uint32_t kTmemCols = 2 * BN;      // two accumulator buffers
@@ -267,9 +293,22 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap tmA, LayerView L, Dims d, DevC
   int* fin = reinterpret_cast<int*>(smem + SL::kOffFin);
   float* w_s = reinterpret_cast<float*>(smem + SL::kOffW);
 
+  const Dims& d = p.d;
+  DevCounters* C = p.C;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_tiles = GEMM2 ? P->n_tiles2 : P->n_tiles1;
-  const int Kdim = GEMM2 ? d.I : d.H;
+  int n_tiles, layer;
+  if (MODE == kModeAtt) {
+    const bool picked = p.sd.ctl->pick_kind == 1;
+    n_tiles = picked ? p.sd.ctl->att_tiles : 0;
+    layer = picked ? p.sd.ctl->pick_layer : 0;
+  } else {
+    n_tiles = MODE == kModeGemm2 ? p.P->n_tiles2 : p.P->n_tiles1;
+    layer = p.P->layer;
+  }
+  if (layer < 0 || layer >= kMaxLayers) n_tiles = 0;
+  const LayerView& L = p.views[layer < 0 || layer >= kMaxLayers ? 0 : layer];
+  const CUtensorMap* tmA = &p.mapA[layer < 0 || layer >= kMaxLayers ? 0 : layer];
+  const int Kdim = MODE == kModeGemm2 ? d.I : d.H;
   const int nk = (Kdim + kBK - 1) / kBK;
 
   if (threadIdx.x == 0) {
@@ -300,13 +339,13 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap tmA, LayerView L, Dims d, DevC
       uint32_t it = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
-        const Tile tl = decode_tile<BN>(P, t, GEMM2);
+        const Tile tl = decode_tile<BN, MODE>(p, t);
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1u;
           if (!(ok = mbar_wait(&empty[s], ph ^ 1u, abort_flag, C))) break;
           mbar_arrive_expect_tx(&full[s], SL::kA);
-          tma_load_3d(smem_u32(smem + SL::kOffA + s * SL::kA), &tmA, &full[s], kb * kBK, tl.fti * kBM,
+          tma_load_3d(smem_u32(smem + SL::kOffA + s * SL::kA), tmA, &full[s], kb * kBK, tl.fti * kBM,
                       tl.expert, pol);
         }
       }
@@ -318,19 +357,21 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap tmA, LayerView L, Dims d, DevC
     int issued = 0, signaled = 0;            // stages issued / signalled by this warp
     bool ok = true;
     for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
-      const Tile tl = decode_tile<BN>(P, t, GEMM2);
+      const Tile tl = decode_tile<BN, MODE>(p, t);
       __syncwarp();
       for (int r = lane; r < tl.nmma; r += 32) {
-        const __nv_bfloat16* p = nullptr;
+        const __nv_bfloat16* rp = nullptr;
         if (r < tl.nj) {
-          if (GEMM2) {
-            p = hbuf + (size_t)(tl.row_base + tl.j0 + r) * d.I;
+          if (MODE == kModeGemm2) {
+            rp = p.hbuf + (size_t)(tl.row_base + tl.j0 + r) * d.I;
+          } else if (MODE == kModeAtt) {
+            rp = static_cast<const __nv_bfloat16*>(p.sd.att_rowptr[tl.j0 + r]);
           } else {
             const int rec = record_at(L, d, tl.expert, tl.head + tl.j0 + r);
-            p = reinterpret_cast<const __nv_bfloat16*>(pool) + (size_t)(rec >> kKShift) * d.H;
+            rp = reinterpret_cast<const __nv_bfloat16*>(pool) + (size_t)(rec >> kKShift) * d.H;
           }
         }
-        rowptr[r] = p;
+        rowptr[r] = rp;
       }
       __syncwarp();
       for (int kb = 0; kb < nk; ++kb, ++it) {
@@ -370,7 +411,7 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap tmA, LayerView L, Dims d, DevC
       uint32_t it = 0, tile_i = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x, ++tile_i) {
-        const Tile tl = decode_tile<BN>(P, t, GEMM2);
+        const Tile tl = decode_tile<BN, MODE>(p, t);
         const int buf = tile_i & 1;
         const uint32_t tph = (tile_i >> 1) & 1u;
         if (!(ok = mbar_wait(&tempty[buf], tph ^ 1u, abort_flag, C))) break;
@@ -398,10 +439,10 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap tmA, LayerView L, Dims d, DevC
     const int et = threadIdx.x - 128;             // 0..127
     uint32_t tile_i = 0;
     for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++tile_i) {
-      const Tile tl = decode_tile<BN>(P, t, GEMM2);
+      const Tile tl = decode_tile<BN, MODE>(p, t);
       const int buf = tile_i & 1;
       const uint32_t tph = (tile_i >> 1) & 1u;
-      if (GEMM2) {
+      if (MODE == kModeGemm2) {
         for (int j = et; j < tl.nj; j += 128) {
           const int rec = record_at(L, d, tl.expert, tl.head + tl.j0 + j);
           const int sl = rec >> kKShift, kk = rec & kKMask;
@@ -409,12 +450,17 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap tmA, LayerView L, Dims d, DevC
           k_s[j] = kk;
           w_s[j] = L.wtab[(size_t)sl * d.KS + kk];
         }
+      } else if (MODE == kModeAtt) {
+        for (int j = et; j < tl.nj; j += 128) {
+          slot_s[j] = p.sd.att_batch[tl.j0 + j];
+          w_s[j] = p.sd.att_scale[tl.j0 + j];
+        }
       }
       const bool w_ok = mbar_wait(&tfull[buf], tph, abort_flag, C);
       if (!epi_bar_and(w_ok)) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN);
-      if (!GEMM2) {
+      if (MODE == kModeGemm1) {
         const int f = tl.fti * (kBM / 2) + 16 * q + (lane & 15);       // feature of this lane pair
         const bool lo = lane < 16;
         for (int c0 = 0; c0 < tl.nj; c0 += 16) {
@@ -428,10 +474,10 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap tmA, LayerView L, Dims d, DevC
             const float g = lo ? v[j] : recv;
             const float u = lo ? recv : v[8 + j];
             if (col < tl.nj && f < d.I)
-              hbuf[(size_t)(tl.row_base + tl.j0 + col) * d.I + f] = __float2bfloat16_rn(silu_f(g) * u);
+              p.hbuf[(size_t)(tl.row_base + tl.j0 + col) * d.I + f] = __float2bfloat16_rn(silu_f(g) * u);
           }
         }
-      } else {
+      } else if (MODE == kModeGemm2) {
         const int f = tl.fti * kBM + 32 * q + lane;                     // output feature of H
         for (int c0 = 0; c0 < tl.nj; c0 += 16) {
           float v[16];
@@ -445,11 +491,30 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap tmA, LayerView L, Dims d, DevC
             }
           }
         }
+      } else {
+        // attention stub: a = RMSNorm(x) P = s * (x P), written to the token pool of the layer
+        const int f = tl.fti * kBM + 32 * q + lane;
+        __nv_bfloat16* pool = static_cast<__nv_bfloat16*>(L.pool);
+        for (int c0 = 0; c0 < tl.nj; c0 += 16) {
+          float v[16];
+          tmem_ld16(tbase + c0, v);
+          if (f < d.H) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const int col = c0 + j;
+              if (col < tl.nj) pool[(size_t)slot_s[col] * d.H + f] = __float2bfloat16_rn(w_s[col] * v[j]);
+            }
+          }
+        }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[buf]);
-      if (GEMM2) land_and_merge<__nv_bfloat16>(L, d, C, slot_s, tl.nj, target, et, 128, fin, EpiBarrier{});
+      if (MODE == kModeGemm2)
+        land_and_merge<__nv_bfloat16>(L, d, C, slot_s, tl.nj, p.target, et, 128, fin, EpiBarrier{},
+                                      p.stream_on ? &p.sd : nullptr, layer);
+      else if (MODE == kModeAtt)
+        asm volatile("bar.sync 1, 128;" ::: "memory");   // slot_s / w_s reused by the next tile
     }
   }
 
@@ -465,8 +530,8 @@ ffn_tc_kernel(const __grid_constant__ CUtensorMap tmA, LayerView L, Dims d, DevC
 // ------------------------------------------------------------------ host side
 
 struct TcState {
-  CUtensorMap map13[64];
-  CUtensorMap map2[64];
+  TcParams gemm1, gemm2, att;       // parameter blocks (tensor maps of every layer)
+  bool att_ready;
 };
 
 constexpr int kBN = 64;
@@ -500,20 +565,28 @@ bool encode_weights(CUtensorMap* m, const void* base, int K, int rows, int nb) {
   return r == CUDA_SUCCESS;
 }
 
-template <int BN, int STAGES, bool GEMM2>
-cudaError_t launch_one(moe_async_s* h, const CUtensorMap& map, int layer, cudaStream_t s) {
+template <int BN, int STAGES, int MODE>
+cudaError_t set_attrs() {
   using SL = SmemLayout<BN, STAGES>;
-  auto kern = ffn_tc_kernel<BN, STAGES, GEMM2>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SL::kAlloc);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-  const int target = h->dims.KS * h->parts_per_pair;
-  kern<<<h->num_sms, kThreads, SL::kAlloc, s>>>(map, h->layers[layer], h->dims, h->counters, h->plan,
-                                                static_cast<__nv_bfloat16*>(h->h), target);
+  return cudaFuncSetAttribute(ffn_tc_kernel<BN, STAGES, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              SL::kAlloc);
+}
+
+template <int BN, int STAGES, int MODE>
+cudaError_t launch_one(moe_async_s* h, const TcParams& prm, cudaStream_t s) {
+  using SL = SmemLayout<BN, STAGES>;
+  ffn_tc_kernel<BN, STAGES, MODE><<<h->num_sms, kThreads, SL::kAlloc, s>>>(prm);
   return cudaGetLastError();
+}
+
+void fill_common(moe_async_s* h, TcParams& p) {
+  for (int l = 0; l < h->cfg.num_layers; ++l) p.views[l] = h->layers[l];
+  p.d = h->dims;
+  p.C = h->counters;
+  p.P = h->plan;
+  p.hbuf = static_cast<__nv_bfloat16*>(h->h);
+  p.target = h->dims.KS * h->parts_per_pair;
+  p.stream_on = 0;
 }
 
 }  // namespace
@@ -521,13 +594,20 @@ cudaError_t launch_one(moe_async_s* h, const CUtensorMap& map, int layer, cudaSt
 TileGeom tc_geom() { return TileGeom{kBN, kBM, kBN, kBM}; }
 
 moe_status tc_setup(moe_async_s* h) {
-  if (h->cfg.num_layers > 64) return MOE_ERR_UNSUPPORTED;
+  if (h->cfg.num_layers > kMaxLayers) return MOE_ERR_UNSUPPORTED;
+  // dynamic shared memory limits, set once per handle outside any stream capture
+  if (set_attrs<kBN, kStages, kModeGemm1>() != cudaSuccess || set_attrs<kBN, kStages, kModeGemm2>() != cudaSuccess ||
+      set_attrs<kBN, kStages, kModeAtt>() != cudaSuccess)
+    return MOE_ERR_CUDA;
   TcState* st = new (std::nothrow) TcState();
   if (!st) return MOE_ERR_CUDA;
+  std::memset(static_cast<void*>(st), 0, sizeof(TcState));
   const Dims& d = h->dims;
+  fill_common(h, st->gemm1);
+  fill_common(h, st->gemm2);
   for (int l = 0; l < h->cfg.num_layers; ++l) {
-    if (!encode_weights(&st->map13[l], h->layers[l].w13, d.H, 2 * d.I, d.NB) ||
-        !encode_weights(&st->map2[l], h->layers[l].w2, d.I, d.H, d.NB)) {
+    if (!encode_weights(&st->gemm1.mapA[l], h->layers[l].w13, d.H, 2 * d.I, d.NB) ||
+        !encode_weights(&st->gemm2.mapA[l], h->layers[l].w2, d.I, d.H, d.NB)) {
       delete st;
       return MOE_ERR_CUDA;
     }
@@ -542,16 +622,39 @@ void tc_teardown(moe_async_s* h) {
 }
 
 moe_status launch_ffn_tc(moe_async_s* h, int layer, cudaStream_t s) {
+  (void)layer;                                     // the plan carries the layer
   TcState* st = static_cast<TcState*>(h->tc_state);
   if (!st) return MOE_ERR_INVALID;
   prof_begin(h, MOE_KERNEL_FFN1, s);
-  cudaError_t e = launch_one<kBN, kStages, false>(h, st->map13[layer], layer, s);
+  cudaError_t e = launch_one<kBN, kStages, kModeGemm1>(h, st->gemm1, s);
   prof_end(h, MOE_KERNEL_FFN1, s);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   prof_begin(h, MOE_KERNEL_FFN2, s);
-  e = launch_one<kBN, kStages, true>(h, st->map2[layer], layer, s);
+  e = launch_one<kBN, kStages, kModeGemm2>(h, st->gemm2, s);
   prof_end(h, MOE_KERNEL_FFN2, s);
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// Streaming runtime: attach the attention-stub projections (packed P^T per layer) and the
+// stream state; GEMM2 merges then feed the streaming runtime.
+moe_status tc_stream_setup(moe_async_s* h, const void* const* proj_packed, const StreamDev& sd) {
+  TcState* st = static_cast<TcState*>(h->tc_state);
+  if (!st) return MOE_ERR_UNSUPPORTED;
+  fill_common(h, st->att);
+  for (int l = 0; l < h->cfg.num_layers; ++l)
+    if (!encode_weights(&st->att.mapA[l], proj_packed[l], h->dims.H, h->dims.H, 1)) return MOE_ERR_CUDA;
+  st->att.sd = sd;
+  st->att.stream_on = 1;
+  st->gemm2.sd = sd;
+  st->gemm2.stream_on = 1;
+  st->att_ready = true;
+  return MOE_OK;
+}
+
+moe_status launch_att_tc(moe_async_s* h, cudaStream_t s) {
+  TcState* st = static_cast<TcState*>(h->tc_state);
+  if (!st || !st->att_ready) return MOE_ERR_INVALID;
+  return launch_one<kBN, kStages, kModeAtt>(h, st->att, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 }  // namespace moe

@@ -85,6 +85,49 @@ struct Dims {
   int32_t expert_kind;
 };
 
+constexpr int kMaxLayers = 8;
+
+// Control block of the streaming multi-layer runtime (one per handle, device memory).
+struct StreamCtl {
+  int32_t tick;                     // logical clock (one scheduling decision per tick)
+  int32_t combined;                 // merges completed (token-layer steps)
+  int32_t pick_kind;                // 0 none, 1 attention queue, 2 expert queue
+  int32_t pick_layer;
+  int32_t att_count;                // requests in the current attention batch
+  int32_t att_tiles;                // projection GEMM tiles of that batch
+  int32_t in_transit;               // dispatched requests whose pairs have not arrived
+  int32_t done;                     // 1 once nothing is left to do
+  int32_t exp_tokens[kMaxLayers];   // tokens whose pairs wait in layer l's expert queue
+  int32_t pad[4];
+};
+
+// Device pointers of the streaming runtime, passed by value to its kernels.
+//   req_n[r]            completed layer-steps of request r (its state is x^(req_n))
+//   arr_tick[r]         tick at which r's dispatched pairs arrive (-1: none in transit)
+//   att_ring[l][R] + att_ht[l][2]   attention queue of layer l (ring of request ids)
+//   route_idx/route_w   [R][K] routing of r's current step
+//   logits [R][n_max][E], delay [R][n_max]   per-(request, step) inputs
+//   hist [R][n_max+1][H]   x^(n) of every request; hist[r][0] = x^(0)
+//   done_tick [R][n_max+1] tick at which step n completed
+//   att_batch / att_scale / att_rowptr [R]   the current attention batch
+struct StreamDev {
+  StreamCtl* ctl;
+  int32_t R, n_max, stop, L;
+  int32_t* req_n;
+  int32_t* arr_tick;
+  int32_t* att_ring;
+  uint32_t* att_ht;
+  int32_t* route_idx;
+  float* route_w;
+  const float* logits;
+  const int32_t* delay;
+  void* hist;
+  int32_t* done_tick;
+  int32_t* att_batch;
+  float* att_scale;
+  const void** att_rowptr;
+};
+
 // Tile geometry of the FFN kernels in use; the scheduler counts tiles with it and the
 // merge target is KS * parts_per_pair (GEMM2 tiles covering H for one token).
 struct TileGeom {
@@ -114,6 +157,7 @@ struct moe_async_s {
   int64_t launches;                 // kernels launched (host count)
   void* tc_state;                   // tensor maps etc. of the tcgen05 path (device)
   void* prof;                       // per-launch CUDA event pairs while profiling
+  void* stream_state;               // streaming multi-layer runtime (moe_async_stream_*)
 };
 
 namespace moe {
@@ -145,6 +189,50 @@ __device__ __forceinline__ int find_item(const StepPlan* p, int t, bool second) 
   return lo;
 }
 
+// Top-K of one row of E <= 1024 logits by one warp: (logit desc, index asc); then
+// w_k = exp(z_k - m) / sum_{j in top K} exp(z_j - m) with m the largest kept logit, which
+// equals softmax over all E renormalised over the top K (the full denominator cancels).
+// Lane 0 writes idx[0..K) and w[0..K).
+__device__ inline void warp_topk(const float* __restrict__ row, int E, int K, int lane,
+                                 int32_t* __restrict__ idx, float* __restrict__ wout) {
+  float v[32];
+  const int per = (E + 31) / 32;
+  for (int i = 0; i < 32; ++i) {
+    const int e = lane + 32 * i;
+    v[i] = (i < per && e < E) ? row[e] : -INFINITY;
+  }
+  uint32_t taken = 0;
+  float selv[32];
+  int seli[32];
+  for (int k = 0; k < K; ++k) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+    for (int i = 0; i < per; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && !(taken >> i & 1u)) {
+        if (bi == 0x7fffffff || v[i] > bv || (v[i] == bv && e < bi)) { bv = v[i]; bi = e; }
+      }
+    }
+    for (int off = 16; off > 0; off >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+      if (oi != 0x7fffffff && (bi == 0x7fffffff || ov > bv || (ov == bv && oi < bi))) { bv = ov; bi = oi; }
+    }
+    if ((bi & 31) == lane && bi != 0x7fffffff) taken |= 1u << (bi >> 5);
+    selv[k] = bv;
+    seli[k] = bi;
+  }
+  if (lane == 0) {
+    const float m = selv[0];
+    float den = 0.f;
+    for (int k = 0; k < K; ++k) den += expf(selv[k] - m);
+    for (int k = 0; k < K; ++k) {
+      idx[k] = seli[k];
+      wout[k] = expf(selv[k] - m) / den;
+    }
+  }
+}
+
 __device__ __forceinline__ int32_t record_at(const LayerView& L, const Dims& d, int e, uint32_t pos) {
   return L.records[(size_t)e * d.cap + (pos % (uint32_t)d.cap)];
 }
@@ -156,7 +244,7 @@ __device__ __forceinline__ int32_t record_at(const LayerView& L, const Dims& d, 
 // barrier) before.  Reads of other CTAs' slot rows go through L2 (ld.global.cg).
 template <typename T>
 __device__ void merge_token(const LayerView& L, const Dims& d, DevCounters* C, int slot,
-                            int tid, int nthr) {
+                            int tid, int nthr, T* dst2 = nullptr) {
   const float* src = L.slotbuf + (size_t)slot * d.KS * d.H;
   T* dst = reinterpret_cast<T*>(L.y) + (size_t)slot * d.H;
   for (int f = tid * 4; f < d.H; f += nthr * 4) {     // H % 8 == 0
@@ -165,10 +253,30 @@ __device__ void merge_token(const LayerView& L, const Dims& d, DevCounters* C, i
       float4 v = __ldcg(reinterpret_cast<const float4*>(src + (size_t)k * d.H + f));
       acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
     }
-    dst[f + 0] = from_f<T>(acc.x);
-    dst[f + 1] = from_f<T>(acc.y);
-    dst[f + 2] = from_f<T>(acc.z);
-    dst[f + 3] = from_f<T>(acc.w);
+    const T o0 = from_f<T>(acc.x), o1 = from_f<T>(acc.y), o2 = from_f<T>(acc.z), o3 = from_f<T>(acc.w);
+    dst[f + 0] = o0; dst[f + 1] = o1; dst[f + 2] = o2; dst[f + 3] = o3;
+    if (dst2) { dst2[f + 0] = o0; dst2[f + 1] = o1; dst2[f + 2] = o2; dst2[f + 3] = o3; }
+  }
+}
+
+// Streaming runtime: request r finished its step at `layer` (its merged output is already in
+// hist[r][n+1]).  Advance its step count, record the tick, reclaim its slot in this layer,
+// and queue it for the next layer's attention stage unless it reached its last step.
+__device__ __forceinline__ void stream_complete(const LayerView& L, DevCounters* C, const StreamDev& sd,
+                                                int layer, int r) {
+  const int n = sd.req_n[r] + 1;
+  sd.req_n[r] = n;
+  sd.done_tick[(size_t)r * (sd.n_max + 1) + n] = sd.ctl->tick;
+  L.enq_mask[r] = 0u;
+  L.done[r] = 0u;
+  L.gen[r] = L.gen[r] + 1u;
+  atomicAdd(&sd.ctl->combined, 1);
+  atomicSub(&C->open_tokens, 1);
+  atomicAdd(&C->tokens_combined, 1ull);
+  if (n < sd.n_max) {
+    const int l2 = (layer + 1) % sd.L;
+    const uint32_t pos = atomicAdd(&sd.att_ht[2 * l2 + 1], 1u);
+    sd.att_ring[(size_t)l2 * sd.R + (pos % (uint32_t)sd.R)] = r;
   }
 }
 
@@ -179,6 +287,114 @@ __device__ __forceinline__ void publish_ready(const LayerView& L, const Dims& d,
   atomicAdd(&C->ready, 1);
   atomicSub(&C->open_tokens, 1);
   atomicAdd(&C->tokens_combined, 1ull);
+}
+
+// One CTA (blockDim multiple of 32, >= 32).  Reads every bucket depth of the layer,
+// applies the policy, drains the picked buckets whole (head += depth) and writes the work
+// list the FFN kernels consume.  MTFS (StreamEP section 4): deepest first, equal depth ->
+// lower bucket id.  THRESHOLD (streamFFN reading): buckets with depth >= min_batch, deepest
+// first; if none, MTFS over non-empty buckets limited to fallback_groups.  With
+// enabled = false the plan is written empty and nothing is drained or counted.
+struct PlanScratch {
+  int depth[kMaxBuckets];
+  int order[kMaxBuckets];
+  int n_elig, n_nonempty;
+};
+
+__device__ inline void plan_layer(const LayerView& L, const Dims& d, StepPlan* P, DevCounters* C,
+                                  const moe_async_policy& pol, const TileGeom& g, int layer,
+                                  int trace_cap, int4* trace, long long weight_bytes_per_run,
+                                  int trace_step, bool enabled, PlanScratch& sc) {
+  int* depth = sc.depth;
+  int* order = sc.order;
+  const int tid = threadIdx.x, nt = blockDim.x;
+  if (tid == 0) { sc.n_elig = 0; sc.n_nonempty = 0; }
+  __syncthreads();
+  for (int b = tid; b < d.NB; b += nt) {
+    const int dep = enabled ? min((int)(L.tail[b] - L.head[b]), d.cap) : 0;
+    depth[b] = dep;
+    if (dep > 0) atomicAdd(&sc.n_nonempty, 1);
+    if (dep > 0 && (pol.kind != MOE_POLICY_THRESHOLD || dep >= pol.min_batch)) atomicAdd(&sc.n_elig, 1);
+  }
+  __syncthreads();
+  const int n_elig = sc.n_elig, n_nonempty = sc.n_nonempty;
+  int minb = 1, G = pol.max_groups;
+  if (pol.kind == MOE_POLICY_THRESHOLD) {
+    if (n_elig > 0) minb = pol.min_batch > 1 ? pol.min_batch : 1;
+    else G = pol.fallback_groups > 0 ? pol.fallback_groups : 1;
+  }
+  const int ne = (pol.kind == MOE_POLICY_THRESHOLD && n_elig == 0) ? n_nonempty : n_elig;
+  // After an overflow or an out-of-range id the queues no longer describe valid pairs:
+  // stop executing (the sticky error is reported to the host).
+  const uint32_t err = *(volatile uint32_t*)&C->error;
+  const bool halted = err == MOE_ERR_CAPACITY || err == MOE_ERR_INVALID;
+  const int n = halted ? 0 : ((G > 0 && G < ne) ? G : ne);
+  for (int b = tid; b < d.NB; b += nt) {
+    const int db = depth[b];
+    if (db >= minb) {
+      int r = 0;
+      for (int c = 0; c < d.NB; ++c) {
+        const int dc = depth[c];
+        r += (dc >= minb) && (dc > db || (dc == db && c < b));
+      }
+      if (r < n) order[r] = b;
+    }
+  }
+  __syncthreads();
+  if (tid < 32) {
+    const int lane = tid;
+    int row_run = 0, t1_run = 0, t2_run = 0;
+    const int ft1 = (2 * d.I + g.bm1 - 1) / g.bm1;
+    const int ft2 = (d.H + g.bm2 - 1) / g.bm2;
+    for (int c0 = 0; c0 < n; c0 += 32) {
+      const int r = c0 + lane;
+      int b = 0, cnt = 0, t1 = 0, t2 = 0;
+      if (r < n) {
+        b = order[r];
+        cnt = depth[b];
+        t1 = ((cnt + g.bn1 - 1) / g.bn1) * ft1;
+        t2 = ((cnt + g.bn2 - 1) / g.bn2) * ft2;
+      }
+      int s_cnt = cnt, s_t1 = t1, s_t2 = t2;      // inclusive prefix sums within the chunk
+      for (int off = 1; off < 32; off <<= 1) {
+        int a = __shfl_up_sync(0xffffffffu, s_cnt, off);
+        int b1 = __shfl_up_sync(0xffffffffu, s_t1, off);
+        int b2 = __shfl_up_sync(0xffffffffu, s_t2, off);
+        if (lane >= off) { s_cnt += a; s_t1 += b1; s_t2 += b2; }
+      }
+      if (r < n) {
+        WorkItem it;
+        it.expert = b;
+        it.head = L.head[b];
+        it.count = cnt;
+        it.row_base = row_run + s_cnt - cnt;
+        it.t1_base = t1_run + s_t1 - t1;
+        it.t2_base = t2_run + s_t2 - t2;
+        P->items[r] = it;
+        L.head[b] = it.head + (uint32_t)cnt;
+        if (trace && trace_cap > 0) {
+          const int ti = atomicAdd(&C->trace_n, 1);
+          if (ti < trace_cap) trace[ti] = make_int4(trace_step, layer, b, cnt);
+        }
+      }
+      row_run += __shfl_sync(0xffffffffu, s_cnt, 31);
+      t1_run += __shfl_sync(0xffffffffu, s_t1, 31);
+      t2_run += __shfl_sync(0xffffffffu, s_t2, 31);
+    }
+    if (lane == 0) {
+      P->layer = layer;
+      P->n_work = n;
+      P->n_tiles1 = t1_run;
+      P->n_tiles2 = t2_run;
+      P->rows = row_run;
+      if (!enabled) return;
+      C->steps += 1ull;
+      C->pairs_executed += (unsigned long long)row_run;
+      C->expert_runs += (unsigned long long)n;
+      C->weight_bytes += (unsigned long long)n * (unsigned long long)weight_bytes_per_run;
+      C->pending_pairs -= row_run;
+    }
+  }
 }
 
 struct CtaBarrier {
@@ -195,7 +411,7 @@ struct CtaBarrier {
 template <typename T, typename Bar>
 __device__ void land_and_merge(const LayerView& L, const Dims& d, DevCounters* C,
                                const int* slots, int nj, int target, int tid, int nthr,
-                               int* fin, Bar bar) {
+                               int* fin, Bar bar, const StreamDev* sd = nullptr, int layer = 0) {
   __threadfence();
   bar();
   for (int j = tid; j < nj; j += nthr) {
@@ -206,9 +422,18 @@ __device__ void land_and_merge(const LayerView& L, const Dims& d, DevCounters* C
   __threadfence();
   bar();
   for (int j = 0; j < nj; ++j) {
-    if (fin[j]) {
-      merge_token<T>(L, d, C, slots[j], tid, nthr);
-      if (tid == 0) publish_ready(L, d, C, slots[j]);
+    if (fin[j]) {                                    // uniform across the group
+      T* hist_row = nullptr;
+      if (sd)
+        hist_row = static_cast<T*>(sd->hist) +
+                   ((size_t)slots[j] * (sd->n_max + 1) + sd->req_n[slots[j]] + 1) * d.H;
+      merge_token<T>(L, d, C, slots[j], tid, nthr, hist_row);
+      if (sd) {
+        bar();                                       // every thread has read req_n
+        if (tid == 0) stream_complete(L, C, *sd, layer, slots[j]);
+      } else if (tid == 0) {
+        publish_ready(L, d, C, slots[j]);
+      }
     }
   }
   bar();
@@ -234,6 +459,11 @@ moe_status launch_identity(moe_async_s* h, int layer, cudaStream_t s);
 moe_status tc_setup(moe_async_s* h);                 // tensor maps for the tcgen05 path
 void tc_teardown(moe_async_s* h);
 moe_status launch_ffn_tc(moe_async_s* h, int layer, cudaStream_t s);
+moe_status tc_stream_setup(moe_async_s* h, const void* const* proj_packed, const StreamDev& sd);
+// out[r][c] = in[c][r] for a bf16 [C][R] matrix (K-major packing of a projection).
+cudaError_t pack_transpose_bf16(const void* in, void* out, int C, int R, cudaStream_t s);
+moe_status launch_att_tc(moe_async_s* h, cudaStream_t s);
+void stream_teardown(moe_async_s* h);
 TileGeom simt_geom();
 TileGeom tc_geom();
 

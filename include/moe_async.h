@@ -205,6 +205,48 @@ moe_status moe_async_get_trace(moe_async_t h, void* stream, int32_t* h_buf, int3
 moe_status moe_async_snapshot(moe_async_t h, int32_t layer, void* stream, int32_t* h_depth,
                               int32_t* h_records, int32_t cap, int32_t* h_n);
 
+/* ---- Streaming multi-layer decode on the 2L micro-queues --------------------------------
+ * "SOSP'26 StreamEP" section 3: each layer has an attention queue and an expert queue; a
+ * request's token is served by its layer's attention stage, routed, dispatched to the expert
+ * queue, merged back and queued for the next layer's attention -- each request advances at
+ * its own pace, with no barrier across requests.  Section 4: one queue is served per
+ * scheduling decision, the one holding the most tokens (MTFS; equal counts -> lower layer,
+ * attention before expert).  The attention stage is a stub: a = RMSNorm(x) P_l (eps 1e-6,
+ * no gain), x^(n+1) = MoE_l(a) with l = n mod L.  All state lives on the device and one
+ * scheduling decision ("tick") runs as a CUDA graph with no host round trip. */
+typedef struct {
+  int32_t num_requests;     /* R <= max_slots; request r uses combine slot r in every layer    */
+  int32_t max_steps;        /* steps per request at most (history depth)                       */
+  int32_t stop_combines;    /* attention queues are closed once this many merges are done      */
+} moe_stream_config;
+
+/* Set up the streaming runtime on a bf16 SwiGLU handle (its merges then feed the runtime,
+ * not the collect ring).  Synchronises `stream`.
+ *   d_proj[l]   : [H, H] bf16 projection of layer l's attention stub (x @ P); packed, may be freed
+ *   d_x0        : [R, H] bf16 initial states (copied into the history)
+ *   d_logits    : [R, max_steps, E] fp32 router logits of (request, step)   (borrowed)
+ *   d_delay     : [R, max_steps] int32 dispatch delay in ticks, >= 1       (borrowed)
+ *   d_history   : [R, max_steps + 1, H] bf16 out: x^(n) of every request, x^(0) at n = 0
+ *   d_done_tick : [R, max_steps + 1] int32 out: tick at which step n completed (-1 = not)
+ * Every request starts in layer 0's attention queue.  MOE_ERR_UNSUPPORTED for fp32 or
+ * identity handles or more than 8 layers. */
+moe_status moe_async_stream_setup(moe_async_t h, const moe_stream_config* sc,
+                                  const void* const* d_proj, const void* d_x0,
+                                  const float* d_logits, const int32_t* d_delay,
+                                  void* d_history, int32_t* d_done_tick, void* stream);
+
+/* Run ticks until nothing is left (no dispatch in transit, expert queues empty, attention
+ * queues closed or empty), reading the control block every `check_every` ticks; at most
+ * max_ticks ticks (then MOE_ERR_TIMEOUT).  Synchronises; *h_ticks = ticks run,
+ * *h_combined = merges completed. */
+moe_status moe_async_stream_run(moe_async_t h, int32_t max_ticks, int32_t check_every,
+                                int32_t* h_ticks, int32_t* h_combined, void* stream);
+
+/* Synchronise and copy the tick trace: 4 int32 per tick (tick, kind, layer, count), kind
+ * 1 = attention queue, 2 = expert queue, 0 = idle (only dispatches in transit). */
+moe_status moe_async_stream_trace(moe_async_t h, void* stream, int32_t* h_buf, int32_t cap,
+                                  int32_t* h_n);
+
 /* Per-kernel timing (tracing).  enable = 1 brackets every later kernel launch of the handle
  * with a pair of CUDA events on its stream (up to 65536 launches are kept); enable = 0 stops.
  * Host-side events only: no device memory is allocated. */

@@ -1,0 +1,137 @@
+"""Streaming multi-layer decode on the GPU (2L micro-queues, device-side layer-level MTFS,
+dispatch delays, attention stub) against the streaming oracle.
+
+Bookkeeping is compared exactly: the queue picked at every tick and its size, the tick at
+which every (request, step) completed, every request's final step count.  Values: the chain
+x^(n+1) = MoE_l(RMSNorm(x^(n)) P_l) is chaotic -- a bf16 rounding difference grows ~1.5x per
+step -- so outputs are compared elementwise for the first steps of every request (where the
+bound holds by a wide margin), and beyond that the GPU must reproduce itself bit for bit when
+only the dispatch delays (hence the batching and completion order) change.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import moe_oracle as om
+from workloads import get_config, make_stream_inputs
+from workloads.build import make_layer_weights
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pkg():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import __graft_entry__ as g
+    g.build()
+    import asynchronous_expert_execution_gb300 as p
+    return p
+
+
+def _gpu_stream(pkg, spec, M, seed=0, delay_seed=None, weights=None):
+    lay = spec.layer
+    R, H, NL = spec.tokens, lay.hidden, spec.num_layers
+    wl = make_stream_inputs(spec, seed, M, weights=False, delay_seed=delay_seed)
+    if weights is None:
+        weights = [make_layer_weights(lay, seed, l, device="cuda") for l in range(NL)]
+    moe = pkg.MoEAsync(lay.num_experts, lay.top_k, H, lay.inter, torch.bfloat16, R, weights=weights,
+                       num_layers=NL)
+    proj = [p.cuda() for p in wl.proj]
+    hist = torch.zeros((R, M + 1, H), dtype=torch.bfloat16, device="cuda")
+    done = torch.empty((R, M + 1), dtype=torch.int32, device="cuda")
+    delays = torch.as_tensor(wl.delays, dtype=torch.int32).cuda()
+    moe.stream_setup(proj, wl.x0.cuda(), wl.logits.cuda(), delays, M, spec.stream_steps, hist, done)
+    st, ticks, comb = moe.stream_run(max_ticks=100000, check_every=16)
+    trace = moe.stream_trace()
+    stats = moe.stats()
+    moe.close()
+    return dict(wl=wl, weights=weights, status=st, ticks=ticks, combined=comb, trace=trace, stats=stats,
+                hist=hist.float().cpu().numpy().astype(np.float64), done=done.cpu().numpy())
+
+
+def _oracle_stream(spec, wl, weights, values, compute=None):
+    lay = spec.layer
+    lg = wl.logits.numpy()
+    proj = [p.double().numpy() for p in wl.proj]
+    cache = {}
+
+    def experts(l, e):
+        if (l, e) not in cache:
+            cache[(l, e)] = tuple(weights[l][k][e].to("cpu", torch.float64).numpy() for k in ("w1", "w3", "w2"))
+        return cache[(l, e)]
+    return om.StreamOracle(spec.num_layers, lay.top_k, wl.x0.double().numpy(), lambda l: proj[l],
+                           lambda r, n: lg[r, n], wl.delays, experts, spec.stream_steps, wl.max_steps,
+                           values=values, compute=compute).run()
+
+
+def _check_bookkeeping(res, sim):
+    kinds = {"idle": 0, "att": 1, "exp": 2}
+    want = [(t.tick, kinds[t.kind], t.layer, t.count) for t in sim.trace]
+    got = [tuple(x) for x in res["trace"].tolist()]
+    assert got == want
+    assert res["ticks"] == sim.tick and res["combined"] == sim.combined
+    R, M1 = res["done"].shape
+    for r in range(R):
+        for n in range(1, M1):
+            assert res["done"][r, n] == sim.done_tick.get((r, n), -1), (r, n)
+
+
+def test_stream_small_parity(pkg):
+    spec = get_config("s1")
+    M = 16
+    res = _gpu_stream(pkg, spec, M)
+    assert res["status"] == 0
+    sim = _oracle_stream(spec, res["wl"], res["weights"], values=True)
+    _check_bookkeeping(res, sim)
+    # values: every request's first two steps, elementwise
+    errs = []
+    for r in range(spec.tokens):
+        for n in range(1, min(int(sim.n[r]), 2) + 1):
+            ref = sim.history[r][n]
+            errs.append(np.abs(res["hist"][r, n] - ref).max() / np.abs(ref).max())
+    assert errs and max(errs) <= 2e-2, max(errs)
+
+
+def test_stream_small_bitwise_invariant_to_delays(pkg):
+    spec = get_config("s1")
+    M = 16
+    a = _gpu_stream(pkg, spec, M, delay_seed=0)
+    b = _gpu_stream(pkg, spec, M, delay_seed=1, weights=a["weights"])
+    assert a["status"] == 0 and b["status"] == 0
+    assert [tuple(x) for x in a["trace"].tolist()] != [tuple(x) for x in b["trace"].tolist()]
+    na = (a["done"] >= 0).sum(1)
+    nb = (b["done"] >= 0).sum(1)
+    compared = 0
+    for r in range(spec.tokens):
+        for n in range(1, min(na[r], nb[r]) + 1):
+            assert np.array_equal(a["hist"][r, n], b["hist"][r, n]), (r, n)
+            compared += 1
+    assert compared >= spec.tokens
+
+
+def test_stream_c5_fullsize(pkg):
+    """512 requests, 4 GPT-OSS-shaped layers, until 10,000 token-layer steps."""
+    spec = get_config("c5")
+    M = 64
+    res = _gpu_stream(pkg, spec, M)
+    assert res["status"] == 0
+    assert res["combined"] >= spec.stream_steps
+    sim = _oracle_stream(spec, res["wl"], res["weights"], values=False)
+    _check_bookkeeping(res, sim)
+    # first step of a seeded sample of requests, elementwise against the float64 chain
+    rng = np.random.default_rng(9)
+    sample = sorted(rng.choice(spec.tokens, size=6, replace=False).tolist())
+    wl = res["wl"]
+    x0 = wl.x0.double().numpy()
+    P0 = wl.proj[0].double().numpy()
+    lg = wl.logits.numpy()
+    errs = []
+    for r in sample:
+        a = om.attention_stub(x0[r:r + 1], P0)
+        idx, w = om.route(lg[r, 0][None, :], spec.layer.top_k)
+        contribs = [w[0, k] * om.expert_ffn(a, *(res["weights"][0][kk][int(idx[0, k])].to("cpu", torch.float64).numpy()
+                                                 for kk in ("w1", "w3", "w2")))[0] for k in range(spec.layer.top_k)]
+        ref = om.combine(contribs)
+        errs.append(np.abs(res["hist"][r, 1] - ref).max() / np.abs(ref).max())
+    assert max(errs) <= 2e-2, errs

@@ -21,5 +21,5 @@ from .configs import (  # noqa: F401
 )
 from .build import (  # noqa: F401
     Workload, Wave, make_workload, make_layer_weights, expert_weight_slice, make_tokens,
-    make_logits, make_waves, shuffled_waves, repartitioned_waves,
+    make_logits, make_waves, shuffled_waves, repartitioned_waves, StreamWorkload, make_stream_inputs,
 )

@@ -174,6 +174,47 @@ def make_workload(spec, seed=0, device="cpu", weights=True):
     return Workload(spec=spec, seed=seed, x=x, logits=logits, weights=ws, waves=make_waves(spec, seed))
 
 
+_S_DELAY = 10
+
+
+@dataclass
+class StreamWorkload:
+    """Inputs of the streaming multi-layer decode (config c5 and its smaller variants).
+
+    x0      [R, H]        initial request states, N(0, 1)
+    proj    [L] x [H, H]  attention-stub projections, N(0, sd 1/sqrt(H))
+    weights [L] x dict    routed experts of every layer (as make_layer_weights)
+    logits  [R, M, E]     router logits of (request r, step n), U(0, 1) like c2
+    delays  [R, M]        dispatch delay in ticks: ceil(LogNormal(0, sigma)), at least 1
+    """
+    spec: WorkloadSpec
+    seed: int
+    max_steps: int
+    x0: torch.Tensor
+    proj: list
+    weights: list
+    logits: torch.Tensor
+    delays: np.ndarray
+
+
+def make_stream_inputs(spec, seed, max_steps, device="cpu", weights=True, requests=None, delay_seed=None):
+    L, lay = spec.num_layers, spec.layer
+    R = spec.tokens if requests is None else requests
+    H, E = lay.hidden, lay.num_experts
+    x0 = make_tokens(spec, seed, n=R, device=device)
+    proj = []
+    for l in range(L):
+        v = counter_normal(seed, _stream(l, _S_PROJ), H * H, device=device) / math.sqrt(H)
+        proj.append(to_dtype_exact(v, lay.dtype).view(H, H))
+    ws = [make_layer_weights(lay, seed, l, device) for l in range(L)] if weights else []
+    logits = counter_uniform(seed, _stream(0, _S_LOGIT) + 7, R * max_steps * E, device=device)
+    logits = logits.to(torch.float32).view(R, max_steps, E)
+    z = counter_normal(seed if delay_seed is None else delay_seed, _stream(0, _S_DELAY), R * max_steps).numpy()
+    delays = np.maximum(1, np.ceil(np.exp(spec.stream_sigma * z))).astype(np.int32).reshape(R, max_steps)
+    return StreamWorkload(spec=spec, seed=seed, max_steps=max_steps, x0=x0, proj=proj, weights=ws,
+                          logits=logits, delays=delays)
+
+
 def shuffled_waves(waves, seed):
     """Same deliveries, re-ordered arrival ticks (for arrival-order invariance)."""
     rng = np.random.default_rng([seed, 303])

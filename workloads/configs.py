@@ -97,6 +97,11 @@ TEST_CONFIGS = {
     "p1": WorkloadSpec(
         name="p1_gptoss_slice", layer=GPT_OSS_LAYER.__class__(32, 4, 2880, 2880, "bf16"), tokens=64,
         router="uniform", waves="even", num_waves=4, arrival="index", policy="mtfs"),
+    # streaming multi-layer decode, small: 4 layers, ragged H (2.5 tiles of 128), 48 requests.
+    "s1": WorkloadSpec(
+        name="s1_stream_small", layer=LayerSpec(16, 4, 320, 192, "bf16"), tokens=48, router="uniform",
+        waves="stream", num_waves=16, arrival="lognormal", policy="mtfs", num_layers=4,
+        stream_steps=150, stream_ranks=16, stream_sigma=1.0),
     # bf16 decode-like: many experts, few tokens each.
     "m4": WorkloadSpec(
         name="m4_bf16_decode", layer=LayerSpec(64, 4, 1024, 512, "bf16"), tokens=64,
