@@ -14,5 +14,5 @@ brute-force enumeration, closed forms, invariants).
 from .moe_oracle import (  # noqa: F401
     route, route_bruteforce, silu, expert_ffn, combine, dense_moe,
     mtfs_pick, threshold_pick, defrag_score, AsyncMoEOracle, StepRecord,
-    rmsnorm, attention_stub, replay_layer, y_sample, layer_pick, StreamOracle, TickRecord,
+    rmsnorm, attention_stub, replay_layer, y_sample, layer_pick, chain_pick, StreamOracle, TickRecord,
 )

@@ -178,8 +178,10 @@ def defrag_score(q_now, lookahead, delta):
     ``lookahead`` lists (Q(s_j), H(s_j)) for j = 1..W along the execution chain
     attention -> expert -> next attention."""
     s = float(q_now)
-    for j, (q, h) in enumerate(lookahead, start=1):
-        s += (delta ** j) * (q + h)
+    dj = 1.0
+    for q, h in lookahead:
+        dj = dj * delta                    # delta^j, j = 1..W
+        s += dj * (q + h)
     return s
 
 
@@ -374,6 +376,46 @@ def layer_pick(att_depth, exp_depth, allow_attention=True):
     return ("att" if kind == 0 else "exp", l)
 
 
+def chain_pick(att_depth, exp_depth, policy, allow_attention=True, drained=None, window=2, decay=0.5,
+               in_transit=0):
+    """Layer-level policies over the 2L micro-queues in chain order att_0, exp_0, att_1, ...
+
+    mtfs    -- most tokens first (``layer_pick``), StreamEP section 4.
+    flfs    -- first layer first: the earliest non-empty queue in the chain (section 4).
+    defrag  -- the defragmenting score of section 4, S(s) = Q(s) + sum_{j=1..W} delta^j
+               [Q(s_j) + H(s_j)], s_j the j-th queue after s along the chain (truncated at
+               the last layer, the paper's version); H = tokens drained from a queue over the
+               recent ticks (``drained``); highest score first, equal scores -> earlier queue.
+    barrier -- the synchronous baseline: serve a queue only when nothing is in transit and it
+               holds every token still being served (lockstep layers); if tokens are split
+               with nothing in transit, serve the earliest queue so progress continues.
+    Closed attention queues (after the stop) count as empty everywhere."""
+    L = len(att_depth)
+    Q = []
+    for l in range(L):
+        Q.append(att_depth[l] if allow_attention else 0)
+        Q.append(exp_depth[l])
+    nonempty = [q for q in range(2 * L) if Q[q] > 0]
+    if not nonempty:
+        return None
+    as_pick = lambda q: ("att" if q % 2 == 0 else "exp", q // 2)
+    if policy == "mtfs":
+        return layer_pick(att_depth, exp_depth, allow_attention)
+    if policy == "flfs":
+        return as_pick(nonempty[0])
+    if policy == "defrag":
+        best, best_s = None, None
+        for q in nonempty:
+            look = [(Q[q + j], drained[q + j]) for j in range(1, window + 1) if q + j < 2 * L]
+            s = defrag_score(Q[q], look, decay)
+            if best is None or s > best_s:
+                best, best_s = q, s
+        return as_pick(best)
+    if policy == "barrier":
+        return None if in_transit > 0 else as_pick(nonempty[0])
+    raise ValueError(policy)
+
+
 @dataclass
 class TickRecord:
     tick: int
@@ -401,8 +443,10 @@ class StreamOracle:
     """
 
     def __init__(self, L, K, x0, proj, logits, delays, experts, stop, max_steps,
-                 values=True, compute=None):
+                 values=True, compute=None, policy="mtfs", window=2, decay=0.5, hist_window=8):
         self.L, self.K = L, K
+        self.policy, self.window, self.decay, self.hist_window = policy, window, decay, hist_window
+        self.drain_log = []               # per tick: tokens drained from each of the 2L queues
         self.R = len(x0)
         self.x0 = np.asarray(x0, dtype=np.float64)
         self.proj, self.logits, self.delays = proj, logits, np.asarray(delays)
@@ -433,8 +477,13 @@ class StreamOracle:
         for r in sorted(r for r, t in self.transit.items() if t == self.tick):
             del self.transit[r]
             self.pending[int(self.n[r]) % self.L].add(r)
-        pick = layer_pick([len(a) for a in self.att], [len(p) for p in self.pending],
-                          allow_attention=self.combined < self.stop)
+        recent = self.drain_log[-self.hist_window:] if self.hist_window > 0 else []
+        drained = [sum(v[q] for v in recent) for q in range(2 * self.L)]
+        pick = chain_pick([len(a) for a in self.att], [len(p) for p in self.pending], self.policy,
+                          allow_attention=self.combined < self.stop, drained=drained,
+                          window=self.window, decay=self.decay, in_transit=len(self.transit))
+        tick_drain = [0] * (2 * self.L)
+        self.drain_log.append(tick_drain)
         if pick is None:
             self.trace.append(TickRecord(self.tick, "idle", -1, 0))
             return
@@ -465,6 +514,7 @@ class StreamOracle:
                 self.combined += 1
                 if n + 1 < self.max_steps:
                     self.att[(n + 1) % self.L].add(r)
+        tick_drain[2 * l + (0 if kind == "att" else 1)] = len(batch)
         self.trace.append(TickRecord(self.tick, kind, l, len(batch)))
 
     def run(self, max_ticks=1000000):

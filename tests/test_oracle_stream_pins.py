@@ -140,3 +140,57 @@ def test_stream_pins_catch_planted_mistakes(monkeypatch):
     except AssertionError:
         caught = True
     assert caught
+
+
+def pin_chain_policies():
+    # worked example of the defragmenting score embedded in a 3-layer chain: candidate att_0
+    # holds 20 tokens; the next two queues are empty now but drained 100 and 80 recently;
+    # an isolated exp_2 holds 60 (no queue after it).  S(att_0) = 20 + .5*100 + .25*80 = 90.
+    att, exp = [20, 0, 0], [0, 0, 60]
+    drained = [0, 100, 80, 0, 0, 0]
+    assert om.chain_pick(att, exp, "defrag", drained=drained, window=2, decay=0.5) == ("att", 0)
+    assert om.chain_pick(att, exp, "mtfs") == ("exp", 2)
+    assert om.chain_pick(att, exp, "flfs") == ("att", 0)
+    assert om.chain_pick([0, 3], [2, 5], "flfs") == ("exp", 0)
+    # window 1: S(att_0) = 20 + 0.5 * 100 = 70 > 60 still; decay 0.2: 20 + 20 + 3.2 = 43.2 < 60
+    assert om.chain_pick(att, exp, "defrag", drained=drained, window=1, decay=0.5) == ("att", 0)
+    assert om.chain_pick(att, exp, "defrag", drained=drained, window=2, decay=0.2) == ("exp", 2)
+    # barrier: nothing is served while a dispatch is in flight
+    assert om.chain_pick([0, 0], [3, 0], "barrier", in_transit=1) is None
+    assert om.chain_pick([0, 2], [3, 0], "barrier", in_transit=0) == ("exp", 0)
+    # closed attention queues count as empty
+    assert om.chain_pick([9, 0], [1, 0], "defrag", allow_attention=False, drained=[0] * 4) == ("exp", 0)
+
+
+def test_chain_policies():
+    pin_chain_policies()
+
+
+def test_barrier_trace_hand():
+    delays = np.ones((2, 8), dtype=np.int64)
+    delays[1, 0] = 3
+    s = _mk(R=2, L=2, E=2, K=1, H=3, delays=delays, stop=4, max_steps=8, values=False)
+    s.policy = "barrier"
+    s.run()
+    got = [(t.tick, t.kind, t.layer, t.count) for t in s.trace][:6]
+    # t1 att L0 {0,1}; t2, t3 idle (request 1 in flight); t4 exp L0 {0,1}; t5 att L1; t6 exp L1
+    assert got == [(1, "att", 0, 2), (2, "idle", -1, 0), (3, "idle", -1, 0), (4, "exp", 0, 2),
+                   (5, "att", 1, 2), (6, "exp", 1, 2)]
+
+
+def test_policies_same_values_and_conservation():
+    R, L, E, K, H, M = 10, 3, 4, 2, 5, 8
+    d = np.random.default_rng(11).integers(1, 5, size=(R, M))
+    runs = {}
+    for pol in ("mtfs", "flfs", "defrag", "barrier"):
+        s = _mk(R, L, E, K, H, d, stop=40, max_steps=M)
+        s.policy = pol
+        s.run()
+        assert s.combined == int(s.n.sum()) and 40 <= s.combined < 40 + R
+        assert not s.transit and not any(s.pending)
+        runs[pol] = s
+    ref = runs["mtfs"]
+    for pol, s in runs.items():
+        for r in range(R):
+            for n in range(min(len(s.history[r]), len(ref.history[r]))):
+                assert np.array_equal(s.history[r][n], ref.history[r][n]), (pol, r, n)
