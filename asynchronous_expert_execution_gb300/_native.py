@@ -45,7 +45,12 @@ class Stats(ctypes.Structure):
 
 
 class StreamConfig(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_int32) for n in ("num_requests", "max_steps", "stop_combines")]
+    _fields_ = [(n, ctypes.c_int32) for n in ("num_requests", "max_steps", "stop_combines", "policy",
+                                              "defrag_window", "history_window")] + \
+               [("defrag_decay", ctypes.c_double)]
+
+
+STREAM_POLICIES = {"mtfs": 0, "flfs": 1, "defrag": 2, "barrier": 3}
 
 
 class MoEError(RuntimeError):

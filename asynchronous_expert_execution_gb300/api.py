@@ -142,13 +142,15 @@ class MoEAsync:
         return depths, out
 
     # -- streaming multi-layer decode (2L micro-queues) --------------------------
-    def stream_setup(self, proj, x0, logits, delays, max_steps, stop, history, done_tick, stream=None):
+    def stream_setup(self, proj, x0, logits, delays, max_steps, stop, history, done_tick, policy="mtfs",
+                     window=2, decay=0.5, hist_window=8, stream=None):
         """proj: list of L [H, H] device tensors; x0 [R, H]; logits [R, M, E] fp32; delays
-        [R, M] int32; history [R, M+1, H] and done_tick [R, M+1] int32 are outputs."""
+        [R, M] int32; history [R, M+1, H] and done_tick [R, M+1] int32 are outputs.
+        policy: "mtfs" | "flfs" | "defrag" | "barrier" (layer-level queue choice)."""
         R = x0.shape[0]
         arr = ctypes.c_void_p * len(proj)
         self._stream_keep = (logits, delays, history, done_tick)
-        cfg = N.StreamConfig(R, max_steps, stop)
+        cfg = N.StreamConfig(R, max_steps, stop, N.STREAM_POLICIES[policy], window, hist_window, decay)
         st = self.lib.moe_async_stream_setup(self.h, ctypes.byref(cfg), arr(*[p.data_ptr() for p in proj]),
                                              _ptr(x0), _ptr(logits), _ptr(delays), _ptr(history),
                                              _ptr(done_tick), _stream(stream))

@@ -99,7 +99,10 @@ struct StreamCtl {
   int32_t done;                     // 1 once nothing is left to do
   int32_t exp_tokens[kMaxLayers];   // tokens whose pairs wait in layer l's expert queue
   int32_t pad[4];
+  int32_t drained[16][2 * kMaxLayers];   // tokens drained per queue, ring over the last ticks
 };
+
+constexpr int kMaxHistoryWindow = 16;
 
 // Device pointers of the streaming runtime, passed by value to its kernels.
 //   req_n[r]            completed layer-steps of request r (its state is x^(req_n))
@@ -113,6 +116,8 @@ struct StreamCtl {
 struct StreamDev {
   StreamCtl* ctl;
   int32_t R, n_max, stop, L;
+  int32_t policy, window, hist_window;   // moe_stream_policy and its DEFRAG parameters
+  double decay;
   int32_t* req_n;
   int32_t* arr_tick;
   int32_t* att_ring;

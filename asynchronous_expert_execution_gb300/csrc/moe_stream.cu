@@ -98,15 +98,46 @@ __global__ void __launch_bounds__(1024) stream_tick_kernel(const __grid_constant
   __threadfence();
   __syncthreads();
   if (tid == 0) {
-    int kind = 0, layer = 0, best = 0;
+    int kind = 0, layer = 0;
     if (s_busy) {
+      // the 2L queues in chain order att_0, exp_0, att_1, exp_1, ... (tokens; closed
+      // attention queues count as empty)
       const bool allow_att = ctl->combined < sd.stop;
-      for (int l = 0; l < Lc; ++l) {                 // order: layer asc, attention before expert
-        const int da = allow_att ? (int)(sd.att_ht[2 * l + 1] - sd.att_ht[2 * l]) : 0;
-        const int de = ctl->exp_tokens[l];
-        if (da > best) { best = da; kind = 1; layer = l; }
-        if (de > best) { best = de; kind = 2; layer = l; }
+      int Q[2 * kMaxLayers];
+      for (int l = 0; l < Lc; ++l) {
+        Q[2 * l] = allow_att ? (int)(sd.att_ht[2 * l + 1] - sd.att_ht[2 * l]) : 0;
+        Q[2 * l + 1] = ctl->exp_tokens[l];
       }
+      const int nq = 2 * Lc;
+      int pick = -1;
+      if (sd.policy == MOE_STREAM_FLFS ||
+          (sd.policy == MOE_STREAM_BARRIER && ctl->in_transit == 0)) {
+        for (int q = 0; q < nq && pick < 0; ++q)
+          if (Q[q] > 0) pick = q;
+      } else if (sd.policy == MOE_STREAM_DEFRAG) {
+        int Hd[2 * kMaxLayers];
+        const int hw = min(sd.hist_window, kMaxHistoryWindow);
+        for (int q = 0; q < nq; ++q) {
+          int h = 0;
+          for (int i = 0; i < hw; ++i) h += ctl->drained[i][q];
+          Hd[q] = h;
+        }
+        double best_s = 0.0;
+        for (int q = 0; q < nq; ++q) {
+          if (Q[q] <= 0) continue;
+          double s = (double)Q[q], dj = 1.0;
+          for (int j = 1; j <= sd.window && q + j < nq; ++j) {
+            dj = dj * sd.decay;
+            s += dj * (double)(Q[q + j] + Hd[q + j]);
+          }
+          if (pick < 0 || s > best_s) { pick = q; best_s = s; }
+        }
+      } else if (sd.policy == MOE_STREAM_MTFS) {
+        int best = 0;
+        for (int q = 0; q < nq; ++q)
+          if (Q[q] > best) { best = Q[q]; pick = q; }
+      }
+      if (pick >= 0) { kind = 1 + (pick & 1); layer = pick >> 1; }
     } else {
       ctl->done = 1;
     }
@@ -141,6 +172,11 @@ __global__ void __launch_bounds__(1024) stream_tick_kernel(const __grid_constant
     ctl->pick_kind = kind;
     ctl->pick_layer = layer;
     ctl->tick = tick;
+    if (s_busy && sd.hist_window > 0) {               // this tick's drain, for H(s)
+      int* row = ctl->drained[tick % min(sd.hist_window, kMaxHistoryWindow)];
+      for (int q = 0; q < 2 * kMaxLayers; ++q) row[q] = 0;
+      if (kind) row[2 * layer + (kind - 1)] = cnt;
+    }
     if (s_busy) {
       const int ti = atomicAdd(a.trace_n, 1);
       if (ti < kStreamTraceCap) a.trace[ti] = make_int4(tick, kind, kind ? layer : -1, cnt);
@@ -257,7 +293,9 @@ extern "C" moe_status moe_async_stream_setup(moe_async_t h, const moe_stream_con
   if (!h || !sc || !d_proj || !d_x0 || !d_logits || !d_delay || !d_history || !d_done_tick)
     return MOE_ERR_INVALID;
   if (!h->use_tc || h->cfg.num_layers > kMaxLayers) return MOE_ERR_UNSUPPORTED;
-  if (sc->num_requests < 1 || sc->num_requests > h->dims.S || sc->max_steps < 1 || sc->stop_combines < 0)
+  if (sc->num_requests < 1 || sc->num_requests > h->dims.S || sc->max_steps < 1 || sc->stop_combines < 0 ||
+      sc->policy < MOE_STREAM_MTFS || sc->policy > MOE_STREAM_BARRIER || sc->defrag_window < 0 ||
+      sc->history_window < 0 || sc->history_window > kMaxHistoryWindow || !(sc->defrag_decay == sc->defrag_decay))
     return MOE_ERR_INVALID;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (h->stream_state) stream_teardown(h);
@@ -272,6 +310,10 @@ extern "C" moe_status moe_async_stream_setup(moe_async_t h, const moe_stream_con
   sd.n_max = sc->max_steps;
   sd.stop = sc->stop_combines;
   sd.L = L;
+  sd.policy = sc->policy;
+  sd.window = sc->defrag_window;
+  sd.hist_window = sc->history_window;
+  sd.decay = sc->defrag_decay;
   sd.logits = d_logits;
   sd.delay = d_delay;
   sd.hist = d_history;

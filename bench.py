@@ -42,6 +42,11 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--policy", default="mtfs", choices=["mtfs", "flfs", "defrag", "barrier"],
+                    help="layer-level policy of the streaming workloads (c5, s1)")
+    ap.add_argument("--defrag-window", type=int, default=2)
+    ap.add_argument("--defrag-decay", type=float, default=0.5)
+    ap.add_argument("--history-window", type=int, default=8)
     return ap.parse_args()
 
 
@@ -256,6 +261,76 @@ def run_reference(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
+def run_stream(args, pkg, dev):
+    """Streaming multi-layer decode (c5 shape): sustained pairs/s of the device-resident
+    runtime under a layer-level policy, with its schedule statistics.  Each step sets the
+    stream up again (untimed: projection packing, graph capture) and times the run."""
+    from workloads import get_config, make_stream_inputs
+    from workloads.build import make_layer_weights
+    spec = get_config(args.workload)
+    lay = spec.layer
+    R, H, NL, M = spec.tokens, lay.hidden, spec.num_layers, 64
+    wl = make_stream_inputs(spec, args.seed, M, weights=False)
+    weights = [make_layer_weights(lay, args.seed, l, device=dev) for l in range(NL)]
+    moe = pkg.MoEAsync(lay.num_experts, lay.top_k, H, lay.inter, torch.bfloat16, R, weights=weights,
+                       num_layers=NL)
+    del weights
+    torch.cuda.empty_cache()
+    proj = [p.to(dev) for p in wl.proj]
+    x0, logits = wl.x0.to(dev), wl.logits.to(dev)
+    delays = torch.as_tensor(wl.delays, dtype=torch.int32).to(dev)
+    hist = torch.zeros((R, M + 1, H), dtype=torch.bfloat16, device=dev)
+    done = torch.empty((R, M + 1), dtype=torch.int32, device=dev)
+    pol = dict(policy=args.policy, window=args.defrag_window, decay=args.defrag_decay,
+               hist_window=args.history_window)
+    stream = torch.cuda.current_stream()
+    times, out = [], None
+    for i in range(args.warmup + args.steps):
+        moe.stream_setup(proj, x0, logits, delays, M, spec.stream_steps, hist, done, **pol)
+        s0 = moe.stats()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        st, ticks, comb = moe.stream_run(max_ticks=100000, check_every=16)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        assert st == 0, st
+        s1 = moe.stats()
+        if i >= args.warmup:
+            times.append(e0.elapsed_time(e1))
+            out = (ticks, comb, s1["expert_runs"] - s0["expert_runs"], s1["weight_bytes"] - s0["weight_bytes"],
+                   s1["kernel_launches"] - s0["kernel_launches"])
+    tr = moe.stream_trace()
+    dn = done.cpu().numpy()
+    moe.close()
+    ticks, comb, runs, wbytes, launches = out
+    lat = []
+    for r in range(R):
+        ts = [0] + [int(t) for t in dn[r, 1:] if t >= 0]
+        lat += list(np.diff(ts))
+    ms = float(np.median(times))
+    pairs = comb * lay.top_k
+    hbm, tf_burst, tf_sust, src = peaks()
+    exp_passes = int((tr[:, 1] == 2).sum())
+    att_passes = int((tr[:, 1] == 1).sum())
+    t_roof = (wbytes + att_passes * H * H * 2) / (hbm * 1e9)
+    line = {"metric": METRIC, "value": pairs / (ms / 1e3), "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": spec.name, "layers": NL, "requests": R, "stop_merges": spec.stream_steps,
+                       "policy": args.policy, "defrag_window": args.defrag_window,
+                       "defrag_decay": args.defrag_decay, "history_window": args.history_window},
+            "schedule": {"ticks": ticks, "merges": comb, "expert_passes": exp_passes, "attention_passes": att_passes,
+                         "expert_runs": runs, "weight_bytes": wbytes,
+                         "reread_vs_lockstep": exp_passes / max(1, -(-comb // R)),
+                         "step_latency_ticks_mean": float(np.mean(lat)),
+                         "step_latency_ticks_p99": float(np.percentile(lat, 99))},
+            "path_roofline": {"t_roof_ms": 1e3 * t_roof, "frac": 1e3 * t_roof / ms, "peak": hbm,
+                              "peak_source": src},
+            "gpu_launches": int(launches)}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     rank = int(os.environ.get("RANK", "0"))
@@ -263,6 +338,13 @@ def main():
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         return run_reference(args, rank, world)
+    from workloads import get_config as _gc
+    if _gc(args.workload).num_layers > 1:
+        import __graft_entry__ as g
+        g.build()
+        import asynchronous_expert_execution_gb300 as pkg
+        torch.cuda.set_device(local)
+        return run_stream(args, pkg, torch.device("cuda", local))
 
     import __graft_entry__ as g
     g.build()

@@ -214,10 +214,21 @@ moe_status moe_async_snapshot(moe_async_t h, int32_t layer, void* stream, int32_
  * attention before expert).  The attention stage is a stub: a = RMSNorm(x) P_l (eps 1e-6,
  * no gain), x^(n+1) = MoE_l(a) with l = n mod L.  All state lives on the device and one
  * scheduling decision ("tick") runs as a CUDA graph with no host round trip. */
+typedef enum {
+  MOE_STREAM_MTFS = 0,      /* most tokens first (StreamEP section 4)                             */
+  MOE_STREAM_FLFS = 1,      /* first layer first: earliest non-empty queue of the chain           */
+  MOE_STREAM_DEFRAG = 2,    /* S(s) = Q(s) + sum_{j=1..W} decay^j [Q(s_j) + H(s_j)] (section 4)   */
+  MOE_STREAM_BARRIER = 3    /* synchronous baseline: nothing served while a dispatch is in flight */
+} moe_stream_policy;
+
 typedef struct {
   int32_t num_requests;     /* R <= max_slots; request r uses combine slot r in every layer    */
   int32_t max_steps;        /* steps per request at most (history depth)                       */
   int32_t stop_combines;    /* attention queues are closed once this many merges are done      */
+  int32_t policy;           /* moe_stream_policy                                               */
+  int32_t defrag_window;    /* DEFRAG: W, queues looked ahead along att_0, exp_0, att_1, ...  */
+  int32_t history_window;   /* DEFRAG: H(s) = tokens drained from s over the last N ticks, <=16 */
+  double defrag_decay;      /* DEFRAG: decay per lookahead step (scores in fp64)               */
 } moe_stream_config;
 
 /* Set up the streaming runtime on a bf16 SwiGLU handle (its merges then feed the runtime,

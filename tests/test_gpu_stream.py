@@ -29,7 +29,7 @@ def pkg():
     return p
 
 
-def _gpu_stream(pkg, spec, M, seed=0, delay_seed=None, weights=None):
+def _gpu_stream(pkg, spec, M, seed=0, delay_seed=None, weights=None, policy="mtfs"):
     lay = spec.layer
     R, H, NL = spec.tokens, lay.hidden, spec.num_layers
     wl = make_stream_inputs(spec, seed, M, weights=False, delay_seed=delay_seed)
@@ -41,7 +41,8 @@ def _gpu_stream(pkg, spec, M, seed=0, delay_seed=None, weights=None):
     hist = torch.zeros((R, M + 1, H), dtype=torch.bfloat16, device="cuda")
     done = torch.empty((R, M + 1), dtype=torch.int32, device="cuda")
     delays = torch.as_tensor(wl.delays, dtype=torch.int32).cuda()
-    moe.stream_setup(proj, wl.x0.cuda(), wl.logits.cuda(), delays, M, spec.stream_steps, hist, done)
+    moe.stream_setup(proj, wl.x0.cuda(), wl.logits.cuda(), delays, M, spec.stream_steps, hist, done,
+                     policy=policy, window=2, decay=0.5, hist_window=8)
     st, ticks, comb = moe.stream_run(max_ticks=100000, check_every=16)
     trace = moe.stream_trace()
     stats = moe.stats()
@@ -50,7 +51,7 @@ def _gpu_stream(pkg, spec, M, seed=0, delay_seed=None, weights=None):
                 hist=hist.float().cpu().numpy().astype(np.float64), done=done.cpu().numpy())
 
 
-def _oracle_stream(spec, wl, weights, values, compute=None):
+def _oracle_stream(spec, wl, weights, values, compute=None, policy="mtfs"):
     lay = spec.layer
     lg = wl.logits.numpy()
     proj = [p.double().numpy() for p in wl.proj]
@@ -62,7 +63,8 @@ def _oracle_stream(spec, wl, weights, values, compute=None):
         return cache[(l, e)]
     return om.StreamOracle(spec.num_layers, lay.top_k, wl.x0.double().numpy(), lambda l: proj[l],
                            lambda r, n: lg[r, n], wl.delays, experts, spec.stream_steps, wl.max_steps,
-                           values=values, compute=compute).run()
+                           values=values, compute=compute, policy=policy, window=2, decay=0.5,
+                           hist_window=8).run()
 
 
 def _check_bookkeeping(res, sim):
@@ -135,3 +137,30 @@ def test_stream_c5_fullsize(pkg):
         ref = om.combine(contribs)
         errs.append(np.abs(res["hist"][r, 1] - ref).max() / np.abs(ref).max())
     assert max(errs) <= 2e-2, errs
+
+
+@pytest.mark.parametrize("policy", ["flfs", "defrag", "barrier"])
+def test_stream_small_policies(pkg, policy):
+    """Each layer-level policy: exact bookkeeping against the oracle, and values bit-identical
+    to the most-tokens-first run (the values do not depend on the schedule)."""
+    spec = get_config("s1")
+    M = 16
+    base = _gpu_stream(pkg, spec, M)
+    res = _gpu_stream(pkg, spec, M, policy=policy, weights=base["weights"])
+    assert res["status"] == 0
+    sim = _oracle_stream(spec, res["wl"], res["weights"], values=False, policy=policy)
+    _check_bookkeeping(res, sim)
+    na = (base["done"] >= 0).sum(1)
+    nb = (res["done"] >= 0).sum(1)
+    for r in range(spec.tokens):
+        for n in range(1, min(na[r], nb[r]) + 1):
+            assert np.array_equal(base["hist"][r, n], res["hist"][r, n]), (r, n)
+
+
+def test_stream_c5_defrag_fullsize(pkg):
+    spec = get_config("c5")
+    M = 64
+    res = _gpu_stream(pkg, spec, M, policy="defrag")
+    assert res["status"] == 0
+    sim = _oracle_stream(spec, res["wl"], res["weights"], values=False, policy="defrag")
+    _check_bookkeeping(res, sim)
