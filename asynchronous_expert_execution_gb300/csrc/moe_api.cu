@@ -166,7 +166,7 @@ __global__ void __launch_bounds__(1024) schedule_kernel(LayerView L, Dims d, Ste
 template <typename T>
 __global__ void collect_kernel(LayerView L, Dims d, int max_out, T* __restrict__ y_out,
                                int32_t* __restrict__ slot_out, uint32_t* __restrict__ gen_out,
-                               const int32_t* __restrict__ n_io, int append) {
+                               const int32_t* __restrict__ n_io, int append, int parts) {
   const uint32_t rh = L.ready_ht[0], rt = L.ready_ht[1];
   const int base = append ? *n_io : 0;
   const int n = max(0, min((int)(rt - rh), max_out - base));
@@ -177,6 +177,7 @@ __global__ void collect_kernel(LayerView L, Dims d, int max_out, T* __restrict__
     const int4* src = reinterpret_cast<const int4*>(static_cast<const T*>(L.y) + (size_t)slot * d.H);
     int4* dst = reinterpret_cast<int4*>(y_out + (size_t)(base + i) * d.H);
     for (int c = threadIdx.x; c < chunks; c += blockDim.x) dst[c] = __ldcg(src + c);
+    for (int p = threadIdx.x; p < parts; p += blockDim.x) L.done_part[(size_t)slot * parts + p] = 0u;
     __syncthreads();
     if (threadIdx.x == 0) {
       slot_out[base + i] = slot;
@@ -216,7 +217,7 @@ void free_handle(moe_async_s* h) {
   if (h->layers) {
     for (int l = 0; l < h->cfg.num_layers; ++l) {
       LayerView& L = h->layers[l];
-      void* ptrs[] = {L.pool, L.wtab, L.enq_mask, L.done, L.gen, L.slotbuf, L.y, L.records,
+      void* ptrs[] = {L.pool, L.wtab, L.enq_mask, L.done, L.done_part, L.gen, L.slotbuf, L.y, L.records,
                       L.head, L.tail, L.ready, L.ready_ht, const_cast<void*>(L.w13),
                       const_cast<void*>(L.w2)};
       for (void* p : ptrs) if (p) cudaFree(p);
@@ -366,6 +367,7 @@ moe_status moe_async_create(const moe_async_config* cfg, const void* const* w1,
     ok = ok && dalloc(&L.wtab, S * KS * 4) == cudaSuccess;
     ok = ok && dalloc(&L.enq_mask, S * 4) == cudaSuccess;
     ok = ok && dalloc(&L.done, S * 4) == cudaSuccess;
+    ok = ok && dalloc(&L.done_part, S * (size_t)h->parts_per_pair * 4) == cudaSuccess;
     ok = ok && dalloc(&L.gen, S * 4) == cudaSuccess;
     ok = ok && dalloc(&L.slotbuf, S * KS * H * 4) == cudaSuccess;
     ok = ok && dalloc(&L.y, S * H * es) == cudaSuccess;
@@ -386,6 +388,7 @@ moe_status moe_async_create(const moe_async_config* cfg, const void* const* w1,
     if (ok) {
       ok = cudaMemsetAsync(L.enq_mask, 0, S * 4, s) == cudaSuccess &&
            cudaMemsetAsync(L.done, 0, S * 4, s) == cudaSuccess &&
+           cudaMemsetAsync(L.done_part, 0, S * (size_t)h->parts_per_pair * 4, s) == cudaSuccess &&
            cudaMemsetAsync(L.gen, 0, S * 4, s) == cudaSuccess &&
            cudaMemsetAsync(L.head, 0, (size_t)d.NB * 4, s) == cudaSuccess &&
            cudaMemsetAsync(L.tail, 0, (size_t)d.NB * 4, s) == cudaSuccess &&
@@ -498,10 +501,10 @@ moe_status moe_async_collect(moe_async_t h, int32_t layer, int32_t max_out, void
   if (max_out > 0) {
     if (d.dtype == MOE_BF16)
       collect_kernel<__nv_bfloat16><<<grid, 128, 0, s>>>(h->layers[layer], d, max_out,
-          static_cast<__nv_bfloat16*>(d_y_out), d_slot_out, d_gen_out, d_n_out, append);
+          static_cast<__nv_bfloat16*>(d_y_out), d_slot_out, d_gen_out, d_n_out, append, h->parts_per_pair);
     else
       collect_kernel<float><<<grid, 128, 0, s>>>(h->layers[layer], d, max_out,
-          static_cast<float*>(d_y_out), d_slot_out, d_gen_out, d_n_out, append);
+          static_cast<float*>(d_y_out), d_slot_out, d_gen_out, d_n_out, append, h->parts_per_pair);
   }
   collect_finish_kernel<<<1, 1, 0, s>>>(h->layers[layer], d, h->counters, max_out, d_n_out, append);
   h->launches += max_out > 0 ? 1 : 0;

@@ -88,7 +88,7 @@ __global__ void __launch_bounds__(256) ffn1_simt_kernel(LayerView L, Dims d, con
 template <typename T>
 __global__ void __launch_bounds__(256) ffn2_simt_kernel(LayerView L, Dims d, DevCounters* C,
                                                         const StepPlan* __restrict__ P,
-                                                        const T* __restrict__ hbuf, int target) {
+                                                        const T* __restrict__ hbuf, int parts) {
   __shared__ float hs[kBT][kKC + 1];
   __shared__ float ws[kBH][kKC + 1];
   __shared__ int slot_s[kBT], k_s[kBT], fin[kBT];
@@ -146,14 +146,14 @@ __global__ void __launch_bounds__(256) ffn2_simt_kernel(LayerView L, Dims d, Dev
           L.slotbuf[((size_t)slot_s[j] * d.KS + k_s[j]) * d.H + f] = w_s[j] * acc[m];
       }
     }
-    land_and_merge<T>(L, d, C, slot_s, nj, target, tid, 256, fin, CtaBarrier{});
+    land_and_merge<T>(L, d, C, slot_s, nj, fti, parts, f0, kBH, tid, 256, fin, CtaBarrier{});
   }
 }
 
 // Identity experts: slotbuf[slot][k] = w * x (one part per pair), then landing and merges.
 template <typename T>
 __global__ void __launch_bounds__(256) identity_kernel(LayerView L, Dims d, DevCounters* C,
-                                                       const StepPlan* __restrict__ P, int target) {
+                                                       const StepPlan* __restrict__ P) {
   __shared__ int slot_s[kBT], k_s[kBT], fin[kBT];
   __shared__ float w_s[kBT];
   const int tid = threadIdx.x;
@@ -180,7 +180,7 @@ __global__ void __launch_bounds__(256) identity_kernel(LayerView L, Dims d, DevC
       float* dst = L.slotbuf + ((size_t)slot_s[j] * d.KS + k_s[j]) * d.H;
       for (int f = tid; f < d.H; f += 256) dst[f] = w_s[j] * to_f(src[f]);
     }
-    land_and_merge<T>(L, d, C, slot_s, nj, target, tid, 256, fin, CtaBarrier{});
+    land_and_merge<T>(L, d, C, slot_s, nj, 0, 1, 0, d.H, tid, 256, fin, CtaBarrier{});
   }
 }
 
@@ -192,7 +192,7 @@ moe_status launch_ffn_simt(moe_async_s* h, int layer, cudaStream_t s) {
   const Dims& d = h->dims;
   const LayerView& L = h->layers[layer];
   const int grid = h->num_sms * 4;
-  const int target = d.KS * h->parts_per_pair;
+  const int parts = h->parts_per_pair;
   prof_begin(h, MOE_KERNEL_FFN1, s);
   if (d.dtype == MOE_BF16)
     ffn1_simt_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(L, d, h->plan, static_cast<__nv_bfloat16*>(h->h));
@@ -202,10 +202,10 @@ moe_status launch_ffn_simt(moe_async_s* h, int layer, cudaStream_t s) {
   prof_begin(h, MOE_KERNEL_FFN2, s);
   if (d.dtype == MOE_BF16)
     ffn2_simt_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(L, d, h->counters, h->plan,
-                                                          static_cast<const __nv_bfloat16*>(h->h), target);
+                                                          static_cast<const __nv_bfloat16*>(h->h), parts);
   else
     ffn2_simt_kernel<float><<<grid, 256, 0, s>>>(L, d, h->counters, h->plan,
-                                                  static_cast<const float*>(h->h), target);
+                                                  static_cast<const float*>(h->h), parts);
   prof_end(h, MOE_KERNEL_FFN2, s);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
@@ -213,12 +213,11 @@ moe_status launch_ffn_simt(moe_async_s* h, int layer, cudaStream_t s) {
 moe_status launch_identity(moe_async_s* h, int layer, cudaStream_t s) {
   const Dims& d = h->dims;
   const int grid = h->num_sms * 4;
-  const int target = d.KS;
   prof_begin(h, MOE_KERNEL_FFN1, s);
   if (d.dtype == MOE_BF16)
-    identity_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(h->layers[layer], d, h->counters, h->plan, target);
+    identity_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(h->layers[layer], d, h->counters, h->plan);
   else
-    identity_kernel<float><<<grid, 256, 0, s>>>(h->layers[layer], d, h->counters, h->plan, target);
+    identity_kernel<float><<<grid, 256, 0, s>>>(h->layers[layer], d, h->counters, h->plan);
   prof_end(h, MOE_KERNEL_FFN1, s);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

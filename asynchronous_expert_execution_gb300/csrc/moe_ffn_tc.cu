@@ -103,6 +103,12 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   return p;
 }
 
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
                : "memory");
@@ -210,7 +216,7 @@ struct TcParams {
   DevCounters* C;
   const StepPlan* P;
   __nv_bfloat16* hbuf;
-  int target;                       // landing target per token (GEMM2)
+  int parts;                        // feature slices per token (GEMM2 tiles covering H)
   int stream_on;                    // GEMM2 merges feed the streaming runtime
   StreamDev sd;
 };
@@ -223,6 +229,7 @@ struct Tile {
   int j0;       // first token of the tile within the item
   int nj;       // valid tokens
   int nmma;     // MMA N (multiple of 16, >= nj)
+  bool single;  // the item has one token tile: its A rows are read once
 };
 
 template <int BN, int MODE>
@@ -245,6 +252,7 @@ __device__ __forceinline__ Tile decode_tile(const TcParams& p, int t) {
     tl.row_base = it.row_base;
   }
   const int ntt = (count + BN - 1) / BN;
+  tl.single = ntt <= 1;
   tl.fti = local / ntt;
   tl.j0 = (local % ntt) * BN;
   tl.nj = min(BN, count - tl.j0);
@@ -310,6 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
   const CUtensorMap* tmA = &p.mapA[layer < 0 || layer >= kMaxLayers ? 0 : layer];
   const int Kdim = MODE == kModeGemm2 ? d.I : d.H;
   const int nk = (Kdim + kBK - 1) / kBK;
+  if ((int)blockIdx.x >= n_tiles) return;        // no tile for this CTA: skip all set-up
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -335,11 +344,16 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
   if (warp == 0) {
     // ------------------------------------------------ A producer: TMA of weight tiles
     if (lane == 0) {
-      const uint64_t pol = policy_evict_first();
+      // weights read by one token tile only are streamed with L2 evict-first; tiles whose A
+      // rows are shared by several token tiles (a popular expert) keep the normal policy so
+      // the concurrent readers hit L2
+      const uint64_t pol_stream = policy_evict_first();
+      const uint64_t pol_reuse = policy_evict_normal();
       uint32_t it = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
         const Tile tl = decode_tile<BN, MODE>(p, t);
+        const uint64_t pol = tl.single ? pol_stream : pol_reuse;
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1u;
@@ -511,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[buf]);
       if (MODE == kModeGemm2)
-        land_and_merge<__nv_bfloat16>(L, d, C, slot_s, tl.nj, p.target, et, 128, fin, EpiBarrier{},
+        land_and_merge<__nv_bfloat16>(L, d, C, slot_s, tl.nj, tl.fti, p.parts, tl.fti * kBM, kBM, et, 128, fin, EpiBarrier{},
                                       p.stream_on ? &p.sd : nullptr, layer);
       else if (MODE == kModeAtt)
         asm volatile("bar.sync 1, 128;" ::: "memory");   // slot_s / w_s reused by the next tile
@@ -585,7 +599,7 @@ void fill_common(moe_async_s* h, TcParams& p) {
   p.C = h->counters;
   p.P = h->plan;
   p.hbuf = static_cast<__nv_bfloat16*>(h->h);
-  p.target = h->dims.KS * h->parts_per_pair;
+  p.parts = h->parts_per_pair;
   p.stream_on = 0;
 }
 

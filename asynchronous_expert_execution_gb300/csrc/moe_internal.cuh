@@ -65,7 +65,8 @@ struct LayerView {
   void* pool;
   float* wtab;
   uint32_t* enq_mask;
-  uint32_t* done;
+  uint32_t* done;       // [S] feature slices merged (target = parts)
+  uint32_t* done_part;  // [S][parts] results landed per feature slice (target = KS)
   uint32_t* gen;
   float* slotbuf;
   void* y;
@@ -242,28 +243,6 @@ __device__ __forceinline__ int32_t record_at(const LayerView& L, const Dims& d, 
   return L.records[(size_t)e * d.cap + (pos % (uint32_t)d.cap)];
 }
 
-// Merge of one token whose K (+shared) results have all landed: y[slot] = sum over k in
-// ascending order of slotbuf[slot][k] (StreamEP section 3: y = sum_j w_j E_j(x)), then
-// publish the slot on the ready ring.  Called by `nthr` threads of one CTA (thread index
-// `tid`), all of which must call it; the caller has made the landing visible (fence +
-// barrier) before.  Reads of other CTAs' slot rows go through L2 (ld.global.cg).
-template <typename T>
-__device__ void merge_token(const LayerView& L, const Dims& d, DevCounters* C, int slot,
-                            int tid, int nthr, T* dst2 = nullptr) {
-  const float* src = L.slotbuf + (size_t)slot * d.KS * d.H;
-  T* dst = reinterpret_cast<T*>(L.y) + (size_t)slot * d.H;
-  for (int f = tid * 4; f < d.H; f += nthr * 4) {     // H % 8 == 0
-    float4 acc = __ldcg(reinterpret_cast<const float4*>(src + f));
-    for (int k = 1; k < d.KS; ++k) {
-      float4 v = __ldcg(reinterpret_cast<const float4*>(src + (size_t)k * d.H + f));
-      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
-    }
-    const T o0 = from_f<T>(acc.x), o1 = from_f<T>(acc.y), o2 = from_f<T>(acc.z), o3 = from_f<T>(acc.w);
-    dst[f + 0] = o0; dst[f + 1] = o1; dst[f + 2] = o2; dst[f + 3] = o3;
-    if (dst2) { dst2[f + 0] = o0; dst2[f + 1] = o1; dst2[f + 2] = o2; dst2[f + 3] = o3; }
-  }
-}
-
 // Streaming runtime: request r finished its step at `layer` (its merged output is already in
 // hist[r][n+1]).  Advance its step count, record the tick, reclaim its slot in this layer,
 // and queue it for the next layer's attention stage unless it reached its last step.
@@ -413,31 +392,56 @@ struct CtaBarrier {
 // its merge (acquire fence, then reads through L2) and publishes it on the ready ring
 // ("inferred obligations": readiness only after the payload is visible).  `bar` is a
 // barrier over exactly these threads; `fin` is scratch of >= nj ints visible to them.
+//
+// The merge is split by feature slice: a tile covering features [f0, f0 + fcount) (slice
+// `part` of `parts`) counts, per token, the results landed in that slice; the tile that
+// completes a slice (all KS results) sums that slice (ascending k) into y, and the slice
+// merges are counted per token in turn -- the last one publishes the token.  So the merge
+// work of a token is spread over the CTAs of its slices instead of falling on one.
 template <typename T, typename Bar>
 __device__ void land_and_merge(const LayerView& L, const Dims& d, DevCounters* C,
-                               const int* slots, int nj, int target, int tid, int nthr,
-                               int* fin, Bar bar, const StreamDev* sd = nullptr, int layer = 0) {
+                               const int* slots, int nj, int part, int parts, int f0, int fcount,
+                               int tid, int nthr, int* fin, Bar bar, const StreamDev* sd = nullptr,
+                               int layer = 0) {
   __threadfence();
   bar();
   for (int j = tid; j < nj; j += nthr) {
-    const uint32_t old = atomicAdd(&L.done[slots[j]], 1u);
-    fin[j] = (old + 1u == (uint32_t)target);
-    if (old + 1u > (uint32_t)target) set_error(C, MOE_ERR_DUPLICATE);
+    const uint32_t old = atomicAdd(&L.done_part[(size_t)slots[j] * parts + part], 1u);
+    fin[j] = (old + 1u == (uint32_t)d.KS);
+    if (old + 1u > (uint32_t)d.KS) set_error(C, MOE_ERR_DUPLICATE);
   }
   __threadfence();
   bar();
+  const int fend = min(f0 + fcount, d.H);
   for (int j = 0; j < nj; ++j) {
     if (fin[j]) {                                    // uniform across the group
-      T* hist_row = nullptr;
-      if (sd)
-        hist_row = static_cast<T*>(sd->hist) +
-                   ((size_t)slots[j] * (sd->n_max + 1) + sd->req_n[slots[j]] + 1) * d.H;
-      merge_token<T>(L, d, C, slots[j], tid, nthr, hist_row);
-      if (sd) {
-        bar();                                       // every thread has read req_n
-        if (tid == 0) stream_complete(L, C, *sd, layer, slots[j]);
-      } else if (tid == 0) {
-        publish_ready(L, d, C, slots[j]);
+      const int slot = slots[j];
+      const float* src = L.slotbuf + (size_t)slot * d.KS * d.H;
+      T* dst = reinterpret_cast<T*>(L.y) + (size_t)slot * d.H;
+      T* dst2 = nullptr;
+      if (sd)                                        // req_n is stable until the last slice
+        dst2 = static_cast<T*>(sd->hist) + ((size_t)slot * (sd->n_max + 1) + sd->req_n[slot] + 1) * d.H;
+      for (int f = f0 + tid; f < fend; f += nthr) {
+        float acc = __ldcg(src + f);
+        for (int k = 1; k < d.KS; ++k) acc += __ldcg(src + (size_t)k * d.H + f);
+        const T o = from_f<T>(acc);
+        dst[f] = o;
+        if (dst2) dst2[f] = o;
+      }
+    }
+  }
+  __threadfence();
+  bar();
+  for (int j = tid; j < nj; j += nthr) {
+    if (fin[j]) {
+      const uint32_t old = atomicAdd(&L.done[slots[j]], 1u);
+      if (old + 1u == (uint32_t)parts) {             // every slice merged: publish
+        if (sd) {
+          for (int p = 0; p < parts; ++p) L.done_part[(size_t)slots[j] * parts + p] = 0u;
+          stream_complete(L, C, *sd, layer, slots[j]);
+        } else {
+          publish_ready(L, d, C, slots[j]);
+        }
       }
     }
   }

@@ -187,6 +187,12 @@ class Pass:
                 nxt += 1
             moe.schedule_step(0, self.policy)
             moe.collect(0, self.y, self.slots, self.n, append=True)
+        if self.policy.kind != "mtfs" or self.policy.max_groups > 0:
+            # a policy that may leave buckets behind after the last arrival keeps stepping
+            # until every token is merged (this reads the device counters: host syncs)
+            st = moe.wait(0, self.policy, max_steps=100000, check_every=8)
+            assert st == 0, st
+            moe.collect(0, self.y, self.slots, self.n, append=True)
 
 
 # ------------------------------------------------------------ CPU baseline

@@ -97,6 +97,11 @@ TEST_CONFIGS = {
     "p1": WorkloadSpec(
         name="p1_gptoss_slice", layer=GPT_OSS_LAYER.__class__(32, 4, 2880, 2880, "bf16"), tokens=64,
         router="uniform", waves="even", num_waves=4, arrival="index", policy="mtfs"),
+    # profiling-sized slice of the skewed prefill layer: 32 GPT-OSS experts, Zipf(1.2)
+    # popularity, 2048 tokens -- the popular experts get hundreds of rows per step.
+    "p3": WorkloadSpec(
+        name="p3_gptoss_prefill_slice", layer=GPT_OSS_LAYER.__class__(32, 4, 2880, 2880, "bf16"), tokens=2048,
+        router="zipf", zipf_s=1.2, waves="even", num_waves=4, arrival="index", policy="mtfs"),
     # streaming multi-layer decode, small: 4 layers, ragged H (2.5 tiles of 128), 48 requests.
     "s1": WorkloadSpec(
         name="s1_stream_small", layer=LayerSpec(16, 4, 320, 192, "bf16"), tokens=48, router="uniform",
