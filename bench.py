@@ -135,6 +135,19 @@ def traffic_for(kernel):
     return None if k is None else k.get("bytes_per_launch_full_size")
 
 
+def aggregate(ms_local, units_per_step, steps, world, device):
+    """Whole-job throughput over `world` ranks that each processed `units_per_step` units per
+    step for `steps` steps: the slowest rank's time sets the clock (max over ranks), the units
+    of all ranks count.  Returns (ms_max, units_per_second)."""
+    ms = float(ms_local)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms, world * units_per_step * steps / (ms / 1e3)
+
+
 # ---------------------------------------------------------------- workload
 
 def build_inputs(spec, seed, dev):
@@ -400,17 +413,12 @@ def main():
     ev1.record(stream)
     barrier()
     clk = clocks.stop()
-    ms = ev0.elapsed_time(ev1)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    routed_pairs_step = spec.tokens * L.top_k
+    ms, value = aggregate(ev0.elapsed_time(ev1), routed_pairs_step, args.steps, world, dev)
     s1 = moe.stats()
     assert s1["error"] == 0 and int(run.n.item()) == spec.tokens
     pairs_step = (s1["pairs_executed"] - s0["pairs_executed"]) / args.steps
-    routed_pairs_step = spec.tokens * L.top_k
     launches = (s1["kernel_launches"] - s0["kernel_launches"]) + args.steps   # + one route per step
-    value = world * routed_pairs_step * args.steps / (ms / 1e3)
 
     # per-kernel durations: a second pass of K steps with every launch bracketed by events
     moe.profile(True)
@@ -466,14 +474,10 @@ def main():
         sh.copy_(run.slots, non_blocking=True)
     e1.record(stream)
     barrier()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms, e2e_value = aggregate(e0.elapsed_time(e1), routed_pairs_step, args.e2e_steps, world, dev)
     h2d = xh.numel() * xh.element_size() + lh.numel() * lh.element_size()
     d2h = yh.numel() * yh.element_size() + sh.numel() * sh.element_size()
-    e2e = {"value": world * routed_pairs_step * args.e2e_steps / (e2e_ms / 1e3), "unit": UNIT,
+    e2e = {"value": e2e_value, "unit": UNIT,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps}
 
     cpu = None
