@@ -19,7 +19,8 @@ EXPORTS = ("moe_async_create", "moe_async_route", "moe_async_enqueue", "moe_asyn
            "moe_async_collect", "moe_async_wait", "moe_async_sync", "moe_async_get_stats",
            "moe_async_get_trace", "moe_async_snapshot", "moe_async_destroy",
            "moe_async_status_string", "moe_async_profile", "moe_async_profile_read",
-           "moe_async_stream_setup", "moe_async_stream_run", "moe_async_stream_trace")
+           "moe_async_stream_setup", "moe_async_stream_run", "moe_async_stream_trace",
+           "moe_async_cancel")
 
 KERNEL_KINDS = ("enqueue", "schedule", "ffn1", "ffn2", "collect")
 
@@ -41,7 +42,7 @@ class Stats(ctypes.Structure):
                 ("stale", ctypes.c_int64), ("open_tokens", ctypes.c_int32),
                 ("pending_pairs", ctypes.c_int32), ("ready", ctypes.c_int32),
                 ("error", ctypes.c_int32), ("packed_weight_bytes", ctypes.c_int64),
-                ("kernel_launches", ctypes.c_int64)]
+                ("kernel_launches", ctypes.c_int64), ("cancelled", ctypes.c_int64)]
 
 
 class StreamConfig(ctypes.Structure):
@@ -85,6 +86,7 @@ def load():
         "moe_async_snapshot": [P, I32, P, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32),
                                I32, ctypes.POINTER(ctypes.c_int32)],
         "moe_async_destroy": [P, P],
+        "moe_async_cancel": [P, I32, I32, I32P, P],
         "moe_async_profile": [P, I32],
         "moe_async_profile_read": [P, P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64), I32],
         "moe_async_status_string": [ctypes.c_int],

@@ -106,6 +106,11 @@ class MoEAsync:
                                         _ptr(n_out), int(append), _stream(stream))
         N.check(st, "moe_async_collect")
 
+    def cancel(self, layer, slots, stream=None):
+        """Retire the current request of each slot (int32 device tensor of slot ids)."""
+        N.check(self.lib.moe_async_cancel(self.h, layer, slots.numel(), _ptr(slots), _stream(stream)),
+                "moe_async_cancel")
+
     def wait(self, layer, policy, max_steps=1000, check_every=4, stream=None):
         p = policy.c()
         return self.lib.moe_async_wait(self.h, layer, ctypes.byref(p), max_steps, check_every, _stream(stream))

@@ -106,6 +106,7 @@ __global__ void enqueue_kernel(LayerView L, Dims d, DevCounters* C, int n,
         e = expert[(size_t)row * d.K + k];
         if (e < 0 || e >= d.E) { set_error(C, MOE_ERR_INVALID); ok = false; }
       }
+      if (ok && (L.enq_mask[slot] & kRetired)) ok = false;   // late pair of a cancelled request
       if (ok) {
         const uint32_t bit = 1u << k;
         const uint32_t old = atomicOr(&L.enq_mask[slot], bit);
@@ -184,8 +185,35 @@ __global__ void collect_kernel(LayerView L, Dims d, int max_out, T* __restrict__
       if (gen_out) gen_out[base + i] = L.gen[slot];
       L.enq_mask[slot] = 0u;
       L.done[slot] = 0u;
+      L.landed[slot] = 0u;
       L.gen[slot] = L.gen[slot] + 1u;
     }
+  }
+}
+
+// ----------------------------------------------------------- cancellation
+// Retire the current request of each listed slot ("asynchronous MoE serving" notes: an
+// abandoned operation retires its buffer until a quiescent point; CascadeEP: readiness is
+// tracked apart from reclamation).  A retired slot accepts no more pairs, is never merged
+// or published, and is freed -- generation advanced -- when its last accepted result has
+// landed (at once if none is queued).  Free slots and already merged ones are left alone.
+__global__ void cancel_kernel(LayerView L, Dims d, DevCounters* C, int n, const int32_t* __restrict__ slots,
+                              int parts) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+    const int slot = slots[i];
+    if (slot < 0 || slot >= d.S) { set_error(C, MOE_ERR_INVALID); continue; }
+    if (L.done[slot] == (uint32_t)parts) continue;              // merged already: too late
+    uint32_t old = L.enq_mask[slot];
+    bool mine = false;
+    while (old != 0u && !(old & kRetired)) {                      // duplicates in the list: one wins
+      const uint32_t prev = atomicCAS(&L.enq_mask[slot], old, old | kRetired);
+      if (prev == old) { mine = true; break; }
+      old = prev;
+    }
+    if (!mine) continue;
+    atomicSub(&C->open_tokens, 1);
+    atomicAdd(&C->cancelled, 1ull);
+    if (retired_quiescent(old | kRetired, L.landed[slot], parts)) reclaim_slot(L, parts, slot);
   }
 }
 
@@ -217,7 +245,7 @@ void free_handle(moe_async_s* h) {
   if (h->layers) {
     for (int l = 0; l < h->cfg.num_layers; ++l) {
       LayerView& L = h->layers[l];
-      void* ptrs[] = {L.pool, L.wtab, L.enq_mask, L.done, L.done_part, L.gen, L.slotbuf, L.y, L.records,
+      void* ptrs[] = {L.pool, L.wtab, L.enq_mask, L.done, L.done_part, L.landed, L.gen, L.slotbuf, L.y, L.records,
                       L.head, L.tail, L.ready, L.ready_ht, const_cast<void*>(L.w13),
                       const_cast<void*>(L.w2)};
       for (void* p : ptrs) if (p) cudaFree(p);
@@ -368,6 +396,7 @@ moe_status moe_async_create(const moe_async_config* cfg, const void* const* w1,
     ok = ok && dalloc(&L.enq_mask, S * 4) == cudaSuccess;
     ok = ok && dalloc(&L.done, S * 4) == cudaSuccess;
     ok = ok && dalloc(&L.done_part, S * (size_t)h->parts_per_pair * 4) == cudaSuccess;
+    ok = ok && dalloc(&L.landed, S * 4) == cudaSuccess;
     ok = ok && dalloc(&L.gen, S * 4) == cudaSuccess;
     ok = ok && dalloc(&L.slotbuf, S * KS * H * 4) == cudaSuccess;
     ok = ok && dalloc(&L.y, S * H * es) == cudaSuccess;
@@ -389,6 +418,7 @@ moe_status moe_async_create(const moe_async_config* cfg, const void* const* w1,
       ok = cudaMemsetAsync(L.enq_mask, 0, S * 4, s) == cudaSuccess &&
            cudaMemsetAsync(L.done, 0, S * 4, s) == cudaSuccess &&
            cudaMemsetAsync(L.done_part, 0, S * (size_t)h->parts_per_pair * 4, s) == cudaSuccess &&
+           cudaMemsetAsync(L.landed, 0, S * 4, s) == cudaSuccess &&
            cudaMemsetAsync(L.gen, 0, S * 4, s) == cudaSuccess &&
            cudaMemsetAsync(L.head, 0, (size_t)d.NB * 4, s) == cudaSuccess &&
            cudaMemsetAsync(L.tail, 0, (size_t)d.NB * 4, s) == cudaSuccess &&
@@ -550,6 +580,7 @@ moe_status moe_async_get_stats(moe_async_t h, void* stream, moe_async_stats* out
   out->tokens_combined = (int64_t)c.tokens_combined;
   out->duplicates = (int64_t)c.duplicates;
   out->stale = (int64_t)c.stale;
+  out->cancelled = (int64_t)c.cancelled;
   out->open_tokens = c.open_tokens;
   out->pending_pairs = c.pending_pairs;
   out->ready = c.ready;
@@ -635,6 +666,19 @@ moe_status moe_async_snapshot(moe_async_t h, int32_t layer, void* stream, int32_
   std::free(tail);
   std::free(recs);
   return st;
+}
+
+moe_status moe_async_cancel(moe_async_t h, int32_t layer, int32_t n, const int32_t* d_slots, void* stream) {
+  if (!valid_stream_layer(h, layer) || n < 0) return MOE_ERR_INVALID;
+  if (h->stream_state) return MOE_ERR_UNSUPPORTED;
+  if (n == 0) return MOE_OK;
+  if (!d_slots) return MOE_ERR_INVALID;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  prof_begin(h, MOE_KERNEL_ENQUEUE, s);
+  cancel_kernel<<<(n + 255) / 256, 256, 0, s>>>(h->layers[layer], h->dims, h->counters, n, d_slots,
+                                                h->parts_per_pair);
+  prof_end(h, MOE_KERNEL_ENQUEUE, s);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 moe_status moe_async_destroy(moe_async_t h, void* stream) {

@@ -32,6 +32,7 @@ constexpr int kMaxExperts = 1024;
 constexpr int kMaxBuckets = kMaxExperts + 1;
 constexpr int kKShift = 5;            // record = slot << 5 | k
 constexpr int kKMask = 31;
+constexpr uint32_t kRetired = 1u << 31;   // enq_mask flag: the slot's request was cancelled
 
 struct WorkItem {
   int32_t expert;     // bucket id (E = shared expert)
@@ -54,7 +55,7 @@ struct StepPlan {
 
 struct DevCounters {
   unsigned long long steps, pairs_executed, expert_runs, weight_bytes, tokens_combined;
-  unsigned long long duplicates, stale;
+  unsigned long long duplicates, stale, cancelled;
   int32_t open_tokens, pending_pairs, ready;
   uint32_t error;
   int32_t trace_n;
@@ -67,6 +68,7 @@ struct LayerView {
   uint32_t* enq_mask;
   uint32_t* done;       // [S] feature slices merged (target = parts)
   uint32_t* done_part;  // [S][parts] results landed per feature slice (target = KS)
+  uint32_t* landed;     // [S] results landed over all slices (for retirement)
   uint32_t* gen;
   float* slotbuf;
   void* y;
@@ -253,6 +255,7 @@ __device__ __forceinline__ void stream_complete(const LayerView& L, DevCounters*
   sd.done_tick[(size_t)r * (sd.n_max + 1) + n] = sd.ctl->tick;
   L.enq_mask[r] = 0u;
   L.done[r] = 0u;
+  L.landed[r] = 0u;
   L.gen[r] = L.gen[r] + 1u;
   atomicAdd(&sd.ctl->combined, 1);
   atomicSub(&C->open_tokens, 1);
@@ -262,6 +265,21 @@ __device__ __forceinline__ void stream_complete(const LayerView& L, DevCounters*
     const uint32_t pos = atomicAdd(&sd.att_ht[2 * l2 + 1], 1u);
     sd.att_ring[(size_t)l2 * sd.R + (pos % (uint32_t)sd.R)] = r;
   }
+}
+
+// Free a slot: clear every per-request counter and advance its generation.
+__device__ __forceinline__ void reclaim_slot(const LayerView& L, int parts, int slot) {
+  for (int p = 0; p < parts; ++p) L.done_part[(size_t)slot * parts + p] = 0u;
+  L.done[slot] = 0u;
+  L.landed[slot] = 0u;
+  L.enq_mask[slot] = 0u;
+  L.gen[slot] = L.gen[slot] + 1u;
+}
+
+// A cancelled (retired) slot is freed only when every result it accepted has landed: until
+// then records of its request may still sit in the queues ("retire until quiescent").
+__device__ __forceinline__ bool retired_quiescent(uint32_t mask, uint32_t landed, int parts) {
+  return (mask & kRetired) && landed == (uint32_t)__popc(mask & ~kRetired) * (uint32_t)parts;
 }
 
 __device__ __forceinline__ void publish_ready(const LayerView& L, const Dims& d, DevCounters* C, int slot) {
@@ -406,9 +424,13 @@ __device__ void land_and_merge(const LayerView& L, const Dims& d, DevCounters* C
   __threadfence();
   bar();
   for (int j = tid; j < nj; j += nthr) {
-    const uint32_t old = atomicAdd(&L.done_part[(size_t)slots[j] * parts + part], 1u);
-    fin[j] = (old + 1u == (uint32_t)d.KS);
+    const int slot = slots[j];
+    const uint32_t mask = L.enq_mask[slot];              // stable during a step
+    const uint32_t old = atomicAdd(&L.done_part[(size_t)slot * parts + part], 1u);
+    const uint32_t landed = atomicAdd(&L.landed[slot], 1u) + 1u;
+    fin[j] = (old + 1u == (uint32_t)d.KS) && !(mask & kRetired);
     if (old + 1u > (uint32_t)d.KS) set_error(C, MOE_ERR_DUPLICATE);
+    if (retired_quiescent(mask, landed, parts)) reclaim_slot(L, parts, slot);   // last landing
   }
   __threadfence();
   bar();

@@ -101,6 +101,7 @@ typedef struct {
   int32_t error;            /* sticky device error (moe_status)                                */
   int64_t packed_weight_bytes; /* library-owned packed weight copy made at create              */
   int64_t kernel_launches;  /* kernels this handle has launched since create                   */
+  int64_t cancelled;        /* requests retired by moe_async_cancel                            */
 } moe_async_stats;
 
 /* Kernel kinds timed by moe_async_profile (index into the arrays of moe_async_profile_read). */
@@ -179,6 +180,17 @@ moe_status moe_async_schedule_step(moe_async_t h, int32_t layer, const moe_async
 moe_status moe_async_collect(moe_async_t h, int32_t layer, int32_t max_out, void* d_y_out,
                              int32_t* d_slot_out, uint32_t* d_gen_out, int32_t* d_n_out,
                              int32_t append, void* stream);
+
+/* Cancel the current request of each slot in d_slots[0..n) (int32, device) of `layer`.
+ * "asynchronous MoE serving" notes: an abandoned operation retires its buffer until a quiescent
+ * point, and output readiness is tracked separately from buffer reclamation (CascadeEP).  The
+ * slot is retired: later pairs for it are dropped on arrival, pairs already queued still run
+ * but their results are neither merged nor published, and the slot is freed (generation
+ * advanced, reusable) when its last queued result has landed -- at once if nothing is queued.
+ * Free slots and slots whose output is already merged are left unchanged.  Not available on a
+ * handle running the streaming runtime (MOE_ERR_UNSUPPORTED). */
+moe_status moe_async_cancel(moe_async_t h, int32_t layer, int32_t n, const int32_t* d_slots,
+                            void* stream);
 
 /* Run scheduling steps of `layer` under `policy` until no token of the handle is open
  * (accepted but not yet combined, in any layer), checking the device counters every `check_every` steps;

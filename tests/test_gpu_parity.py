@@ -277,3 +277,89 @@ def test_empty_inputs(pkg):
     i0, w0 = pkg.route(e0, 2)
     assert i0.shape == (0, 2)
     moe.close()
+
+
+# ------------------------------------------------------------- cancellation
+
+def _ident(pkg, T=64, E=8, K=2, H=64):
+    moe = pkg.MoEAsync(E, K, H, 64, torch.float32, T, expert_kind="identity")
+    rng = np.random.default_rng(21)
+    x = torch.tensor(rng.integers(-8, 8, size=(T, H)).astype(np.float32)).cuda()
+    idx = torch.tensor(np.stack([rng.permutation(E)[:K] for _ in range(T)]).astype(np.int32)).cuda()
+    w = torch.tensor((rng.integers(1, 3, size=(T, K)) / 4.0).astype(np.float32)).cuda()
+    return moe, x, idx, w
+
+
+def _collect_all(moe, T, H):
+    y = torch.empty((T, H), dtype=torch.float32, device="cuda")
+    slots = torch.empty(T, dtype=torch.int32, device="cuda")
+    gens = torch.empty(T, dtype=torch.int32, device="cuda")
+    n = torch.zeros(1, dtype=torch.int32, device="cuda")
+    moe.collect(0, y, slots, n, gen_out=gens)
+    k = int(n.item())
+    return slots[:k].cpu().numpy(), y[:k].cpu().numpy(), gens[:k].cpu().numpy()
+
+
+def test_cancel_withheld_request_then_reuse(pkg):
+    """A request whose second pair never comes is cancelled: the others complete, its slot is
+    freed once its queued pair has run, and a new request then uses the slot cleanly."""
+    T, H = 64, 64
+    moe, x, idx, w = _ident(pkg, T=T, H=H)
+    kmask = torch.full((T,), 3, dtype=torch.int32, device="cuda")
+    kmask[5] = 1                                                   # pair k = 1 of token 5 withheld
+    moe.enqueue(0, x, idx, w, kmask=kmask)
+    moe.cancel(0, torch.tensor([5], dtype=torch.int32, device="cuda"))
+    assert moe.wait(0, pkg.Policy(), max_steps=8) == 0             # nothing open after the cancel
+    slots, y, gens = _collect_all(moe, T, H)
+    assert sorted(slots.tolist()) == [t for t in range(T) if t != 5]
+    st = moe.stats()
+    assert st["cancelled"] == 1 and st["open_tokens"] == 0 and st["error"] == 0
+    # the slot was reclaimed after its queued pair ran: generation 1 takes it
+    x2 = (x[5:6] * 2 + 1).contiguous()
+    moe.enqueue(0, x2, idx[5:6].contiguous(), w[5:6].contiguous(), slots=torch.tensor([5], dtype=torch.int32, device="cuda"),
+                gen=torch.ones(1, dtype=torch.int32, device="cuda"))
+    assert moe.wait(0, pkg.Policy(), max_steps=8) == 0
+    slots, y, gens = _collect_all(moe, T, H)
+    assert slots.tolist() == [5] and gens.tolist() == [1]
+    want = w[5].sum().item() * x2[0].cpu().numpy()
+    assert np.array_equal(y[0], want)                              # no trace of the old request
+    # the old request's late pair is stale now
+    moe.enqueue(0, x, idx, w, rows=torch.tensor([5], dtype=torch.int32, device="cuda"),
+                kmask=torch.tensor([2], dtype=torch.int32, device="cuda"),
+                gen=torch.zeros(1, dtype=torch.int32, device="cuda"))
+    assert moe.sync() == 4
+    moe.close()
+
+
+def test_cancel_queued_requests_are_not_published(pkg):
+    T, H = 64, 64
+    moe, x, idx, w = _ident(pkg, T=T, H=H)
+    moe.enqueue(0, x, idx, w)
+    moe.cancel(0, torch.tensor([3, 7, 7], dtype=torch.int32, device="cuda"))   # duplicate id: once
+    assert moe.wait(0, pkg.Policy(), max_steps=8) == 0
+    slots, y, _ = _collect_all(moe, T, H)
+    assert sorted(slots.tolist()) == [t for t in range(T) if t not in (3, 7)]
+    xs, ws = x.cpu().numpy().astype(np.float64), w.cpu().numpy().astype(np.float64)
+    for s, row in zip(slots, y):
+        assert np.array_equal(row, ws[s].sum() * xs[s])
+    st = moe.stats()
+    assert st["cancelled"] == 2 and st["error"] == 0
+    # both slots are free again (generation 1)
+    moe.enqueue(0, x, idx, w, rows=torch.tensor([3, 7], dtype=torch.int32, device="cuda"),
+                gen=torch.ones(2, dtype=torch.int32, device="cuda"))
+    assert moe.wait(0, pkg.Policy(), max_steps=8) == 0
+    slots, y, gens = _collect_all(moe, T, H)
+    assert sorted(slots.tolist()) == [3, 7] and gens.tolist() == [1, 1]
+    moe.close()
+
+
+def test_cancel_after_merge_is_too_late(pkg):
+    T, H = 64, 64
+    moe, x, idx, w = _ident(pkg, T=T, H=H)
+    moe.enqueue(0, x, idx, w)
+    assert moe.wait(0, pkg.Policy(), max_steps=8) == 0
+    moe.cancel(0, torch.tensor([2], dtype=torch.int32, device="cuda"))
+    slots, _, _ = _collect_all(moe, T, H)
+    assert sorted(slots.tolist()) == list(range(T))
+    assert moe.stats()["cancelled"] == 0
+    moe.close()
