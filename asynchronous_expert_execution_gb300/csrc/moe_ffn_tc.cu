@@ -97,6 +97,14 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
+      : "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -211,6 +219,7 @@ enum : int { kModeGemm1 = 0, kModeGemm2 = 1, kModeAtt = 2 };
 // device (the step plan, or the streaming runtime's pick), so one launch serves any layer.
 struct TcParams {
   CUtensorMap mapA[kMaxLayers];     // GEMM1: packed W13, GEMM2: packed W2^T, ATT: packed P^T
+  CUtensorMap mapB16, mapB64;       // GEMM2: the step's h rows [S*KS, I], boxes of 16 / 64 rows
   LayerView views[kMaxLayers];
   Dims d;
   DevCounters* C;
@@ -322,7 +331,8 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1 + 32);    // A producer's expect_tx arrive + 32 B-producer lanes
+      // GEMM2: one expect_tx arrive (A and B both by TMA); else + 32 cp.async B-producer lanes
+      mbar_init(&full[s], MODE == kModeGemm2 ? 1 : 1 + 32);
       mbar_init(&empty[s], 1);        // tcgen05.commit
     }
     for (int b = 0; b < 2; ++b) {
@@ -358,13 +368,22 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1u;
           if (!(ok = mbar_wait(&empty[s], ph ^ 1u, abort_flag, C))) break;
-          mbar_arrive_expect_tx(&full[s], SL::kA);
+          if (MODE == kModeGemm2) {
+            // B = the item's contiguous h rows: a 16- or 64-row box (rows past the item feed
+            // MMA columns the epilogue ignores; rows past the buffer are zero-filled)
+            const bool small = tl.nmma <= 16;
+            mbar_arrive_expect_tx(&full[s], SL::kA + (small ? 16 : BN) * kBK * 2);
+            tma_load_2d(smem_u32(smem + SL::kOffB + s * SL::kB), small ? &p.mapB16 : &p.mapB64, &full[s],
+                        kb * kBK, tl.row_base + tl.j0);
+          } else {
+            mbar_arrive_expect_tx(&full[s], SL::kA);
+          }
           tma_load_3d(smem_u32(smem + SL::kOffA + s * SL::kA), tmA, &full[s], kb * kBK, tl.fti * kBM,
                       tl.expert, pol);
         }
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == 1 && MODE != kModeGemm2) {
     // ------------------------------------------ B producer: gathered rows via cp.async
     const char* pool = static_cast<const char*>(L.pool);
     uint32_t it = 0;
@@ -579,6 +598,20 @@ bool encode_weights(CUtensorMap* m, const void* base, int K, int rows, int nb) {
   return r == CUDA_SUCCESS;
 }
 
+// 2-D map over row-major bf16 rows [rows][K], box 64 x box_rows, 128B swizzle, zero fill.
+bool encode_rows(CUtensorMap* m, const void* base, int K, int rows, int box_rows) {
+  auto fn = get_encode();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  cuuint32_t box[2] = {kBK, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 template <int BN, int STAGES, int MODE>
 cudaError_t set_attrs() {
   using SL = SmemLayout<BN, STAGES>;
@@ -619,6 +652,11 @@ moe_status tc_setup(moe_async_s* h) {
   const Dims& d = h->dims;
   fill_common(h, st->gemm1);
   fill_common(h, st->gemm2);
+  const int hrows = h->dims.S * h->dims.KS;
+  if (!encode_rows(&st->gemm2.mapB16, h->h, d.I, hrows, 16) || !encode_rows(&st->gemm2.mapB64, h->h, d.I, hrows, kBN)) {
+    delete st;
+    return MOE_ERR_CUDA;
+  }
   for (int l = 0; l < h->cfg.num_layers; ++l) {
     if (!encode_weights(&st->gemm1.mapA[l], h->layers[l].w13, d.H, 2 * d.I, d.NB) ||
         !encode_weights(&st->gemm2.mapA[l], h->layers[l].w2, d.I, d.H, d.NB)) {
