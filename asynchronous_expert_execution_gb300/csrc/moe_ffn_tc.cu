@@ -567,8 +567,18 @@ struct TcState {
   bool att_ready;
 };
 
-constexpr int kBN = 64;
-constexpr int kStages = 8;
+// Token-tile width and pipeline depth (smem ring = kStages x (16 KB A + kBN*128 B B)).
+// Measured on GB300 (bench c2/c3/c4, pairs/s): 32 x 10 stages is best for decode and for
+// steps with few experts (more weight bytes in flight per SM, more CTAs per expert);
+// prefill with very popular experts prefers wider tiles (64 x 8: c3 +9%, c2 -1.7%, c4 -22%).
+#ifndef MOE_TC_BN
+#define MOE_TC_BN 32
+#endif
+#ifndef MOE_TC_STAGES
+#define MOE_TC_STAGES 10
+#endif
+constexpr int kBN = MOE_TC_BN;
+constexpr int kStages = MOE_TC_STAGES;
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
