@@ -158,6 +158,7 @@ __global__ void __launch_bounds__(1024) schedule_kernel(LayerView L, Dims d, Ste
                                                         TileGeom g, int layer, int trace_cap,
                                                         int4* trace, long long weight_bytes_per_run) {
   __shared__ PlanScratch sc;
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");   // GEMM1 may start; it waits
   plan_layer(L, d, P, C, pol, g, layer, trace_cap, trace, weight_bytes_per_run, (int)C->steps + 1, true, sc);
 }
 

@@ -105,6 +105,11 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
@@ -313,6 +318,13 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
   const Dims& d = p.d;
   DevCounters* C = p.C;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // Programmatic dependent launch: GEMM1 may start while the scheduling kernel runs and waits
+  // here for its plan; it then lets GEMM2 start on SMs as they free up.  (A no-op when the
+  // kernel was launched without a programmatic dependency.)
+  if (MODE == kModeGemm1) {
+    griddep_wait();
+    griddep_launch_dependents();
+  }
   int n_tiles, layer;
   if (MODE == kModeAtt) {
     const bool picked = p.sd.ctl->pick_kind == 1;
@@ -361,6 +373,12 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
       const uint64_t pol_reuse = policy_evict_normal();
       uint32_t it = 0;
       bool ok = true;
+      // GEMM2 runs as a programmatic dependent of GEMM1: the weights do not depend on GEMM1,
+      // so the first ring of W2 stages is requested at once; the h rows (GEMM1's output) only
+      // after griddepcontrol.wait.
+      int deferred = MODE == kModeGemm2 ? min(STAGES, nk) : 0;
+      int def_row = 0;
+      bool def_small = false;
       for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
         const Tile tl = decode_tile<BN, MODE>(p, t);
         const uint64_t pol = tl.single ? pol_stream : pol_reuse;
@@ -369,10 +387,24 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
           const uint32_t ph = (it / STAGES) & 1u;
           if (!(ok = mbar_wait(&empty[s], ph ^ 1u, abort_flag, C))) break;
           if (MODE == kModeGemm2) {
-            // B = the item's contiguous h rows: a 16- or 64-row box (rows past the item feed
+            // B = the item's contiguous h rows: a 16- or BN-row box (rows past the item feed
             // MMA columns the epilogue ignores; rows past the buffer are zero-filled)
             const bool small = tl.nmma <= 16;
             mbar_arrive_expect_tx(&full[s], SL::kA + (small ? 16 : BN) * kBK * 2);
+            if (deferred > 0) {                         // first ring of the first tile: A only
+              def_row = tl.row_base + tl.j0;
+              def_small = small;
+              tma_load_3d(smem_u32(smem + SL::kOffA + s * SL::kA), tmA, &full[s], kb * kBK, tl.fti * kBM,
+                          tl.expert, pol);
+              if (kb + 1 == deferred) {                 // then wait for GEMM1, and fetch its B
+                griddep_wait();
+                for (int k2 = 0; k2 < deferred; ++k2)
+                  tma_load_2d(smem_u32(smem + SL::kOffB + k2 * SL::kB), def_small ? &p.mapB16 : &p.mapB64,
+                              &full[k2], k2 * kBK, def_row);
+                deferred = 0;
+              }
+              continue;
+            }
             tma_load_2d(smem_u32(smem + SL::kOffB + s * SL::kB), small ? &p.mapB16 : &p.mapB64, &full[s],
                         kb * kBK, tl.row_base + tl.j0);
           } else {
@@ -629,11 +661,22 @@ cudaError_t set_attrs() {
                               SL::kAlloc);
 }
 
+// GEMM1 and GEMM2 are launched as programmatic dependents of the kernel before them (PDL):
+// their CTAs may start early and order themselves with griddepcontrol.wait.
 template <int BN, int STAGES, int MODE>
 cudaError_t launch_one(moe_async_s* h, const TcParams& prm, cudaStream_t s) {
   using SL = SmemLayout<BN, STAGES>;
-  ffn_tc_kernel<BN, STAGES, MODE><<<h->num_sms, kThreads, SL::kAlloc, s>>>(prm);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(h->num_sms);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = SL::kAlloc;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = MODE == kModeAtt ? 0 : 1;
+  return cudaLaunchKernelEx(&cfg, ffn_tc_kernel<BN, STAGES, MODE>, prm);
 }
 
 void fill_common(moe_async_s* h, TcParams& p) {
