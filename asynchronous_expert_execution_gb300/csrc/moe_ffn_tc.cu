@@ -126,7 +126,11 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
                : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// The executing thread's prior cp.async copies trigger one arrive on `bar` when they complete
+// (the barrier's expected count includes this arrival).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
@@ -298,7 +302,6 @@ struct SmemLayout {
 template <int BN, int STAGES, int MODE>
 __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_constant__ TcParams p) {
   using SL = SmemLayout<BN, STAGES>;
-  constexpr int kLag = STAGES - 2;            // cp.async groups kept in flight by the B producer
   constexpr uint32_t kTmemCols = 2 * BN;      // two accumulator buffers
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -419,7 +422,6 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
     // ------------------------------------------ B producer: gathered rows via cp.async
     const char* pool = static_cast<const char*>(L.pool);
     uint32_t it = 0;
-    int issued = 0, signaled = 0;            // stages issued / signalled by this warp
     bool ok = true;
     for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
       const Tile tl = decode_tile<BN, MODE>(p, t);
@@ -454,22 +456,13 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
           const void* src = valid ? static_cast<const void*>(rp + col) : static_cast<const void*>(pool);
           cp_async16(bs + r * 128 + ((c ^ (r & 7)) << 4), src, valid ? 16u : 0u);
         }
-        cp_async_commit();
-        ++issued;
-        if (issued - signaled > kLag) {
-          cp_async_wait<kLag>();
-          fence_proxy_async();
-          mbar_arrive(&full[signaled % STAGES]);
-          ++signaled;
-        }
+        // each lane's copies arrive on the stage barrier when they complete -- no waiting
+        // here, so the producer runs a full ring ahead; the consumer issues the generic ->
+        // async proxy fence after it observes the barrier
+        cp_async_arrive_noinc(&full[s]);
       }
     }
     cp_async_wait<0>();
-    fence_proxy_async();
-    while (signaled < issued) {
-      mbar_arrive(&full[signaled % STAGES]);
-      ++signaled;
-    }
   } else if (warp == 2) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
@@ -488,6 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
           const uint32_t ph = (it / STAGES) & 1u;
           if (!(ok = mbar_wait(&full[s], ph, abort_flag, C))) break;
           tc_fence_after();
+          if (MODE != kModeGemm2) fence_proxy_async();   // B came through cp.async (generic proxy)
           const uint32_t a0 = smem_u32(smem + SL::kOffA + s * SL::kA);
           const uint32_t b0 = smem_u32(smem + SL::kOffB + s * SL::kB);
 #pragma unroll
