@@ -237,7 +237,31 @@ struct TcParams {
   int parts;                        // feature slices per token (GEMM2 tiles covering H)
   int stream_on;                    // GEMM2 merges feed the streaming runtime
   StreamDev sd;
+  // K is cut into `nchunk` fixed chunks; each chunk's product starts from a zero accumulator
+  // and the chunk partials are added in ascending chunk order, so a result never depends on
+  // whether a tile's chunks ran on one CTA or on several (split steps).
+  int nchunk;
+  int split_cap;                    // most tiles a launch may split (workspace capacity)
+  float* ws;                        // [split_cap][nchunk][BN][128] fp32 chunk partials
+  int* cnt;                         // [split_cap] arrivals per split tile (zero between launches)
 };
+
+// A unit of work: one tile and a range of its K chunks [c0, c1).
+struct Unit {
+  int t, c0, c1;
+};
+
+__device__ __forceinline__ Unit unit_of(int u, int nsplit, int nchunk) {
+  Unit x;
+  x.t = u / nsplit;
+  const int per = nchunk / nsplit;
+  x.c0 = (u % nsplit) * per;
+  x.c1 = x.c0 + per;
+  return x;
+}
+
+// first k-block of chunk c (chunk c covers [chunk_kb(c), chunk_kb(c + 1)))
+__device__ __forceinline__ int chunk_kb(int c, int nk, int nchunk) { return (int)(((long long)c * nk) / nchunk); }
 
 struct Tile {
   int expert;
@@ -293,7 +317,8 @@ struct SmemLayout {
   static constexpr int kOffK = kOffSlot + BN * 4;
   static constexpr int kOffFin = kOffK + BN * 4;
   static constexpr int kOffW = kOffFin + BN * 4;
-  static constexpr int kBytes = kOffW + BN * 4;
+  static constexpr int kOffFlag = kOffW + BN * 4;
+  static constexpr int kBytes = kOffFlag + 16;
   static constexpr int kAlloc = kBytes + 1024;               // room to align the base to 1024
 };
 
@@ -317,6 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
   int* k_s = reinterpret_cast<int*>(smem + SL::kOffK);
   int* fin = reinterpret_cast<int*>(smem + SL::kOffFin);
   float* w_s = reinterpret_cast<float*>(smem + SL::kOffW);
+  volatile int* last_flag = reinterpret_cast<volatile int*>(smem + SL::kOffFlag);
 
   const Dims& d = p.d;
   DevCounters* C = p.C;
@@ -342,7 +368,19 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
   const CUtensorMap* tmA = &p.mapA[layer < 0 || layer >= kMaxLayers ? 0 : layer];
   const int Kdim = MODE == kModeGemm2 ? d.I : d.H;
   const int nk = (Kdim + kBK - 1) / kBK;
-  if ((int)blockIdx.x >= n_tiles) return;        // no tile for this CTA: skip all set-up
+  // A launch with few tiles for the grid splits each tile into its K chunks (one unit each)
+  // when that shortens the launch: a single SM streams weights far below the HBM rate, so
+  // a lone expert needs many SMs.  Every role derives the same split from the plan.
+  const int nchunk = p.nchunk;
+  int nsplit = 1;
+  if (nchunk > 1 && n_tiles <= p.split_cap) {
+    const int G = (int)gridDim.x;
+    const long long whole = (long long)((n_tiles + G - 1) / G) * nchunk;   // in chunk times
+    const long long split = ((long long)n_tiles * nchunk + G - 1) / G;
+    if (split < whole) nsplit = nchunk;
+  }
+  const int n_units = n_tiles * nsplit;
+  if ((int)blockIdx.x >= n_units) return;        // no work for this CTA: skip all set-up
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -379,13 +417,17 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
       // GEMM2 runs as a programmatic dependent of GEMM1: the weights do not depend on GEMM1,
       // so the first ring of W2 stages is requested at once; the h rows (GEMM1's output) only
       // after griddepcontrol.wait.
-      int deferred = MODE == kModeGemm2 ? min(STAGES, nk) : 0;
+      const Unit u0 = unit_of(blockIdx.x, nsplit, nchunk);
+      const int kb00 = chunk_kb(u0.c0, nk, nchunk);
+      int deferred = MODE == kModeGemm2 ? min(STAGES, chunk_kb(u0.c1, nk, nchunk) - kb00) : 0;
       int def_row = 0;
       bool def_small = false;
-      for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
-        const Tile tl = decode_tile<BN, MODE>(p, t);
+      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+        const Unit un = unit_of(u, nsplit, nchunk);
+        const Tile tl = decode_tile<BN, MODE>(p, un.t);
         const uint64_t pol = tl.single ? pol_stream : pol_reuse;
-        for (int kb = 0; kb < nk; ++kb, ++it) {
+        const int kb_end = chunk_kb(un.c1, nk, nchunk);
+        for (int kb = chunk_kb(un.c0, nk, nchunk); kb < kb_end; ++kb, ++it) {
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1u;
           if (!(ok = mbar_wait(&empty[s], ph ^ 1u, abort_flag, C))) break;
@@ -399,11 +441,11 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
               def_small = small;
               tma_load_3d(smem_u32(smem + SL::kOffA + s * SL::kA), tmA, &full[s], kb * kBK, tl.fti * kBM,
                           tl.expert, pol);
-              if (kb + 1 == deferred) {                 // then wait for GEMM1, and fetch its B
+              if (kb + 1 - kb00 == deferred) {          // then wait for GEMM1, and fetch its B
                 griddep_wait();
                 for (int k2 = 0; k2 < deferred; ++k2)
                   tma_load_2d(smem_u32(smem + SL::kOffB + k2 * SL::kB), def_small ? &p.mapB16 : &p.mapB64,
-                              &full[k2], k2 * kBK, def_row);
+                              &full[k2], (kb00 + k2) * kBK, def_row);
                 deferred = 0;
               }
               continue;
@@ -423,8 +465,9 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
     const char* pool = static_cast<const char*>(L.pool);
     uint32_t it = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
-      const Tile tl = decode_tile<BN, MODE>(p, t);
+    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+      const Unit un = unit_of(u, nsplit, nchunk);
+      const Tile tl = decode_tile<BN, MODE>(p, un.t);
       __syncwarp();
       for (int r = lane; r < tl.nmma; r += 32) {
         const __nv_bfloat16* rp = nullptr;
@@ -441,7 +484,8 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
         rowptr[r] = rp;
       }
       __syncwarp();
-      for (int kb = 0; kb < nk; ++kb, ++it) {
+      const int kb_end = chunk_kb(un.c1, nk, nchunk);
+      for (int kb = chunk_kb(un.c0, nk, nchunk); kb < kb_end; ++kb, ++it) {
         const int s = it % STAGES;
         const uint32_t ph = (it / STAGES) & 1u;
         const bool w_ok = mbar_wait(&empty[s], ph ^ 1u, abort_flag, C);
@@ -466,41 +510,47 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
   } else if (warp == 2) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      uint32_t it = 0, tile_i = 0;
+      uint32_t it = 0, acc_i = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x, ++tile_i) {
-        const Tile tl = decode_tile<BN, MODE>(p, t);
-        const int buf = tile_i & 1;
-        const uint32_t tph = (tile_i >> 1) & 1u;
-        if (!(ok = mbar_wait(&tempty[buf], tph ^ 1u, abort_flag, C))) break;
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
+      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+        const Unit un = unit_of(u, nsplit, nchunk);
+        const Tile tl = decode_tile<BN, MODE>(p, un.t);
         const uint32_t idesc = idesc_bf16(kBM, tl.nmma);
-        for (int kb = 0; kb < nk; ++kb, ++it) {
-          const int s = it % STAGES;
-          const uint32_t ph = (it / STAGES) & 1u;
-          if (!(ok = mbar_wait(&full[s], ph, abort_flag, C))) break;
+        // one accumulator buffer per chunk, alternating, so the epilogue drains chunk c
+        // while chunk c + 1 accumulates
+        for (int c = un.c0; c < un.c1 && ok; ++c, ++acc_i) {
+          const int buf = acc_i & 1;
+          const uint32_t tph = (acc_i >> 1) & 1u;
+          if (!(ok = mbar_wait(&tempty[buf], tph ^ 1u, abort_flag, C))) break;
           tc_fence_after();
-          if (MODE != kModeGemm2) fence_proxy_async();   // B came through cp.async (generic proxy)
-          const uint32_t a0 = smem_u32(smem + SL::kOffA + s * SL::kA);
-          const uint32_t b0 = smem_u32(smem + SL::kOffB + s * SL::kB);
+          const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
+          const int kb0 = chunk_kb(c, nk, nchunk), kb1 = chunk_kb(c + 1, nk, nchunk);
+          for (int kb = kb0; kb < kb1; ++kb, ++it) {
+            const int s = it % STAGES;
+            const uint32_t ph = (it / STAGES) & 1u;
+            if (!(ok = mbar_wait(&full[s], ph, abort_flag, C))) break;
+            tc_fence_after();
+            if (MODE != kModeGemm2) fence_proxy_async();   // B came through cp.async (generic proxy)
+            const uint32_t a0 = smem_u32(smem + SL::kOffA + s * SL::kA);
+            const uint32_t b0 = smem_u32(smem + SL::kOffB + s * SL::kB);
 #pragma unroll
-          for (int k = 0; k < kBK / 16; ++k)
-            mma_bf16(d_tmem, sw128_desc(a0 + k * 32), sw128_desc(b0 + k * 32), idesc, (kb | k) != 0);
-          mma_commit(&empty[s]);
+            for (int k = 0; k < kBK / 16; ++k)
+              mma_bf16(d_tmem, sw128_desc(a0 + k * 32), sw128_desc(b0 + k * 32), idesc, (kb != kb0) || (k != 0));
+            mma_commit(&empty[s]);
+          }
+          if (ok) mma_commit(&tfull[buf]);
         }
-        if (ok) mma_commit(&tfull[buf]);
       }
     }
   } else if (warp >= 4) {
     // ------------------------------------------------------------------ epilogue
     const int q = warp - 4;                       // TMEM lane quarter
     const int et = threadIdx.x - 128;             // 0..127
-    uint32_t tile_i = 0;
-    for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++tile_i) {
-      const Tile tl = decode_tile<BN, MODE>(p, t);
-      const int buf = tile_i & 1;
-      const uint32_t tph = (tile_i >> 1) & 1u;
+    const int row = 32 * q + lane;                // accumulator row (A row of the tile)
+    uint32_t acc_i = 0;
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+      const Unit un = unit_of(u, nsplit, nchunk);
+      const Tile tl = decode_tile<BN, MODE>(p, un.t);
       if (MODE == kModeGemm2) {
         for (int j = et; j < tl.nj; j += 128) {
           const int rec = record_at(L, d, tl.expert, tl.head + tl.j0 + j);
@@ -515,65 +565,121 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
           w_s[j] = p.sd.att_scale[tl.j0 + j];
         }
       }
-      const bool w_ok = mbar_wait(&tfull[buf], tph, abort_flag, C);
-      if (!epi_bar_and(w_ok)) break;
-      tc_fence_after();
-      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN);
+      // chunk partials, added in ascending chunk order as each accumulator completes
+      float acc[BN];
+      bool ok = true;
+      for (int c = un.c0; c < un.c1; ++c, ++acc_i) {
+        const int buf = acc_i & 1;
+        const uint32_t tph = (acc_i >> 1) & 1u;
+        const bool w_ok = mbar_wait(&tfull[buf], tph, abort_flag, C);
+        if (!(ok = epi_bar_and(w_ok))) break;
+        tc_fence_after();
+        const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN);
+#pragma unroll
+        for (int c0 = 0; c0 < BN; c0 += 16) {
+          if (c0 < tl.nj) {
+            float v[16];
+            tmem_ld16(tbase + c0, v);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) acc[c0 + j] = c == un.c0 ? v[j] : acc[c0 + j] + v[j];
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[buf]);
+      }
+      if (!ok) break;
+      if (nsplit > 1) {
+        // this unit holds one chunk of the tile: publish its partial; the unit that arrives
+        // last adds all partials of the tile in chunk order and runs the epilogue
+        float* wt = p.ws + (size_t)un.t * nchunk * BN * kBM;
+#pragma unroll
+        for (int c0 = 0; c0 < BN; c0 += 16) {
+          if (c0 < tl.nj) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+              if (c0 + j < tl.nj) __stcg(wt + ((size_t)un.c0 * BN + c0 + j) * kBM + row, acc[c0 + j]);
+          }
+        }
+        __threadfence();
+        EpiBarrier{}();
+        if (et == 0) {
+          const int old = atomicAdd(p.cnt + un.t, 1);
+          const int last = old == nchunk - 1;
+          if (last) p.cnt[un.t] = 0;              // every arrival of this launch is in
+          *last_flag = last;
+        }
+        EpiBarrier{}();
+        if (!*last_flag) continue;
+        __threadfence();
+        for (int c = 0; c < nchunk; ++c) {
+#pragma unroll
+          for (int c0 = 0; c0 < BN; c0 += 16) {
+            if (c0 < tl.nj) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const float v = c0 + j < tl.nj ? __ldcg(wt + ((size_t)c * BN + c0 + j) * kBM + row) : 0.f;
+                acc[c0 + j] = c == 0 ? v : acc[c0 + j] + v;
+              }
+            }
+          }
+        }
+      }
       if (MODE == kModeGemm1) {
         const int f = tl.fti * (kBM / 2) + 16 * q + (lane & 15);       // feature of this lane pair
         const bool lo = lane < 16;
-        for (int c0 = 0; c0 < tl.nj; c0 += 16) {
-          float v[16];
-          tmem_ld16(tbase + c0, v);
 #pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float send = lo ? v[8 + j] : v[j];
-            const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
-            const int col = c0 + (lo ? j : 8 + j);
-            const float g = lo ? v[j] : recv;
-            const float u = lo ? recv : v[8 + j];
-            if (col < tl.nj && f < d.I)
-              p.hbuf[(size_t)(tl.row_base + tl.j0 + col) * d.I + f] = __float2bfloat16_rn(silu_f(g) * u);
+        for (int c0 = 0; c0 < BN; c0 += 16) {
+          if (c0 < tl.nj) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const float send = lo ? acc[c0 + 8 + j] : acc[c0 + j];
+              const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
+              const int col = c0 + (lo ? j : 8 + j);
+              const float g = lo ? acc[c0 + j] : recv;
+              const float uu = lo ? recv : acc[c0 + 8 + j];
+              if (col < tl.nj && f < d.I)
+                p.hbuf[(size_t)(tl.row_base + tl.j0 + col) * d.I + f] = __float2bfloat16_rn(silu_f(g) * uu);
+            }
           }
         }
       } else if (MODE == kModeGemm2) {
-        const int f = tl.fti * kBM + 32 * q + lane;                     // output feature of H
-        for (int c0 = 0; c0 < tl.nj; c0 += 16) {
-          float v[16];
-          tmem_ld16(tbase + c0, v);
-          if (f < d.H) {
+        const int f = tl.fti * kBM + row;                               // output feature of H
+        if (f < d.H) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int col = c0 + j;
-              if (col < tl.nj)
-                L.slotbuf[((size_t)slot_s[col] * d.KS + k_s[col]) * d.H + f] = w_s[col] * v[j];
+          for (int c0 = 0; c0 < BN; c0 += 16) {
+            if (c0 < tl.nj) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const int col = c0 + j;
+                if (col < tl.nj)
+                  L.slotbuf[((size_t)slot_s[col] * d.KS + k_s[col]) * d.H + f] = w_s[col] * acc[col];
+              }
             }
           }
         }
       } else {
         // attention stub: a = RMSNorm(x) P = s * (x P), written to the token pool of the layer
-        const int f = tl.fti * kBM + 32 * q + lane;
+        const int f = tl.fti * kBM + row;
         __nv_bfloat16* pool = static_cast<__nv_bfloat16*>(L.pool);
-        for (int c0 = 0; c0 < tl.nj; c0 += 16) {
-          float v[16];
-          tmem_ld16(tbase + c0, v);
-          if (f < d.H) {
+        if (f < d.H) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const int col = c0 + j;
-              if (col < tl.nj) pool[(size_t)slot_s[col] * d.H + f] = __float2bfloat16_rn(w_s[col] * v[j]);
+          for (int c0 = 0; c0 < BN; c0 += 16) {
+            if (c0 < tl.nj) {
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const int col = c0 + j;
+                if (col < tl.nj) pool[(size_t)slot_s[col] * d.H + f] = __float2bfloat16_rn(w_s[col] * acc[col]);
+              }
             }
           }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&tempty[buf]);
       if (MODE == kModeGemm2)
         land_and_merge<__nv_bfloat16>(L, d, C, slot_s, tl.nj, tl.fti, p.parts, tl.fti * kBM, kBM, et, 128, fin, EpiBarrier{},
                                       p.stream_on ? &p.sd : nullptr, layer);
-      else if (MODE == kModeAtt)
-        asm volatile("bar.sync 1, 128;" ::: "memory");   // slot_s / w_s reused by the next tile
+      else
+        asm volatile("bar.sync 1, 128;" ::: "memory");   // slot_s / w_s / last_flag reused by the next unit
     }
   }
 
@@ -591,6 +697,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
 struct TcState {
   TcParams gemm1, gemm2, att;       // parameter blocks (tensor maps of every layer)
   bool att_ready;
+  void* split_buf[2];               // GEMM1 / GEMM2 chunk-partial workspace + arrival counters
 };
 
 // Token-tile width and pipeline depth (smem ring = kStages x (16 KB A + kBN*128 B B)).
@@ -681,6 +788,38 @@ void fill_common(moe_async_s* h, TcParams& p) {
   p.hbuf = static_cast<__nv_bfloat16*>(h->h);
   p.parts = h->parts_per_pair;
   p.stream_on = 0;
+  p.nchunk = 1;
+  p.split_cap = 0;
+  p.ws = nullptr;
+  p.cnt = nullptr;
+}
+
+// K chunks for a contraction of nk k-blocks: 1, 2 or 4 chunks of at least MOE_SPLIT_MIN_KB
+// k-blocks each, so a chunk's partial (BN x 128 fp32) stays small next to the weight bytes
+// the chunk streams.  Measured on GB300 (pairs/s): 24 leaves the GPT-OSS shapes (45 k-blocks)
+// whole and cuts the 7168-deep GEMM1 of the DeepSeek-wide layer in 4 -- c4 +15%; 16 also
+// cuts the GPT-OSS GEMMs in 2, which costs decode 0.5% and prefill 1.2%.
+#ifndef MOE_SPLIT_MIN_KB
+#define MOE_SPLIT_MIN_KB 24
+#endif
+int chunks_for(int nk) {
+  const int q = nk / MOE_SPLIT_MIN_KB;
+  return q >= 4 ? 4 : q >= 2 ? 2 : 1;
+}
+
+// Workspace for launches that split tiles over their K chunks: up to two tiles per SM.
+cudaError_t setup_split(moe_async_s* h, TcParams& p, int K, void** buf) {
+  const int nk = (K + kBK - 1) / kBK;
+  p.nchunk = chunks_for(nk);
+  if (p.nchunk == 1) return cudaSuccess;
+  p.split_cap = 2 * h->num_sms;
+  const size_t ws_bytes = (size_t)p.split_cap * p.nchunk * kBN * kBM * sizeof(float);
+  const size_t cnt_bytes = (size_t)p.split_cap * sizeof(int);
+  cudaError_t e = cudaMalloc(buf, ws_bytes + cnt_bytes);
+  if (e != cudaSuccess) return e;
+  p.ws = static_cast<float*>(*buf);
+  p.cnt = reinterpret_cast<int*>(static_cast<char*>(*buf) + ws_bytes);
+  return cudaMemset(p.cnt, 0, cnt_bytes);
 }
 
 }  // namespace
@@ -712,11 +851,21 @@ moe_status tc_setup(moe_async_s* h) {
     }
   }
   h->tc_state = st;
+  if (setup_split(h, st->gemm1, d.H, &st->split_buf[0]) != cudaSuccess ||
+      setup_split(h, st->gemm2, d.I, &st->split_buf[1]) != cudaSuccess) {
+    tc_teardown(h);
+    return MOE_ERR_CUDA;
+  }
   return MOE_OK;
 }
 
 void tc_teardown(moe_async_s* h) {
-  delete static_cast<TcState*>(h->tc_state);
+  TcState* st = static_cast<TcState*>(h->tc_state);
+  if (st) {
+    for (void* b : st->split_buf)
+      if (b) cudaFree(b);
+  }
+  delete st;
   h->tc_state = nullptr;
 }
 

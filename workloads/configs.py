@@ -107,6 +107,12 @@ TEST_CONFIGS = {
         name="s1_stream_small", layer=LayerSpec(16, 4, 320, 192, "bf16"), tokens=48, router="uniform",
         waves="stream", num_waves=16, arrival="lognormal", policy="mtfs", num_layers=4,
         stream_steps=150, stream_ranks=16, stream_sigma=1.0),
+    # deep K, split over K chunks when a step has few tiles: H = 6136 (96 k-blocks, the last
+    # 56 wide -> 4 chunks of 24), I = 3088 (49 k-blocks, the last 16 wide -> 2 chunks of
+    # 24/25), 2I = 6176 (48 tiles + 32 rows), H = 47 tiles + 120 rows.
+    "k1": WorkloadSpec(
+        name="k1_bf16_deep_k", layer=LayerSpec(8, 2, 6136, 3088, "bf16"), tokens=32,
+        router="normal", waves="even", num_waves=1, arrival="index", policy="mtfs"),
     # bf16 decode-like: many experts, few tokens each.
     "m4": WorkloadSpec(
         name="m4_bf16_decode", layer=LayerSpec(64, 4, 1024, 512, "bf16"), tokens=64,
