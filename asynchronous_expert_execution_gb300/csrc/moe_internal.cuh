@@ -186,6 +186,17 @@ template <typename T> __device__ __forceinline__ T from_f(float v);
 template <> __device__ __forceinline__ float from_f<float>(float v) { return v; }
 template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
 
+// four consecutive outputs (16-byte aligned for fp32, 8-byte aligned for bf16)
+template <typename T> __device__ __forceinline__ void store4(T* p, float4 v);
+template <> __device__ __forceinline__ void store4<float>(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
+template <> __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* p, float4 v) {
+  __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+  uint2 u;
+  u.x = *reinterpret_cast<uint32_t*>(&lo);
+  u.y = *reinterpret_cast<uint32_t*>(&hi);
+  *reinterpret_cast<uint2*>(p) = u;
+}
+
 // Locate the work item owning global tile `t` (items' bases are ascending).
 __device__ __forceinline__ int find_item(const StepPlan* p, int t, bool second) {
   int lo = 0, hi = p->n_work - 1;
@@ -434,23 +445,29 @@ __device__ void land_and_merge(const LayerView& L, const Dims& d, DevCounters* C
   }
   __threadfence();
   bar();
+  // the merge of every finished token's slice: (token, 4 features) items spread over the
+  // group, so the loads of different tokens are in flight together (H % 8 == 0 and f0 a
+  // multiple of 8 make every item 16-byte aligned)
   const int fend = min(f0 + fcount, d.H);
-  for (int j = 0; j < nj; ++j) {
-    if (fin[j]) {                                    // uniform across the group
-      const int slot = slots[j];
-      const float* src = L.slotbuf + (size_t)slot * d.KS * d.H;
-      T* dst = reinterpret_cast<T*>(L.y) + (size_t)slot * d.H;
-      T* dst2 = nullptr;
-      if (sd)                                        // req_n is stable until the last slice
-        dst2 = static_cast<T*>(sd->hist) + ((size_t)slot * (sd->n_max + 1) + sd->req_n[slot] + 1) * d.H;
-      for (int f = f0 + tid; f < fend; f += nthr) {
-        float acc = __ldcg(src + f);
-        for (int k = 1; k < d.KS; ++k) acc += __ldcg(src + (size_t)k * d.H + f);
-        const T o = from_f<T>(acc);
-        dst[f] = o;
-        if (dst2) dst2[f] = o;
-      }
+  const int nvec = (fend - f0) >> 2;
+  for (int w = tid; w < nj * nvec; w += nthr) {
+    const int j = w / nvec;
+    if (!fin[j]) continue;
+    const int f = f0 + 4 * (w - j * nvec);
+    const int slot = slots[j];
+    const float* src = L.slotbuf + (size_t)slot * d.KS * d.H + f;
+    float4 a = __ldcg(reinterpret_cast<const float4*>(src));
+#pragma unroll 8
+    for (int k = 1; k < d.KS; ++k) {
+      const float4 b = __ldcg(reinterpret_cast<const float4*>(src + (size_t)k * d.H));
+      a.x += b.x;
+      a.y += b.y;
+      a.z += b.z;
+      a.w += b.w;
     }
+    store4<T>(reinterpret_cast<T*>(L.y) + (size_t)slot * d.H + f, a);
+    if (sd)                                          // req_n is stable until the last slice
+      store4<T>(static_cast<T*>(sd->hist) + ((size_t)slot * (sd->n_max + 1) + sd->req_n[slot] + 1) * d.H + f, a);
   }
   __threadfence();
   bar();
