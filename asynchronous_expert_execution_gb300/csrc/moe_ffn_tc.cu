@@ -29,7 +29,15 @@ namespace moe {
 namespace {
 
 constexpr int kBM = 128;              // MMA M (weight rows per tile)
-constexpr int kBK = 64;               // K per pipeline stage (one 128-byte swizzle atom)
+constexpr int kBK = 64;               // K per k-block (one 128-byte swizzle atom)
+// k-blocks moved per pipeline stage: a stage's fixed cost (barrier round trip, TMA issue,
+// MMA commit) is paid once per kKps k-blocks.  Measured on GB300 with an MMA consumer: a
+// lone SM streams 36 / 53 / 69 GB/s with 16 / 32 / 64 KB weight stages, and 152 SMs
+// 5.3 / 6.1 TB/s with 16 / 32 KB stages.
+#ifndef MOE_TC_KPS
+#define MOE_TC_KPS 3
+#endif
+constexpr int kKps = MOE_TC_KPS;
 constexpr int kThreads = 256;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // 2 s per wait
 
@@ -263,6 +271,12 @@ __device__ __forceinline__ Unit unit_of(int u, int nsplit, int nchunk) {
 // first k-block of chunk c (chunk c covers [chunk_kb(c), chunk_kb(c + 1)))
 __device__ __forceinline__ int chunk_kb(int c, int nk, int nchunk) { return (int)(((long long)c * nk) / nchunk); }
 
+// A chunk's k-blocks move kKps at a time: stage st of chunk c starts at chunk_kb(c) + st kKps
+// and holds min(kKps, chunk end - start) k-blocks (a stage never spans two chunks).
+__device__ __forceinline__ int chunk_nstages(int c, int nk, int nchunk) {
+  return (chunk_kb(c + 1, nk, nchunk) - chunk_kb(c, nk, nchunk) + kKps - 1) / kKps;
+}
+
 struct Tile {
   int expert;
   uint32_t head;
@@ -304,8 +318,10 @@ __device__ __forceinline__ Tile decode_tile(const TcParams& p, int t) {
 
 template <int BN, int STAGES>
 struct SmemLayout {
-  static constexpr int kA = kBM * kBK * 2;                   // 16 KB
-  static constexpr int kB = BN * kBK * 2;
+  static constexpr int kA1 = kBM * kBK * 2;                  // 16 KB: one k-block of A
+  static constexpr int kB1 = BN * kBK * 2;                   // one k-block of B
+  static constexpr int kA = kKps * kA1;                      // a stage: kKps k-blocks
+  static constexpr int kB = kKps * kB1;
   static constexpr int kOffA = 0;
   static constexpr int kOffB = kOffA + STAGES * kA;
   static constexpr int kOffBar = kOffB + STAGES * kB;
@@ -418,45 +434,60 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
       // so the first ring of W2 stages is requested at once; the h rows (GEMM1's output) only
       // after griddepcontrol.wait.
       const Unit u0 = unit_of(blockIdx.x, nsplit, nchunk);
-      const int kb00 = chunk_kb(u0.c0, nk, nchunk);
-      int deferred = MODE == kModeGemm2 ? min(STAGES, chunk_kb(u0.c1, nk, nchunk) - kb00) : 0;
-      int def_row = 0;
+      int deferred = 0;
+      if (MODE == kModeGemm2) {
+        for (int c = u0.c0; c < u0.c1; ++c) deferred += chunk_nstages(c, nk, nchunk);
+        deferred = min(STAGES, deferred);
+      }
+      int def_row = 0, def_n = 0;
       bool def_small = false;
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
         const Unit un = unit_of(u, nsplit, nchunk);
         const Tile tl = decode_tile<BN, MODE>(p, un.t);
         const uint64_t pol = tl.single ? pol_stream : pol_reuse;
-        const int kb_end = chunk_kb(un.c1, nk, nchunk);
-        for (int kb = chunk_kb(un.c0, nk, nchunk); kb < kb_end; ++kb, ++it) {
-          const int s = it % STAGES;
-          const uint32_t ph = (it / STAGES) & 1u;
-          if (!(ok = mbar_wait(&empty[s], ph ^ 1u, abort_flag, C))) break;
-          if (MODE == kModeGemm2) {
-            // B = the item's contiguous h rows: a 16- or BN-row box (rows past the item feed
-            // MMA columns the epilogue ignores; rows past the buffer are zero-filled)
-            const bool small = tl.nmma <= 16;
-            mbar_arrive_expect_tx(&full[s], SL::kA + (small ? 16 : BN) * kBK * 2);
-            if (deferred > 0) {                         // first ring of the first tile: A only
-              def_row = tl.row_base + tl.j0;
-              def_small = small;
-              tma_load_3d(smem_u32(smem + SL::kOffA + s * SL::kA), tmA, &full[s], kb * kBK, tl.fti * kBM,
-                          tl.expert, pol);
-              if (kb + 1 - kb00 == deferred) {          // then wait for GEMM1, and fetch its B
-                griddep_wait();
-                for (int k2 = 0; k2 < deferred; ++k2)
-                  tma_load_2d(smem_u32(smem + SL::kOffB + k2 * SL::kB), def_small ? &p.mapB16 : &p.mapB64,
-                              &full[k2], (kb00 + k2) * kBK, def_row);
-                deferred = 0;
+        for (int c = un.c0; c < un.c1 && ok; ++c) {
+          const int kb1 = chunk_kb(c + 1, nk, nchunk);
+          for (int kbs = chunk_kb(c, nk, nchunk); kbs < kb1; kbs += kKps, ++it) {
+            const int nv = min(kKps, kb1 - kbs);
+            const int s = it % STAGES;
+            const uint32_t ph = (it / STAGES) & 1u;
+            if (!(ok = mbar_wait(&empty[s], ph ^ 1u, abort_flag, C))) break;
+            const uint32_t a_s = smem_u32(smem + SL::kOffA + s * SL::kA);
+            if (MODE == kModeGemm2) {
+              // B = the item's contiguous h rows: a 16- or BN-row box (rows past the item feed
+              // MMA columns the epilogue ignores; rows past the buffer are zero-filled)
+              const bool small = tl.nmma <= 16;
+              mbar_arrive_expect_tx(&full[s], nv * (SL::kA1 + (small ? 16 : BN) * kBK * 2));
+              for (int j = 0; j < nv; ++j)
+                tma_load_3d(a_s + j * SL::kA1, tmA, &full[s], (kbs + j) * kBK, tl.fti * kBM, tl.expert, pol);
+              if (deferred > 0) {                       // first ring of the first unit: A only
+                def_row = tl.row_base + tl.j0;
+                def_small = small;
+                if (++def_n == deferred) {              // then wait for GEMM1, and fetch its B
+                  griddep_wait();
+                  int idx = 0;
+                  for (int c2 = u0.c0; c2 < u0.c1 && idx < deferred; ++c2) {
+                    const int e2 = chunk_kb(c2 + 1, nk, nchunk);
+                    for (int k2 = chunk_kb(c2, nk, nchunk); k2 < e2 && idx < deferred; k2 += kKps, ++idx) {
+                      const int n2 = min(kKps, e2 - k2);
+                      for (int j = 0; j < n2; ++j)
+                        tma_load_2d(smem_u32(smem + SL::kOffB + idx * SL::kB + j * SL::kB1),
+                                    def_small ? &p.mapB16 : &p.mapB64, &full[idx], (k2 + j) * kBK, def_row);
+                    }
+                  }
+                  deferred = 0;
+                }
+                continue;
               }
-              continue;
+              for (int j = 0; j < nv; ++j)
+                tma_load_2d(smem_u32(smem + SL::kOffB + s * SL::kB + j * SL::kB1), small ? &p.mapB16 : &p.mapB64,
+                            &full[s], (kbs + j) * kBK, tl.row_base + tl.j0);
+            } else {
+              mbar_arrive_expect_tx(&full[s], nv * SL::kA1);
+              for (int j = 0; j < nv; ++j)
+                tma_load_3d(a_s + j * SL::kA1, tmA, &full[s], (kbs + j) * kBK, tl.fti * kBM, tl.expert, pol);
             }
-            tma_load_2d(smem_u32(smem + SL::kOffB + s * SL::kB), small ? &p.mapB16 : &p.mapB64, &full[s],
-                        kb * kBK, tl.row_base + tl.j0);
-          } else {
-            mbar_arrive_expect_tx(&full[s], SL::kA);
           }
-          tma_load_3d(smem_u32(smem + SL::kOffA + s * SL::kA), tmA, &full[s], kb * kBK, tl.fti * kBM,
-                      tl.expert, pol);
         }
       }
     }
@@ -484,26 +515,31 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
         rowptr[r] = rp;
       }
       __syncwarp();
-      const int kb_end = chunk_kb(un.c1, nk, nchunk);
-      for (int kb = chunk_kb(un.c0, nk, nchunk); kb < kb_end; ++kb, ++it) {
-        const int s = it % STAGES;
-        const uint32_t ph = (it / STAGES) & 1u;
-        const bool w_ok = mbar_wait(&empty[s], ph ^ 1u, abort_flag, C);
-        if (!(ok = __all_sync(0xffffffffu, w_ok))) break;
-        const uint32_t bs = smem_u32(smem + SL::kOffB + s * SL::kB);
-        const int col0 = kb * kBK;
-        for (int q = lane; q < tl.nmma * 8; q += 32) {
-          const int r = q >> 3, c = q & 7;
-          const __nv_bfloat16* rp = rowptr[r];
-          const int col = col0 + c * 8;
-          const bool valid = rp != nullptr && col < Kdim;
-          const void* src = valid ? static_cast<const void*>(rp + col) : static_cast<const void*>(pool);
-          cp_async16(bs + r * 128 + ((c ^ (r & 7)) << 4), src, valid ? 16u : 0u);
+      for (int ch = un.c0; ch < un.c1 && ok; ++ch) {
+        const int kb1 = chunk_kb(ch + 1, nk, nchunk);
+        for (int kbs = chunk_kb(ch, nk, nchunk); kbs < kb1; kbs += kKps, ++it) {
+          const int nv = min(kKps, kb1 - kbs);
+          const int s = it % STAGES;
+          const uint32_t ph = (it / STAGES) & 1u;
+          const bool w_ok = mbar_wait(&empty[s], ph ^ 1u, abort_flag, C);
+          if (!(ok = __all_sync(0xffffffffu, w_ok))) break;
+          for (int j = 0; j < nv; ++j) {
+            const uint32_t bs = smem_u32(smem + SL::kOffB + s * SL::kB + j * SL::kB1);
+            const int col0 = (kbs + j) * kBK;
+            for (int q = lane; q < tl.nmma * 8; q += 32) {
+              const int r = q >> 3, c = q & 7;
+              const __nv_bfloat16* rp = rowptr[r];
+              const int col = col0 + c * 8;
+              const bool valid = rp != nullptr && col < Kdim;
+              const void* src = valid ? static_cast<const void*>(rp + col) : static_cast<const void*>(pool);
+              cp_async16(bs + r * 128 + ((c ^ (r & 7)) << 4), src, valid ? 16u : 0u);
+            }
+          }
+          // each lane's copies arrive on the stage barrier when they complete -- no waiting
+          // here, so the producer runs a full ring ahead; the consumer issues the generic ->
+          // async proxy fence after it observes the barrier
+          cp_async_arrive_noinc(&full[s]);
         }
-        // each lane's copies arrive on the stage barrier when they complete -- no waiting
-        // here, so the producer runs a full ring ahead; the consumer issues the generic ->
-        // async proxy fence after it observes the barrier
-        cp_async_arrive_noinc(&full[s]);
       }
     }
     cp_async_wait<0>();
@@ -525,17 +561,21 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
           const int kb0 = chunk_kb(c, nk, nchunk), kb1 = chunk_kb(c + 1, nk, nchunk);
-          for (int kb = kb0; kb < kb1; ++kb, ++it) {
+          for (int kbs = kb0; kbs < kb1; kbs += kKps, ++it) {
+            const int nv = min(kKps, kb1 - kbs);
             const int s = it % STAGES;
             const uint32_t ph = (it / STAGES) & 1u;
             if (!(ok = mbar_wait(&full[s], ph, abort_flag, C))) break;
             tc_fence_after();
             if (MODE != kModeGemm2) fence_proxy_async();   // B came through cp.async (generic proxy)
-            const uint32_t a0 = smem_u32(smem + SL::kOffA + s * SL::kA);
-            const uint32_t b0 = smem_u32(smem + SL::kOffB + s * SL::kB);
+            for (int j = 0; j < nv; ++j) {
+              const uint32_t a0 = smem_u32(smem + SL::kOffA + s * SL::kA + j * SL::kA1);
+              const uint32_t b0 = smem_u32(smem + SL::kOffB + s * SL::kB + j * SL::kB1);
 #pragma unroll
-            for (int k = 0; k < kBK / 16; ++k)
-              mma_bf16(d_tmem, sw128_desc(a0 + k * 32), sw128_desc(b0 + k * 32), idesc, (kb != kb0) || (k != 0));
+              for (int k = 0; k < kBK / 16; ++k)
+                mma_bf16(d_tmem, sw128_desc(a0 + k * 32), sw128_desc(b0 + k * 32), idesc,
+                         (kbs + j != kb0) || (k != 0));
+            }
             mma_commit(&empty[s]);
           }
           if (ok) mma_commit(&tfull[buf]);
@@ -700,15 +740,18 @@ struct TcState {
   void* split_buf[2];               // GEMM1 / GEMM2 chunk-partial workspace + arrival counters
 };
 
-// Token-tile width and pipeline depth (smem ring = kStages x (16 KB A + kBN*128 B B)).
-// Measured on GB300 (bench c2/c3/c4, pairs/s): 32 x 10 stages is best for decode and for
-// steps with few experts (more weight bytes in flight per SM, more CTAs per expert);
-// prefill with very popular experts prefers wider tiles (64 x 8: c3 +9%, c2 -1.7%, c4 -22%).
+// Token-tile width and pipeline depth (smem ring = kStages x kKps x (16 KB A + kBN*128 B B)).
+// Measured on GB300 (bench c2/c3/c4, pairs/s): 32-token tiles suit decode and steps with few
+// experts (more CTAs per expert); prefill with very popular experts prefers wider tiles
+// (64: c3 +9%, c2 -1.7%, c4 -22%).  Stages of kKps k-blocks x kStages, same tile:
+// 1 x 10 -- c2 176.5 K, c3 2.61 M, c4 1.08 M; 2 x 5 -- 179.1 K, 2.79 M, 1.15 M;
+// 3 x 3 -- 181.8 K, 2.92 M, 1.19 M; 4 x 2 -- 175.3 K, 2.91 M, 1.18 M; 5 x 2 -- 181.4 K,
+// 2.98 M, 1.20 M.
 #ifndef MOE_TC_BN
 #define MOE_TC_BN 32
 #endif
 #ifndef MOE_TC_STAGES
-#define MOE_TC_STAGES 10
+#define MOE_TC_STAGES 3
 #endif
 constexpr int kBN = MOE_TC_BN;
 constexpr int kStages = MOE_TC_STAGES;
