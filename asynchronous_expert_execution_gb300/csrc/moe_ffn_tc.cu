@@ -113,6 +113,11 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
+// Bring a tensor map's descriptor on chip ahead of its first TMA.
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -288,8 +293,9 @@ struct Tile {
   bool single;  // the item has one token tile: its A rows are read once
 };
 
+// tb = the step's first-tile indices of the work items, staged in shared memory
 template <int BN, int MODE>
-__device__ __forceinline__ Tile decode_tile(const TcParams& p, int t) {
+__device__ __forceinline__ Tile decode_tile(const TcParams& p, const int* tb, int t) {
   Tile tl;
   int local, count;
   if (MODE == kModeAtt) {
@@ -300,7 +306,12 @@ __device__ __forceinline__ Tile decode_tile(const TcParams& p, int t) {
     tl.row_base = 0;
   } else {
     const StepPlan* P = p.P;
-    const WorkItem it = P->items[find_item(P, t, MODE == kModeGemm2)];
+    int lo = 0, hi = P->n_work - 1;                 // last item whose first tile is <= t
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (tb[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    const WorkItem it = P->items[lo];
     local = t - (MODE == kModeGemm2 ? it.t2_base : it.t1_base);
     count = it.count;
     tl.expert = it.expert;
@@ -334,7 +345,8 @@ struct SmemLayout {
   static constexpr int kOffFin = kOffK + BN * 4;
   static constexpr int kOffW = kOffFin + BN * 4;
   static constexpr int kOffFlag = kOffW + BN * 4;
-  static constexpr int kBytes = kOffFlag + 16;
+  static constexpr int kOffTb = kOffFlag + 16;
+  static constexpr int kBytes = kOffTb + kMaxBuckets * 4;
   static constexpr int kAlloc = kBytes + 1024;               // room to align the base to 1024
 };
 
@@ -359,6 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
   int* fin = reinterpret_cast<int*>(smem + SL::kOffFin);
   float* w_s = reinterpret_cast<float*>(smem + SL::kOffW);
   volatile int* last_flag = reinterpret_cast<volatile int*>(smem + SL::kOffFlag);
+  int* tb_s = reinterpret_cast<int*>(smem + SL::kOffTb);
 
   const Dims& d = p.d;
   DevCounters* C = p.C;
@@ -399,6 +412,11 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
   if ((int)blockIdx.x >= n_units) return;        // no work for this CTA: skip all set-up
 
   if (threadIdx.x == 0) {
+    prefetch_tmap(tmA);                        // descriptors load while the CTA sets up
+    if (MODE == kModeGemm2) {
+      prefetch_tmap(&p.mapB16);
+      prefetch_tmap(&p.mapB64);
+    }
     for (int s = 0; s < STAGES; ++s) {
       // GEMM2: one expect_tx arrive (A and B both by TMA); else + 32 cp.async B-producer lanes
       mbar_init(&full[s], MODE == kModeGemm2 ? 1 : 1 + 32);
@@ -414,6 +432,11 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
   if (warp == 2) {
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
+  }
+  if (MODE != kModeAtt) {                       // item lookups then search shared memory
+    const int nw = min(p.P->n_work, kMaxBuckets);
+    for (int i = threadIdx.x; i < nw; i += blockDim.x)
+      tb_s[i] = MODE == kModeGemm2 ? p.P->items[i].t2_base : p.P->items[i].t1_base;
   }
   tc_fence_before();
   __syncthreads();
@@ -443,7 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
       bool def_small = false;
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
         const Unit un = unit_of(u, nsplit, nchunk);
-        const Tile tl = decode_tile<BN, MODE>(p, un.t);
+        const Tile tl = decode_tile<BN, MODE>(p, tb_s, un.t);
         const uint64_t pol = tl.single ? pol_stream : pol_reuse;
         for (int c = un.c0; c < un.c1 && ok; ++c) {
           const int kb1 = chunk_kb(c + 1, nk, nchunk);
@@ -498,7 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
     bool ok = true;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
       const Unit un = unit_of(u, nsplit, nchunk);
-      const Tile tl = decode_tile<BN, MODE>(p, un.t);
+      const Tile tl = decode_tile<BN, MODE>(p, tb_s, un.t);
       __syncwarp();
       for (int r = lane; r < tl.nmma; r += 32) {
         const __nv_bfloat16* rp = nullptr;
@@ -550,7 +573,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
       bool ok = true;
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
         const Unit un = unit_of(u, nsplit, nchunk);
-        const Tile tl = decode_tile<BN, MODE>(p, un.t);
+        const Tile tl = decode_tile<BN, MODE>(p, tb_s, un.t);
         const uint32_t idesc = idesc_bf16(kBM, tl.nmma);
         // one accumulator buffer per chunk, alternating, so the epilogue drains chunk c
         // while chunk c + 1 accumulates
@@ -590,7 +613,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
     uint32_t acc_i = 0;
     for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
       const Unit un = unit_of(u, nsplit, nchunk);
-      const Tile tl = decode_tile<BN, MODE>(p, un.t);
+      const Tile tl = decode_tile<BN, MODE>(p, tb_s, un.t);
       if (MODE == kModeGemm2) {
         for (int j = et; j < tl.nj; j += 128) {
           const int rec = record_at(L, d, tl.expert, tl.head + tl.j0 + j);
