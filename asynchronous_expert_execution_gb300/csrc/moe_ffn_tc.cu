@@ -37,7 +37,22 @@ constexpr int kBK = 64;               // K per k-block (one 128-byte swizzle ato
 #ifndef MOE_TC_KPS
 #define MOE_TC_KPS 3
 #endif
-constexpr int kKps = MOE_TC_KPS;
+constexpr int kKps = MOE_TC_KPS;      // narrow tiles
+// Wide tiles: an item with at least MOE_TC_WIDE_MIN tokens (a popular expert in prefill) is
+// cut into MOE_TC_BNW-token tiles, so its weight rows are read once per BNW tokens and each
+// MMA is wide enough for the tensor pipe (measured: 46 cycles per 128 x N x 16 MMA for
+// N <= 64, 64 for N = 128, 128 for N = 256).  0 turns wide tiles off.
+#ifndef MOE_TC_BNW
+#define MOE_TC_BNW 128
+#endif
+#ifndef MOE_TC_KPSW
+#define MOE_TC_KPSW 2
+#endif
+#ifndef MOE_TC_WIDE_MIN
+#define MOE_TC_WIDE_MIN 128
+#endif
+constexpr int kKpsW = MOE_TC_KPSW;
+constexpr int kWideMin = MOE_TC_WIDE_MIN;
 constexpr int kThreads = 256;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // 2 s per wait
 
@@ -241,7 +256,7 @@ enum : int { kModeGemm1 = 0, kModeGemm2 = 1, kModeAtt = 2 };
 // device (the step plan, or the streaming runtime's pick), so one launch serves any layer.
 struct TcParams {
   CUtensorMap mapA[kMaxLayers];     // GEMM1: packed W13, GEMM2: packed W2^T, ATT: packed P^T
-  CUtensorMap mapB16, mapB64;       // GEMM2: the step's h rows [S*KS, I], boxes of 16 / 64 rows
+  CUtensorMap mapB16, mapBn, mapBw; // GEMM2: the step's h rows [S*KS, I], boxes of 16 / narrow / wide rows
   LayerView views[kMaxLayers];
   Dims d;
   DevCounters* C;
@@ -255,7 +270,7 @@ struct TcParams {
   // whether a tile's chunks ran on one CTA or on several (split steps).
   int nchunk;
   int split_cap;                    // most tiles a launch may split (workspace capacity)
-  float* ws;                        // [split_cap][nchunk][BN][128] fp32 chunk partials
+  float* ws;                        // [split_cap][nchunk][BNW][128] fp32 chunk partials
   int* cnt;                         // [split_cap] arrivals per split tile (zero between launches)
 };
 
@@ -276,10 +291,11 @@ __device__ __forceinline__ Unit unit_of(int u, int nsplit, int nchunk) {
 // first k-block of chunk c (chunk c covers [chunk_kb(c), chunk_kb(c + 1)))
 __device__ __forceinline__ int chunk_kb(int c, int nk, int nchunk) { return (int)(((long long)c * nk) / nchunk); }
 
-// A chunk's k-blocks move kKps at a time: stage st of chunk c starts at chunk_kb(c) + st kKps
-// and holds min(kKps, chunk end - start) k-blocks (a stage never spans two chunks).
-__device__ __forceinline__ int chunk_nstages(int c, int nk, int nchunk) {
-  return (chunk_kb(c + 1, nk, nchunk) - chunk_kb(c, nk, nchunk) + kKps - 1) / kKps;
+// A chunk's k-blocks move kps at a time (kps: the tile's k-blocks per stage): stage st of
+// chunk c starts at chunk_kb(c) + st kps and holds min(kps, chunk end - start) k-blocks (a
+// stage never spans two chunks).
+__device__ __forceinline__ int chunk_nstages(int c, int nk, int nchunk, int kps) {
+  return (chunk_kb(c + 1, nk, nchunk) - chunk_kb(c, nk, nchunk) + kps - 1) / kps;
 }
 
 struct Tile {
@@ -290,11 +306,13 @@ struct Tile {
   int j0;       // first token of the tile within the item
   int nj;       // valid tokens
   int nmma;     // MMA N (multiple of 16, >= nj)
+  int bn;       // tile width: narrow or wide
+  int kps;      // k-blocks per pipeline stage for this tile width
   bool single;  // the item has one token tile: its A rows are read once
 };
 
 // tb = the step's first-tile indices of the work items, staged in shared memory
-template <int BN, int MODE>
+template <int BN, int BNW, int MODE>
 __device__ __forceinline__ Tile decode_tile(const TcParams& p, const int* tb, int t) {
   Tile tl;
   int local, count;
@@ -318,33 +336,36 @@ __device__ __forceinline__ Tile decode_tile(const TcParams& p, const int* tb, in
     tl.head = it.head;
     tl.row_base = it.row_base;
   }
-  const int ntt = (count + BN - 1) / BN;
+  const bool wide = BNW > BN && count >= kWideMin;   // the planner applies the same rule
+  tl.bn = wide ? BNW : BN;
+  tl.kps = wide ? kKpsW : kKps;
+  const int ntt = (count + tl.bn - 1) / tl.bn;
   tl.single = ntt <= 1;
   tl.fti = local / ntt;
-  tl.j0 = (local % ntt) * BN;
-  tl.nj = min(BN, count - tl.j0);
-  tl.nmma = min(BN, max(16, (tl.nj + 15) & ~15));
+  tl.j0 = (local % ntt) * tl.bn;
+  tl.nj = min(tl.bn, count - tl.j0);
+  tl.nmma = min(tl.bn, max(16, (tl.nj + 15) & ~15));
   return tl;
 }
 
-template <int BN, int STAGES>
+// A stage holds kps k-blocks of a tile: A sub-blocks (16 KB each) from the stage base, then
+// B sub-blocks (bn x 128 B each).  Its size fits either tile width.
+template <int BN, int BNW, int STAGES>
 struct SmemLayout {
   static constexpr int kA1 = kBM * kBK * 2;                  // 16 KB: one k-block of A
-  static constexpr int kB1 = BN * kBK * 2;                   // one k-block of B
-  static constexpr int kA = kKps * kA1;                      // a stage: kKps k-blocks
-  static constexpr int kB = kKps * kB1;
-  static constexpr int kOffA = 0;
-  static constexpr int kOffB = kOffA + STAGES * kA;
-  static constexpr int kOffBar = kOffB + STAGES * kB;
+  static constexpr int kStageN = kKps * (kA1 + BN * kBK * 2);
+  static constexpr int kStageW = BNW > BN ? kKpsW * (kA1 + BNW * kBK * 2) : 0;
+  static constexpr int kStage = ((kStageN > kStageW ? kStageN : kStageW) + 1023) & ~1023;
+  static constexpr int kOffBar = STAGES * kStage;
   static constexpr int kNumBars = 2 * STAGES + 4;
   static constexpr int kOffTmem = kOffBar + kNumBars * 8;
   static constexpr int kOffAbort = kOffTmem + 4;
   static constexpr int kOffRowPtr = (kOffAbort + 4 + 15) & ~15;
-  static constexpr int kOffSlot = kOffRowPtr + BN * 8;
-  static constexpr int kOffK = kOffSlot + BN * 4;
-  static constexpr int kOffFin = kOffK + BN * 4;
-  static constexpr int kOffW = kOffFin + BN * 4;
-  static constexpr int kOffFlag = kOffW + BN * 4;
+  static constexpr int kOffSlot = kOffRowPtr + 2 * BNW * 8;   // row pointers of both B warps
+  static constexpr int kOffK = kOffSlot + BNW * 4;
+  static constexpr int kOffFin = kOffK + BNW * 4;
+  static constexpr int kOffW = kOffFin + BNW * 4;
+  static constexpr int kOffFlag = kOffW + BNW * 4;
   static constexpr int kOffTb = kOffFlag + 16;
   static constexpr int kBytes = kOffTb + kMaxBuckets * 4;
   static constexpr int kAlloc = kBytes + 1024;               // room to align the base to 1024
@@ -352,10 +373,10 @@ struct SmemLayout {
 
 // ------------------------------------------------------------------ the kernel
 
-template <int BN, int STAGES, int MODE>
+template <int BN, int BNW, int STAGES, int MODE>
 __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_constant__ TcParams p) {
-  using SL = SmemLayout<BN, STAGES>;
-  constexpr uint32_t kTmemCols = 2 * BN;      // two accumulator buffers
+  using SL = SmemLayout<BN, BNW, STAGES>;
+  constexpr uint32_t kTmemCols = 2 * BNW;     // two accumulator buffers (the wider width)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SL::kOffBar);
@@ -415,11 +436,12 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
     prefetch_tmap(tmA);                        // descriptors load while the CTA sets up
     if (MODE == kModeGemm2) {
       prefetch_tmap(&p.mapB16);
-      prefetch_tmap(&p.mapB64);
+      prefetch_tmap(&p.mapBn);
+      prefetch_tmap(&p.mapBw);
     }
     for (int s = 0; s < STAGES; ++s) {
-      // GEMM2: one expect_tx arrive (A and B both by TMA); else + 32 cp.async B-producer lanes
-      mbar_init(&full[s], MODE == kModeGemm2 ? 1 : 1 + 32);
+      // GEMM2: one expect_tx arrive (A and B both by TMA); else + 64 cp.async B-producer lanes
+      mbar_init(&full[s], MODE == kModeGemm2 ? 1 : 1 + 64);
       mbar_init(&empty[s], 1);        // tcgen05.commit
     }
     for (int b = 0; b < 2; ++b) {
@@ -457,45 +479,47 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
       // so the first ring of W2 stages is requested at once; the h rows (GEMM1's output) only
       // after griddepcontrol.wait.
       const Unit u0 = unit_of(blockIdx.x, nsplit, nchunk);
+      const Tile t0 = decode_tile<BN, BNW, MODE>(p, tb_s, u0.t);
       int deferred = 0;
       if (MODE == kModeGemm2) {
-        for (int c = u0.c0; c < u0.c1; ++c) deferred += chunk_nstages(c, nk, nchunk);
+        for (int c = u0.c0; c < u0.c1; ++c) deferred += chunk_nstages(c, nk, nchunk, t0.kps);
         deferred = min(STAGES, deferred);
       }
-      int def_row = 0, def_n = 0;
-      bool def_small = false;
+      int def_n = 0;
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
         const Unit un = unit_of(u, nsplit, nchunk);
-        const Tile tl = decode_tile<BN, MODE>(p, tb_s, un.t);
+        const Tile tl = decode_tile<BN, BNW, MODE>(p, tb_s, un.t);
         const uint64_t pol = tl.single ? pol_stream : pol_reuse;
+        // GEMM2's B = the item's contiguous h rows: a 16-row or tile-wide box (rows past the
+        // item feed MMA columns the epilogue ignores; rows past the buffer are zero-filled)
+        const int brows = tl.nmma <= 16 ? 16 : tl.bn;
+        const CUtensorMap* mapB = tl.nmma <= 16 ? &p.mapB16 : (tl.bn == BN ? &p.mapBn : &p.mapBw);
         for (int c = un.c0; c < un.c1 && ok; ++c) {
           const int kb1 = chunk_kb(c + 1, nk, nchunk);
-          for (int kbs = chunk_kb(c, nk, nchunk); kbs < kb1; kbs += kKps, ++it) {
-            const int nv = min(kKps, kb1 - kbs);
+          for (int kbs = chunk_kb(c, nk, nchunk); kbs < kb1; kbs += tl.kps, ++it) {
+            const int nv = min(tl.kps, kb1 - kbs);
             const int s = it % STAGES;
             const uint32_t ph = (it / STAGES) & 1u;
             if (!(ok = mbar_wait(&empty[s], ph ^ 1u, abort_flag, C))) break;
-            const uint32_t a_s = smem_u32(smem + SL::kOffA + s * SL::kA);
+            const uint32_t a_s = smem_u32(smem + s * SL::kStage);
+            const uint32_t b_s = a_s + tl.kps * SL::kA1;
             if (MODE == kModeGemm2) {
-              // B = the item's contiguous h rows: a 16- or BN-row box (rows past the item feed
-              // MMA columns the epilogue ignores; rows past the buffer are zero-filled)
-              const bool small = tl.nmma <= 16;
-              mbar_arrive_expect_tx(&full[s], nv * (SL::kA1 + (small ? 16 : BN) * kBK * 2));
+              mbar_arrive_expect_tx(&full[s], nv * (SL::kA1 + brows * kBK * 2));
               for (int j = 0; j < nv; ++j)
                 tma_load_3d(a_s + j * SL::kA1, tmA, &full[s], (kbs + j) * kBK, tl.fti * kBM, tl.expert, pol);
               if (deferred > 0) {                       // first ring of the first unit: A only
-                def_row = tl.row_base + tl.j0;
-                def_small = small;
                 if (++def_n == deferred) {              // then wait for GEMM1, and fetch its B
                   griddep_wait();
+                  const CUtensorMap* mapB0 = t0.nmma <= 16 ? &p.mapB16 : (t0.bn == BN ? &p.mapBn : &p.mapBw);
+                  const int row0 = t0.row_base + t0.j0;
                   int idx = 0;
                   for (int c2 = u0.c0; c2 < u0.c1 && idx < deferred; ++c2) {
                     const int e2 = chunk_kb(c2 + 1, nk, nchunk);
-                    for (int k2 = chunk_kb(c2, nk, nchunk); k2 < e2 && idx < deferred; k2 += kKps, ++idx) {
-                      const int n2 = min(kKps, e2 - k2);
+                    for (int k2 = chunk_kb(c2, nk, nchunk); k2 < e2 && idx < deferred; k2 += t0.kps, ++idx) {
+                      const int n2 = min(t0.kps, e2 - k2);
+                      const uint32_t b0s = smem_u32(smem + idx * SL::kStage) + t0.kps * SL::kA1;
                       for (int j = 0; j < n2; ++j)
-                        tma_load_2d(smem_u32(smem + SL::kOffB + idx * SL::kB + j * SL::kB1),
-                                    def_small ? &p.mapB16 : &p.mapB64, &full[idx], (k2 + j) * kBK, def_row);
+                        tma_load_2d(b0s + j * t0.bn * kBK * 2, mapB0, &full[idx], (k2 + j) * kBK, row0);
                     }
                   }
                   deferred = 0;
@@ -503,8 +527,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
                 continue;
               }
               for (int j = 0; j < nv; ++j)
-                tma_load_2d(smem_u32(smem + SL::kOffB + s * SL::kB + j * SL::kB1), small ? &p.mapB16 : &p.mapB64,
-                            &full[s], (kbs + j) * kBK, tl.row_base + tl.j0);
+                tma_load_2d(b_s + j * tl.bn * kBK * 2, mapB, &full[s], (kbs + j) * kBK, tl.row_base + tl.j0);
             } else {
               mbar_arrive_expect_tx(&full[s], nv * SL::kA1);
               for (int j = 0; j < nv; ++j)
@@ -514,44 +537,45 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
         }
       }
     }
-  } else if (warp == 1 && MODE != kModeGemm2) {
-    // ------------------------------------------ B producer: gathered rows via cp.async
+  } else if ((warp == 1 || warp == 3) && MODE != kModeGemm2) {
+    // ------------------------------- B producer (two warps): gathered rows via cp.async
+    const int wi = warp == 1 ? 0 : 1;               // each warp copies half of every stage
+    const __nv_bfloat16** rp_w = rowptr + wi * BNW;
     const char* pool = static_cast<const char*>(L.pool);
     uint32_t it = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
       const Unit un = unit_of(u, nsplit, nchunk);
-      const Tile tl = decode_tile<BN, MODE>(p, tb_s, un.t);
+      const Tile tl = decode_tile<BN, BNW, MODE>(p, tb_s, un.t);
       __syncwarp();
       for (int r = lane; r < tl.nmma; r += 32) {
         const __nv_bfloat16* rp = nullptr;
         if (r < tl.nj) {
-          if (MODE == kModeGemm2) {
-            rp = p.hbuf + (size_t)(tl.row_base + tl.j0 + r) * d.I;
-          } else if (MODE == kModeAtt) {
+          if (MODE == kModeAtt) {
             rp = static_cast<const __nv_bfloat16*>(p.sd.att_rowptr[tl.j0 + r]);
           } else {
             const int rec = record_at(L, d, tl.expert, tl.head + tl.j0 + r);
             rp = reinterpret_cast<const __nv_bfloat16*>(pool) + (size_t)(rec >> kKShift) * d.H;
           }
         }
-        rowptr[r] = rp;
+        rp_w[r] = rp;
       }
       __syncwarp();
       for (int ch = un.c0; ch < un.c1 && ok; ++ch) {
         const int kb1 = chunk_kb(ch + 1, nk, nchunk);
-        for (int kbs = chunk_kb(ch, nk, nchunk); kbs < kb1; kbs += kKps, ++it) {
-          const int nv = min(kKps, kb1 - kbs);
+        for (int kbs = chunk_kb(ch, nk, nchunk); kbs < kb1; kbs += tl.kps, ++it) {
+          const int nv = min(tl.kps, kb1 - kbs);
           const int s = it % STAGES;
           const uint32_t ph = (it / STAGES) & 1u;
           const bool w_ok = mbar_wait(&empty[s], ph ^ 1u, abort_flag, C);
           if (!(ok = __all_sync(0xffffffffu, w_ok))) break;
+          const uint32_t b_s = smem_u32(smem + s * SL::kStage) + tl.kps * SL::kA1;
           for (int j = 0; j < nv; ++j) {
-            const uint32_t bs = smem_u32(smem + SL::kOffB + s * SL::kB + j * SL::kB1);
+            const uint32_t bs = b_s + j * tl.bn * kBK * 2;
             const int col0 = (kbs + j) * kBK;
-            for (int q = lane; q < tl.nmma * 8; q += 32) {
+            for (int q = wi * 32 + lane; q < tl.nmma * 8; q += 64) {
               const int r = q >> 3, c = q & 7;
-              const __nv_bfloat16* rp = rowptr[r];
+              const __nv_bfloat16* rp = rp_w[r];
               const int col = col0 + c * 8;
               const bool valid = rp != nullptr && col < Kdim;
               const void* src = valid ? static_cast<const void*>(rp + col) : static_cast<const void*>(pool);
@@ -573,7 +597,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
       bool ok = true;
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
         const Unit un = unit_of(u, nsplit, nchunk);
-        const Tile tl = decode_tile<BN, MODE>(p, tb_s, un.t);
+        const Tile tl = decode_tile<BN, BNW, MODE>(p, tb_s, un.t);
         const uint32_t idesc = idesc_bf16(kBM, tl.nmma);
         // one accumulator buffer per chunk, alternating, so the epilogue drains chunk c
         // while chunk c + 1 accumulates
@@ -582,18 +606,19 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
           const uint32_t tph = (acc_i >> 1) & 1u;
           if (!(ok = mbar_wait(&tempty[buf], tph ^ 1u, abort_flag, C))) break;
           tc_fence_after();
-          const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
+          const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BNW);
           const int kb0 = chunk_kb(c, nk, nchunk), kb1 = chunk_kb(c + 1, nk, nchunk);
-          for (int kbs = kb0; kbs < kb1; kbs += kKps, ++it) {
-            const int nv = min(kKps, kb1 - kbs);
+          for (int kbs = kb0; kbs < kb1; kbs += tl.kps, ++it) {
+            const int nv = min(tl.kps, kb1 - kbs);
             const int s = it % STAGES;
             const uint32_t ph = (it / STAGES) & 1u;
             if (!(ok = mbar_wait(&full[s], ph, abort_flag, C))) break;
             tc_fence_after();
             if (MODE != kModeGemm2) fence_proxy_async();   // B came through cp.async (generic proxy)
+            const uint32_t a_s = smem_u32(smem + s * SL::kStage);
             for (int j = 0; j < nv; ++j) {
-              const uint32_t a0 = smem_u32(smem + SL::kOffA + s * SL::kA + j * SL::kA1);
-              const uint32_t b0 = smem_u32(smem + SL::kOffB + s * SL::kB + j * SL::kB1);
+              const uint32_t a0 = a_s + j * SL::kA1;
+              const uint32_t b0 = a_s + tl.kps * SL::kA1 + j * tl.bn * kBK * 2;
 #pragma unroll
               for (int k = 0; k < kBK / 16; ++k)
                 mma_bf16(d_tmem, sw128_desc(a0 + k * 32), sw128_desc(b0 + k * 32), idesc,
@@ -613,7 +638,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
     uint32_t acc_i = 0;
     for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
       const Unit un = unit_of(u, nsplit, nchunk);
-      const Tile tl = decode_tile<BN, MODE>(p, tb_s, un.t);
+      const Tile tl = decode_tile<BN, BNW, MODE>(p, tb_s, un.t);
       if (MODE == kModeGemm2) {
         for (int j = et; j < tl.nj; j += 128) {
           const int rec = record_at(L, d, tl.expert, tl.head + tl.j0 + j);
@@ -629,7 +654,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
         }
       }
       // chunk partials, added in ascending chunk order as each accumulator completes
-      float acc[BN];
+      float acc[BNW];
       bool ok = true;
       for (int c = un.c0; c < un.c1; ++c, ++acc_i) {
         const int buf = acc_i & 1;
@@ -637,9 +662,9 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
         const bool w_ok = mbar_wait(&tfull[buf], tph, abort_flag, C);
         if (!(ok = epi_bar_and(w_ok))) break;
         tc_fence_after();
-        const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BN);
+        const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * BNW);
 #pragma unroll
-        for (int c0 = 0; c0 < BN; c0 += 16) {
+        for (int c0 = 0; c0 < BNW; c0 += 16) {
           if (c0 < tl.nj) {
             float v[16];
             tmem_ld16(tbase + c0, v);
@@ -655,13 +680,13 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
       if (nsplit > 1) {
         // this unit holds one chunk of the tile: publish its partial; the unit that arrives
         // last adds all partials of the tile in chunk order and runs the epilogue
-        float* wt = p.ws + (size_t)un.t * nchunk * BN * kBM;
+        float* wt = p.ws + (size_t)un.t * nchunk * BNW * kBM;
 #pragma unroll
-        for (int c0 = 0; c0 < BN; c0 += 16) {
+        for (int c0 = 0; c0 < BNW; c0 += 16) {
           if (c0 < tl.nj) {
 #pragma unroll
             for (int j = 0; j < 16; ++j)
-              if (c0 + j < tl.nj) __stcg(wt + ((size_t)un.c0 * BN + c0 + j) * kBM + row, acc[c0 + j]);
+              if (c0 + j < tl.nj) __stcg(wt + ((size_t)un.c0 * BNW + c0 + j) * kBM + row, acc[c0 + j]);
           }
         }
         __threadfence();
@@ -677,11 +702,11 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
         __threadfence();
         for (int c = 0; c < nchunk; ++c) {
 #pragma unroll
-          for (int c0 = 0; c0 < BN; c0 += 16) {
+          for (int c0 = 0; c0 < BNW; c0 += 16) {
             if (c0 < tl.nj) {
 #pragma unroll
               for (int j = 0; j < 16; ++j) {
-                const float v = c0 + j < tl.nj ? __ldcg(wt + ((size_t)c * BN + c0 + j) * kBM + row) : 0.f;
+                const float v = c0 + j < tl.nj ? __ldcg(wt + ((size_t)c * BNW + c0 + j) * kBM + row) : 0.f;
                 acc[c0 + j] = c == 0 ? v : acc[c0 + j] + v;
               }
             }
@@ -692,7 +717,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
         const int f = tl.fti * (kBM / 2) + 16 * q + (lane & 15);       // feature of this lane pair
         const bool lo = lane < 16;
 #pragma unroll
-        for (int c0 = 0; c0 < BN; c0 += 16) {
+        for (int c0 = 0; c0 < BNW; c0 += 16) {
           if (c0 < tl.nj) {
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
@@ -710,7 +735,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
         const int f = tl.fti * kBM + row;                               // output feature of H
         if (f < d.H) {
 #pragma unroll
-          for (int c0 = 0; c0 < BN; c0 += 16) {
+          for (int c0 = 0; c0 < BNW; c0 += 16) {
             if (c0 < tl.nj) {
 #pragma unroll
               for (int j = 0; j < 16; ++j) {
@@ -727,7 +752,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
         __nv_bfloat16* pool = static_cast<__nv_bfloat16*>(L.pool);
         if (f < d.H) {
 #pragma unroll
-          for (int c0 = 0; c0 < BN; c0 += 16) {
+          for (int c0 = 0; c0 < BNW; c0 += 16) {
             if (c0 < tl.nj) {
 #pragma unroll
               for (int j = 0; j < 16; ++j) {
@@ -777,6 +802,7 @@ struct TcState {
 #define MOE_TC_STAGES 3
 #endif
 constexpr int kBN = MOE_TC_BN;
+constexpr int kBNW = kWideMin > 0 && MOE_TC_BNW > MOE_TC_BN ? MOE_TC_BNW : MOE_TC_BN;
 constexpr int kStages = MOE_TC_STAGES;
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
@@ -821,18 +847,18 @@ bool encode_rows(CUtensorMap* m, const void* base, int K, int rows, int box_rows
   return r == CUDA_SUCCESS;
 }
 
-template <int BN, int STAGES, int MODE>
+template <int BN, int BNW, int STAGES, int MODE>
 cudaError_t set_attrs() {
-  using SL = SmemLayout<BN, STAGES>;
-  return cudaFuncSetAttribute(ffn_tc_kernel<BN, STAGES, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  using SL = SmemLayout<BN, BNW, STAGES>;
+  return cudaFuncSetAttribute(ffn_tc_kernel<BN, BNW, STAGES, MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               SL::kAlloc);
 }
 
 // GEMM1 and GEMM2 are launched as programmatic dependents of the kernel before them (PDL):
 // their CTAs may start early and order themselves with griddepcontrol.wait.
-template <int BN, int STAGES, int MODE>
+template <int BN, int BNW, int STAGES, int MODE>
 cudaError_t launch_one(moe_async_s* h, const TcParams& prm, cudaStream_t s) {
-  using SL = SmemLayout<BN, STAGES>;
+  using SL = SmemLayout<BN, BNW, STAGES>;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(h->num_sms);
   cfg.blockDim = dim3(kThreads);
@@ -843,7 +869,7 @@ cudaError_t launch_one(moe_async_s* h, const TcParams& prm, cudaStream_t s) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = MODE == kModeAtt ? 0 : 1;
-  return cudaLaunchKernelEx(&cfg, ffn_tc_kernel<BN, STAGES, MODE>, prm);
+  return cudaLaunchKernelEx(&cfg, ffn_tc_kernel<BN, BNW, STAGES, MODE>, prm);
 }
 
 void fill_common(moe_async_s* h, TcParams& p) {
@@ -879,7 +905,7 @@ cudaError_t setup_split(moe_async_s* h, TcParams& p, int K, void** buf) {
   p.nchunk = chunks_for(nk);
   if (p.nchunk == 1) return cudaSuccess;
   p.split_cap = 2 * h->num_sms;
-  const size_t ws_bytes = (size_t)p.split_cap * p.nchunk * kBN * kBM * sizeof(float);
+  const size_t ws_bytes = (size_t)p.split_cap * p.nchunk * kBNW * kBM * sizeof(float);
   const size_t cnt_bytes = (size_t)p.split_cap * sizeof(int);
   cudaError_t e = cudaMalloc(buf, ws_bytes + cnt_bytes);
   if (e != cudaSuccess) return e;
@@ -890,13 +916,14 @@ cudaError_t setup_split(moe_async_s* h, TcParams& p, int K, void** buf) {
 
 }  // namespace
 
-TileGeom tc_geom() { return TileGeom{kBN, kBM, kBN, kBM}; }
+TileGeom tc_geom() { return TileGeom{kBN, kBM, kBN, kBM, kBNW > kBN ? kBNW : 0, kWideMin}; }
 
 moe_status tc_setup(moe_async_s* h) {
   if (h->cfg.num_layers > kMaxLayers) return MOE_ERR_UNSUPPORTED;
   // dynamic shared memory limits, set once per handle outside any stream capture
-  if (set_attrs<kBN, kStages, kModeGemm1>() != cudaSuccess || set_attrs<kBN, kStages, kModeGemm2>() != cudaSuccess ||
-      set_attrs<kBN, kStages, kModeAtt>() != cudaSuccess)
+  if (set_attrs<kBN, kBNW, kStages, kModeGemm1>() != cudaSuccess ||
+      set_attrs<kBN, kBNW, kStages, kModeGemm2>() != cudaSuccess ||
+      set_attrs<kBN, kBNW, kStages, kModeAtt>() != cudaSuccess)
     return MOE_ERR_CUDA;
   TcState* st = new (std::nothrow) TcState();
   if (!st) return MOE_ERR_CUDA;
@@ -905,7 +932,8 @@ moe_status tc_setup(moe_async_s* h) {
   fill_common(h, st->gemm1);
   fill_common(h, st->gemm2);
   const int hrows = h->dims.S * h->dims.KS;
-  if (!encode_rows(&st->gemm2.mapB16, h->h, d.I, hrows, 16) || !encode_rows(&st->gemm2.mapB64, h->h, d.I, hrows, kBN)) {
+  if (!encode_rows(&st->gemm2.mapB16, h->h, d.I, hrows, 16) || !encode_rows(&st->gemm2.mapBn, h->h, d.I, hrows, kBN) ||
+      !encode_rows(&st->gemm2.mapBw, h->h, d.I, hrows, kBNW)) {
     delete st;
     return MOE_ERR_CUDA;
   }
@@ -940,11 +968,11 @@ moe_status launch_ffn_tc(moe_async_s* h, int layer, cudaStream_t s) {
   TcState* st = static_cast<TcState*>(h->tc_state);
   if (!st) return MOE_ERR_INVALID;
   prof_begin(h, MOE_KERNEL_FFN1, s);
-  cudaError_t e = launch_one<kBN, kStages, kModeGemm1>(h, st->gemm1, s);
+  cudaError_t e = launch_one<kBN, kBNW, kStages, kModeGemm1>(h, st->gemm1, s);
   prof_end(h, MOE_KERNEL_FFN1, s);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   prof_begin(h, MOE_KERNEL_FFN2, s);
-  e = launch_one<kBN, kStages, kModeGemm2>(h, st->gemm2, s);
+  e = launch_one<kBN, kBNW, kStages, kModeGemm2>(h, st->gemm2, s);
   prof_end(h, MOE_KERNEL_FFN2, s);
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
@@ -968,7 +996,7 @@ moe_status tc_stream_setup(moe_async_s* h, const void* const* proj_packed, const
 moe_status launch_att_tc(moe_async_s* h, cudaStream_t s) {
   TcState* st = static_cast<TcState*>(h->tc_state);
   if (!st || !st->att_ready) return MOE_ERR_INVALID;
-  return launch_one<kBN, kStages, kModeAtt>(h, st->att, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  return launch_one<kBN, kBNW, kStages, kModeAtt>(h, st->att, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 }  // namespace moe

@@ -143,7 +143,14 @@ struct TileGeom {
   int32_t bm1;          // packed W13 rows per GEMM1 tile
   int32_t bn2;          // tokens per GEMM2 tile
   int32_t bm2;          // H rows per GEMM2 tile
+  int32_t bnw;          // tokens per tile of a wide item (0: no wide tiles)
+  int32_t wide_min;     // an item of at least this many tokens is cut into wide tiles
 };
+
+// Tokens per tile of an item of `count` tokens (bn: the narrow width of the GEMM).
+__host__ __device__ __forceinline__ int tile_tokens(const TileGeom& g, int count, int bn) {
+  return (g.bnw > 0 && count >= g.wide_min) ? g.bnw : bn;
+}
 
 }  // namespace moe
 
@@ -365,8 +372,9 @@ __device__ inline void plan_layer(const LayerView& L, const Dims& d, StepPlan* P
       if (r < n) {
         b = order[r];
         cnt = depth[b];
-        t1 = ((cnt + g.bn1 - 1) / g.bn1) * ft1;
-        t2 = ((cnt + g.bn2 - 1) / g.bn2) * ft2;
+        const int w1 = tile_tokens(g, cnt, g.bn1), w2 = tile_tokens(g, cnt, g.bn2);
+        t1 = ((cnt + w1 - 1) / w1) * ft1;
+        t2 = ((cnt + w2 - 1) / w2) * ft2;
       }
       int s_cnt = cnt, s_t1 = t1, s_t2 = t2;      // inclusive prefix sums within the chunk
       for (int off = 1; off < 32; off <<= 1) {

@@ -113,6 +113,11 @@ TEST_CONFIGS = {
     "k1": WorkloadSpec(
         name="k1_bf16_deep_k", layer=LayerSpec(8, 2, 6136, 3088, "bf16"), tokens=32,
         router="normal", waves="even", num_waves=1, arrival="index", policy="mtfs"),
+    # wide token tiles: 2 experts, top-2, so each item holds every token (256 >= the wide
+    # threshold of 128); H = 1000 and 2I = 992 leave ragged M and K tails.
+    "w1": WorkloadSpec(
+        name="w1_bf16_wide_tiles", layer=LayerSpec(2, 2, 1000, 496, "bf16"), tokens=256,
+        router="normal", waves="even", num_waves=1, arrival="index", policy="mtfs"),
     # bf16 decode-like: many experts, few tokens each.
     "m4": WorkloadSpec(
         name="m4_bf16_decode", layer=LayerSpec(64, 4, 1024, 512, "bf16"), tokens=64,
