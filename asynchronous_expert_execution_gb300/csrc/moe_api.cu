@@ -381,7 +381,7 @@ moe_status moe_async_create(const moe_async_config* cfg, const void* const* w1,
   }
   h->use_tc = swiglu && c.dtype == MOE_BF16;
   h->geom = h->use_tc ? tc_geom() : simt_geom();
-  if (!swiglu) h->geom = TileGeom{16, 2 * c.inter, 16, c.hidden, 0, 0};
+  if (!swiglu) h->geom = TileGeom{16, 2 * c.inter, 16, c.hidden, 0, 0, 0};
   h->parts_per_pair = (d.H + h->geom.bm2 - 1) / h->geom.bm2;
 
   const size_t es = elem_size(c.dtype);

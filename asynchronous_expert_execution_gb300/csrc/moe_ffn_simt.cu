@@ -186,7 +186,7 @@ __global__ void __launch_bounds__(256) identity_kernel(LayerView L, Dims d, DevC
 
 }  // namespace
 
-TileGeom simt_geom() { return TileGeom{kBT, 2 * kBF, kBT, kBH, 0, 0}; }
+TileGeom simt_geom() { return TileGeom{kBT, 2 * kBF, kBT, kBH, 0, 0, 0}; }
 
 moe_status launch_ffn_simt(moe_async_s* h, int layer, cudaStream_t s) {
   const Dims& d = h->dims;

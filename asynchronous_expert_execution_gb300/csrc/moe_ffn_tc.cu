@@ -38,21 +38,28 @@ constexpr int kBK = 64;               // K per k-block (one 128-byte swizzle ato
 #define MOE_TC_KPS 3
 #endif
 constexpr int kKps = MOE_TC_KPS;      // narrow tiles
-// Wide tiles: an item with at least MOE_TC_WIDE_MIN tokens (a popular expert in prefill) is
-// cut into MOE_TC_BNW-token tiles, so its weight rows are read once per BNW tokens and each
-// MMA is wide enough for the tensor pipe (measured: 46 cycles per 128 x N x 16 MMA for
-// N <= 64, 64 for N = 128, 128 for N = 256).  0 turns wide tiles off.
+// Wide tiles: an item with at least MOE_TC_WIDE_MIN1 (GEMM1, attention stub) or
+// MOE_TC_WIDE_MIN2 (GEMM2) tokens is cut into MOE_TC_BNW-token tiles, so its weight rows are
+// read once per BNW tokens and each MMA is wide enough for the tensor pipe (measured: 46
+// cycles per 128 x N x 16 MMA for N <= 64, 64 for N = 128, 128 for N = 256).  Measured on
+// GB300 (pairs/s, c3 / c4): one threshold for both GEMMs of 128 -- 3.48 M / 1.17 M; 64 --
+// 3.66 M / 1.28 M; 33 -- 3.76 M / 1.24 M (GEMM1 gains from 33, GEMM2 loses from 48 on the
+// DeepSeek-wide layer, whose 63-token items then run on half as many CTAs).  Decode is
+// unchanged.  0 turns wide tiles off.
 #ifndef MOE_TC_BNW
 #define MOE_TC_BNW 128
 #endif
 #ifndef MOE_TC_KPSW
 #define MOE_TC_KPSW 2
 #endif
-#ifndef MOE_TC_WIDE_MIN
-#define MOE_TC_WIDE_MIN 128
+#ifndef MOE_TC_WIDE_MIN1
+#define MOE_TC_WIDE_MIN1 33
+#endif
+#ifndef MOE_TC_WIDE_MIN2
+#define MOE_TC_WIDE_MIN2 64
 #endif
 constexpr int kKpsW = MOE_TC_KPSW;
-constexpr int kWideMin = MOE_TC_WIDE_MIN;
+constexpr int kWideMin1 = MOE_TC_WIDE_MIN1, kWideMin2 = MOE_TC_WIDE_MIN2;
 constexpr int kThreads = 256;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // 2 s per wait
 
@@ -336,7 +343,8 @@ __device__ __forceinline__ Tile decode_tile(const TcParams& p, const int* tb, in
     tl.head = it.head;
     tl.row_base = it.row_base;
   }
-  const bool wide = BNW > BN && count >= kWideMin;   // the planner applies the same rule
+  // the planner applies the same rule
+  const bool wide = BNW > BN && count >= (MODE == kModeGemm2 ? kWideMin2 : kWideMin1);
   tl.bn = wide ? BNW : BN;
   tl.kps = wide ? kKpsW : kKps;
   const int ntt = (count + tl.bn - 1) / tl.bn;
@@ -802,7 +810,7 @@ struct TcState {
 #define MOE_TC_STAGES 3
 #endif
 constexpr int kBN = MOE_TC_BN;
-constexpr int kBNW = kWideMin > 0 && MOE_TC_BNW > MOE_TC_BN ? MOE_TC_BNW : MOE_TC_BN;
+constexpr int kBNW = kWideMin1 > 0 && kWideMin2 > 0 && MOE_TC_BNW > MOE_TC_BN ? MOE_TC_BNW : MOE_TC_BN;
 constexpr int kStages = MOE_TC_STAGES;
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
@@ -916,7 +924,7 @@ cudaError_t setup_split(moe_async_s* h, TcParams& p, int K, void** buf) {
 
 }  // namespace
 
-TileGeom tc_geom() { return TileGeom{kBN, kBM, kBN, kBM, kBNW > kBN ? kBNW : 0, kWideMin}; }
+TileGeom tc_geom() { return TileGeom{kBN, kBM, kBN, kBM, kBNW > kBN ? kBNW : 0, kWideMin1, kWideMin2}; }
 
 moe_status tc_setup(moe_async_s* h) {
   if (h->cfg.num_layers > kMaxLayers) return MOE_ERR_UNSUPPORTED;

@@ -144,12 +144,14 @@ struct TileGeom {
   int32_t bn2;          // tokens per GEMM2 tile
   int32_t bm2;          // H rows per GEMM2 tile
   int32_t bnw;          // tokens per tile of a wide item (0: no wide tiles)
-  int32_t wide_min;     // an item of at least this many tokens is cut into wide tiles
+  int32_t wide_min1;    // GEMM1 (and the attention stub): an item of at least this many
+  int32_t wide_min2;    //   tokens is cut into wide tiles; GEMM2: the same
 };
 
-// Tokens per tile of an item of `count` tokens (bn: the narrow width of the GEMM).
-__host__ __device__ __forceinline__ int tile_tokens(const TileGeom& g, int count, int bn) {
-  return (g.bnw > 0 && count >= g.wide_min) ? g.bnw : bn;
+// Tokens per tile of an item of `count` tokens (bn: the narrow width of the GEMM, wide_min
+// its wide threshold).
+__host__ __device__ __forceinline__ int tile_tokens(const TileGeom& g, int count, int bn, int wide_min) {
+  return (g.bnw > 0 && count >= wide_min) ? g.bnw : bn;
 }
 
 }  // namespace moe
@@ -372,7 +374,7 @@ __device__ inline void plan_layer(const LayerView& L, const Dims& d, StepPlan* P
       if (r < n) {
         b = order[r];
         cnt = depth[b];
-        const int w1 = tile_tokens(g, cnt, g.bn1), w2 = tile_tokens(g, cnt, g.bn2);
+        const int w1 = tile_tokens(g, cnt, g.bn1, g.wide_min1), w2 = tile_tokens(g, cnt, g.bn2, g.wide_min2);
         t1 = ((cnt + w1 - 1) / w1) * ft1;
         t2 = ((cnt + w2 - 1) / w2) * ft2;
       }

@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(1024) stream_tick_kernel(const __grid_constant
     if (kind == 1) {
       sd.att_ht[2 * layer] += (uint32_t)cnt;
       ctl->att_count = cnt;
-      const int wt = tile_tokens(a.g, cnt, a.g.bn1);
+      const int wt = tile_tokens(a.g, cnt, a.g.bn1, a.g.wide_min1);
       ctl->att_tiles = ((cnt + wt - 1) / wt) * ((a.d.H + a.g.bm2 - 1) / a.g.bm2);
     } else {
       ctl->att_count = 0;
