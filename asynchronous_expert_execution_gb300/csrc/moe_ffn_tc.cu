@@ -281,22 +281,37 @@ struct TcParams {
   int* cnt;                         // [split_cap] arrivals per split tile (zero between launches)
 };
 
-// A unit of work: one tile and a range of its K chunks [c0, c1).
+// A unit of work: one tile and a range of its K chunks [c0, c1).  The first n_whole tiles of a
+// launch are one unit each (all chunks); each later tile is split into one unit per chunk.
 struct Unit {
   int t, c0, c1;
+  bool split;
 };
 
-__device__ __forceinline__ Unit unit_of(int u, int nsplit, int nchunk) {
+__device__ __forceinline__ Unit unit_of(int u, int n_whole, int nchunk) {
   Unit x;
-  x.t = u / nsplit;
-  const int per = nchunk / nsplit;
-  x.c0 = (u % nsplit) * per;
-  x.c1 = x.c0 + per;
+  if (u < n_whole) {
+    x.t = u;
+    x.c0 = 0;
+    x.c1 = nchunk;
+    x.split = false;
+  } else {
+    const int v = u - n_whole;
+    x.t = n_whole + v / nchunk;
+    x.c0 = v % nchunk;
+    x.c1 = x.c0 + 1;
+    x.split = true;
+  }
   return x;
 }
 
-// first k-block of chunk c (chunk c covers [chunk_kb(c), chunk_kb(c + 1)))
-__device__ __forceinline__ int chunk_kb(int c, int nk, int nchunk) { return (int)(((long long)c * nk) / nchunk); }
+// first k-block of chunk c (chunk c covers [chunk_kb(c), chunk_kb(c + 1))): the even cut,
+// rounded to a multiple of 6 k-blocks so chunks hold whole stages of both tile widths
+__device__ __forceinline__ int chunk_kb(int c, int nk, int nchunk) {
+  if (c >= nchunk) return nk;
+  const int e = (int)(((long long)c * nk) / nchunk);
+  return min(nk, (e + 3) / 6 * 6);
+}
 
 // A chunk's k-blocks move kps at a time (kps: the tile's k-blocks per stage): stage st of
 // chunk c starts at chunk_kb(c) + st kps and holds min(kps, chunk end - start) k-blocks (a
@@ -426,18 +441,24 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
   const CUtensorMap* tmA = &p.mapA[layer < 0 || layer >= kMaxLayers ? 0 : layer];
   const int Kdim = MODE == kModeGemm2 ? d.I : d.H;
   const int nk = (Kdim + kBK - 1) / kBK;
-  // A launch with few tiles for the grid splits each tile into its K chunks (one unit each)
-  // when that shortens the launch: a single SM streams weights far below the HBM rate, so
-  // a lone expert needs many SMs.  Every role derives the same split from the plan.
+  // Tiles are split into their K chunks (one unit each) where that shortens the launch: all
+  // of them when the launch has few tiles for the grid (a single SM streams weights far
+  // below the HBM rate, so a lone expert needs many SMs), else the tiles of the last,
+  // partial round, so the round ends sooner on more SMs.  Every role derives the same split
+  // from the plan.
   const int nchunk = p.nchunk;
-  int nsplit = 1;
-  if (nchunk > 1 && n_tiles <= p.split_cap) {
+  int n_whole = n_tiles;
+  if (nchunk > 1) {
     const int G = (int)gridDim.x;
     const long long whole = (long long)((n_tiles + G - 1) / G) * nchunk;   // in chunk times
     const long long split = ((long long)n_tiles * nchunk + G - 1) / G;
-    if (split < whole) nsplit = nchunk;
+    const int tail = n_tiles % G;
+    if (n_tiles <= p.split_cap && split < whole)
+      n_whole = 0;
+    else if (tail > 0 && tail <= p.split_cap && tail * nchunk <= G)
+      n_whole = n_tiles - tail;
   }
-  const int n_units = n_tiles * nsplit;
+  const int n_units = n_whole + (n_tiles - n_whole) * nchunk;
   if ((int)blockIdx.x >= n_units) return;        // no work for this CTA: skip all set-up
 
   if (threadIdx.x == 0) {
@@ -486,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
       // GEMM2 runs as a programmatic dependent of GEMM1: the weights do not depend on GEMM1,
       // so the first ring of W2 stages is requested at once; the h rows (GEMM1's output) only
       // after griddepcontrol.wait.
-      const Unit u0 = unit_of(blockIdx.x, nsplit, nchunk);
+      const Unit u0 = unit_of(blockIdx.x, n_whole, nchunk);
       const Tile t0 = decode_tile<BN, BNW, MODE>(p, tb_s, u0.t);
       int deferred = 0;
       if (MODE == kModeGemm2) {
@@ -495,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
       }
       int def_n = 0;
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-        const Unit un = unit_of(u, nsplit, nchunk);
+        const Unit un = unit_of(u, n_whole, nchunk);
         const Tile tl = decode_tile<BN, BNW, MODE>(p, tb_s, un.t);
         const uint64_t pol = tl.single ? pol_stream : pol_reuse;
         // GEMM2's B = the item's contiguous h rows: a 16-row or tile-wide box (rows past the
@@ -553,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
     uint32_t it = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-      const Unit un = unit_of(u, nsplit, nchunk);
+      const Unit un = unit_of(u, n_whole, nchunk);
       const Tile tl = decode_tile<BN, BNW, MODE>(p, tb_s, un.t);
       __syncwarp();
       for (int r = lane; r < tl.nmma; r += 32) {
@@ -604,7 +625,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
       uint32_t it = 0, acc_i = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
-        const Unit un = unit_of(u, nsplit, nchunk);
+        const Unit un = unit_of(u, n_whole, nchunk);
         const Tile tl = decode_tile<BN, BNW, MODE>(p, tb_s, un.t);
         const uint32_t idesc = idesc_bf16(kBM, tl.nmma);
         // one accumulator buffer per chunk, alternating, so the epilogue drains chunk c
@@ -645,7 +666,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
     const int row = 32 * q + lane;                // accumulator row (A row of the tile)
     uint32_t acc_i = 0;
     for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
-      const Unit un = unit_of(u, nsplit, nchunk);
+      const Unit un = unit_of(u, n_whole, nchunk);
       const Tile tl = decode_tile<BN, BNW, MODE>(p, tb_s, un.t);
       if (MODE == kModeGemm2) {
         for (int j = et; j < tl.nj; j += 128) {
@@ -685,10 +706,11 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
         if (lane == 0) mbar_arrive(&tempty[buf]);
       }
       if (!ok) break;
-      if (nsplit > 1) {
+      if (un.split) {
         // this unit holds one chunk of the tile: publish its partial; the unit that arrives
         // last adds all partials of the tile in chunk order and runs the epilogue
-        float* wt = p.ws + (size_t)un.t * nchunk * BNW * kBM;
+        const int st = un.t - n_whole;              // split tiles: [0, split_cap)
+        float* wt = p.ws + (size_t)st * nchunk * BNW * kBM;
 #pragma unroll
         for (int c0 = 0; c0 < BNW; c0 += 16) {
           if (c0 < tl.nj) {
@@ -700,9 +722,9 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
         __threadfence();
         EpiBarrier{}();
         if (et == 0) {
-          const int old = atomicAdd(p.cnt + un.t, 1);
+          const int old = atomicAdd(p.cnt + st, 1);
           const int last = old == nchunk - 1;
-          if (last) p.cnt[un.t] = 0;              // every arrival of this launch is in
+          if (last) p.cnt[st] = 0;                // every arrival of this launch is in
           *last_flag = last;
         }
         EpiBarrier{}();
@@ -898,7 +920,8 @@ void fill_common(moe_async_s* h, TcParams& p) {
 // k-blocks each, so a chunk's partial (BN x 128 fp32) stays small next to the weight bytes
 // the chunk streams.  Measured on GB300 (pairs/s): 24 leaves the GPT-OSS shapes (45 k-blocks)
 // whole and cuts the 7168-deep GEMM1 of the DeepSeek-wide layer in 4 -- c4 +15%; 16 also
-// cuts the GPT-OSS GEMMs in 2, which costs decode 0.5% and prefill 1.2%.
+// cuts the GPT-OSS GEMMs in 2, which costs decode 0.5% and prefill 1.2%; 22 cuts them in 2
+// so the last round's tiles can be split: decode -0.4%, prefill -1.5%, streaming -0.8%.
 #ifndef MOE_SPLIT_MIN_KB
 #define MOE_SPLIT_MIN_KB 24
 #endif

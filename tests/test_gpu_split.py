@@ -18,7 +18,8 @@ from tests.gpu_helpers import TOL, rel_err, expert_getter
 pytestmark = pytest.mark.gpu
 
 # the kernels' rules: a contraction of nk 64-wide k-blocks has 1, 2 or 4 chunks of >= 24
-# k-blocks; a launch of n tiles on G CTAs is split when n <= 2 G and ceil(n c / G) < ceil(n / G) c
+# k-blocks; a launch of n tiles on G CTAs splits all its tiles when n <= 2 G and
+# ceil(n c / G) < ceil(n / G) c (otherwise at most the tiles of its last, partial round)
 def _chunks(nk):
     q = nk // 24
     return 4 if q >= 4 else 2 if q >= 2 else 1
