@@ -81,6 +81,7 @@ __global__ void enqueue_kernel(LayerView L, Dims d, DevCounters* C, int n,
                                const float* __restrict__ w, const uint32_t* __restrict__ kmask,
                                const uint32_t* __restrict__ gens) {
   const int lane = threadIdx.x & 31;
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");   // the scheduler may start; it waits
   const long long total = (long long)n * d.KS;
   const long long total_r = (total + 31) & ~31ll;
   const long long stride = (long long)gridDim.x * blockDim.x;
@@ -158,7 +159,10 @@ __global__ void __launch_bounds__(1024) schedule_kernel(LayerView L, Dims d, Ste
                                                         TileGeom g, int layer, int trace_cap,
                                                         int4* trace, long long weight_bytes_per_run) {
   __shared__ PlanScratch sc;
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");   // GEMM1 may start; it waits
+  // launched as a programmatic dependent of the kernel before it (the last enqueue or
+  // GEMM2): wait for it, then let GEMM1 start; GEMM1 waits for this plan
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   plan_layer(L, d, P, C, pol, g, layer, trace_cap, trace, weight_bytes_per_run, (int)C->steps + 1, true, sc);
 }
 
@@ -166,9 +170,10 @@ __global__ void __launch_bounds__(1024) schedule_kernel(LayerView L, Dims d, Ste
 // Copy ready rows (in completion order) to the caller, then reclaim each slot: clear its
 // accepted mask and landing count and advance its generation, after the row was read.
 template <typename T>
-__global__ void collect_kernel(LayerView L, Dims d, int max_out, T* __restrict__ y_out,
+__global__ void collect_kernel(LayerView L, Dims d, DevCounters* C, int max_out, T* __restrict__ y_out,
                                int32_t* __restrict__ slot_out, uint32_t* __restrict__ gen_out,
-                               const int32_t* __restrict__ n_io, int append, int parts) {
+                               int32_t* __restrict__ n_io, int append, int parts) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");   // launched as a dependent of GEMM2
   const uint32_t rh = L.ready_ht[0], rt = L.ready_ht[1];
   const int base = append ? *n_io : 0;
   const int n = max(0, min((int)(rt - rh), max_out - base));
@@ -188,6 +193,18 @@ __global__ void collect_kernel(LayerView L, Dims d, int max_out, T* __restrict__
       L.done[slot] = 0u;
       L.landed[slot] = 0u;
       L.gen[slot] = L.gen[slot] + 1u;
+    }
+  }
+  // the block that finishes last (every block has read the ring and the caller's count by
+  // then) advances the ring head and writes the count
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(&L.ready_ht[2], 1u) == gridDim.x - 1) {
+      L.ready_ht[2] = 0u;
+      L.ready_ht[0] = rh + (uint32_t)n;
+      C->ready -= n;
+      *n_io = base + n;
     }
   }
 }
@@ -218,17 +235,24 @@ __global__ void cancel_kernel(LayerView L, Dims d, DevCounters* C, int n, const 
   }
 }
 
-__global__ void collect_finish_kernel(LayerView L, Dims d, DevCounters* C, int max_out,
-                                      int32_t* n_io, int append) {
-  const uint32_t rh = L.ready_ht[0], rt = L.ready_ht[1];
-  const int base = append ? *n_io : 0;
-  const int n = max(0, min((int)(rt - rh), max_out - base));
-  L.ready_ht[0] = rh + (uint32_t)n;
-  C->ready -= n;
-  *n_io = base + n;
-}
-
 // -------------------------------------------------------------- utilities
+
+// Launch as a programmatic dependent of the previous kernel in the stream: the kernel may
+// start before that one finishes and orders itself with griddepcontrol.wait.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
 
 bool valid_stream_layer(moe_async_t h, int layer) {
   return h && layer >= 0 && layer < h->cfg.num_layers;
@@ -405,7 +429,7 @@ moe_status moe_async_create(const moe_async_config* cfg, const void* const* w1,
     ok = ok && dalloc(&L.head, (size_t)d.NB * 4) == cudaSuccess;
     ok = ok && dalloc(&L.tail, (size_t)d.NB * 4) == cudaSuccess;
     ok = ok && dalloc(&L.ready, S * 4) == cudaSuccess;
-    ok = ok && dalloc(&L.ready_ht, 2 * 4) == cudaSuccess;
+    ok = ok && dalloc(&L.ready_ht, 4 * 4) == cudaSuccess;
     if (ok && swiglu) {
       void* p13 = nullptr;
       void* p2 = nullptr;
@@ -423,7 +447,7 @@ moe_status moe_async_create(const moe_async_config* cfg, const void* const* w1,
            cudaMemsetAsync(L.gen, 0, S * 4, s) == cudaSuccess &&
            cudaMemsetAsync(L.head, 0, (size_t)d.NB * 4, s) == cudaSuccess &&
            cudaMemsetAsync(L.tail, 0, (size_t)d.NB * 4, s) == cudaSuccess &&
-           cudaMemsetAsync(L.ready_ht, 0, 8, s) == cudaSuccess &&
+           cudaMemsetAsync(L.ready_ht, 0, 16, s) == cudaSuccess &&
            cudaMemsetAsync(L.records, 0, (size_t)d.NB * d.cap * 4, s) == cudaSuccess &&
            cudaMemsetAsync(L.slotbuf, 0, S * KS * H * 4, s) == cudaSuccess;
     }
@@ -510,10 +534,11 @@ moe_status moe_async_schedule_step(moe_async_t h, int32_t layer, const moe_async
   const long long wbytes = h->cfg.expert_kind == MOE_EXPERT_SWIGLU
                                ? 3ll * d.H * d.I * (long long)elem_size(d.dtype) : 0ll;
   prof_begin(h, MOE_KERNEL_SCHEDULE, s);
-  schedule_kernel<<<1, 1024, 0, s>>>(h->layers[layer], d, h->plan, h->counters, *policy, h->geom,
-                                     layer, h->cfg.trace_capacity, h->trace, wbytes);
+  const cudaError_t e = launch_dependent(schedule_kernel, dim3(1), dim3(1024), s, h->layers[layer], d, h->plan,
+                                         h->counters, *policy, h->geom, (int)layer, (int)h->cfg.trace_capacity,
+                                         h->trace, wbytes);
   prof_end(h, MOE_KERNEL_SCHEDULE, s);
-  if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
   if (h->cfg.expert_kind == MOE_EXPERT_IDENTITY) return launch_identity(h, layer, s);
   if (h->use_tc) return launch_ffn_tc(h, layer, s);
   return launch_ffn_simt(h, layer, s);
@@ -529,18 +554,17 @@ moe_status moe_async_collect(moe_async_t h, int32_t layer, int32_t max_out, void
   const Dims& d = h->dims;
   const int grid = std::max(1, std::min(max_out, h->num_sms * 4));
   prof_begin(h, MOE_KERNEL_COLLECT, s);
-  if (max_out > 0) {
-    if (d.dtype == MOE_BF16)
-      collect_kernel<__nv_bfloat16><<<grid, 128, 0, s>>>(h->layers[layer], d, max_out,
-          static_cast<__nv_bfloat16*>(d_y_out), d_slot_out, d_gen_out, d_n_out, append, h->parts_per_pair);
-    else
-      collect_kernel<float><<<grid, 128, 0, s>>>(h->layers[layer], d, max_out,
-          static_cast<float*>(d_y_out), d_slot_out, d_gen_out, d_n_out, append, h->parts_per_pair);
-  }
-  collect_finish_kernel<<<1, 1, 0, s>>>(h->layers[layer], d, h->counters, max_out, d_n_out, append);
-  h->launches += max_out > 0 ? 1 : 0;
+  cudaError_t e;
+  if (d.dtype == MOE_BF16)
+    e = launch_dependent(collect_kernel<__nv_bfloat16>, dim3(grid), dim3(128), s, h->layers[layer], d, h->counters,
+                     (int)max_out, static_cast<__nv_bfloat16*>(d_y_out), d_slot_out, d_gen_out, d_n_out,
+                     (int)append, h->parts_per_pair);
+  else
+    e = launch_dependent(collect_kernel<float>, dim3(grid), dim3(128), s, h->layers[layer], d, h->counters,
+                     (int)max_out, static_cast<float*>(d_y_out), d_slot_out, d_gen_out, d_n_out, (int)append,
+                     h->parts_per_pair);
   prof_end(h, MOE_KERNEL_COLLECT, s);
-  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 moe_status moe_async_sync(moe_async_t h, void* stream) {

@@ -427,6 +427,9 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
     griddep_wait();
     griddep_launch_dependents();
   }
+  // GEMM2: the collect launched after it may start and wait (GEMM2 itself waits for GEMM1
+  // before reading h, so its completion implies GEMM1's)
+  if (MODE == kModeGemm2) griddep_launch_dependents();
   int n_tiles, layer;
   if (MODE == kModeAtt) {
     const bool picked = p.sd.ctl->pick_kind == 1;

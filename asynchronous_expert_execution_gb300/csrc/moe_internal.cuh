@@ -76,7 +76,8 @@ struct LayerView {
   uint32_t* head;
   uint32_t* tail;
   int32_t* ready;
-  uint32_t* ready_ht;   // [0] = head (collected up to), [1] = tail (appended up to)
+  uint32_t* ready_ht;   // [0] = head (collected up to), [1] = tail (appended up to),
+                        // [2] = blocks of the running collect that have finished
   const void* w13;
   const void* w2;
 };
