@@ -3,8 +3,8 @@
 //
 // Swap-AB grouped GEMM.  Each tile computes D[128 x N] = A[128 x K] * B[N x K]^T where
 //   A = 128 rows of an expert's packed weights (K-major, 128B-swizzled, loaded by TMA), and
-//   B = N <= BN gathered token rows of the step's batch for that expert (K-major, 128B
-//       swizzle applied by the loader),
+//   B = N gathered token rows of the step's batch for that expert (K-major, 128B swizzle
+//       applied by the loader), N <= 32 for a small item and <= 128 for a large one,
 // so a decode batch of a few tokens per expert still fills the 128-row MMA with weights and
 // the kernel streams each picked expert's weights once per token tile.
 //   GEMM1: A = W13 (gate/up rows interleaved in blocks of 16), K = H, B = pool rows of the
@@ -12,9 +12,12 @@
 //          the operand load); epilogue: h = silu(gate) * up, stored bf16.
 //   GEMM2: A = W2^T, K = I, B = the expert's h rows; epilogue: slotbuf[slot][k] = w * o
 //          (fp32), then readiness counting and the top-k merge y = sum_k (ascending k).
+// K may be cut into fixed chunks whose partials are added in chunk order; a launch with few
+// tiles spreads a tile's chunks over CTAs (see Unit).
 //
 // Warp roles (256 threads, one persistent CTA per SM):
-//   warp 0  lane 0: TMA producer for A       warp 1: cp.async producer for B (gather)
+//   warp 0  lane 0: TMA producer for A (and for GEMM2's B)
+//   warps 1, 3: cp.async producers for the gathered B (GEMM1, attention projection)
 //   warp 2  lane 0: MMA issuer; warp 2 allocates / frees TMEM
 //   warps 4-7: epilogue (TMEM lanes 32*(warp-4) ..), double-buffered accumulators
 // Every wait is bounded in time; a timeout latches MOE_ERR_TIMEOUT, stops all roles, and the
