@@ -457,28 +457,48 @@ __device__ void land_and_merge(const LayerView& L, const Dims& d, DevCounters* C
   __threadfence();
   bar();
   // the merge of every finished token's slice: (token, 4 features) items spread over the
-  // group, so the loads of different tokens are in flight together (H % 8 == 0 and f0 a
-  // multiple of 8 make every item 16-byte aligned)
+  // group, four items per thread at a time, so the loads of different tokens are in flight
+  // together (H % 8 == 0 and f0 a multiple of 8 make every item 16-byte aligned)
   const int fend = min(f0 + fcount, d.H);
   const int nvec = (fend - f0) >> 2;
-  for (int w = tid; w < nj * nvec; w += nthr) {
-    const int j = w / nvec;
-    if (!fin[j]) continue;
-    const int f = f0 + 4 * (w - j * nvec);
-    const int slot = slots[j];
-    const float* src = L.slotbuf + (size_t)slot * d.KS * d.H + f;
-    float4 a = __ldcg(reinterpret_cast<const float4*>(src));
-#pragma unroll 8
-    for (int k = 1; k < d.KS; ++k) {
-      const float4 b = __ldcg(reinterpret_cast<const float4*>(src + (size_t)k * d.H));
-      a.x += b.x;
-      a.y += b.y;
-      a.z += b.z;
-      a.w += b.w;
+  const int total = nj * nvec;
+  constexpr int kU = 4;
+  for (int w0 = tid; w0 < total; w0 += kU * nthr) {
+    const float* src[kU];
+    int slot[kU], f[kU];
+    bool act[kU];
+    float4 a[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int w = w0 + u * nthr;
+      const int j = w < total ? w / nvec : 0;
+      act[u] = w < total && fin[j];
+      slot[u] = act[u] ? slots[j] : 0;
+      f[u] = f0 + 4 * (w - j * nvec);
+      src[u] = L.slotbuf + (size_t)slot[u] * d.KS * d.H + f[u];
+      if (act[u]) a[u] = __ldcg(reinterpret_cast<const float4*>(src[u]));
     }
-    store4<T>(reinterpret_cast<T*>(L.y) + (size_t)slot * d.H + f, a);
-    if (sd)                                          // req_n is stable until the last slice
-      store4<T>(static_cast<T*>(sd->hist) + ((size_t)slot * (sd->n_max + 1) + sd->req_n[slot] + 1) * d.H + f, a);
+#pragma unroll 4
+    for (int k = 1; k < d.KS; ++k) {
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        if (act[u]) {
+          const float4 b = __ldcg(reinterpret_cast<const float4*>(src[u] + (size_t)k * d.H));
+          a[u].x += b.x;
+          a[u].y += b.y;
+          a[u].z += b.z;
+          a[u].w += b.w;
+        }
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      if (!act[u]) continue;
+      store4<T>(reinterpret_cast<T*>(L.y) + (size_t)slot[u] * d.H + f[u], a[u]);
+      if (sd)                                        // req_n is stable until the last slice
+        store4<T>(static_cast<T*>(sd->hist) + ((size_t)slot[u] * (sd->n_max + 1) + sd->req_n[slot[u]] + 1) * d.H + f[u],
+                  a[u]);
+    }
   }
   __threadfence();
   bar();
