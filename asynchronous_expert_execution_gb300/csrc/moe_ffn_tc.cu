@@ -285,7 +285,8 @@ struct TcParams {
 };
 
 // A unit of work: one tile and a range of its K chunks [c0, c1).  The first n_whole tiles of a
-// launch are one unit each (all chunks); each later tile is split into one unit per chunk.
+// launch are one unit each (all chunks); each later tile is split into one unit per chunk
+// (n_whole is 0 or the launch's tile count).
 struct Unit {
   int t, c0, c1;
   bool split;
@@ -447,22 +448,18 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
   const CUtensorMap* tmA = &p.mapA[layer < 0 || layer >= kMaxLayers ? 0 : layer];
   const int Kdim = MODE == kModeGemm2 ? d.I : d.H;
   const int nk = (Kdim + kBK - 1) / kBK;
-  // Tiles are split into their K chunks (one unit each) where that shortens the launch: all
-  // of them when the launch has few tiles for the grid (a single SM streams weights far
-  // below the HBM rate, so a lone expert needs many SMs), else the tiles of the last,
-  // partial round, so the round ends sooner on more SMs.  Every role derives the same split
-  // from the plan.
+  // A launch with few tiles for the grid splits every tile into its K chunks (one unit each)
+  // when that shortens the launch: a single SM streams weights far below the HBM rate, so a
+  // lone expert needs many SMs.  Every role derives the same split from the plan.  (Splitting
+  // only the last, partial round's tiles was measured too: with the 45-k-block GPT-OSS
+  // contractions cut in 2 for it, decode lost 0.4% and prefill 1.5%.)
   const int nchunk = p.nchunk;
   int n_whole = n_tiles;
-  if (nchunk > 1) {
+  if (nchunk > 1 && n_tiles <= p.split_cap) {
     const int G = (int)gridDim.x;
     const long long whole = (long long)((n_tiles + G - 1) / G) * nchunk;   // in chunk times
     const long long split = ((long long)n_tiles * nchunk + G - 1) / G;
-    const int tail = n_tiles % G;
-    if (n_tiles <= p.split_cap && split < whole)
-      n_whole = 0;
-    else if (tail > 0 && tail <= p.split_cap && tail * nchunk <= G)
-      n_whole = n_tiles - tail;
+    if (split < whole) n_whole = 0;
   }
   const int n_units = n_whole + (n_tiles - n_whole) * nchunk;
   if ((int)blockIdx.x >= n_units) return;        // no work for this CTA: skip all set-up
@@ -926,8 +923,7 @@ void fill_common(moe_async_s* h, TcParams& p) {
 // k-blocks each, so a chunk's partial (BN x 128 fp32) stays small next to the weight bytes
 // the chunk streams.  Measured on GB300 (pairs/s): 24 leaves the GPT-OSS shapes (45 k-blocks)
 // whole and cuts the 7168-deep GEMM1 of the DeepSeek-wide layer in 4 -- c4 +15%; 16 also
-// cuts the GPT-OSS GEMMs in 2, which costs decode 0.5% and prefill 1.2%; 22 cuts them in 2
-// so the last round's tiles can be split: decode -0.4%, prefill -1.5%, streaming -0.8%.
+// cuts the GPT-OSS GEMMs in 2, which costs decode 0.5% and prefill 1.2%.
 #ifndef MOE_SPLIT_MIN_KB
 #define MOE_SPLIT_MIN_KB 24
 #endif

@@ -19,7 +19,7 @@ pytestmark = pytest.mark.gpu
 
 # the kernels' rules: a contraction of nk 64-wide k-blocks has 1, 2 or 4 chunks of >= 24
 # k-blocks; a launch of n tiles on G CTAs splits all its tiles when n <= 2 G and
-# ceil(n c / G) < ceil(n / G) c (otherwise at most the tiles of its last, partial round)
+# ceil(n c / G) < ceil(n / G) c
 def _chunks(nk):
     q = nk // 24
     return 4 if q >= 4 else 2 if q >= 2 else 1
