@@ -81,7 +81,10 @@ __global__ void enqueue_kernel(LayerView L, Dims d, DevCounters* C, int n,
                                const float* __restrict__ w, const uint32_t* __restrict__ kmask,
                                const uint32_t* __restrict__ gens) {
   const int lane = threadIdx.x & 31;
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");   // the scheduler may start; it waits
+  // launched as a programmatic dependent of the kernel before it (e.g. the previous collect):
+  // wait for it, then let the scheduler start; the scheduler waits for this kernel
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const long long total = (long long)n * d.KS;
   const long long total_r = (total + 31) & ~31ll;
   const long long stride = (long long)gridDim.x * blockDim.x;
@@ -174,6 +177,7 @@ __global__ void collect_kernel(LayerView L, Dims d, DevCounters* C, int max_out,
                                int32_t* __restrict__ slot_out, uint32_t* __restrict__ gen_out,
                                int32_t* __restrict__ n_io, int append, int parts) {
   asm volatile("griddepcontrol.wait;" ::: "memory");   // launched as a dependent of GEMM2
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const uint32_t rh = L.ready_ht[0], rt = L.ready_ht[1];
   const int base = append ? *n_io : 0;
   const int n = max(0, min((int)(rt - rh), max_out - base));
@@ -514,14 +518,16 @@ moe_status moe_async_enqueue(moe_async_t h, int32_t layer, int32_t n, const int3
   int grid = (int)std::min<long long>((work + 255) / 256, (long long)h->num_sms * 8);
   if (grid < 1) grid = 1;
   prof_begin(h, MOE_KERNEL_ENQUEUE, s);
+  cudaError_t e;
   if (d.dtype == MOE_BF16)
-    enqueue_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(h->layers[layer], d, h->counters, n, d_rows, d_slot,
-        static_cast<const __nv_bfloat16*>(d_x), d_expert, d_w, d_kmask, d_gen);
+    e = launch_dependent(enqueue_kernel<__nv_bfloat16>, dim3(grid), dim3(256), s, h->layers[layer], d, h->counters,
+                         (int)n, d_rows, d_slot, static_cast<const __nv_bfloat16*>(d_x), d_expert, d_w, d_kmask,
+                         d_gen);
   else
-    enqueue_kernel<float><<<grid, 256, 0, s>>>(h->layers[layer], d, h->counters, n, d_rows, d_slot,
-        static_cast<const float*>(d_x), d_expert, d_w, d_kmask, d_gen);
+    e = launch_dependent(enqueue_kernel<float>, dim3(grid), dim3(256), s, h->layers[layer], d, h->counters, (int)n,
+                         d_rows, d_slot, static_cast<const float*>(d_x), d_expert, d_w, d_kmask, d_gen);
   prof_end(h, MOE_KERNEL_ENQUEUE, s);
-  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 moe_status moe_async_schedule_step(moe_async_t h, int32_t layer, const moe_async_policy* policy,
