@@ -462,7 +462,12 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
     if (split < whole) n_whole = 0;
   }
   const int n_units = n_whole + (n_tiles - n_whole) * nchunk;
-  if ((int)blockIdx.x >= n_units) return;        // no work for this CTA: skip all set-up
+  if ((int)blockIdx.x >= n_units) {              // no work for this CTA: skip all set-up
+    // every CTA of a programmatic dependent waits for its predecessor before it ends, so this
+    // launch's completion implies GEMM1's even when it has no work
+    if (MODE == kModeGemm2) griddep_wait();
+    return;
+  }
 
   if (threadIdx.x == 0) {
     prefetch_tmap(tmA);                        // descriptors load while the CTA sets up
