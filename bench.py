@@ -13,6 +13,7 @@ Prints one JSON line.  With N > 1 (torchrun) every rank runs an independent repl
 workload (weak scaling, no data-path collective); the timing is the max over ranks.
 """
 import argparse
+import re
 import hashlib
 import json
 import math
@@ -113,12 +114,17 @@ KERNEL_SOURCES = ("moe_ffn_tc.cu", "moe_internal.cuh")
 
 
 def source_hash(files=KERNEL_SOURCES):
-    """Hash of the sources the FFN kernels are built from (ncu counters go stale on change)."""
+    """Hash of the code the FFN kernels are built from (ncu counters go stale when it changes).
+    Comments and whitespace are left out, so editing a comment keeps the counters valid."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, "asynchronous_expert_execution_gb300", "csrc")
     for f in sorted(files):
-        with open(os.path.join(d, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+        with open(os.path.join(d, f), encoding="utf-8") as fh:
+            code = fh.read()
+        code = re.sub(r"/\*.*?\*/", " ", code, flags=re.S)        # block comments
+        code = re.sub(r"//[^\n]*", " ", code)                       # line comments
+        code = " ".join(code.split())
+        h.update(f.encode() + code.encode())
     return h.hexdigest()[:16]
 
 
