@@ -77,6 +77,16 @@ def test_host_validation_without_gpu(lib):
     assert lib.moe_async_schedule_step(None, 0, ctypes.byref(pol), None) == N.MOE_ERR_INVALID
     assert lib.moe_async_enqueue(None, 0, 1, None, None, None, None, None, None, None, None) == N.MOE_ERR_INVALID
     assert lib.moe_async_destroy(None, None) == N.MOE_ERR_INVALID
+    # allocation-free forward: argument and size checks come before any CUDA call
+    fwd = lib.moe_async_forward_noalloc
+    p = ctypes.c_void_p(256)                   # never dereferenced: every call below returns early
+    assert fwd(-1, 8, 2, 64, 128, 1, p, p, p, p, p, p, p, None) == N.MOE_ERR_INVALID
+    assert fwd(4, 8, 9, 64, 128, 1, p, p, p, p, p, p, p, None) == N.MOE_ERR_INVALID       # K > E
+    assert fwd(4, 8, 2, 64, 128, 7, p, p, p, p, p, p, p, None) == N.MOE_ERR_INVALID       # dtype
+    assert fwd(4, 8, 2, 64, 128, 1, None, p, p, p, p, p, p, None) == N.MOE_ERR_INVALID    # no x
+    assert fwd(0, 8, 2, 64, 128, 1, None, None, None, None, None, None, None, None) == N.MOE_OK
+    # scratch is 16 MiB of fp32 h rows: T * K * I * 4 bytes must fit
+    assert fwd(1024, 8, 2, 64, 4096, 1, p, p, p, p, p, p, p, None) == N.MOE_ERR_CAPACITY   # 32 MiB
 
 
 def test_product_path_has_no_oracle_import():
