@@ -31,6 +31,10 @@
  *     _get_stats) and stays set until moe_async_destroy.
  *   - No call blocks without bound: moe_async_wait is limited by a step count.
  *   - Thread safety: a handle is not thread-safe; distinct handles are.
+ *   - Kernels are launched as programmatic dependents of the kernel before them
+ *     in the stream (they may start early and wait on the device for it to
+ *     finish), so every call still sees all earlier work of the stream; the
+ *     caller's own kernels, copies and events order as usual.
  */
 #ifndef MOE_ASYNC_H
 #define MOE_ASYNC_H
