@@ -280,7 +280,9 @@ def run_reference(args, rank, world):
             "warmup": args.warmup, "ms_per_step": 1e3 * tot_t / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "impl": "reference",
-            "config": {"workload": spec.name, "sample": desc},
+            "config": {"workload": spec.name, "experts": spec.layer.num_experts, "top_k": spec.layer.top_k,
+                       "hidden": spec.layer.hidden, "inter": spec.layer.inter, "tokens": spec.tokens,
+                       "waves": spec.num_waves, "policy": spec.policy, "sample": desc},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
