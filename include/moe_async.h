@@ -53,7 +53,10 @@ typedef enum {
   MOE_ERR_CAPACITY = 2,     /* a per-expert bucket or the ready ring overflowed          */
   MOE_ERR_DUPLICATE = 3,    /* a (slot, k) pair was delivered twice; the copy is dropped */
   MOE_ERR_STALE = 4,        /* a pair carried an out-of-date slot generation; dropped    */
-  MOE_ERR_TIMEOUT = 5,      /* moe_async_wait ran out of steps with tokens still open    */
+  MOE_ERR_TIMEOUT = 5,      /* moe_async_wait ran out of steps with tokens still open;   */
+                            /* or (sticky) a device wait in the tensor-core kernels     */
+                            /* exceeded its 2 s bound -- the handle's state is then     */
+                            /* undefined and it should be destroyed                     */
   MOE_ERR_CUDA = 6,         /* a CUDA runtime call failed                                */
   MOE_ERR_UNSUPPORTED = 7   /* shape/dtype combination not supported by the kernels      */
 } moe_status;
