@@ -171,6 +171,33 @@ def threshold_pick(depths, min_batch, max_groups=0, fallback_groups=1):
     return mtfs_pick(depths, fallback_groups)
 
 
+def rank_pick(depths, ranks, steal=True):
+    """Simulated expert-parallel ranks on one device ("asynchronous MoE serving" notes,
+    CascadeEP v1: unstarted expert work can be reassigned to an idle helper; StreamEP section
+    4 for the pick within a rank).
+
+    Expert e belongs to rank ``e mod ranks``.  Each rank runs its own deepest non-empty
+    bucket (equal depth -> lower id).  With ``steal``, every rank that owns no non-empty
+    bucket then takes, in rank order, the deepest non-empty bucket that no rank has picked
+    (equal depth -> lower id).  Returns the picks in rank order."""
+    picks = [None] * ranks
+    for r in range(ranks):
+        own = [(-depths[e], e) for e in range(r, len(depths), ranks) if depths[e] > 0]
+        if own:
+            picks[r] = min(own)[1]
+    if steal:
+        taken = {e for e in picks if e is not None}
+        for r in range(ranks):
+            if picks[r] is not None:
+                continue
+            for e in mtfs_pick(depths):
+                if e not in taken:
+                    picks[r] = e
+                    taken.add(e)
+                    break
+    return [e for e in picks if e is not None]
+
+
 def defrag_score(q_now, lookahead, delta):
     """Defragmenting score, StreamEP section 4:
     S(s) = Q(s) + sum_{j=1..W} delta^j [Q(s_j) + H(s_j)].

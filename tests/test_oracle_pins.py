@@ -249,6 +249,47 @@ def pin_policies_hand():
     assert om.threshold_pick([0, 0, 0], 1) == []
 
 
+def pin_rank_pick_hand():
+    # worked by hand: expert e belongs to rank e mod R; a rank runs its deepest bucket (tie ->
+    # lower id); an idle rank steals the deepest bucket nobody picked; picks in rank order
+    d = [5, 0, 3, 0, 2, 7, 0, 1]
+    assert om.rank_pick(d, 2) == [0, 5]
+    assert om.rank_pick(d, 4) == [0, 5, 2, 7]
+    d = [5, 0, 0, 0, 2, 0, 4, 0]
+    assert om.rank_pick(d, 4) == [0, 4, 6]                   # rank 1 steals bucket 4
+    assert om.rank_pick(d, 4, steal=False) == [0, 6]
+    assert om.rank_pick([2, 2, 2, 2], 2) == [0, 1]
+    assert om.rank_pick([2, 2, 2, 2], 3) == [0, 1, 2]
+    assert om.rank_pick([0, 3, 0, 3, 0, 0], 3) == [3, 1]     # nothing left to steal
+    assert om.rank_pick([6, 0, 5, 0], 2) == [0, 2]
+    assert om.rank_pick([6, 0, 5, 0], 2, steal=False) == [0]
+    assert om.rank_pick([5, 0, 0, 0, 4, 0, 1, 0], 2) == [0, 4]   # the deeper of two candidates
+    assert om.rank_pick([5, 0, 0, 0, 4, 0, 1, 0], 4) == [0, 4, 6]
+    assert om.rank_pick([0, 0, 0], 2) == []
+
+
+def test_rank_pick_hand():
+    pin_rank_pick_hand()
+
+
+def test_rank_pick_invariants():
+    rng = np.random.default_rng(7)
+    for _ in range(300):
+        nb = int(rng.integers(1, 12))
+        R = int(rng.integers(1, 14))
+        d = [int(v) if rng.random() < 0.6 else 0 for v in rng.integers(1, 5, nb)]
+        nonempty = [e for e in range(nb) if d[e] > 0]
+        owners = {r for r in range(R) if any(d[e] > 0 for e in range(r, nb, R))}
+        for steal in (True, False):
+            p = om.rank_pick(d, R, steal)
+            assert len(set(p)) == len(p) and all(d[e] > 0 for e in p)
+            assert len(p) == (min(R, len(nonempty)) if steal else len(owners))
+        if R == 1:                                       # one rank: plain MTFS, one bucket
+            assert om.rank_pick(d, 1) == om.mtfs_pick(d, 1)
+        if R >= nb:                                      # a rank per bucket: every non-empty one
+            assert om.rank_pick(d, R) == nonempty
+
+
 def pin_schedule_trace_hand():
     # t0 -> e0, t1 -> e1, t2 -> e1, t3 -> e2 (K = 1); waves at ticks 1, 1, 3
     idx = np.array([[0], [1], [1], [2]])
@@ -351,9 +392,26 @@ def test_pins_catch_planted_mistakes(monkeypatch):
     # 6. defrag score without the decay exponent
     monkeypatch.setattr(om, "defrag_score", lambda q, la, dl: q + sum(dl * (a + b) for a, b in la))
     assert _fails(pin_defrag_golden)
+    monkeypatch.undo()
+    # 7. stealing the shallowest bucket instead of the deepest
+    real_rank = om.rank_pick
+
+    def rank_shallow(d, R, steal=True):
+        own = real_rank(d, R, steal=False)
+        if not steal:
+            return own
+        picks = {r: e for r in range(R) for e in own if e % R == r}
+        left = [e for e in reversed(om.mtfs_pick(d)) if e not in own]
+        for r in range(R):
+            if r not in picks and left:
+                picks[r] = left.pop(0)
+        return [picks[r] for r in range(R) if r in picks]
+    monkeypatch.setattr(om, "rank_pick", rank_shallow)
+    assert _fails(pin_rank_pick_hand)
 
 
 def test_pins_pass_unmodified():
+    pin_rank_pick_hand()
     for p in (pin_route_bruteforce, pin_route_hand, pin_silu, pin_ffn_closed_form,
               pin_identity_experts_exact, pin_policies_hand, pin_schedule_trace_hand, pin_defrag_golden):
         p()
