@@ -8,7 +8,7 @@ LIB_PATH = os.path.join(_HERE, "libmoe_async.so")
 MOE_OK, MOE_ERR_INVALID, MOE_ERR_CAPACITY, MOE_ERR_DUPLICATE, MOE_ERR_STALE, \
     MOE_ERR_TIMEOUT, MOE_ERR_CUDA, MOE_ERR_UNSUPPORTED = range(8)
 MOE_F32, MOE_BF16 = 0, 1
-MOE_POLICY_MTFS, MOE_POLICY_THRESHOLD = 0, 1
+MOE_POLICY_MTFS, MOE_POLICY_THRESHOLD, MOE_POLICY_RANKS = 0, 1, 2
 MOE_EXPERT_SWIGLU, MOE_EXPERT_IDENTITY = 0, 1
 
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID", 2: "MOE_ERR_CAPACITY", 3: "MOE_ERR_DUPLICATE",

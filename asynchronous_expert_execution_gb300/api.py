@@ -27,14 +27,15 @@ def _stream(stream):
 @dataclass
 class Policy:
     """Scheduling policy of one step (mirrors moe_async_policy)."""
-    kind: str = "mtfs"            # "mtfs" | "threshold"
-    max_groups: int = 0           # 0 = every qualifying bucket
+    kind: str = "mtfs"            # "mtfs" | "threshold" | "ranks"
+    max_groups: int = 0           # 0 = every qualifying bucket; "ranks": the number of ranks
     min_batch: int = 64
-    fallback_groups: int = 1
+    fallback_groups: int = 1      # "threshold": buckets taken when none qualifies; "ranks": steal
+
+    _KINDS = {"mtfs": N.MOE_POLICY_MTFS, "threshold": N.MOE_POLICY_THRESHOLD, "ranks": N.MOE_POLICY_RANKS}
 
     def c(self):
-        k = N.MOE_POLICY_MTFS if self.kind == "mtfs" else N.MOE_POLICY_THRESHOLD
-        return N.Policy(k, self.max_groups, self.min_batch, self.fallback_groups)
+        return N.Policy(self._KINDS[self.kind], self.max_groups, self.min_batch, self.fallback_groups)
 
     @staticmethod
     def from_spec(spec):

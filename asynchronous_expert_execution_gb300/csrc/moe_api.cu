@@ -7,7 +7,7 @@
 #include <cstring>
 #include <algorithm>
 #include <new>
-#include "moe_internal.cuh"
+#include "moe_plan.cuh"
 
 using namespace moe;
 
@@ -533,8 +533,10 @@ moe_status moe_async_enqueue(moe_async_t h, int32_t layer, int32_t n, const int3
 moe_status moe_async_schedule_step(moe_async_t h, int32_t layer, const moe_async_policy* policy,
                                    void* stream) {
   if (!valid_stream_layer(h, layer) || !policy) return MOE_ERR_INVALID;
-  if (policy->kind != MOE_POLICY_MTFS && policy->kind != MOE_POLICY_THRESHOLD) return MOE_ERR_INVALID;
+  if (policy->kind != MOE_POLICY_MTFS && policy->kind != MOE_POLICY_THRESHOLD && policy->kind != MOE_POLICY_RANKS)
+    return MOE_ERR_INVALID;
   if (policy->max_groups < 0 || policy->min_batch < 0 || policy->fallback_groups < 0) return MOE_ERR_INVALID;
+  if (policy->kind == MOE_POLICY_RANKS && policy->max_groups < 1) return MOE_ERR_INVALID;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const Dims& d = h->dims;
   const long long wbytes = h->cfg.expert_kind == MOE_EXPERT_SWIGLU

@@ -1,0 +1,154 @@
+// Device-side scheduling of one layer's micro-queues: reads every bucket depth, applies the
+// pick policy and writes the step's work list (StepPlan).  Kept apart from the FFN kernels'
+// header: only the scheduling and streaming kernels compile it.
+#pragma once
+#include "moe_internal.cuh"
+
+namespace moe {
+
+// One CTA (blockDim multiple of 32, >= 32).  Reads every bucket depth of the layer,
+// applies the policy, drains the picked buckets whole (head += depth) and writes the work
+// list the FFN kernels consume.  MTFS (StreamEP section 4): deepest first, equal depth ->
+// lower bucket id.  THRESHOLD (streamFFN reading): buckets with depth >= min_batch, deepest
+// first; if none, MTFS over non-empty buckets limited to fallback_groups.  With
+// enabled = false the plan is written empty and nothing is drained or counted.
+struct PlanScratch {
+  int depth[kMaxBuckets];
+  int order[kMaxBuckets];
+  int pick[kMaxBuckets];          // RANKS: each rank's bucket (-1: none)
+  unsigned char taken[kMaxBuckets];
+  int n_elig, n_nonempty, n_picks;
+};
+
+__device__ inline void plan_layer(const LayerView& L, const Dims& d, StepPlan* P, DevCounters* C,
+                                  const moe_async_policy& pol, const TileGeom& g, int layer,
+                                  int trace_cap, int4* trace, long long weight_bytes_per_run,
+                                  int trace_step, bool enabled, PlanScratch& sc) {
+  int* depth = sc.depth;
+  int* order = sc.order;
+  const int tid = threadIdx.x, nt = blockDim.x;
+  if (tid == 0) { sc.n_elig = 0; sc.n_nonempty = 0; }
+  __syncthreads();
+  for (int b = tid; b < d.NB; b += nt) {
+    const int dep = enabled ? min((int)(L.tail[b] - L.head[b]), d.cap) : 0;
+    depth[b] = dep;
+    if (dep > 0) atomicAdd(&sc.n_nonempty, 1);
+    if (dep > 0 && (pol.kind != MOE_POLICY_THRESHOLD || dep >= pol.min_batch)) atomicAdd(&sc.n_elig, 1);
+  }
+  __syncthreads();
+  const int n_elig = sc.n_elig, n_nonempty = sc.n_nonempty;
+  int minb = 1, G = pol.kind == MOE_POLICY_RANKS ? 0 : pol.max_groups;
+  if (pol.kind == MOE_POLICY_THRESHOLD) {
+    if (n_elig > 0) minb = pol.min_batch > 1 ? pol.min_batch : 1;
+    else G = pol.fallback_groups > 0 ? pol.fallback_groups : 1;
+  }
+  const int ne = (pol.kind == MOE_POLICY_THRESHOLD && n_elig == 0) ? n_nonempty : n_elig;
+  // After an overflow or an out-of-range id the queues no longer describe valid pairs:
+  // stop executing (the sticky error is reported to the host).
+  const uint32_t err = *(volatile uint32_t*)&C->error;
+  const bool halted = err == MOE_ERR_CAPACITY || err == MOE_ERR_INVALID;
+  int n = halted ? 0 : ((G > 0 && G < ne) ? G : ne);
+  for (int b = tid; b < d.NB; b += nt) {
+    const int db = depth[b];
+    if (db >= minb) {
+      int r = 0;
+      for (int c = 0; c < d.NB; ++c) {
+        const int dc = depth[c];
+        r += (dc >= minb) && (dc > db || (dc == db && c < b));
+      }
+      if (r < n) order[r] = b;
+    }
+  }
+  __syncthreads();
+  if (pol.kind == MOE_POLICY_RANKS) {
+    // simulated expert-parallel ranks: bucket b belongs to rank b mod R; each rank runs its
+    // deepest bucket (equal depth -> lower id); then each rank that owns no non-empty bucket
+    // takes, in rank order, the deepest bucket no rank has picked (order[] holds every
+    // non-empty bucket deepest first); the work list is the picks in rank order
+    const int R = min(max(pol.max_groups, 1), kMaxBuckets);
+    for (int r = tid; r < R; r += nt) {
+      int best = -1;
+      for (int b = r; b < d.NB; b += R)
+        if (depth[b] > 0 && (best < 0 || depth[b] > depth[best])) best = b;
+      sc.pick[r] = best;
+    }
+    for (int b = tid; b < d.NB; b += nt) sc.taken[b] = 0;
+    __syncthreads();
+    if (tid == 0) {
+      for (int r = 0; r < R; ++r)
+        if (sc.pick[r] >= 0) sc.taken[sc.pick[r]] = 1;
+      int q = 0, m = 0;
+      for (int r = 0; r < R; ++r) {
+        if (sc.pick[r] < 0 && pol.fallback_groups != 0) {
+          while (q < n && sc.taken[order[q]]) ++q;
+          if (q < n) {
+            sc.pick[r] = order[q];
+            sc.taken[order[q]] = 1;
+          }
+        }
+        if (sc.pick[r] >= 0) sc.pick[m++] = sc.pick[r];   // compact in rank order (m <= r)
+      }
+      for (int i = 0; i < m; ++i) order[i] = sc.pick[i];
+      sc.n_picks = halted ? 0 : m;
+    }
+    __syncthreads();
+    n = sc.n_picks;
+  }
+  if (tid < 32) {
+    const int lane = tid;
+    int row_run = 0, t1_run = 0, t2_run = 0;
+    const int ft1 = (2 * d.I + g.bm1 - 1) / g.bm1;
+    const int ft2 = (d.H + g.bm2 - 1) / g.bm2;
+    for (int c0 = 0; c0 < n; c0 += 32) {
+      const int r = c0 + lane;
+      int b = 0, cnt = 0, t1 = 0, t2 = 0;
+      if (r < n) {
+        b = order[r];
+        cnt = depth[b];
+        const int w1 = tile_tokens(g, cnt, g.bn1, g.wide_min1), w2 = tile_tokens(g, cnt, g.bn2, g.wide_min2);
+        t1 = ((cnt + w1 - 1) / w1) * ft1;
+        t2 = ((cnt + w2 - 1) / w2) * ft2;
+      }
+      int s_cnt = cnt, s_t1 = t1, s_t2 = t2;      // inclusive prefix sums within the chunk
+      for (int off = 1; off < 32; off <<= 1) {
+        int a = __shfl_up_sync(0xffffffffu, s_cnt, off);
+        int b1 = __shfl_up_sync(0xffffffffu, s_t1, off);
+        int b2 = __shfl_up_sync(0xffffffffu, s_t2, off);
+        if (lane >= off) { s_cnt += a; s_t1 += b1; s_t2 += b2; }
+      }
+      if (r < n) {
+        WorkItem it;
+        it.expert = b;
+        it.head = L.head[b];
+        it.count = cnt;
+        it.row_base = row_run + s_cnt - cnt;
+        it.t1_base = t1_run + s_t1 - t1;
+        it.t2_base = t2_run + s_t2 - t2;
+        P->items[r] = it;
+        L.head[b] = it.head + (uint32_t)cnt;
+        if (trace && trace_cap > 0) {
+          const int ti = atomicAdd(&C->trace_n, 1);
+          if (ti < trace_cap) trace[ti] = make_int4(trace_step, layer, b, cnt);
+        }
+      }
+      row_run += __shfl_sync(0xffffffffu, s_cnt, 31);
+      t1_run += __shfl_sync(0xffffffffu, s_t1, 31);
+      t2_run += __shfl_sync(0xffffffffu, s_t2, 31);
+    }
+    if (lane == 0) {
+      P->layer = layer;
+      P->n_work = n;
+      P->n_tiles1 = t1_run;
+      P->n_tiles2 = t2_run;
+      P->rows = row_run;
+      if (!enabled) return;
+      C->steps += 1ull;
+      C->pairs_executed += (unsigned long long)row_run;
+      C->expert_runs += (unsigned long long)n;
+      C->weight_bytes += (unsigned long long)n * (unsigned long long)weight_bytes_per_run;
+      C->pending_pairs -= row_run;
+    }
+  }
+}
+
+}  // namespace moe

@@ -24,7 +24,7 @@
 #include <algorithm>
 #include <cstring>
 #include <new>
-#include "moe_internal.cuh"
+#include "moe_plan.cuh"
 
 namespace moe {
 namespace {

@@ -65,7 +65,13 @@ typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
 
 typedef enum {
   MOE_POLICY_MTFS = 0,       /* most tokens first: deepest buckets first (StreamEP, section 4) */
-  MOE_POLICY_THRESHOLD = 1   /* buckets holding >= min_batch tokens; else MTFS fallback         */
+  MOE_POLICY_THRESHOLD = 1,  /* buckets holding >= min_batch tokens; else MTFS fallback         */
+  MOE_POLICY_RANKS = 2       /* simulated expert-parallel ranks with work stealing: expert e
+                              * belongs to rank e mod max_groups; each rank runs its deepest
+                              * bucket; with fallback_groups != 0 a rank owning no non-empty
+                              * bucket takes the deepest bucket no rank picked (unstarted work
+                              * reassigned to an idle helper: "asynchronous MoE serving" notes,
+                              * CascadeEP v1).  Picks are planned in rank order.              */
 } moe_policy_kind;
 
 typedef enum {
@@ -89,9 +95,11 @@ typedef struct {
 
 typedef struct {
   int32_t kind;             /* moe_policy_kind                                                 */
-  int32_t max_groups;       /* at most this many buckets per step; 0 = no limit                */
+  int32_t max_groups;       /* at most this many buckets per step; 0 = no limit;
+                             * RANKS: the number of ranks, >= 1                                */
   int32_t min_batch;        /* THRESHOLD: minimum bucket depth to run                          */
-  int32_t fallback_groups;  /* THRESHOLD: buckets taken (deepest first) when none qualifies    */
+  int32_t fallback_groups;  /* THRESHOLD: buckets taken (deepest first) when none qualifies;
+                             * RANKS: nonzero = idle ranks steal                               */
 } moe_async_policy;
 
 typedef struct {

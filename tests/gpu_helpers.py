@@ -31,6 +31,8 @@ def expert_getter(weights, E, host=True):
 def oracle_policy(spec):
     if spec.policy == "mtfs":
         return lambda d: om.mtfs_pick(d, spec.max_groups)
+    if spec.policy == "ranks":
+        return lambda d: om.rank_pick(d, spec.max_groups, spec.fallback_groups != 0)
     return lambda d: om.threshold_pick(d, spec.min_batch, spec.max_groups, spec.fallback_groups)
 
 

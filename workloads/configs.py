@@ -34,7 +34,7 @@ class WorkloadSpec:
     arrival: str = "permute"          # "permute" | "exp" | "index"
     straggler_frac: float = 0.30
     dirichlet_alpha: float = 0.5
-    policy: str = "mtfs"              # "mtfs" | "threshold"
+    policy: str = "mtfs"              # "mtfs" | "threshold" | "ranks" (max_groups = ranks, fallback_groups != 0 = steal)
     min_batch: int = 64
     max_groups: int = 0               # 0 = all qualifying buckets
     fallback_groups: int = 1
@@ -118,6 +118,16 @@ TEST_CONFIGS = {
     "w1": WorkloadSpec(
         name="w1_bf16_wide_tiles", layer=LayerSpec(2, 2, 1000, 496, "bf16"), tokens=256,
         router="normal", waves="even", num_waves=1, arrival="index", policy="mtfs"),
+    # the m1 layer under simulated expert-parallel ranks: 4 ranks with work stealing, and 5
+    # ranks (uneven ownership) without.
+    "r1": WorkloadSpec(
+        name="r1_bf16_ranks_steal", layer=LayerSpec(16, 4, 584, 208, "bf16"), tokens=200,
+        router="normal", waves="even", num_waves=5, arrival="exp", policy="ranks", max_groups=4,
+        fallback_groups=1),
+    "r2": WorkloadSpec(
+        name="r2_bf16_ranks_no_steal", layer=LayerSpec(16, 4, 584, 208, "bf16"), tokens=200,
+        router="normal", waves="even", num_waves=5, arrival="exp", policy="ranks", max_groups=5,
+        fallback_groups=0),
     # bf16 decode-like: many experts, few tokens each.
     "m4": WorkloadSpec(
         name="m4_bf16_decode", layer=LayerSpec(64, 4, 1024, 512, "bf16"), tokens=64,
