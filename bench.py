@@ -13,6 +13,7 @@ Prints one JSON line.  With N > 1 (torchrun) every rank runs an independent repl
 workload (weak scaling, no data-path collective); the timing is the max over ranks.
 """
 import argparse
+import dataclasses
 import re
 import hashlib
 import json
@@ -48,7 +49,26 @@ def parse():
     ap.add_argument("--defrag-window", type=int, default=2)
     ap.add_argument("--defrag-decay", type=float, default=0.5)
     ap.add_argument("--history-window", type=int, default=8)
+    ap.add_argument("--ranks", type=int, default=0,
+                    help="pick policy of the per-layer workloads: R > 0 replaces the workload's policy "
+                         "by R simulated expert-parallel ranks (expert e on rank e mod R)")
+    ap.add_argument("--no-steal", action="store_true", help="with --ranks: idle ranks do not steal")
     return ap.parse_args()
+
+
+def policy_name(spec):
+    if spec.policy == "ranks":
+        return f"ranks (R = {spec.max_groups}, {'with' if spec.fallback_groups else 'no'} stealing)"
+    return spec.policy
+
+
+def workload_spec(args):
+    from workloads import get_config
+    spec = get_config(args.workload)
+    if args.ranks > 0:
+        spec = dataclasses.replace(spec, policy="ranks", max_groups=args.ranks,
+                                   fallback_groups=0 if args.no_steal else 1)
+    return spec
 
 
 # ------------------------------------------------------------------ helpers
@@ -235,8 +255,14 @@ def oracle_sample(spec, x_host, logits_host, ws_host, waves):
     sim = om.AsyncMoEOracle(L.num_experts, L.top_k, x_host.to(torch.float64).numpy(), experts,
                             has_shared=False, compute=set(tokens.tolist()))
     sim.deliver(tokens, idx, w)
+    if spec.policy == "ranks":
+        pick = lambda d: om.rank_pick(d, spec.max_groups, spec.fallback_groups != 0)
+    elif spec.policy == "threshold":
+        pick = lambda d: om.threshold_pick(d, spec.min_batch, spec.max_groups, spec.fallback_groups)
+    else:
+        pick = lambda d: om.mtfs_pick(d, spec.max_groups)
     while sim.pending():
-        sim.step(om.mtfs_pick)
+        sim.step(pick)
     dt = time.perf_counter() - t0
     pairs = len(tokens) * L.top_k
     return pairs, dt, f"first-arriving wave: {len(tokens)} tokens = {pairs} routed pairs (oracle, float64)"
@@ -259,7 +285,7 @@ def host_weights_for_sample(ws, waves, logits_host, K):
 def run_reference(args, rank, world):
     """The oracle on the host cores: each step a bounded sample of the workload."""
     from workloads import get_config, make_tokens, make_logits, make_waves
-    spec = get_config(args.workload)
+    spec = workload_spec(args)
     if rank != 0:
         return
     dev = "cuda" if torch.cuda.is_available() else "cpu"
@@ -282,7 +308,7 @@ def run_reference(args, rank, world):
             "impl": "reference",
             "config": {"workload": spec.name, "experts": spec.layer.num_experts, "top_k": spec.layer.top_k,
                        "hidden": spec.layer.hidden, "inter": spec.layer.inter, "tokens": spec.tokens,
-                       "waves": spec.num_waves, "policy": spec.policy, "sample": desc},
+                       "waves": spec.num_waves, "policy": policy_name(spec), "sample": desc},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -294,7 +320,7 @@ def run_stream(args, pkg, dev):
     stream up again (untimed: projection packing, graph capture) and times the run."""
     from workloads import get_config, make_stream_inputs
     from workloads.build import make_layer_weights
-    spec = get_config(args.workload)
+    spec = workload_spec(args)
     lay = spec.layer
     R, H, NL, M = spec.tokens, lay.hidden, spec.num_layers, 64
     wl = make_stream_inputs(spec, args.seed, M, weights=False)
@@ -384,7 +410,7 @@ def main():
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
-    spec = get_config(args.workload)
+    spec = workload_spec(args)
     L = spec.layer
     assert args.warmup >= 3, "at least 3 warm-up steps"
 
@@ -500,7 +526,7 @@ def main():
                 "scaling": "weak", "vs_baseline": None, "dtype": L.dtype, "data": "synthetic",
                 "config": {"workload": spec.name, "experts": L.num_experts, "top_k": L.top_k,
                            "hidden": H, "inter": I, "tokens": spec.tokens, "waves": spec.num_waves,
-                           "ticks": run.last_tick, "policy": spec.policy,
+                           "ticks": run.last_tick, "policy": policy_name(spec),
                            "routed_pairs_per_step": routed_pairs_step,
                            "l2": "inputs larger than L2: every step streams the scheduled experts' "
                                  f"weights ({wbytes_step / 1e9:.1f} GB) through HBM",
