@@ -53,13 +53,15 @@ def parse():
                     help="pick policy of the per-layer workloads: R > 0 replaces the workload's policy "
                          "by R simulated expert-parallel ranks (expert e on rank e mod R)")
     ap.add_argument("--no-steal", action="store_true", help="with --ranks: idle ranks do not steal")
+    ap.add_argument("--max-groups", type=int, default=-1,
+                    help="MTFS / threshold: G >= 0 replaces the workload's bucket limit per step (0 = all)")
     return ap.parse_args()
 
 
 def policy_name(spec):
     if spec.policy == "ranks":
         return f"ranks (R = {spec.max_groups}, {'with' if spec.fallback_groups else 'no'} stealing)"
-    return spec.policy
+    return spec.policy + (f" (G = {spec.max_groups})" if spec.max_groups > 0 else "")
 
 
 def workload_spec(args):
@@ -68,6 +70,8 @@ def workload_spec(args):
     if args.ranks > 0:
         spec = dataclasses.replace(spec, policy="ranks", max_groups=args.ranks,
                                    fallback_groups=0 if args.no_steal else 1)
+    elif args.max_groups >= 0:
+        spec = dataclasses.replace(spec, max_groups=args.max_groups)
     return spec
 
 
