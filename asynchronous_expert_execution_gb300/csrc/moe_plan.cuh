@@ -10,7 +10,9 @@ namespace moe {
 // applies the policy, drains the picked buckets whole (head += depth) and writes the work
 // list the FFN kernels consume.  MTFS (StreamEP section 4): deepest first, equal depth ->
 // lower bucket id.  THRESHOLD (streamFFN reading): buckets with depth >= min_batch, deepest
-// first; if none, MTFS over non-empty buckets limited to fallback_groups.  With
+// first; if none, MTFS over non-empty buckets limited to fallback_groups.  RANKS (simulated
+// expert-parallel ranks, R = max_groups): each rank drains its deepest bucket; with
+// fallback_groups != 0 each idle rank then takes the deepest bucket no rank picked.  With
 // enabled = false the plan is written empty and nothing is drained or counted.
 struct PlanScratch {
   int depth[kMaxBuckets];
