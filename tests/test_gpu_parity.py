@@ -83,7 +83,7 @@ def test_identity_experts_bitexact(pkg, dtype, shared):
 
 # ------------------------------------------------------------- SwiGLU layers
 
-@pytest.mark.parametrize("name", ["c1", "m1", "m2", "m3", "m4", "r1", "r2"])
+@pytest.mark.parametrize("name", ["c1", "m1", "m2", "m3", "m4", "r1", "r2", "r3", "r4"])
 def test_layer_parity(pkg, name):
     spec = get_config(name)
     L = spec.layer

@@ -128,6 +128,16 @@ TEST_CONFIGS = {
         name="r2_bf16_ranks_no_steal", layer=LayerSpec(16, 4, 584, 208, "bf16"), tokens=200,
         router="normal", waves="even", num_waves=5, arrival="exp", policy="ranks", max_groups=5,
         fallback_groups=0),
+    # degenerate rank counts: one rank (one bucket a step, deepest first) and more ranks than
+    # buckets (every non-empty bucket runs on its owner; the extra ranks find nothing to steal)
+    "r3": WorkloadSpec(
+        name="r3_bf16_one_rank", layer=LayerSpec(16, 4, 584, 208, "bf16"), tokens=200,
+        router="normal", waves="even", num_waves=5, arrival="exp", policy="ranks", max_groups=1,
+        fallback_groups=1),
+    "r4": WorkloadSpec(
+        name="r4_bf16_more_ranks_than_buckets", layer=LayerSpec(16, 4, 584, 208, "bf16"), tokens=200,
+        router="normal", waves="even", num_waves=5, arrival="exp", policy="ranks", max_groups=24,
+        fallback_groups=1),
     # bf16 decode-like: many experts, few tokens each.
     "m4": WorkloadSpec(
         name="m4_bf16_decode", layer=LayerSpec(64, 4, 1024, 512, "bf16"), tokens=64,
