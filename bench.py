@@ -240,46 +240,68 @@ class Pass:
 
 # ------------------------------------------------------------ CPU baseline
 
-def oracle_sample(spec, x_host, logits_host, ws_host, waves):
-    """Time the oracle as it stands on a bounded sample: the first-arriving wave."""
+def oracle_sample(spec, x_host, logits_host, ws_host, waves, budget_s=0.0):
+    """Time the oracle as it stands on a bounded sample of the workload: the waves in arrival
+    order, each delivered to a fresh oracle and run until its pairs are merged, until
+    `budget_s` seconds of oracle time are spent (at least the first wave; only waves whose
+    experts are in `ws_host`)."""
     from oracle import moe_oracle as om
     L = spec.layer
-    first = sorted(waves, key=lambda w: w.tick)[0]
-    tokens = np.asarray(first.tokens)
-    cache = {}
-
-    def experts(e):
-        if e not in cache:
-            cache[e] = tuple(ws_host[k][e].to(torch.float64).numpy() for k in ("w1", "w3", "w2"))
-        return cache[e]
-
-    t0 = time.perf_counter()
-    z = logits_host.numpy()
-    idx, w = om.route(z, L.top_k)
-    sim = om.AsyncMoEOracle(L.num_experts, L.top_k, x_host.to(torch.float64).numpy(), experts,
-                            has_shared=False, compute=set(tokens.tolist()))
-    sim.deliver(tokens, idx, w)
     if spec.policy == "ranks":
         pick = lambda d: om.rank_pick(d, spec.max_groups, spec.fallback_groups != 0)
     elif spec.policy == "threshold":
         pick = lambda d: om.threshold_pick(d, spec.min_batch, spec.max_groups, spec.fallback_groups)
     else:
         pick = lambda d: om.mtfs_pick(d, spec.max_groups)
-    while sim.pending():
-        sim.step(pick)
-    dt = time.perf_counter() - t0
-    pairs = len(tokens) * L.top_k
-    return pairs, dt, f"first-arriving wave: {len(tokens)} tokens = {pairs} routed pairs (oracle, float64)"
+    x64 = x_host.to(torch.float64).numpy()
+    z = logits_host.numpy()
+    pairs, dt, n_waves, n_tokens = 0, 0.0, 0, 0
+    for wave in sorted(waves, key=lambda w: w.tick):
+        tokens = np.asarray(wave.tokens)
+        if len(tokens) == 0:
+            continue
+        if n_waves > 0 and dt >= budget_s:
+            break
+        cache = {}
+
+        def experts(e, cache=cache):
+            if e not in cache:
+                cache[e] = tuple(ws_host[k][e].to(torch.float64).numpy() for k in ("w1", "w3", "w2"))
+            return cache[e]
+
+        t0 = time.perf_counter()
+        idx, w = om.route(z, L.top_k)
+        if not all(int(e) in ws_host["w1"] for e in np.unique(idx[tokens])):
+            break                                   # experts not copied to the host: sample ends
+        sim = om.AsyncMoEOracle(L.num_experts, L.top_k, x64, experts, has_shared=False,
+                                compute=set(tokens.tolist()))
+        sim.deliver(tokens, idx, w)
+        while sim.pending():
+            sim.step(pick)
+        dt += time.perf_counter() - t0
+        pairs += len(tokens) * L.top_k
+        n_waves += 1
+        n_tokens += len(tokens)
+        del cache, sim
+    return pairs, dt, (f"first {n_waves} arriving wave(s): {n_tokens} tokens = {pairs} routed pairs "
+                       f"(oracle, float64)")
 
 
-def host_weights_for_sample(ws, waves, logits_host, K):
+def host_weights_for_sample(ws, waves, logits_host, K, max_waves=1, max_bytes=8 << 30):
+    """Host copies of the experts the first `max_waves` arriving waves route to (the first
+    wave always; later waves while the copies stay under `max_bytes`)."""
     from oracle import moe_oracle as om
-    first = sorted(waves, key=lambda w: w.tick)[0]
     idx, _ = om.route(logits_host.numpy(), K)
-    need = sorted(set(idx[np.asarray(first.tokens)].ravel().tolist()))
+    per_expert = sum(ws[k][0].numel() * ws[k][0].element_size() for k in ("w1", "w3", "w2"))
+    need = set()
+    for i, wave in enumerate(sorted(waves, key=lambda w: w.tick)[:max_waves]):
+        more = need | set(idx[np.asarray(wave.tokens, dtype=np.int64)].ravel().tolist())
+        if i > 0 and len(more) * per_expert > max_bytes:
+            break
+        need = more
     out = {k: {} for k in ("w1", "w3", "w2")}
     for k in out:
-        for e in need:
+        for e in sorted(need):
             out[k][e] = ws[k][e].cpu()
     return out
 
@@ -424,7 +446,7 @@ def main():
                        has_shared=L.has_shared)
     cpu_ws = None
     if rank == 0 and not args.no_cpu_baseline:
-        cpu_ws = host_weights_for_sample(ws, waves, logits.cpu(), L.top_k)
+        cpu_ws = host_weights_for_sample(ws, waves, logits.cpu(), L.top_k, max_waves=len(waves))
     del weights, ws
     torch.cuda.empty_cache()
     run = Pass(pkg, spec, moe, waves, dev)
@@ -520,7 +542,7 @@ def main():
 
     cpu = None
     if rank == 0 and cpu_ws is not None:
-        p, t, desc = oracle_sample(spec, x.cpu(), logits.cpu(), cpu_ws, waves)
+        p, t, desc = oracle_sample(spec, x.cpu(), logits.cpu(), cpu_ws, waves, budget_s=10.0)
         cpu = {"value": p / t, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle", "sample": desc,
                "seconds": t}
 
