@@ -85,7 +85,28 @@ def test_identity_experts_bitexact(pkg, dtype, shared):
 
 @pytest.mark.parametrize("name", ["c1", "m1", "m2", "m3", "m4", "r1", "r2", "r3", "r4"])
 def test_layer_parity(pkg, name):
-    spec = get_config(name)
+    _check_layer(pkg, get_config(name))
+
+
+# degenerate shapes the method admits: one expert, top-1, every expert picked (K = E), one
+# token, top-1 with the shared expert
+@pytest.mark.parametrize("E,K,H,I,T,dtype,shared", [
+    (1, 1, 64, 64, 40, "bf16", False),
+    (32, 1, 256, 128, 100, "bf16", False),
+    (6, 6, 128, 64, 50, "f32", False),
+    (6, 6, 136, 80, 50, "bf16", False),
+    (8, 2, 64, 64, 1, "bf16", False),
+    (4, 1, 200, 96, 30, "bf16", True),
+])
+def test_layer_parity_degenerate(pkg, E, K, H, I, T, dtype, shared):
+    from workloads import LayerSpec, WorkloadSpec
+    spec = WorkloadSpec(name="degenerate", layer=LayerSpec(E, K, H, I, dtype, has_shared=shared, shared_inter=I),
+                        tokens=T, router="normal", waves="even", num_waves=min(3, T), arrival="exp",
+                        policy="mtfs")
+    _check_layer(pkg, spec)
+
+
+def _check_layer(pkg, spec):
     L = spec.layer
     wl = make_workload(spec, seed=0)
     res = gpu_layer(pkg, spec, wl)
