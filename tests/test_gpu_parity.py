@@ -89,8 +89,11 @@ def test_layer_parity(pkg, name):
 
 
 # degenerate shapes the method admits: one expert, top-1, every expert picked (K = E), one
-# token, top-1 with the shared expert
+# token, top-1 with the shared expert; and the largest the library accepts: 1024 routed
+# experts plus the shared one (1025 buckets), top-30
 @pytest.mark.parametrize("E,K,H,I,T,dtype,shared", [
+    (1024, 8, 64, 64, 256, "bf16", True),
+    (32, 30, 64, 64, 20, "bf16", False),
     (1, 1, 64, 64, 40, "bf16", False),
     (32, 1, 256, 128, 100, "bf16", False),
     (6, 6, 128, 64, 50, "f32", False),
