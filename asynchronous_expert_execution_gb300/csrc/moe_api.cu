@@ -582,6 +582,19 @@ moe_status moe_async_sync(moe_async_t h, void* stream) {
   return static_cast<moe_status>(h->host_counters->error);
 }
 
+// Steps the layer's queues need at least before they are empty, when nothing new arrives:
+// every step drains its picks whole, and takes at most max_groups (MTFS), R (RANKS) or, once
+// no bucket reaches min_batch, fallback_groups (THRESHOLD) buckets.  0 = no useful bound.
+int drain_steps_lower_bound(const DevCounters& c, int layer, const moe_async_policy& pol) {
+  if (c.plan_layer != layer || c.nonempty_left <= 0) return 0;
+  int per_step = 0;
+  if (pol.kind == MOE_POLICY_MTFS) per_step = pol.max_groups;
+  else if (pol.kind == MOE_POLICY_RANKS) per_step = pol.max_groups;
+  else if (pol.kind == MOE_POLICY_THRESHOLD && c.elig_left == 0)
+    per_step = pol.fallback_groups > 0 ? pol.fallback_groups : 1;
+  return per_step > 0 ? (c.nonempty_left + per_step - 1) / per_step : 0;
+}
+
 moe_status moe_async_wait(moe_async_t h, int32_t layer, const moe_async_policy* policy,
                           int32_t max_steps, int32_t check_every, void* stream) {
   if (!valid_stream_layer(h, layer) || !policy || max_steps < 0) return MOE_ERR_INVALID;
@@ -594,7 +607,11 @@ moe_status moe_async_wait(moe_async_t h, int32_t layer, const moe_async_policy* 
     if (h->host_counters->error) return static_cast<moe_status>(h->host_counters->error);
     if (h->host_counters->open_tokens == 0) return MOE_OK;
     if (steps >= max_steps) return MOE_ERR_TIMEOUT;
-    for (int i = 0; i < check_every && steps < max_steps; ++i, ++steps) {
+    // run as many steps as the queues certainly need before reading the counters again
+    // (fewer host round trips in long drains), else check_every
+    const int need = drain_steps_lower_bound(*h->host_counters, layer, *policy);
+    const int batch = need > 0 ? need : check_every;
+    for (int i = 0; i < batch && steps < max_steps; ++i, ++steps) {
       st = moe_async_schedule_step(h, layer, policy, stream);
       if (st != MOE_OK) return st;
     }

@@ -59,7 +59,10 @@ struct DevCounters {
   int32_t open_tokens, pending_pairs, ready;
   uint32_t error;
   int32_t trace_n;
-  int32_t pad[3];
+  // after the last scheduling step: its layer, the non-empty buckets it left, and how many
+  // of those hold at least the policy's min_batch (the host's drain loop sizes its next
+  // batch of steps from these)
+  int32_t plan_layer, nonempty_left, elig_left;
 };
 
 struct LayerView {

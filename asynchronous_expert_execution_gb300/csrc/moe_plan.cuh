@@ -144,6 +144,9 @@ __device__ inline void plan_layer(const LayerView& L, const Dims& d, StepPlan* P
       P->n_tiles2 = t2_run;
       P->rows = row_run;
       if (!enabled) return;
+      C->plan_layer = layer;
+      C->nonempty_left = n_nonempty - n;          // every pick is a non-empty bucket, drained whole
+      C->elig_left = (pol.kind == MOE_POLICY_THRESHOLD && n_elig > 0) ? n_elig - n : 0;
       C->steps += 1ull;
       C->pairs_executed += (unsigned long long)row_run;
       C->expert_runs += (unsigned long long)n;

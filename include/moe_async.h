@@ -208,9 +208,12 @@ moe_status moe_async_cancel(moe_async_t h, int32_t layer, int32_t n, const int32
                             void* stream);
 
 /* Run scheduling steps of `layer` under `policy` until no token of the handle is open
- * (accepted but not yet combined, in any layer), checking the device counters every `check_every` steps;
- * at most max_steps steps.  Synchronises `stream`.  Returns MOE_ERR_TIMEOUT when tokens are
- * still open after max_steps (e.g. a withheld pair), else the sticky device error. */
+ * (accepted but not yet combined, in any layer); at most max_steps steps.  Between reads of
+ * the device counters it runs as many steps as the layer's queues certainly still need (each
+ * step drains its picks whole and takes at most max_groups buckets under MTFS or RANKS, or
+ * fallback_groups under THRESHOLD once no bucket reaches min_batch), else `check_every`
+ * steps.  Synchronises `stream`.  Returns MOE_ERR_TIMEOUT when tokens are still open after
+ * max_steps (e.g. a withheld pair), else the sticky device error. */
 moe_status moe_async_wait(moe_async_t h, int32_t layer, const moe_async_policy* policy,
                           int32_t max_steps, int32_t check_every, void* stream);
 
