@@ -358,7 +358,12 @@ def replay_layer(num_experts, top_k, x, idx, w, waves, policy, experts,
 
 
 def y_sample(tokens, x, idx, w, experts, shared=None):
-    """y for a few tokens straight from the merge formula (no queues)."""
+    """y for a few tokens straight from the merge formula (no queues).
+
+    StreamEP section 3: y_t = sum_{k} w_{t,k} E_{idx[t,k]}(x_t) in ascending k, plus the
+    shared expert E_shared(x_t) with weight one (added last, outside the renormalised
+    weights).  Pinned against the brute-force dense MoE on every token of a tiny case and
+    against a hand-computed H = I = 1 case, with and without the shared expert."""
     out = {}
     for t in tokens:
         t = int(t)

@@ -345,6 +345,51 @@ def test_rmsnorm_stub_closed_form():
     assert np.allclose(om.attention_stub(x, P), (x / math.sqrt(12.5 + 1e-6)) @ P, atol=1e-15)
 
 
+# ------------------------------------------------- y for sampled tokens
+
+def pin_y_sample_dense():
+    """y_sample (the merge formula per token, no queues) against the brute-force dense MoE
+    on every token of a tiny case, with and without the shared expert."""
+    for shared in (False, True):
+        x, idx, w, ws = _tiny_case(5, E=6, K=3, H=10, I=7, T=12, shared=shared)
+        ex = lambda e: ws[e]
+        sh = ws[6] if shared else None
+        dense = om.dense_moe(x, idx, w, ex, shared=sh)
+        got = om.y_sample(range(12), x, idx, w, ex, shared=sh)
+        for t in range(12):
+            assert np.allclose(got[t], dense[t], rtol=0, atol=1e-13), (shared, t)
+
+
+def pin_y_sample_hand():
+    """H = I = 1 worked by hand: expert e is E_e(x) = silu(a_e x) (c_e x) f_e, so a token
+    x = 2 routed to (2, 0) with weights (3/4, 1/4) gives
+    y = 3/4 silu(0.5) (-4) + 1/4 silu(2) 6 / 2, and the shared expert (a = c = f = 1)
+    adds silu(2) 2 with weight one."""
+    a, c, f = (1.0, -0.5, 0.25), (3.0, 1.0, -2.0), (0.5, 2.0, 1.0)
+    ws = [(np.array([[a[e]]]), np.array([[c[e]]]), np.array([[f[e]]])) for e in range(3)]
+    sh = (np.array([[1.0]]), np.array([[1.0]]), np.array([[1.0]]))
+    x = np.array([[2.0], [-1.0]])
+    idx = np.array([[2, 0], [1, 2]])
+    w = np.array([[0.75, 0.25], [0.4, 0.6]])
+    sig = lambda v: 1.0 / (1.0 + math.exp(-v))
+    s = lambda v: v * sig(v)
+    y0 = 0.75 * s(0.5) * (-4.0) * 1.0 + 0.25 * s(2.0) * 6.0 * 0.5
+    y1 = 0.4 * s(0.5) * (-1.0) * 2.0 + 0.6 * s(-0.25) * 2.0 * 1.0
+    got = om.y_sample([0, 1], x, idx, w, lambda e: ws[e])
+    assert abs(got[0][0] - y0) < 1e-15 and abs(got[1][0] - y1) < 1e-15
+    got = om.y_sample([1, 0], x, idx, w, lambda e: ws[e], shared=sh)
+    assert abs(got[0][0] - (y0 + s(2.0) * 2.0)) < 1e-15
+    assert abs(got[1][0] - (y1 + s(-1.0) * (-1.0))) < 1e-15
+
+
+def test_y_sample_dense():
+    pin_y_sample_dense()
+
+
+def test_y_sample_hand():
+    pin_y_sample_hand()
+
+
 # ------------------------------------------------- planted-mistake detection
 
 def _fails(pin, *args):
@@ -408,12 +453,44 @@ def test_pins_catch_planted_mistakes(monkeypatch):
         return [picks[r] for r in range(R) if r in picks]
     monkeypatch.setattr(om, "rank_pick", rank_shallow)
     assert _fails(pin_rank_pick_hand)
+    monkeypatch.undo()
+    # 8. y_sample weighting the shared expert by the first routed weight
+    real_ffn = om.expert_ffn
+
+    def y_sample_shared_weighted(tokens, x, idx, w, experts, shared=None):
+        out = {}
+        for t in tokens:
+            t = int(t)
+            xt = np.asarray(x[t], float)[None, :]
+            cs = [w[t, k] * real_ffn(xt, *experts(int(idx[t, k])))[0] for k in range(idx.shape[1])]
+            if shared is not None:
+                cs.append(w[t, 0] * real_ffn(xt, *shared)[0])
+            out[t] = om.combine(cs)
+        return out
+    monkeypatch.setattr(om, "y_sample", y_sample_shared_weighted)
+    assert _fails(pin_y_sample_dense) and _fails(pin_y_sample_hand)
+    monkeypatch.undo()
+    # 9. y_sample pairing weight k with the expert of the reversed k order
+    def y_sample_reversed_w(tokens, x, idx, w, experts, shared=None):
+        out = {}
+        K = idx.shape[1]
+        for t in tokens:
+            t = int(t)
+            xt = np.asarray(x[t], float)[None, :]
+            cs = [w[t, K - 1 - k] * real_ffn(xt, *experts(int(idx[t, k])))[0] for k in range(K)]
+            if shared is not None:
+                cs.append(real_ffn(xt, *shared)[0])
+            out[t] = om.combine(cs)
+        return out
+    monkeypatch.setattr(om, "y_sample", y_sample_reversed_w)
+    assert _fails(pin_y_sample_dense) and _fails(pin_y_sample_hand)
 
 
 def test_pins_pass_unmodified():
     pin_rank_pick_hand()
     for p in (pin_route_bruteforce, pin_route_hand, pin_silu, pin_ffn_closed_form,
-              pin_identity_experts_exact, pin_policies_hand, pin_schedule_trace_hand, pin_defrag_golden):
+              pin_identity_experts_exact, pin_policies_hand, pin_schedule_trace_hand, pin_defrag_golden,
+              pin_y_sample_dense, pin_y_sample_hand):
         p()
 
 
