@@ -70,12 +70,16 @@ __global__ void route_kernel(const float* __restrict__ logits, int T, int E, int
 }
 
 // --------------------------------------------------------------- Receptor
-// Pairs: one thread per (token, k) with k <= K (k == K is the shared expert).  Appends use
-// warp-aggregated atomics: lanes bound for the same bucket elect a leader that reserves all
-// of their positions with one atomicAdd on the bucket tail.
-// Token vectors: copied into pool[slot] with 16-byte vector loads/stores.
+// One warp takes `tpw` whole tokens at a time (tpw * KS <= 32): lane l handles pair k = l % KS
+// of token l / KS (k == K is the shared expert).  Appends use warp-aggregated atomics: lanes
+// bound for the same bucket elect a leader that reserves all of their positions with one
+// atomicAdd on the bucket tail.  Then the same warp copies into pool[slot] (16-byte vectors)
+// the row of each of its tokens that had at least one pair accepted by this call: a stale,
+// retired or duplicate delivery leaves the pool row of the slot's current request untouched
+// ("asynchronous MoE serving" notes, inferred obligations: accept exactly the selected
+// contributions).
 template <typename T>
-__global__ void enqueue_kernel(LayerView L, Dims d, DevCounters* C, int n,
+__global__ void enqueue_kernel(LayerView L, Dims d, DevCounters* C, int n, int tpw,
                                const int32_t* __restrict__ rows, const int32_t* __restrict__ slots,
                                const T* __restrict__ x, const int32_t* __restrict__ expert,
                                const float* __restrict__ w, const uint32_t* __restrict__ kmask,
@@ -85,18 +89,20 @@ __global__ void enqueue_kernel(LayerView L, Dims d, DevCounters* C, int n,
   // wait for it, then let the scheduler start; the scheduler waits for this kernel
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const long long total = (long long)n * d.KS;
-  const long long total_r = (total + 31) & ~31ll;
-  const long long stride = (long long)gridDim.x * blockDim.x;
-  for (long long base = (long long)blockIdx.x * blockDim.x + (threadIdx.x & ~31); base < total_r;
-       base += stride) {
-    const long long p = base + lane;
+  const long long nwarps = (long long)gridDim.x * (blockDim.x >> 5);
+  const long long gw = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int jl = lane / d.KS;              // this lane's token within the warp's group
+  const int k = lane % d.KS;
+  const uint32_t kbits = (1u << d.KS) - 1u;  // KS <= 31
+  constexpr int V = 16 / sizeof(T);
+  const int chunks = d.H / V;
+  for (long long g0 = gw * tpw; g0 < n; g0 += nwarps * tpw) {
     int key = -1 - lane;          // unique key for lanes with nothing to append
-    int slot = 0, k = 0;
-    if (p < total) {
-      const int i = (int)(p / d.KS);
-      k = (int)(p % d.KS);
-      const int row = rows ? rows[i] : i;
+    int slot = -1, row = -1;
+    bool accepted = false;
+    if (jl < tpw && g0 + jl < n) {
+      const int i = (int)(g0 + jl);
+      row = rows ? rows[i] : i;
       slot = slots ? slots[i] : row;
       bool ok = true;
       if (slot < 0 || slot >= d.S || row < 0) { set_error(C, MOE_ERR_INVALID); ok = false; }
@@ -121,6 +127,7 @@ __global__ void enqueue_kernel(LayerView L, Dims d, DevCounters* C, int n,
           if (old == 0u) atomicAdd(&C->open_tokens, 1);
           L.wtab[(size_t)slot * d.KS + k] = (k < d.K) ? w[(size_t)row * d.K + k] : 1.0f;
           key = e;
+          accepted = true;
         }
       }
     }
@@ -141,18 +148,17 @@ __global__ void enqueue_kernel(LayerView L, Dims d, DevCounters* C, int n,
         L.records[(size_t)key * d.cap + (pos % (uint32_t)d.cap)] = (slot << kKShift) | k;
       }
     }
-  }
-  // token vectors -> pool rows (16-byte chunks)
-  constexpr int V = 16 / sizeof(T);
-  const int chunks = d.H / V;
-  const long long total_c = (long long)n * chunks;
-  for (long long q = (long long)blockIdx.x * blockDim.x + threadIdx.x; q < total_c; q += stride) {
-    const int i = (int)(q / chunks), c = (int)(q % chunks);
-    const int row = rows ? rows[i] : i;
-    const int slot = slots ? slots[i] : row;
-    if (slot < 0 || slot >= d.S || row < 0) continue;
-    const int4 v = __ldg(reinterpret_cast<const int4*>(x + (size_t)row * d.H) + c);
-    reinterpret_cast<int4*>(static_cast<T*>(L.pool) + (size_t)slot * d.H)[c] = v;
+    // token rows -> pool, only for tokens with a pair accepted here (warp-uniform loop)
+    const uint32_t acc = __ballot_sync(0xffffffffu, accepted);
+    for (int j = 0; j < tpw; ++j) {
+      if (!((acc >> (j * d.KS)) & kbits)) continue;
+      const int row_j = __shfl_sync(0xffffffffu, row, j * d.KS);
+      const int slot_j = __shfl_sync(0xffffffffu, slot, j * d.KS);
+      const int4* src = reinterpret_cast<const int4*>(x + (size_t)row_j * d.H);
+      int4* dst = reinterpret_cast<int4*>(static_cast<T*>(L.pool) + (size_t)slot_j * d.H);
+#pragma unroll 4
+      for (int c = lane; c < chunks; c += 32) dst[c] = __ldg(src + c);
+    }
   }
 }
 
@@ -514,18 +520,22 @@ moe_status moe_async_enqueue(moe_async_t h, int32_t layer, int32_t n, const int3
   if (reinterpret_cast<uintptr_t>(d_x) % 16) return MOE_ERR_INVALID;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const Dims& d = h->dims;
-  const long long work = std::max<long long>((long long)n * d.KS, (long long)n * d.H / 8);
-  int grid = (int)std::min<long long>((work + 255) / 256, (long long)h->num_sms * 8);
-  if (grid < 1) grid = 1;
+  // tokens per warp: one while the wave fits in one round of 16 warps per SM (each warp then
+  // copies one row), more for large waves; whole tokens per warp, tpw * KS <= 32
+  const int tpw_max = 32 / d.KS;
+  const long long warps_one_round = (long long)h->num_sms * 16;
+  const int tpw = (int)std::min<long long>(tpw_max, std::max<long long>(1, (n + warps_one_round - 1) / warps_one_round));
+  const long long warps = (n + tpw - 1) / tpw;
+  const int grid = (int)std::max<long long>(1, std::min<long long>((warps + 7) / 8, (long long)h->num_sms * 8));
   prof_begin(h, MOE_KERNEL_ENQUEUE, s);
   cudaError_t e;
   if (d.dtype == MOE_BF16)
     e = launch_dependent(enqueue_kernel<__nv_bfloat16>, dim3(grid), dim3(256), s, h->layers[layer], d, h->counters,
-                         (int)n, d_rows, d_slot, static_cast<const __nv_bfloat16*>(d_x), d_expert, d_w, d_kmask,
+                         (int)n, tpw, d_rows, d_slot, static_cast<const __nv_bfloat16*>(d_x), d_expert, d_w, d_kmask,
                          d_gen);
   else
     e = launch_dependent(enqueue_kernel<float>, dim3(grid), dim3(256), s, h->layers[layer], d, h->counters, (int)n,
-                         d_rows, d_slot, static_cast<const float*>(d_x), d_expert, d_w, d_kmask, d_gen);
+                         tpw, d_rows, d_slot, static_cast<const float*>(d_x), d_expert, d_w, d_kmask, d_gen);
   prof_end(h, MOE_KERNEL_ENQUEUE, s);
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

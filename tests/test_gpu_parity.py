@@ -387,3 +387,116 @@ def test_cancel_after_merge_is_too_late(pkg):
     assert sorted(slots.tolist()) == list(range(T))
     assert moe.stats()["cancelled"] == 0
     moe.close()
+
+
+# ------------------------------------------- rejected pairs leave the pool alone
+# "asynchronous MoE serving" notes, inferred obligations: accept exactly the selected
+# contributions, and return a slot only after its last read; CascadeEP: generation-tagged
+# readiness.  A delivery whose pairs are all rejected must not touch the token pool row of
+# the slot's current request: the row is what GEMM1 gathers for that request.
+
+def _oracle_y(spec, wl, x_rows, idx, w):
+    L = spec.layer
+    ii, ww = idx.cpu().numpy().astype(np.int64), w.cpu().numpy().astype(np.float64)
+    return om.dense_moe(x_rows, ii, ww, expert_getter(wl.weights[0], L.num_experts))
+
+
+def test_stale_wave_does_not_overwrite_pool(pkg):
+    """Generation 1 of slot 5 is enqueued with a new vector; before any step, a late
+    generation-0 wave for slot 5 arrives carrying the old vector.  Its pairs are stale and
+    dropped, and the step must still compute generation 1 from the new vector."""
+    spec, wl, moe, x, idx, w = _small(pkg, dtype="f32")
+    T, H = spec.tokens, spec.layer.hidden
+    g0 = torch.zeros(T, dtype=torch.int32, device="cuda")
+    moe.enqueue(0, x, idx, w, gen=g0)
+    assert moe.wait(0, pkg.Policy(), max_steps=4) == 0
+    y = torch.empty((T, H), dtype=x.dtype, device="cuda")
+    slots = torch.empty(T, dtype=torch.int32, device="cuda")
+    n = torch.zeros(1, dtype=torch.int32, device="cuda")
+    moe.collect(0, y, slots, n)                                      # every slot -> generation 1
+    assert int(n.item()) == T
+    five = torch.tensor([5], dtype=torch.int32, device="cuda")
+    x_new = (x[5:6] * -1.5 + 0.25).contiguous()
+    moe.enqueue(0, x_new, idx[5:6].contiguous(), w[5:6].contiguous(), slots=five,
+                gen=torch.ones(1, dtype=torch.int32, device="cuda"))
+    moe.enqueue(0, x, idx, w, rows=five, gen=torch.zeros(1, dtype=torch.int32, device="cuda"))   # stale
+    moe.schedule_step(0, pkg.Policy())
+    n.zero_()
+    moe.collect(0, y, slots, n)
+    assert moe.sync() == 4                                          # MOE_ERR_STALE latched
+    assert int(n.item()) == 1 and int(slots[0].item()) == 5
+    want = _oracle_y(spec, wl, x_new.cpu().double().numpy(), idx[5:6], w[5:6])
+    got = y[:1].cpu().double().numpy()
+    assert rel_err(got, want) <= TOL["f32"], rel_err(got, want)
+    assert moe.stats()["stale"] == 1
+    moe.close()
+
+
+def test_retired_slot_late_pair_is_dropped(pkg):
+    """A cancelled request's late pair, carrying another vector, arrives while its slot is
+    retired with a record still queued.  The pair is dropped silently; the queued record runs
+    and is discarded, the slot is freed, and the next request of that slot is computed from
+    its own vector alone (element by element against the oracle).  The retired slot's pool row
+    is read only by records whose results are discarded, so this sequence checks the
+    bookkeeping around the drop; the pool payload itself is checked by the stale and duplicate
+    cases and, over every interleaving, by the protocol model."""
+    spec, wl, moe, x, idx, w = _small(pkg, dtype="f32")
+    T, H = spec.tokens, spec.layer.hidden
+    kmask = torch.full((T,), 3, dtype=torch.int32, device="cuda")
+    kmask[5] = 1                                                   # pair k = 1 of token 5 withheld
+    moe.enqueue(0, x, idx, w, kmask=kmask)
+    five = torch.tensor([5], dtype=torch.int32, device="cuda")
+    moe.cancel(0, five)
+    x_bad = (x * 3.0 - 1.0).contiguous()
+    moe.enqueue(0, x_bad, idx, w, rows=five, kmask=torch.tensor([2], dtype=torch.int32, device="cuda"))
+    moe.schedule_step(0, pkg.Policy())
+    y = torch.empty((T, H), dtype=x.dtype, device="cuda")
+    slots = torch.empty(T, dtype=torch.int32, device="cuda")
+    n = torch.zeros(1, dtype=torch.int32, device="cuda")
+    moe.collect(0, y, slots, n)
+    assert moe.sync() == 0                                          # a retired drop is not an error
+    k = int(n.item())
+    assert sorted(slots[:k].cpu().tolist()) == [t for t in range(T) if t != 5]
+    want = _oracle_y(spec, wl, x.cpu().double().numpy(), idx, w)
+    got = by_token(slots[:k].cpu().numpy(), y[:k].cpu().double().numpy(), T, H)
+    keep = [t for t in range(T) if t != 5]
+    assert rel_err(got[keep], want[keep]) <= TOL["f32"]
+    st = moe.stats()
+    assert st["cancelled"] == 1 and st["open_tokens"] == 0 and st["duplicates"] == 0
+    # generation 1 of slot 5, its own vector
+    x_new = (x[5:6] * 0.5 - 2.0).contiguous()
+    moe.enqueue(0, x_new, idx[5:6].contiguous(), w[5:6].contiguous(), slots=five,
+                gen=torch.ones(1, dtype=torch.int32, device="cuda"))
+    moe.schedule_step(0, pkg.Policy())
+    n.zero_()
+    moe.collect(0, y, slots, n)
+    assert moe.sync() == 0 and int(n.item()) == 1
+    want = _oracle_y(spec, wl, x_new.cpu().double().numpy(), idx[5:6], w[5:6])
+    assert rel_err(y[:1].cpu().double().numpy(), want) <= TOL["f32"]
+    moe.close()
+
+
+def test_duplicate_wave_does_not_overwrite_pool(pkg):
+    """Every token is delivered; before any step a duplicate wave for tokens 3 and 7 arrives
+    carrying other vectors.  The duplicates are dropped (and reported), and every output must
+    still come from the first delivery's vectors."""
+    spec, wl, moe, x, idx, w = _small(pkg, dtype="f32", shared=True)
+    T, H = spec.tokens, spec.layer.hidden
+    moe.enqueue(0, x, idx, w)
+    x_bad = (x * -2.0 + 3.0).contiguous()
+    moe.enqueue(0, x_bad, idx, w, rows=torch.tensor([3, 7], dtype=torch.int32, device="cuda"))
+    moe.schedule_step(0, pkg.Policy())
+    y = torch.empty((T, H), dtype=x.dtype, device="cuda")
+    slots = torch.empty(T, dtype=torch.int32, device="cuda")
+    n = torch.zeros(1, dtype=torch.int32, device="cuda")
+    moe.collect(0, y, slots, n)
+    assert moe.sync() == 3                                          # MOE_ERR_DUPLICATE latched
+    assert int(n.item()) == T
+    L = spec.layer
+    ii, ww = idx.cpu().numpy().astype(np.int64), w.cpu().numpy().astype(np.float64)
+    get = expert_getter(wl.weights[0], L.num_experts)
+    want = om.dense_moe(x.cpu().double().numpy(), ii, ww, get, shared=get(L.num_experts))
+    got = by_token(slots.cpu().numpy(), y.cpu().double().numpy(), T, H)
+    assert rel_err(got, want) <= TOL["f32"], rel_err(got, want)
+    assert moe.stats()["duplicates"] == 2 * L.top_k
+    moe.close()

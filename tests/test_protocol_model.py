@@ -32,3 +32,21 @@ def test_protocol_generation_wraparound_is_harmless_under_quiescence():
     still admits no foreign write, because no record outlives its generation."""
     _, viol, dead = Model(ROUTES, cancel_requests=(0, 1), gen_bits=1).explore()
     assert not viol and not dead
+
+
+def test_protocol_pool_payload_only_from_accepted_pairs():
+    """The token-pool row changes only when a pair is accepted: over every interleaving (with
+    cancellation, so late stale pairs exist), every record reads its own request's vector."""
+    for canc in [(0,), (1,), (0, 1), (0, 1, 2)]:
+        _, viol, dead = Model(ROUTES, cancel_requests=canc).explore()
+        assert not viol and not dead, (canc, viol)
+
+
+def test_protocol_pool_write_on_rejected_pair_is_caught():
+    """Copying a rejected (stale) pair's vector into the pool row lets a late pair of a
+    cancelled request replace the new owner's input before its records run -- the checker
+    must find that ("foreign-input")."""
+    _, viol, _ = Model(ROUTES, cancel_requests=(0,), pool_on_reject=True).explore()
+    assert "foreign-input" in {v[0] for v in viol}
+    _, viol, _ = Model(ROUTES, pool_on_reject=True).explore()      # without cancellation no
+    assert not viol                                                  # pair is ever stale
