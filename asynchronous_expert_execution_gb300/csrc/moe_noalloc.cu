@@ -13,7 +13,6 @@
 // (token, k) pair into the scratch array, the second reads them back for the down
 // projection and the weighted merge.
 #include <algorithm>
-#include <mutex>
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -23,21 +22,17 @@ namespace {
 constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
 static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchBytes / sizeof(float)];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_noalloc_mu;
-float* g_noalloc_ptr[kMaxDevices] = {};
-
-// Device address of the scratch array on the current device.  The array's name is only a
-// host-side stand-in, so the address is looked up once per device, with that device current.
-cudaError_t noalloc_scratch(int dev, float** out) {
-  std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_ptr[dev]) {
-    void* p = nullptr;
-    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess) return e;
-    g_noalloc_ptr[dev] = static_cast<float*>(p);
-  }
-  *out = g_noalloc_ptr[dev];
+// Device address of the scratch array in the current context.  The array's name is only a
+// host-side stand-in, so the address is looked up with cudaGetSymbolAddress -- on every call:
+// the lookup is a host-side table read, and a cached address would go stale when the module
+// is loaded again at another address (after cudaDeviceReset, or under another context made
+// current by the caller).  The first lookup in a context may load the module; that first
+// call belongs before any stream capture.
+cudaError_t noalloc_scratch(float** out) {
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  if (e != cudaSuccess) return e;
+  *out = static_cast<float*>(p);
   return cudaSuccess;
 }
 
@@ -115,10 +110,8 @@ extern "C" moe_status moe_async_forward_noalloc(int32_t T, int32_t E, int32_t K,
   if (T == 0) return MOE_OK;
   if (!d_x || !d_expert || !d_w || !d_w1 || !d_w3 || !d_w2 || !d_y) return MOE_ERR_INVALID;
   if ((size_t)T * (size_t)K * (size_t)I * sizeof(float) > kNoAllocScratchBytes) return MOE_ERR_CAPACITY;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
   float* scratch = nullptr;
-  if (noalloc_scratch(dev, &scratch) != cudaSuccess) return MOE_ERR_CUDA;
+  if (noalloc_scratch(&scratch) != cudaSuccess) return MOE_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const cudaError_t e =
       dtype == MOE_BF16

@@ -308,14 +308,20 @@ moe_status moe_async_destroy(moe_async_t h, void* stream);
  * its input and output buffers).
  *   y[t] = sum_{k=0..K-1, ascending} w[t,k] * E_{expert[t,k]}(x[t]),
  *   E(x) = (silu(x W1) * (x W3)) W2, fp32 accumulation, no shared expert.
- *   d_x [T,H], d_y [T,H] in dtype (moe_dtype); d_expert [T,K] int32 in [0,E) (other ids
- *   contribute nothing); d_w [T,K] fp32; d_w1, d_w3 [E,H,I] and d_w2 [E,I,H] in dtype --
- *   the caller's own weight layout, no packing.  All device pointers, all caller-owned.
+ *   d_x [T,H], d_y [T,H] in dtype (moe_dtype); d_expert [T,K] int32 in [0,E); d_w [T,K]
+ *   fp32; d_w1, d_w3 [E,H,I] and d_w2 [E,I,H] in dtype -- the caller's own weight layout,
+ *   no packing.  All device pointers, all caller-owned.
+ * Expert ids outside [0,E) contribute nothing, silently: unlike moe_async_enqueue, which
+ * latches MOE_ERR_INVALID in its handle's sticky error, this call has no handle to hold an
+ * error, and the ids live in device memory where the host cannot check them without a sync.
  * Scratch: a fixed 16 MiB array compiled into the library (held on every GPU that loads
  * it, until the process exits) holds the T*K*I fp32 SwiGLU activations, so T*K*I*4 bytes
- * may not exceed 16 MiB: larger calls return MOE_ERR_CAPACITY and launch nothing.  The
- * first call on a device looks up the array's device address (no allocation); make that
- * first call before any stream capture.  Every call shares the one array and each call
+ * may not exceed 16 MiB: larger calls return MOE_ERR_CAPACITY and launch nothing.  Every
+ * call looks up the array's device address in the current context (no allocation); the
+ * first call in a context may load the library's device code, so make it before any stream
+ * capture.  Work: each (token, k) pair reads its expert's W1 and W3 columns on its own (no
+ * weight reuse between pairs of one expert), so this path is far slower than the grouped
+ * GEMMs of the handle-based calls.  Every call shares the one array and each call
  * overwrites every element it reads, so nothing has to be cleared, but calls whose kernels
  * overlap on the GPU (different streams, or different host threads) race on it: order them.
  * Calls no cudaMalloc/cudaFree.  Asynchronous on `stream`. */
