@@ -16,7 +16,7 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID", 2: "MOE_ERR_CAPACITY", 3: "MO
 
 # every symbol include/moe_async.h declares
 EXPORTS = ("moe_async_create", "moe_async_route", "moe_async_enqueue", "moe_async_schedule_step",
-           "moe_async_collect", "moe_async_wait", "moe_async_sync", "moe_async_get_stats",
+           "moe_async_schedule_steps", "moe_async_collect", "moe_async_wait", "moe_async_sync", "moe_async_get_stats",
            "moe_async_get_trace", "moe_async_snapshot", "moe_async_destroy",
            "moe_async_status_string", "moe_async_profile", "moe_async_profile_read",
            "moe_async_stream_setup", "moe_async_stream_run", "moe_async_stream_trace",
@@ -78,7 +78,8 @@ def load():
         "moe_async_route": [F32P, I32, I32, I32, I32P, F32P, P],
         "moe_async_enqueue": [P, I32, I32, I32P, I32P, P, I32P, F32P, U32P, U32P, P],
         "moe_async_schedule_step": [P, I32, ctypes.POINTER(Policy), P],
-        "moe_async_collect": [P, I32, I32, P, I32P, U32P, I32P, I32, P],
+        "moe_async_schedule_steps": [P, I32, ctypes.POINTER(Policy), I32, P],
+        "moe_async_collect": [P, I32, I32, P, I32P, U32P, U32P, I32P, I32, P],
         "moe_async_wait": [P, I32, ctypes.POINTER(Policy), I32, I32, P],
         "moe_async_sync": [P, P],
         "moe_async_get_stats": [P, P, ctypes.POINTER(Stats)],

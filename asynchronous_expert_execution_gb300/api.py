@@ -101,10 +101,17 @@ class MoEAsync:
         N.check(self.lib.moe_async_schedule_step(self.h, layer, ctypes.byref(p), _stream(stream)),
                 "moe_async_schedule_step")
 
-    def collect(self, layer, y_out, slot_out, n_out, gen_out=None, append=False, max_out=None, stream=None):
+    def schedule_steps(self, layer, policy, max_steps, stream=None):
+        """Up to `max_steps` consecutive steps in one device plan (MTFS / THRESHOLD)."""
+        p = policy.c()
+        N.check(self.lib.moe_async_schedule_steps(self.h, layer, ctypes.byref(p), max_steps, _stream(stream)),
+                "moe_async_schedule_steps")
+
+    def collect(self, layer, y_out, slot_out, n_out, gen_out=None, append=False, max_out=None, stream=None,
+                step_out=None):
         max_out = y_out.shape[0] if max_out is None else max_out
         st = self.lib.moe_async_collect(self.h, layer, max_out, _ptr(y_out), _ptr(slot_out), _ptr(gen_out),
-                                        _ptr(n_out), int(append), _stream(stream))
+                                        _ptr(step_out), _ptr(n_out), int(append), _stream(stream))
         N.check(st, "moe_async_collect")
 
     def cancel(self, layer, slots, stream=None):

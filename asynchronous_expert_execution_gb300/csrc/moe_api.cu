@@ -166,13 +166,15 @@ __global__ void enqueue_kernel(LayerView L, Dims d, DevCounters* C, int n, int t
 __global__ void __launch_bounds__(1024) schedule_kernel(LayerView L, Dims d, StepPlan* P,
                                                         DevCounters* C, moe_async_policy pol,
                                                         TileGeom g, int layer, int trace_cap,
-                                                        int4* trace, long long weight_bytes_per_run) {
+                                                        int4* trace, long long weight_bytes_per_run,
+                                                        int max_steps) {
   __shared__ PlanScratch sc;
   // launched as a programmatic dependent of the kernel before it (the last enqueue or
   // GEMM2): wait for it, then let GEMM1 start; GEMM1 waits for this plan
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  plan_layer(L, d, P, C, pol, g, layer, trace_cap, trace, weight_bytes_per_run, (int)C->steps + 1, true, sc);
+  plan_layer(L, d, P, C, pol, g, layer, trace_cap, trace, weight_bytes_per_run, (int)C->steps + 1, true, sc,
+             max_steps);
 }
 
 // ---------------------------------------------------------------- collect
@@ -181,7 +183,8 @@ __global__ void __launch_bounds__(1024) schedule_kernel(LayerView L, Dims d, Ste
 template <typename T>
 __global__ void collect_kernel(LayerView L, Dims d, DevCounters* C, int max_out, T* __restrict__ y_out,
                                int32_t* __restrict__ slot_out, uint32_t* __restrict__ gen_out,
-                               int32_t* __restrict__ n_io, int append, int parts) {
+                               uint32_t* __restrict__ step_out, int32_t* __restrict__ n_io, int append,
+                               int parts) {
   asm volatile("griddepcontrol.wait;" ::: "memory");   // launched as a dependent of GEMM2
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const uint32_t rh = L.ready_ht[0], rt = L.ready_ht[1];
@@ -199,9 +202,11 @@ __global__ void collect_kernel(LayerView L, Dims d, DevCounters* C, int max_out,
     if (threadIdx.x == 0) {
       slot_out[base + i] = slot;
       if (gen_out) gen_out[base + i] = L.gen[slot];
+      if (step_out) step_out[base + i] = L.emit_step[slot];
       L.enq_mask[slot] = 0u;
       L.done[slot] = 0u;
       L.landed[slot] = 0u;
+      L.emit_step[slot] = 0u;
       L.gen[slot] = L.gen[slot] + 1u;
     }
   }
@@ -280,7 +285,8 @@ void free_handle(moe_async_s* h) {
   if (h->layers) {
     for (int l = 0; l < h->cfg.num_layers; ++l) {
       LayerView& L = h->layers[l];
-      void* ptrs[] = {L.pool, L.wtab, L.enq_mask, L.done, L.done_part, L.landed, L.gen, L.slotbuf, L.y, L.records,
+      void* ptrs[] = {L.pool, L.wtab, L.enq_mask, L.done, L.done_part, L.landed, L.gen, L.emit_step, L.slotbuf, L.y,
+                      L.records,
                       L.head, L.tail, L.ready, L.ready_ht, const_cast<void*>(L.w13),
                       const_cast<void*>(L.w2)};
       for (void* p : ptrs) if (p) cudaFree(p);
@@ -433,6 +439,7 @@ moe_status moe_async_create(const moe_async_config* cfg, const void* const* w1,
     ok = ok && dalloc(&L.done_part, S * (size_t)h->parts_per_pair * 4) == cudaSuccess;
     ok = ok && dalloc(&L.landed, S * 4) == cudaSuccess;
     ok = ok && dalloc(&L.gen, S * 4) == cudaSuccess;
+    ok = ok && dalloc(&L.emit_step, S * 4) == cudaSuccess;
     ok = ok && dalloc(&L.slotbuf, S * KS * H * 4) == cudaSuccess;
     ok = ok && dalloc(&L.y, S * H * es) == cudaSuccess;
     ok = ok && dalloc(&L.records, (size_t)d.NB * d.cap * 4) == cudaSuccess;
@@ -455,6 +462,7 @@ moe_status moe_async_create(const moe_async_config* cfg, const void* const* w1,
            cudaMemsetAsync(L.done_part, 0, S * (size_t)h->parts_per_pair * 4, s) == cudaSuccess &&
            cudaMemsetAsync(L.landed, 0, S * 4, s) == cudaSuccess &&
            cudaMemsetAsync(L.gen, 0, S * 4, s) == cudaSuccess &&
+           cudaMemsetAsync(L.emit_step, 0, S * 4, s) == cudaSuccess &&
            cudaMemsetAsync(L.head, 0, (size_t)d.NB * 4, s) == cudaSuccess &&
            cudaMemsetAsync(L.tail, 0, (size_t)d.NB * 4, s) == cudaSuccess &&
            cudaMemsetAsync(L.ready_ht, 0, 16, s) == cudaSuccess &&
@@ -540,13 +548,14 @@ moe_status moe_async_enqueue(moe_async_t h, int32_t layer, int32_t n, const int3
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
-moe_status moe_async_schedule_step(moe_async_t h, int32_t layer, const moe_async_policy* policy,
-                                   void* stream) {
-  if (!valid_stream_layer(h, layer) || !policy) return MOE_ERR_INVALID;
+moe_status schedule_impl(moe_async_t h, int32_t layer, const moe_async_policy* policy, int32_t max_steps,
+                         void* stream) {
+  if (!valid_stream_layer(h, layer) || !policy || max_steps < 1) return MOE_ERR_INVALID;
   if (policy->kind != MOE_POLICY_MTFS && policy->kind != MOE_POLICY_THRESHOLD && policy->kind != MOE_POLICY_RANKS)
     return MOE_ERR_INVALID;
   if (policy->max_groups < 0 || policy->min_batch < 0 || policy->fallback_groups < 0) return MOE_ERR_INVALID;
   if (policy->kind == MOE_POLICY_RANKS && policy->max_groups < 1) return MOE_ERR_INVALID;
+  if (policy->kind == MOE_POLICY_RANKS && max_steps > 1) return MOE_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const Dims& d = h->dims;
   const long long wbytes = h->cfg.expert_kind == MOE_EXPERT_SWIGLU
@@ -554,7 +563,7 @@ moe_status moe_async_schedule_step(moe_async_t h, int32_t layer, const moe_async
   prof_begin(h, MOE_KERNEL_SCHEDULE, s);
   const cudaError_t e = launch_dependent(schedule_kernel, dim3(1), dim3(1024), s, h->layers[layer], d, h->plan,
                                          h->counters, *policy, h->geom, (int)layer, (int)h->cfg.trace_capacity,
-                                         h->trace, wbytes);
+                                         h->trace, wbytes, (int)max_steps);
   prof_end(h, MOE_KERNEL_SCHEDULE, s);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   if (h->cfg.expert_kind == MOE_EXPERT_IDENTITY) return launch_identity(h, layer, s);
@@ -562,9 +571,19 @@ moe_status moe_async_schedule_step(moe_async_t h, int32_t layer, const moe_async
   return launch_ffn_simt(h, layer, s);
 }
 
+moe_status moe_async_schedule_step(moe_async_t h, int32_t layer, const moe_async_policy* policy,
+                                   void* stream) {
+  return schedule_impl(h, layer, policy, 1, stream);
+}
+
+moe_status moe_async_schedule_steps(moe_async_t h, int32_t layer, const moe_async_policy* policy,
+                                    int32_t max_steps, void* stream) {
+  return schedule_impl(h, layer, policy, max_steps, stream);
+}
+
 moe_status moe_async_collect(moe_async_t h, int32_t layer, int32_t max_out, void* d_y_out,
-                             int32_t* d_slot_out, uint32_t* d_gen_out, int32_t* d_n_out,
-                             int32_t append, void* stream) {
+                             int32_t* d_slot_out, uint32_t* d_gen_out, uint32_t* d_step_out,
+                             int32_t* d_n_out, int32_t append, void* stream) {
   if (!valid_stream_layer(h, layer) || max_out < 0 || !d_n_out) return MOE_ERR_INVALID;
   if (max_out > 0 && (!d_y_out || !d_slot_out)) return MOE_ERR_INVALID;
   if (reinterpret_cast<uintptr_t>(d_y_out) % 16) return MOE_ERR_INVALID;
@@ -575,12 +594,12 @@ moe_status moe_async_collect(moe_async_t h, int32_t layer, int32_t max_out, void
   cudaError_t e;
   if (d.dtype == MOE_BF16)
     e = launch_dependent(collect_kernel<__nv_bfloat16>, dim3(grid), dim3(128), s, h->layers[layer], d, h->counters,
-                     (int)max_out, static_cast<__nv_bfloat16*>(d_y_out), d_slot_out, d_gen_out, d_n_out,
-                     (int)append, h->parts_per_pair);
+                     (int)max_out, static_cast<__nv_bfloat16*>(d_y_out), d_slot_out, d_gen_out, d_step_out,
+                     d_n_out, (int)append, h->parts_per_pair);
   else
     e = launch_dependent(collect_kernel<float>, dim3(grid), dim3(128), s, h->layers[layer], d, h->counters,
-                     (int)max_out, static_cast<float*>(d_y_out), d_slot_out, d_gen_out, d_n_out, (int)append,
-                     h->parts_per_pair);
+                     (int)max_out, static_cast<float*>(d_y_out), d_slot_out, d_gen_out, d_step_out, d_n_out,
+                     (int)append, h->parts_per_pair);
   prof_end(h, MOE_KERNEL_COLLECT, s);
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
@@ -610,18 +629,36 @@ moe_status moe_async_wait(moe_async_t h, int32_t layer, const moe_async_policy* 
   if (!valid_stream_layer(h, layer) || !policy || max_steps < 0) return MOE_ERR_INVALID;
   if (check_every < 1) check_every = 1;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  int steps = 0;
-  for (;;) {
+  // MTFS and THRESHOLD drains run as one plan of consecutive steps while buckets are left
+  // (nothing arrives during the wait, so the picks are those of single steps); once the
+  // queues are empty and tokens are still open (a pair that has not arrived), or under
+  // RANKS, single steps are run, check_every (or the steps the queues certainly need) at a time
+  const bool fusable = policy->kind == MOE_POLICY_MTFS || policy->kind == MOE_POLICY_THRESHOLD;
+  int64_t steps = 0;
+  unsigned long long seen = 0;
+  for (int iter = 0;; ++iter) {
     moe_status st = read_counters(h, s);
     if (st != MOE_OK) return st;
-    if (h->host_counters->error) return static_cast<moe_status>(h->host_counters->error);
-    if (h->host_counters->open_tokens == 0) return MOE_OK;
+    const DevCounters& c = *h->host_counters;
+    if (iter > 0) steps += (int64_t)(c.steps - seen);
+    seen = c.steps;
+    if (c.error) return static_cast<moe_status>(c.error);
+    if (c.open_tokens == 0) return MOE_OK;
     if (steps >= max_steps) return MOE_ERR_TIMEOUT;
+    const int64_t left = (int64_t)max_steps - steps;
+    // the first plan is always tried (it counts no step if the queues are empty); later ones
+    // only while the last plan of this layer left buckets behind
+    const bool queues_left = iter == 0 || (c.plan_layer == layer && c.nonempty_left > 0);
+    if (fusable && queues_left) {
+      st = schedule_impl(h, layer, policy, (int32_t)left, stream);
+      if (st != MOE_OK) return st;
+      continue;
+    }
     // run as many steps as the queues certainly need before reading the counters again
     // (fewer host round trips in long drains), else check_every
-    const int need = drain_steps_lower_bound(*h->host_counters, layer, *policy);
-    const int batch = need > 0 ? need : check_every;
-    for (int i = 0; i < batch && steps < max_steps; ++i, ++steps) {
+    const int need = drain_steps_lower_bound(c, layer, *policy);
+    const int64_t batch = std::min<int64_t>(need > 0 ? need : check_every, left);
+    for (int64_t i = 0; i < batch; ++i) {
       st = moe_async_schedule_step(h, layer, policy, stream);
       if (st != MOE_OK) return st;
     }

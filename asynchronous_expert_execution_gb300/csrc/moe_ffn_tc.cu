@@ -326,6 +326,7 @@ __device__ __forceinline__ int chunk_nstages(int c, int nk, int nchunk, int kps)
 
 struct Tile {
   int expert;
+  int step;     // scheduling step of the work item
   uint32_t head;
   int row_base;
   int fti;      // feature (A-row) tile
@@ -346,6 +347,7 @@ __device__ __forceinline__ Tile decode_tile(const TcParams& p, const int* tb, in
     count = p.sd.ctl->att_count;
     local = t;
     tl.expert = 0;
+    tl.step = 0;
     tl.head = 0;
     tl.row_base = 0;
   } else {
@@ -359,6 +361,7 @@ __device__ __forceinline__ Tile decode_tile(const TcParams& p, const int* tb, in
     local = t - (MODE == kModeGemm2 ? it.t2_base : it.t1_base);
     count = it.count;
     tl.expert = it.expert;
+    tl.step = it.step;
     tl.head = it.head;
     tl.row_base = it.row_base;
   }
@@ -803,7 +806,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
       }
       if (MODE == kModeGemm2)
         land_and_merge<__nv_bfloat16>(L, d, C, slot_s, tl.nj, tl.fti, p.parts, tl.fti * kBM, kBM, et, 128, fin, EpiBarrier{},
-                                      p.stream_on ? &p.sd : nullptr, layer);
+                                      tl.step, p.stream_on ? &p.sd : nullptr, layer);
       else
         asm volatile("bar.sync 1, 128;" ::: "memory");   // slot_s / w_s / last_flag reused by the next unit
     }

@@ -9,6 +9,7 @@
 //     enq_mask [S]             bit k set = pair k accepted for the slot's current generation
 //     done     [S]             result parts landed (target = KS * parts_per_pair)
 //     gen      [S]             slot generation (advanced when the output is collected)
+//     emit_step[S]             scheduling step in which the slot's last result landed
 //     slotbuf  [S, KS, H] f32  weighted expert results w_k * E_k(x), one row per (slot, k)
 //     y        [S, H]          merged output sum_k slotbuf[slot][k] (ascending k)
 //     records  [NB, cap] i32   per-expert micro-queue (ring) of (slot << 5 | k); NB = E + has_shared
@@ -41,6 +42,7 @@ struct WorkItem {
   int32_t row_base;   // first row of this item in the step's gathered batch (h rows)
   int32_t t1_base;    // first GEMM1 tile of this item
   int32_t t2_base;    // first GEMM2 tile of this item
+  int32_t step;       // scheduling step this item belongs to (a plan may hold several steps)
 };
 
 struct StepPlan {
@@ -73,6 +75,7 @@ struct LayerView {
   uint32_t* done_part;  // [S][parts] results landed per feature slice (target = KS)
   uint32_t* landed;     // [S] results landed over all slices (for retirement)
   uint32_t* gen;
+  uint32_t* emit_step;  // [S] largest step among the slot's landed results (its emission step)
   float* slotbuf;
   void* y;
   int32_t* records;
@@ -280,6 +283,7 @@ __device__ __forceinline__ void stream_complete(const LayerView& L, DevCounters*
   L.enq_mask[r] = 0u;
   L.done[r] = 0u;
   L.landed[r] = 0u;
+  L.emit_step[r] = 0u;
   L.gen[r] = L.gen[r] + 1u;
   atomicAdd(&sd.ctl->combined, 1);
   atomicSub(&C->open_tokens, 1);
@@ -297,6 +301,7 @@ __device__ __forceinline__ void reclaim_slot(const LayerView& L, int parts, int 
   L.done[slot] = 0u;
   L.landed[slot] = 0u;
   L.enq_mask[slot] = 0u;
+  L.emit_step[slot] = 0u;
   L.gen[slot] = L.gen[slot] + 1u;
 }
 
@@ -332,16 +337,19 @@ struct CtaBarrier {
 // completes a slice (all KS results) sums that slice (ascending k) into y, and the slice
 // merges are counted per token in turn -- the last one publishes the token.  So the merge
 // work of a token is spread over the CTAs of its slices instead of falling on one.
+// `step` is the scheduling step of the tile's work item: a token's emission step is the
+// largest step among its results (a plan may hold several consecutive steps).
 template <typename T, typename Bar>
 __device__ void land_and_merge(const LayerView& L, const Dims& d, DevCounters* C,
                                const int* slots, int nj, int part, int parts, int f0, int fcount,
-                               int tid, int nthr, int* fin, Bar bar, const StreamDev* sd = nullptr,
-                               int layer = 0) {
+                               int tid, int nthr, int* fin, Bar bar, int step,
+                               const StreamDev* sd = nullptr, int layer = 0) {
   __threadfence();
   bar();
   for (int j = tid; j < nj; j += nthr) {
     const int slot = slots[j];
     const uint32_t mask = L.enq_mask[slot];              // stable during a step
+    if (!sd) atomicMax(&L.emit_step[slot], (uint32_t)step);
     const uint32_t old = atomicAdd(&L.done_part[(size_t)slot * parts + part], 1u);
     const uint32_t landed = atomicAdd(&L.landed[slot], 1u) + 1u;
     fin[j] = (old + 1u == (uint32_t)d.KS) && !(mask & kRetired);

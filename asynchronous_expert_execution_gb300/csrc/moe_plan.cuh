@@ -14,6 +14,14 @@ namespace moe {
 // expert-parallel ranks, R = max_groups): each rank drains its deepest bucket; with
 // fallback_groups != 0 each idle rank then takes the deepest bucket no rank picked.  With
 // enabled = false the plan is written empty and nothing is drained or counted.
+//
+// Several steps at once (max_steps > 1, MTFS and THRESHOLD): with nothing arriving between
+// them, consecutive steps pick the non-empty buckets in one fixed order -- deepest first,
+// which puts every bucket of at least min_batch ahead of the rest -- so step s takes a
+// closed-form range of that order: MTFS G buckets a step (G = max_groups, 0 = all);
+// THRESHOLD up to max_groups eligible buckets a step while any remain, then
+// fallback_groups a step.  Each work item carries its step; the plan holds the steps up to
+// the last non-empty one (at most max_steps), and only those are counted.
 struct PlanScratch {
   int depth[kMaxBuckets];
   int order[kMaxBuckets];
@@ -22,10 +30,35 @@ struct PlanScratch {
   int n_elig, n_nonempty, n_picks;
 };
 
+// Step (0-based, within this plan) of the r-th bucket in the deepest-first order.
+__device__ __forceinline__ int pick_step(const moe_async_policy& pol, int n_elig, int r) {
+  if (pol.kind == MOE_POLICY_MTFS) return pol.max_groups > 0 ? r / pol.max_groups : 0;
+  if (pol.kind != MOE_POLICY_THRESHOLD) return 0;
+  const int ge = pol.max_groups, fb = pol.fallback_groups > 0 ? pol.fallback_groups : 1;
+  if (r < n_elig) return ge > 0 ? r / ge : 0;
+  const int elig_steps = n_elig > 0 ? (ge > 0 ? (n_elig + ge - 1) / ge : 1) : 0;
+  return elig_steps + (r - n_elig) / fb;
+}
+
+// Buckets the first `max_steps` steps take out of `n_all` non-empty ones (n_elig of them
+// eligible under THRESHOLD), in the deepest-first order.
+__device__ __forceinline__ int picks_within(const moe_async_policy& pol, int n_all, int n_elig, int max_steps) {
+  const long long ms = max_steps;
+  if (pol.kind == MOE_POLICY_MTFS)
+    return pol.max_groups > 0 ? (int)min((long long)n_all, (long long)pol.max_groups * ms) : n_all;
+  const int ge = pol.max_groups, fb = pol.fallback_groups > 0 ? pol.fallback_groups : 1;
+  if (n_elig > 0) {
+    const int elig_steps = ge > 0 ? (n_elig + ge - 1) / ge : 1;
+    if (ms <= elig_steps) return ge > 0 ? (int)min((long long)n_elig, (long long)ge * ms) : n_elig;
+    return (int)min((long long)n_all, (long long)n_elig + (long long)fb * (ms - elig_steps));
+  }
+  return (int)min((long long)n_all, (long long)fb * ms);
+}
+
 __device__ inline void plan_layer(const LayerView& L, const Dims& d, StepPlan* P, DevCounters* C,
                                   const moe_async_policy& pol, const TileGeom& g, int layer,
                                   int trace_cap, int4* trace, long long weight_bytes_per_run,
-                                  int trace_step, bool enabled, PlanScratch& sc) {
+                                  int trace_step, bool enabled, PlanScratch& sc, int max_steps = 1) {
   int* depth = sc.depth;
   int* order = sc.order;
   const int tid = threadIdx.x, nt = blockDim.x;
@@ -39,24 +72,21 @@ __device__ inline void plan_layer(const LayerView& L, const Dims& d, StepPlan* P
   }
   __syncthreads();
   const int n_elig = sc.n_elig, n_nonempty = sc.n_nonempty;
-  int minb = 1, G = pol.kind == MOE_POLICY_RANKS ? 0 : pol.max_groups;
-  if (pol.kind == MOE_POLICY_THRESHOLD) {
-    if (n_elig > 0) minb = pol.min_batch > 1 ? pol.min_batch : 1;
-    else G = pol.fallback_groups > 0 ? pol.fallback_groups : 1;
-  }
-  const int ne = (pol.kind == MOE_POLICY_THRESHOLD && n_elig == 0) ? n_nonempty : n_elig;
   // After an overflow or an out-of-range id the queues no longer describe valid pairs:
   // stop executing (the sticky error is reported to the host).
   const uint32_t err = *(volatile uint32_t*)&C->error;
   const bool halted = err == MOE_ERR_CAPACITY || err == MOE_ERR_INVALID;
-  int n = halted ? 0 : ((G > 0 && G < ne) ? G : ne);
+  // MTFS / THRESHOLD: the picks are a prefix of the deepest-first order of every non-empty
+  // bucket; RANKS ranks the non-empty buckets too (its stealers take from that order)
+  const bool ranks = pol.kind == MOE_POLICY_RANKS;
+  int n = halted ? 0 : (ranks ? n_nonempty : picks_within(pol, n_nonempty, n_elig, max(max_steps, 1)));
   for (int b = tid; b < d.NB; b += nt) {
     const int db = depth[b];
-    if (db >= minb) {
+    if (db >= 1) {
       int r = 0;
       for (int c = 0; c < d.NB; ++c) {
         const int dc = depth[c];
-        r += (dc >= minb) && (dc > db || (dc == db && c < b));
+        r += (dc >= 1) && (dc > db || (dc == db && c < b));
       }
       if (r < n) order[r] = b;
     }
@@ -126,11 +156,12 @@ __device__ inline void plan_layer(const LayerView& L, const Dims& d, StepPlan* P
         it.row_base = row_run + s_cnt - cnt;
         it.t1_base = t1_run + s_t1 - t1;
         it.t2_base = t2_run + s_t2 - t2;
+        it.step = trace_step + (ranks ? 0 : pick_step(pol, n_elig, r));
         P->items[r] = it;
         L.head[b] = it.head + (uint32_t)cnt;
         if (trace && trace_cap > 0) {
           const int ti = atomicAdd(&C->trace_n, 1);
-          if (ti < trace_cap) trace[ti] = make_int4(trace_step, layer, b, cnt);
+          if (ti < trace_cap) trace[ti] = make_int4(it.step, layer, b, cnt);
         }
       }
       row_run += __shfl_sync(0xffffffffu, s_cnt, 31);
@@ -146,8 +177,11 @@ __device__ inline void plan_layer(const LayerView& L, const Dims& d, StepPlan* P
       if (!enabled) return;
       C->plan_layer = layer;
       C->nonempty_left = n_nonempty - n;          // every pick is a non-empty bucket, drained whole
-      C->elig_left = (pol.kind == MOE_POLICY_THRESHOLD && n_elig > 0) ? n_elig - n : 0;
-      C->steps += 1ull;
+      C->elig_left = (pol.kind == MOE_POLICY_THRESHOLD && n_elig > n) ? n_elig - n : 0;
+      // one step is always counted (an empty step too); a plan of several steps counts the
+      // steps up to its last non-empty one
+      const int steps_run = max_steps <= 1 ? 1 : (n > 0 ? pick_step(pol, n_elig, n - 1) + 1 : 0);
+      C->steps += (unsigned long long)steps_run;
       C->pairs_executed += (unsigned long long)row_run;
       C->expert_runs += (unsigned long long)n;
       C->weight_bytes += (unsigned long long)n * (unsigned long long)weight_bytes_per_run;

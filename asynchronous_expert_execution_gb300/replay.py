@@ -37,6 +37,7 @@ class LayerReplay:
         dt = moe.dtype
         self.y_out = torch.empty((num_tokens, moe.H), dtype=dt, device=device)
         self.slot_out = torch.full((num_tokens,), -1, dtype=torch.int32, device=device)
+        self.step_out = torch.zeros((num_tokens,), dtype=torch.int32, device=device)
         self.n_out = torch.zeros(1, dtype=torch.int32, device=device)
         self.tick_counts = torch.zeros(4096, dtype=torch.int32, device=device)
 
@@ -52,10 +53,12 @@ class LayerReplay:
                 nxt += 1
             moe.schedule_step(L, policy, stream=stream)
             if collect_each_step:
-                moe.collect(L, self.y_out, self.slot_out, self.n_out, append=True, stream=stream)
+                moe.collect(L, self.y_out, self.slot_out, self.n_out, append=True, stream=stream,
+                            step_out=self.step_out)
                 self.tick_counts[tick - 1:tick].copy_(self.n_out)
         if not collect_each_step:
-            moe.collect(L, self.y_out, self.slot_out, self.n_out, append=True, stream=stream)
+            moe.collect(L, self.y_out, self.slot_out, self.n_out, append=True, stream=stream,
+                        step_out=self.step_out)
         self.ticks_run = self.last_tick
 
     def drain(self, policy, max_steps=10000, check_every=8, stream=None):
@@ -73,11 +76,26 @@ class LayerReplay:
             for _ in range(check_every):
                 tick += 1
                 moe.schedule_step(L, policy, stream=stream)
-                moe.collect(L, self.y_out, self.slot_out, self.n_out, append=True, stream=stream)
+                moe.collect(L, self.y_out, self.slot_out, self.n_out, append=True, stream=stream,
+                            step_out=self.step_out)
                 if tick - 1 < self.tick_counts.numel():
                     self.tick_counts[tick - 1:tick].copy_(self.n_out)
                 steps += 1
             self.ticks_run = tick
+
+    def finish(self, policy, max_steps=10000, stream=None):
+        """Drain the way the benchmark does: ``moe_async_wait`` (under MTFS / THRESHOLD one
+        device plan of the remaining steps), then one collect.  Returns the wait status."""
+        st = self.moe.wait(self.layer, policy, max_steps=max_steps, check_every=32, stream=stream)
+        self.moe.collect(self.layer, self.y_out, self.slot_out, self.n_out, append=True, stream=stream,
+                         step_out=self.step_out)
+        self.finished = True
+        return st
+
+    def device_steps(self):
+        """Emission step of each collected row, as the device recorded it."""
+        n = int(self.n_out.item())
+        return self.step_out[:n].cpu().numpy().astype(np.int64)
 
     def results(self):
         """(y by token [T, H] on the host as float64 or None rows, emission tick per token)."""

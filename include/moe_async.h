@@ -182,9 +182,27 @@ moe_status moe_async_enqueue(moe_async_t h, int32_t layer, int32_t n,
 moe_status moe_async_schedule_step(moe_async_t h, int32_t layer, const moe_async_policy* policy,
                                    void* stream);
 
+/* Up to max_steps (>= 1) consecutive scheduling steps of layer `layer` in one device plan,
+ * with the same picks, values and emission steps as that many moe_async_schedule_step calls
+ * with nothing enqueued between them.  StreamEP section 4 (MTFS) and the CascadeEP abstract
+ * (streamFFN): with no arrival between steps the queue depths only shrink, so the picks of
+ * consecutive steps are one deepest-first order of the non-empty buckets cut into steps --
+ * MTFS max_groups buckets a step (0 = all in one); THRESHOLD up to max_groups buckets of at
+ * least min_batch a step while any remain, then fallback_groups a step.  All picked buckets
+ * run in one grouped GEMM launch pair, each work item tagged with its step, so a drain of
+ * many one-expert fallback steps streams weights on every SM instead of one expert per
+ * launch.  The steps counter and the pick trace advance by the steps up to the last
+ * non-empty one (a call that finds every bucket empty counts none).  MTFS and THRESHOLD
+ * only: RANKS returns MOE_ERR_UNSUPPORTED for max_steps > 1.  Asynchronous, no host
+ * synchronisation. */
+moe_status moe_async_schedule_steps(moe_async_t h, int32_t layer, const moe_async_policy* policy,
+                                    int32_t max_steps, void* stream);
+
 /* Collect ready tokens of layer `layer` in completion order:
  *   d_y_out    : [max_out, H] cfg dtype     d_slot_out : [max_out] int32
  *   d_gen_out  : [max_out] uint32 (generation the result belongs to; may be NULL)
+ *   d_step_out : [max_out] uint32 (emission step: the scheduling step, counted from 1 over
+ *                the handle's life, in which the token's last result landed; may be NULL)
  *   d_n_out    : [1] int32 on the device
  *   append = 0 : rows are written from index 0 and *d_n_out = number written (<= max_out)
  *   append = 1 : rows are written from index *d_n_out (read on the device) and *d_n_out is
@@ -193,8 +211,8 @@ moe_status moe_async_schedule_step(moe_async_t h, int32_t layer, const moe_async
  * Each collected slot is reclaimed (its generation advances) after its output row is copied,
  * so it may carry a new request from then on. */
 moe_status moe_async_collect(moe_async_t h, int32_t layer, int32_t max_out, void* d_y_out,
-                             int32_t* d_slot_out, uint32_t* d_gen_out, int32_t* d_n_out,
-                             int32_t append, void* stream);
+                             int32_t* d_slot_out, uint32_t* d_gen_out, uint32_t* d_step_out,
+                             int32_t* d_n_out, int32_t append, void* stream);
 
 /* Cancel the current request of each slot in d_slots[0..n) (int32, device) of `layer`.
  * "asynchronous MoE serving" notes: an abandoned operation retires its buffer until a quiescent
@@ -208,11 +226,13 @@ moe_status moe_async_cancel(moe_async_t h, int32_t layer, int32_t n, const int32
                             void* stream);
 
 /* Run scheduling steps of `layer` under `policy` until no token of the handle is open
- * (accepted but not yet combined, in any layer); at most max_steps steps.  Between reads of
- * the device counters it runs as many steps as the layer's queues certainly still need (each
- * step drains its picks whole and takes at most max_groups buckets under MTFS or RANKS, or
- * fallback_groups under THRESHOLD once no bucket reaches min_batch), else `check_every`
- * steps.  Synchronises `stream`.  Returns MOE_ERR_TIMEOUT when tokens are still open after
+ * (accepted but not yet combined, in any layer); at most max_steps steps.  Under MTFS and
+ * THRESHOLD the layer's queued buckets are drained as one plan of consecutive steps
+ * (moe_async_schedule_steps), re-planned while the last plan left buckets behind.  Once the
+ * queues are empty while tokens are still open, and under RANKS, single steps run: between
+ * reads of the device counters as many as the layer's queues certainly still need (each step
+ * drains its picks whole and takes at most max_groups buckets under RANKS), else
+ * `check_every` steps.  Synchronises `stream`.  Returns MOE_ERR_TIMEOUT when tokens are still open after
  * max_steps (e.g. a withheld pair), else the sticky device error. */
 moe_status moe_async_wait(moe_async_t h, int32_t layer, const moe_async_policy* policy,
                           int32_t max_steps, int32_t check_every, void* stream);

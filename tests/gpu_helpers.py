@@ -37,8 +37,13 @@ def oracle_policy(spec):
 
 
 def gpu_layer(pkg, spec, wl, waves=None, dev="cuda", expert_kind="swiglu", x=None, idx=None, w=None,
-              trace_capacity=65536, max_drain=20000, weights_dev=None):
-    """Run one layer of `wl` through the library; returns a dict of host results."""
+              trace_capacity=65536, max_drain=20000, weights_dev=None, drain="steps"):
+    """Run one layer of `wl` through the library; returns a dict of host results.
+
+    drain = "steps": after the last arrival, single steps each followed by a collect (the
+    emission step of every token is also derived on the host from the per-step counts and
+    must equal the device's); "wait": ``moe_async_wait`` then one collect, as the benchmark
+    drains (one device plan of the remaining steps under MTFS / THRESHOLD)."""
     L = spec.layer
     waves = wl.waves if waves is None else waves
     dt = wl.x.dtype
@@ -55,8 +60,14 @@ def gpu_layer(pkg, spec, wl, waves=None, dev="cuda", expert_kind="swiglu", x=Non
     rep = pkg.LayerReplay(moe, waves, spec.tokens, device=dev, idx_host=idx.cpu().numpy())
     pol = pkg.Policy.from_spec(spec)
     rep.run_ticks(xd, idx, w, pol)
-    drained = rep.drain(pol, max_steps=max_drain)
-    slots, y, emit = rep.results()
+    if drain == "wait":
+        drained = 0 if rep.finish(pol, max_steps=max_drain) == 0 else -1
+        slots, y, _ = rep.results()
+        emit = rep.device_steps()
+    else:
+        drained = rep.drain(pol, max_steps=max_drain)
+        slots, y, emit = rep.results()
+        assert np.array_equal(rep.device_steps(), emit), "device emission steps differ from the per-step counts"
     status = moe.sync()
     stats = moe.stats()
     trace = moe.trace()

@@ -54,7 +54,7 @@ def test_fullsize_sampled_parity(pkg, name):
     spec = get_config(name)
     L = spec.layer
     wl, ws = _device_workload(spec, seed=0)
-    res = gpu_layer(pkg, spec, wl, weights_dev=ws, trace_capacity=1 << 20)
+    res = gpu_layer(pkg, spec, wl, weights_dev=ws, trace_capacity=1 << 20, drain="wait")   # as bench.py
     assert res["status"] == 0 and res["drained"] >= 0
     T = spec.tokens
     ii, ww = om.route(wl.logits.numpy(), L.top_k)

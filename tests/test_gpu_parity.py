@@ -389,6 +389,42 @@ def test_cancel_after_merge_is_too_late(pkg):
     moe.close()
 
 
+# ------------------------------------ several steps in one plan (the drain)
+# StreamEP section 4 / CascadeEP streamFFN: with nothing arriving, consecutive steps pick one
+# deepest-first order of the buckets; one device plan of those steps must reproduce them.
+
+@pytest.mark.parametrize("name,over", [
+    ("m2", {}),                                                          # threshold + shared
+    ("m1", {"max_groups": 3}),                                           # MTFS, 3 buckets a step
+    ("c1", {"max_groups": 1}),                                           # fp32 (SIMT path)
+    ("m4", {"policy": "threshold", "min_batch": 6, "max_groups": 2, "fallback_groups": 2}),
+])
+def test_drain_plan_matches_single_steps(pkg, name, over):
+    spec = get_config(name, **over)
+    L = spec.layer
+    wl = make_workload(spec, seed=2)
+    one = gpu_layer(pkg, spec, wl, drain="steps")
+    many = gpu_layer(pkg, spec, wl, drain="wait")
+    assert one["status"] == 0 and many["status"] == 0 and many["drained"] == 0
+    T = spec.tokens
+    ii, ww = om.route(wl.logits.numpy(), L.top_k)
+    sim = om.replay_layer(L.num_experts, L.top_k, wl.x.double().numpy(), ii, ww, wl.waves, oracle_policy(spec),
+                          expert_getter(wl.weights[0], L.num_experts), has_shared=L.has_shared)
+    for res in (one, many):
+        assert trace_steps(res["trace"]) == oracle_steps(sim)          # every step's picks
+        em = np.zeros(T, dtype=np.int64)
+        em[res["slots"]] = res["emit"]
+        assert all(em[t] == sim.emit_step[t] for t in range(T))        # each token's emission step
+        assert res["stats"]["steps"] >= max(sim.emit_step.values())
+    got1 = by_token(one["slots"], one["y"], T, L.hidden)
+    got2 = by_token(many["slots"], many["y"], T, L.hidden)
+    assert np.array_equal(got1, got2)                                  # bitwise: same arithmetic
+    ref = np.stack([sim.y[t] for t in range(T)])
+    assert rel_err(got2, ref) <= TOL[L.dtype]
+    # the plan ran the remaining steps in one scheduling launch pair: fewer launches
+    assert many["stats"]["kernel_launches"] < one["stats"]["kernel_launches"]
+
+
 # ------------------------------------------- rejected pairs leave the pool alone
 # "asynchronous MoE serving" notes, inferred obligations: accept exactly the selected
 # contributions, and return a slot only after its last read; CascadeEP: generation-tagged
