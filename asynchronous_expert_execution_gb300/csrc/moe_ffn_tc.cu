@@ -45,10 +45,12 @@ constexpr int kKps = MOE_TC_KPS;      // narrow tiles
 // MOE_TC_WIDE_MIN2 (GEMM2) tokens is cut into MOE_TC_BNW-token tiles, so its weight rows are
 // read once per BNW tokens and each MMA is wide enough for the tensor pipe (measured: 46
 // cycles per 128 x N x 16 MMA for N <= 64, 64 for N = 128, 128 for N = 256).  Measured on
-// GB300 (pairs/s, c3 / c4): one threshold for both GEMMs of 128 -- 3.48 M / 1.17 M; 64 --
-// 3.66 M / 1.28 M; 33 -- 3.76 M / 1.24 M (GEMM1 gains from 33, GEMM2 loses from 48 on the
-// DeepSeek-wide layer, whose 63-token items then run on half as many CTAs).  Decode is
-// unchanged.  0 turns wide tiles off.
+// GB300 (pairs/s, Zipf prefill / DeepSeek-wide layer): one threshold for both GEMMs of 128
+// -- 3.48 M / 1.17 M; 64 -- 3.66 M / 1.28 M; 33 -- 3.76 M / 1.24 M, when every one-expert
+// step of the DeepSeek-wide layer was its own launch (its 63-token items then ran GEMM2 on
+// half as many CTAs).  Since those steps drain as one plan, GEMM2 gains from 33 as well:
+// 64 -> 33 gives 2.54 M -> 2.71 M and 3.83 M -> 3.86 M, decode unchanged.  0 turns wide
+// tiles off.
 #ifndef MOE_TC_BNW
 #define MOE_TC_BNW 128
 #endif
@@ -59,7 +61,7 @@ constexpr int kKps = MOE_TC_KPS;      // narrow tiles
 #define MOE_TC_WIDE_MIN1 33
 #endif
 #ifndef MOE_TC_WIDE_MIN2
-#define MOE_TC_WIDE_MIN2 64
+#define MOE_TC_WIDE_MIN2 33
 #endif
 constexpr int kKpsW = MOE_TC_KPSW;
 constexpr int kWideMin1 = MOE_TC_WIDE_MIN1, kWideMin2 = MOE_TC_WIDE_MIN2;

@@ -3,16 +3,22 @@
 A step is one pass of the whole hot path over one batch: route the batch's router logits,
 deliver its arrival waves on a logical clock (one scheduling step per tick), run every
 scheduling step (device-side policy, gathered SwiGLU grouped GEMM, weighted scatter,
-readiness-gated merge) and collect the merged outputs.  The workload is the GPT-OSS-120B
-shaped decode layer: 128 experts, top-4, H = I = 2880, bf16, 256 tokens in 16 waves with
-exponential arrival delays, most-tokens-first scheduling.
+readiness-gated merge), drain the queues left after the last arrival, and collect the merged
+outputs.  The headline workload is the DeepSeek-style wide layer: 256 routed experts + 1
+shared, top-8, H = 7168, I = 2048, bf16, 2048 tokens in 8 Dirichlet(0.5) waves, threshold
+scheduling (64 tokens) with a most-tokens-first fallback.  The GPT-OSS decode layer, the Zipf
+prefill chunk and the 4-layer streaming decode are measured after it, in the same run, as
+sub-records of the same JSON line.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c2] [--impl ours|reference]
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload c4] [--subconfigs c2,c3,c5]
+                  [--impl ours|reference]
 
 Prints one JSON line.  With N > 1 (torchrun) every rank runs an independent replica of the
-workload (weak scaling, no data-path collective); the timing is the max over ranks.
+workload (weak scaling, no data-path collective); the timing is the max over ranks, and the
+sub-records are skipped.
 """
 import argparse
+import ctypes
 import dataclasses
 import re
 import hashlib
@@ -34,16 +40,19 @@ METRIC = "routed token-expert pairs/sec (expert FFN+combine) at 1 GB300; % of ro
 UNIT = "pairs/s"
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--workload", default="c2")
+    ap.add_argument("--workload", default="c4")
+    ap.add_argument("--subconfigs", default="c2,c3,c5",
+                    help="workloads measured after the headline one (N = 1 only); '' for none")
+    ap.add_argument("--sub-steps", type=int, default=50, help="timed steps of each sub-record")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--policy", default="mtfs", choices=["mtfs", "flfs", "defrag", "barrier"],
                     help="layer-level policy of the streaming workloads (c5, s1)")
     ap.add_argument("--defrag-window", type=int, default=2)
@@ -55,7 +64,7 @@ def parse():
     ap.add_argument("--no-steal", action="store_true", help="with --ranks: idle ranks do not steal")
     ap.add_argument("--max-groups", type=int, default=-1,
                     help="MTFS / threshold: G >= 0 replaces the workload's bucket limit per step (0 = all)")
-    return ap.parse_args()
+    return ap.parse_args(argv)
 
 
 def policy_name(spec):
@@ -64,9 +73,11 @@ def policy_name(spec):
     return spec.policy + (f" (G = {spec.max_groups})" if spec.max_groups > 0 else "")
 
 
-def workload_spec(args):
+def workload_spec(args, name=None):
     from workloads import get_config
-    spec = get_config(args.workload)
+    spec = get_config(name or args.workload)
+    if spec.num_layers > 1:
+        return spec
     if args.ranks > 0:
         spec = dataclasses.replace(spec, policy="ranks", max_groups=args.ranks,
                                    fallback_groups=0 if args.no_steal else 1)
@@ -87,34 +98,36 @@ def peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clock/throttle sampling during the timed region."""
+    """nvidia-smi clock/throttle sampling during the timed region (every 20 ms)."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index):
+    def __init__(self, gpu_index, interval_ms=20):
         self.gpu = gpu_index
+        self.interval = interval_ms
         self.p = None
 
     def start(self):
         try:
             self.p = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
-                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                       "--format=csv,noheader,nounits", "-lms", str(self.interval)],
                                       stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.1)                     # the first sample lands before the timed region
         except (OSError, FileNotFoundError):
             self.p = None
 
     def stop(self):
         if self.p is None:
             return None
-        time.sleep(0.25)
+        time.sleep(0.05)
         self.p.terminate()
         try:
             out, _ = self.p.communicate(timeout=5)
         except subprocess.TimeoutExpired:
             self.p.kill()
             out, _ = self.p.communicate()
-        sm, mx, reasons = [], [], set()
+        sm, mx, pw, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in out.strip().splitlines():
             f = [x.strip() for x in line.split(",")]
@@ -125,12 +138,17 @@ class ClockSampler:
                 mx.append(float(f[2]))
             except ValueError:
                 continue
+            try:
+                pw.append(float(f[3]))
+            except ValueError:
+                pass
             for n, v in zip(names, f[5:9]):
                 if v.lower().startswith("active"):
                     reasons.add(n)
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "interval_ms": self.interval, "power_w_max": max(pw) if pw else None,
                 "reasons": sorted(reasons)}
 
 
@@ -152,8 +170,9 @@ def source_hash(files=KERNEL_SOURCES):
     return h.hexdigest()[:16]
 
 
-def traffic_for(kernel):
-    """ncu DRAM bytes per launch for `kernel`, if the committed capture matches this source."""
+def traffic_for(workload, kernel):
+    """ncu DRAM bytes per launch of `kernel` on `workload`, if the committed capture matches
+    the current kernel source."""
     p = os.path.join(ROOT, "profiles", "dram_traffic.json")
     if not os.path.exists(p):
         return None
@@ -161,8 +180,8 @@ def traffic_for(kernel):
         d = json.load(f)
     if d.get("source_hash") != source_hash():
         return None
-    k = d.get("kernels", {}).get(kernel)
-    return None if k is None else k.get("bytes_per_launch_full_size")
+    k = d.get("workloads", {}).get(workload, {}).get(kernel)
+    return None if k is None else k.get("bytes_per_launch")
 
 
 def aggregate(ms_local, units_per_step, steps, world, device):
@@ -176,6 +195,32 @@ def aggregate(ms_local, units_per_step, steps, world, device):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         ms = float(t.item())
     return ms, world * units_per_step * steps / (ms / 1e3)
+
+
+def blas_threads():
+    """Threads numpy's BLAS (OpenBLAS) runs with in this process, or None if unknown: read
+    from the loaded library through its own query function."""
+    seen = set()
+    try:
+        with open("/proc/self/maps") as f:
+            for line in f:
+                path = line.split()[-1] if line.split() else ""
+                if "openblas" in path.lower() and ".so" in path:
+                    seen.add(path)
+    except OSError:
+        return None
+    for path in sorted(seen):
+        try:
+            lib = ctypes.CDLL(path)
+        except OSError:
+            continue
+        for sym in ("scipy_openblas_get_num_threads64_", "scipy_openblas_get_num_threads",
+                    "openblas_get_num_threads64_", "openblas_get_num_threads"):
+            fn = getattr(lib, sym, None)
+            if fn is not None:
+                fn.restype = ctypes.c_int
+                return int(fn())
+    return None
 
 
 # ---------------------------------------------------------------- workload
@@ -202,7 +247,7 @@ def build_inputs(spec, seed, dev):
 
 
 class Pass:
-    """One full pass of the hot path over the batch (route, waves, steps, collect)."""
+    """One full pass of the hot path over the batch (route, waves, steps, drain, collect)."""
 
     def __init__(self, pkg, spec, moe, waves, dev):
         self.pkg, self.spec, self.moe = pkg, spec, moe
@@ -216,12 +261,11 @@ class Pass:
         self.n = torch.zeros(1, dtype=torch.int32, device=dev)
         self.last_tick = max(w.tick for w in self.waves)
         self.policy = pkg.Policy.from_spec(spec)
-        self.route_launches = 0
+        self.drains = self.policy.kind != "mtfs" or self.policy.max_groups > 0
 
     def __call__(self, x, logits):
         pkg, moe = self.pkg, self.moe
         pkg.route(logits, self.spec.layer.top_k, self.idx, self.w)
-        self.route_launches += 1
         self.n.zero_()
         nxt = 0
         for tick in range(1, self.last_tick + 1):
@@ -230,23 +274,56 @@ class Pass:
                 nxt += 1
             moe.schedule_step(0, self.policy)
             moe.collect(0, self.y, self.slots, self.n, append=True)
-        if self.policy.kind != "mtfs" or self.policy.max_groups > 0:
-            # a policy that may leave buckets behind after the last arrival keeps stepping
-            # until every token is merged; the host reads the device counters every 32 steps
-            # (measured on the DeepSeek-wide threshold workload: every 8 steps -1.4%, every
-            # 128 steps about the same as 32, the extra empty steps costing what fewer reads save)
+        if self.drains:
+            # a policy that may leave buckets behind after the last arrival drains them:
+            # moe_async_wait runs the remaining steps as one device plan (MTFS / threshold)
             st = moe.wait(0, self.policy, max_steps=100000, check_every=32)
             assert st == 0, st
             moe.collect(0, self.y, self.slots, self.n, append=True)
 
 
+def schedule_independent_bytes(spec, logits):
+    """Weight bytes of one pass if every expert the batch touches were read once (the
+    schedule-independent bound), from the routing of the batch."""
+    from oracle import moe_oracle as om            # routing ids only; the same rule as the kernels
+    L = spec.layer
+    es = 2 if L.dtype == "bf16" else 4
+    idx, _ = om.route(logits.cpu().numpy(), L.top_k)
+    touched = len(np.unique(idx)) + (1 if L.has_shared else 0)
+    return touched, touched * 3 * L.hidden * L.inter * es
+
+
 # ------------------------------------------------------------ CPU baseline
 
-def oracle_sample(spec, x_host, logits_host, ws_host, waves, budget_s=0.0):
-    """Time the oracle as it stands on a bounded sample of the workload: the waves in arrival
-    order, each delivered to a fresh oracle and run until its pairs are merged, until
-    `budget_s` seconds of oracle time are spent (at least the first wave; only waves whose
-    experts are in `ws_host`)."""
+def oracle_sample_tokens(spec, logits_host, waves, max_bytes=4 << 30):
+    """The first tokens in arrival order whose experts' weights fit `max_bytes` of host copies."""
+    from oracle import moe_oracle as om
+    L = spec.layer
+    idx, _ = om.route(logits_host.numpy(), L.top_k)
+    per_expert = 3 * L.hidden * L.inter * (2 if L.dtype == "bf16" else 4)
+    tokens, need = [], set()
+    for wave in sorted(waves, key=lambda w: w.tick):
+        for t in wave.tokens:
+            more = need | set(int(e) for e in idx[int(t)])
+            if tokens and (len(more) + (1 if L.has_shared else 0)) * per_expert > max_bytes:
+                return tokens, need
+            tokens.append(int(t))
+            need = more
+    return tokens, need
+
+
+def host_weights(ws, experts, has_shared):
+    out = {k: {e: ws[k][e].cpu() for e in sorted(experts)} for k in ("w1", "w3", "w2")}
+    if has_shared:
+        out["shared"] = tuple(ws[k].cpu() for k in ("sw1", "sw3", "sw2"))
+    return out
+
+
+def oracle_sample(spec, x_host, logits_host, wh, tokens, budget_s=0.0):
+    """Time the oracle as it stands on a bounded sample of the workload: the sample tokens
+    delivered to a fresh oracle and run until every pair is merged under the workload's
+    policy, repeated until `budget_s` seconds of oracle time are spent (at least once).  The
+    oracle converts the bf16 weights it is handed to float64 itself (inside the timing)."""
     from oracle import moe_oracle as om
     L = spec.layer
     if spec.policy == "ranks":
@@ -257,98 +334,182 @@ def oracle_sample(spec, x_host, logits_host, ws_host, waves, budget_s=0.0):
         pick = lambda d: om.mtfs_pick(d, spec.max_groups)
     x64 = x_host.to(torch.float64).numpy()
     z = logits_host.numpy()
-    pairs, dt, n_waves, n_tokens = 0, 0.0, 0, 0
-    for wave in sorted(waves, key=lambda w: w.tick):
-        tokens = np.asarray(wave.tokens)
-        if len(tokens) == 0:
-            continue
-        if n_waves > 0 and dt >= budget_s:
-            break
-        cache = {}
-
-        def experts(e, cache=cache):
-            if e not in cache:
-                cache[e] = tuple(ws_host[k][e].to(torch.float64).numpy() for k in ("w1", "w3", "w2"))
-            return cache[e]
-
+    pairs, dt, reps = 0, 0.0, 0
+    while reps == 0 or dt < budget_s:
         t0 = time.perf_counter()
-        idx, w = om.route(z, L.top_k)
-        if not all(int(e) in ws_host["w1"] for e in np.unique(idx[tokens])):
-            break                                   # experts not copied to the host: sample ends
-        sim = om.AsyncMoEOracle(L.num_experts, L.top_k, x64, experts, has_shared=False,
-                                compute=set(tokens.tolist()))
+
+        def experts(e):
+            if e == L.num_experts:
+                return tuple(m.to(torch.float64).numpy() for m in wh["shared"])
+            return tuple(wh[k][e].to(torch.float64).numpy() for k in ("w1", "w3", "w2"))
+        idx = np.zeros((z.shape[0], L.top_k), dtype=np.int64)
+        w = np.zeros((z.shape[0], L.top_k))
+        idx[tokens], w[tokens] = om.route(z[tokens], L.top_k)      # only the sample is routed
+        sim = om.AsyncMoEOracle(L.num_experts, L.top_k, x64, experts, has_shared=L.has_shared,
+                                compute=set(tokens))
         sim.deliver(tokens, idx, w)
         while sim.pending():
             sim.step(pick)
         dt += time.perf_counter() - t0
         pairs += len(tokens) * L.top_k
-        n_waves += 1
-        n_tokens += len(tokens)
-        del cache, sim
-    return pairs, dt, (f"first {n_waves} arriving wave(s): {n_tokens} tokens = {pairs} routed pairs "
-                       f"(oracle, float64)")
+        reps += 1
+        del sim
+    threads = blas_threads()
+    desc = (f"the first {len(tokens)} arriving tokens ({len(tokens) * L.top_k} routed pairs"
+            f"{' + shared' if L.has_shared else ''}), run to completion by a fresh oracle {reps} time(s); "
+            f"float64 numpy, BLAS threads: {threads if threads is not None else 'unknown'}")
+    return pairs, dt, desc, threads
 
 
-def host_weights_for_sample(ws, waves, logits_host, K, max_waves=1, max_bytes=8 << 30):
-    """Host copies of the experts the first `max_waves` arriving waves route to (the first
-    wave always; later waves while the copies stay under `max_bytes`)."""
-    from oracle import moe_oracle as om
-    idx, _ = om.route(logits_host.numpy(), K)
-    per_expert = sum(ws[k][0].numel() * ws[k][0].element_size() for k in ("w1", "w3", "w2"))
-    need = set()
-    for i, wave in enumerate(sorted(waves, key=lambda w: w.tick)[:max_waves]):
-        more = need | set(idx[np.asarray(wave.tokens, dtype=np.int64)].ravel().tolist())
-        if i > 0 and len(more) * per_expert > max_bytes:
-            break
-        need = more
-    out = {k: {} for k in ("w1", "w3", "w2")}
-    for k in out:
-        for e in sorted(need):
-            out[k][e] = ws[k][e].cpu()
-    return out
+# ------------------------------------------------------------ measurement
 
-
-# -------------------------------------------------------------------- main
-
-def run_reference(args, rank, world):
-    """The oracle on the host cores: each step a bounded sample of the workload."""
-    from workloads import get_config, make_tokens, make_logits, make_waves
-    spec = workload_spec(args)
-    if rank != 0:
-        return
-    dev = "cuda" if torch.cuda.is_available() else "cpu"
-    x, logits, ws, waves = build_inputs(spec, args.seed, dev)
-    wh = host_weights_for_sample(ws, waves, logits.cpu(), spec.layer.top_k)
+def measure_layer(args, pkg, spec, dev, rank, world, steps, warmup, e2e_steps, with_cpu):
+    """Time `steps` passes of a one-layer workload (inputs resident), then a second pass of
+    `steps` with every launch bracketed by events (per-kernel times), then `e2e_steps` passes
+    end to end from pinned host buffers.  Returns the record of this workload."""
+    L = spec.layer
+    x, logits, ws, waves = build_inputs(spec, args.seed + rank, dev)
+    moe = pkg.MoEAsync(L.num_experts, L.top_k, L.hidden, L.inter, x.dtype, spec.tokens, weights=[ws],
+                       has_shared=L.has_shared)
+    cpu_in = None
+    if with_cpu:
+        tokens, need = oracle_sample_tokens(spec, logits.cpu(), waves)
+        cpu_in = (tokens, host_weights(ws, need, L.has_shared))
     del ws
-    xh, lh = x.cpu(), logits.cpu()
-    for _ in range(args.warmup):
-        oracle_sample(spec, xh, lh, wh, waves)
-    tot_p, tot_t, desc = 0, 0.0, ""
-    for _ in range(args.steps):
-        p, t, desc = oracle_sample(spec, xh, lh, wh, waves)
-        tot_p += p
-        tot_t += t
-    value = tot_p / tot_t
-    cores = os.cpu_count()
-    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": 1e3 * tot_t / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "impl": "reference",
-            "config": {"workload": spec.name, "experts": spec.layer.num_experts, "top_k": spec.layer.top_k,
-                       "hidden": spec.layer.hidden, "inter": spec.layer.inter, "tokens": spec.tokens,
-                       "waves": spec.num_waves, "policy": policy_name(spec), "sample": desc},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc},
-            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-    print(json.dumps(line), flush=True)
+    torch.cuda.empty_cache()
+    run = Pass(pkg, spec, moe, waves, dev)
+
+    def barrier():
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+            torch.cuda.synchronize()
+
+    for _ in range(warmup):
+        run(x, logits)
+    assert moe.sync() == 0, "device error during warm-up"
+    assert int(run.n.item()) == spec.tokens
+    s0 = moe.stats()
+    stream = torch.cuda.current_stream()
+    clocks = ClockSampler(torch.cuda.current_device())
+    barrier()
+    clocks.start()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(steps):
+        run(x, logits)
+    ev1.record(stream)
+    barrier()
+    clk = clocks.stop()
+    routed_pairs_step = spec.tokens * L.top_k
+    ms, value = aggregate(ev0.elapsed_time(ev1), routed_pairs_step, steps, world, dev)
+    s1 = moe.stats()
+    assert s1["error"] == 0 and int(run.n.item()) == spec.tokens
+    launches = (s1["kernel_launches"] - s0["kernel_launches"]) + steps   # + one route per step
+
+    # per-kernel durations: a second pass of K steps with every launch bracketed by events
+    moe.profile(True)
+    s2 = moe.stats()
+    for _ in range(steps):
+        run(x, logits)
+    prof = moe.profile_read()
+    moe.profile(False)
+    s3 = moe.stats()
+    runs = (s3["expert_runs"] - s2["expert_runs"]) / steps
+    pairs_p = (s3["pairs_executed"] - s2["pairs_executed"]) / steps
+    wbytes_step = (s3["weight_bytes"] - s2["weight_bytes"]) / steps
+    H, I = L.hidden, L.inter
+    es = 2 if L.dtype == "bf16" else 4
+    # algorithmic bytes per step of each FFN kernel (weights as scheduled + activations)
+    alg = {"ffn1": runs * 2 * H * I * es + pairs_p * (H + I) * es,
+           "ffn2": runs * H * I * es + pairs_p * I * es + spec.tokens * H * es}
+    kern_ms = {k: prof[k][0] / steps for k in prof}
+    dom = max(("ffn1", "ffn2"), key=lambda k: kern_ms[k])
+    hbm, tf_burst, tf_sust, src = peaks()
+    launches_dom = prof[dom][1] / steps
+    achieved = alg[dom] / (kern_ms[dom] / 1e3) / 1e9
+    roof = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm, "unit": "GB/s",
+            "frac": achieved / hbm, "peak_source": src,
+            "traffic": traffic_for(spec.name, dom),
+            "bytes_per_launch": alg[dom] / launches_dom if launches_dom else None,
+            "ms_per_launch": kern_ms[dom] / launches_dom if launches_dom else None,
+            "launches_per_step": launches_dom}
+    # whole FFN + combine path against its roofline: as scheduled (the weights of every expert
+    # run of every step) and schedule-independent (each touched expert's weights once)
+    flops_step = pairs_p * 6 * H * I
+    act_bytes = pairs_p * (H * es + 12) + spec.tokens * H * es      # gathered rows, records, y
+    bytes_step = wbytes_step + act_bytes
+    touched, w_indep = schedule_independent_bytes(spec, logits)
+    t_roof = max(flops_step / (tf_sust * 1e12), bytes_step / (hbm * 1e9))
+    t_indep = max(flops_step / (tf_sust * 1e12), (w_indep + act_bytes) / (hbm * 1e9))
+    ffn_ms = kern_ms["ffn1"] + kern_ms["ffn2"]
+    step_ms = ms / steps
+    path = {"t_roof_ms": 1e3 * t_roof, "ffn_combine_ms": ffn_ms, "frac": 1e3 * t_roof / ffn_ms,
+            "step_frac": 1e3 * t_roof / step_ms, "weight_bytes_per_step": wbytes_step,
+            "expert_runs_per_step": runs, "flops_per_step": flops_step,
+            "schedule_independent": {"experts_touched": touched, "weight_bytes": w_indep,
+                                     "t_roof_ms": 1e3 * t_indep, "frac": 1e3 * t_indep / ffn_ms,
+                                     "step_frac": 1e3 * t_indep / step_ms},
+            "weight_reread_factor": wbytes_step / w_indep,
+            "kernel_ms_per_step": {k: round(v, 4) for k, v in kern_ms.items()}}
+
+    # end to end through the C ABI from pinned host buffers (H2D inputs, D2H outputs per step)
+    xh = x.cpu().pin_memory()
+    lh = logits.cpu().pin_memory()
+    yh = torch.empty(run.y.shape, dtype=run.y.dtype).pin_memory()
+    sh = torch.empty(run.slots.shape, dtype=run.slots.dtype).pin_memory()
+    xd, ld = torch.empty_like(x), torch.empty_like(logits)
+    barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        xd.copy_(xh, non_blocking=True)
+        ld.copy_(lh, non_blocking=True)
+        run(xd, ld)
+        yh.copy_(run.y, non_blocking=True)
+        sh.copy_(run.slots, non_blocking=True)
+    e1.record(stream)
+    barrier()
+    e2e_ms, e2e_value = aggregate(e0.elapsed_time(e1), routed_pairs_step, e2e_steps, world, dev)
+    h2d = xh.numel() * xh.element_size() + lh.numel() * lh.element_size()
+    d2h = yh.numel() * yh.element_size() + sh.numel() * sh.element_size()
+    e2e = {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "steps": e2e_steps}
+
+    cpu = None
+    if cpu_in is not None:
+        tokens, wh = cpu_in
+        p, t, desc, threads = oracle_sample(spec, x.cpu(), logits.cpu(), wh, tokens, budget_s=10.0)
+        cpu = {"value": p / t, "unit": UNIT, "cores": threads if threads is not None else os.cpu_count(),
+               "host_cores": os.cpu_count(), "kind": "oracle", "sample": desc, "seconds": t}
+    moe.close()
+    del x, logits, moe, run
+    torch.cuda.empty_cache()
+    return {"workload": spec.name, "value": value, "unit": UNIT, "steps": steps, "warmup": warmup,
+            "ms_per_step": step_ms, "dtype": L.dtype,
+            "config": {"workload": spec.name, "experts": L.num_experts, "shared_expert": L.has_shared,
+                       "top_k": L.top_k, "hidden": H, "inter": I, "tokens": spec.tokens,
+                       "waves": spec.num_waves, "ticks": run_ticks(waves), "policy": policy_name(spec),
+                       "routed_pairs_per_step": routed_pairs_step,
+                       "l2": "inputs larger than L2: every step streams the scheduled experts' "
+                             f"weights ({wbytes_step / 1e9:.1f} GB) through HBM"},
+            "roofline": roof, "path_roofline": path, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": int(launches), "clocks": clk}
 
 
-def run_stream(args, pkg, dev):
+def run_ticks(waves):
+    return max(w.tick for w in waves)
+
+
+def measure_stream(args, pkg, spec, dev, steps, warmup, e2e_steps):
     """Streaming multi-layer decode (c5 shape): sustained pairs/s of the device-resident
     runtime under a layer-level policy, with its schedule statistics.  Each step sets the
-    stream up again (untimed: projection packing, graph capture) and times the run."""
-    from workloads import get_config, make_stream_inputs
+    stream up again (untimed: projection packing, graph capture) and times the run; the end
+    to end figure times the setup and run together with the host copies of the inputs and
+    of the outputs (the per-request history and completion ticks)."""
+    from workloads import make_stream_inputs
     from workloads.build import make_layer_weights
-    spec = workload_spec(args)
     lay = spec.layer
     R, H, NL, M = spec.tokens, lay.hidden, spec.num_layers, 64
     wl = make_stream_inputs(spec, args.seed, M, weights=False)
@@ -366,23 +527,47 @@ def run_stream(args, pkg, dev):
                hist_window=args.history_window)
     stream = torch.cuda.current_stream()
     times, out = [], None
-    for i in range(args.warmup + args.steps):
+    clk = None
+    clocks = ClockSampler(torch.cuda.current_device())
+    for i in range(warmup + steps):
         moe.stream_setup(proj, x0, logits, delays, M, spec.stream_steps, hist, done, **pol)
         s0 = moe.stats()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize()
+        if i == warmup:
+            clocks.start()
         e0.record(stream)
         st, ticks, comb = moe.stream_run(max_ticks=100000, check_every=16)
         e1.record(stream)
         torch.cuda.synchronize()
         assert st == 0, st
         s1 = moe.stats()
-        if i >= args.warmup:
+        if i >= warmup:
             times.append(e0.elapsed_time(e1))
             out = (ticks, comb, s1["expert_runs"] - s0["expert_runs"], s1["weight_bytes"] - s0["weight_bytes"],
                    s1["kernel_launches"] - s0["kernel_launches"])
+    clk = clocks.stop()
     tr = moe.stream_trace()
     dn = done.cpu().numpy()
+    # end to end: inputs from pinned host memory, setup + run, outputs back to pinned memory
+    x0h, lh, dh = x0.cpu().pin_memory(), logits.cpu().pin_memory(), delays.cpu().pin_memory()
+    hh = torch.empty(hist.shape, dtype=hist.dtype).pin_memory()
+    doh = torch.empty(done.shape, dtype=done.dtype).pin_memory()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    comb_e2e = 0
+    for _ in range(e2e_steps):
+        x0.copy_(x0h, non_blocking=True)
+        logits.copy_(lh, non_blocking=True)
+        delays.copy_(dh, non_blocking=True)
+        moe.stream_setup(proj, x0, logits, delays, M, spec.stream_steps, hist, done, **pol)
+        st, _, c = moe.stream_run(max_ticks=100000, check_every=16)
+        assert st == 0, st
+        hh.copy_(hist, non_blocking=True)
+        doh.copy_(done, non_blocking=True)
+        comb_e2e += c
+    torch.cuda.synchronize()
+    e2e_s = time.perf_counter() - t0
     moe.close()
     ticks, comb, runs, wbytes, launches = out
     lat = []
@@ -395,20 +580,72 @@ def run_stream(args, pkg, dev):
     exp_passes = int((tr[:, 1] == 2).sum())
     att_passes = int((tr[:, 1] == 1).sum())
     t_roof = (wbytes + att_passes * H * H * 2) / (hbm * 1e9)
-    line = {"metric": METRIC, "value": pairs / (ms / 1e3), "unit": UNIT, "n_gpus": 1, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+    # schedule-independent (lockstep) bound: a cohort of R requests advances one layer per
+    # expert pass, so ceil(merges / R) passes each read every touched expert of the layer once
+    passes_lockstep = -(-comb // R)
+    w_lockstep = passes_lockstep * lay.num_experts * 3 * H * lay.inter * 2
+    t_lock = (w_lockstep + passes_lockstep * H * H * 2) / (hbm * 1e9)
+    del proj, x0, logits, delays, hist, done
+    torch.cuda.empty_cache()
+    return {"workload": spec.name, "value": pairs / (ms / 1e3), "unit": UNIT, "steps": steps, "warmup": warmup,
+            "ms_per_step": ms, "dtype": "bf16",
             "config": {"workload": spec.name, "layers": NL, "requests": R, "stop_merges": spec.stream_steps,
                        "policy": args.policy, "defrag_window": args.defrag_window,
                        "defrag_decay": args.defrag_decay, "history_window": args.history_window},
             "schedule": {"ticks": ticks, "merges": comb, "expert_passes": exp_passes, "attention_passes": att_passes,
                          "expert_runs": runs, "weight_bytes": wbytes,
-                         "reread_vs_lockstep": exp_passes / max(1, -(-comb // R)),
+                         "reread_vs_lockstep": exp_passes / max(1, passes_lockstep),
                          "step_latency_ticks_mean": float(np.mean(lat)),
                          "step_latency_ticks_p99": float(np.percentile(lat, 99))},
             "path_roofline": {"t_roof_ms": 1e3 * t_roof, "frac": 1e3 * t_roof / ms, "peak": hbm,
-                              "peak_source": src},
-            "gpu_launches": int(launches)}
+                              "peak_source": src,
+                              "schedule_independent": {"lockstep_passes": passes_lockstep,
+                                                       "weight_bytes": w_lockstep, "t_roof_ms": 1e3 * t_lock,
+                                                       "frac": 1e3 * t_lock / ms},
+                              "weight_reread_factor": wbytes / w_lockstep},
+            "e2e": {"value": comb_e2e * lay.top_k / e2e_s, "unit": UNIT,
+                    "h2d_bytes_per_step": x0h.numel() * 2 + lh.numel() * 4 + dh.numel() * 4,
+                    "d2h_bytes_per_step": hh.numel() * 2 + doh.numel() * 4, "steps": e2e_steps,
+                    "includes": "stream setup (projection packing, graph capture) and run, host copies"},
+            "gpu_launches": int(launches), "clocks": clk}
+
+
+# -------------------------------------------------------------------- main
+
+def run_reference(args, rank, world):
+    """The oracle on the host cores: each step a bounded sample of the workload."""
+    spec = workload_spec(args)
+    if rank != 0:
+        return
+    if spec.num_layers > 1:
+        print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the oracle on the "
+                          "one-layer workloads; pass --workload c1..c4"}), flush=True)
+        return
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    x, logits, ws, waves = build_inputs(spec, args.seed, dev)
+    tokens, need = oracle_sample_tokens(spec, logits.cpu(), waves)
+    wh = host_weights(ws, need, spec.layer.has_shared)
+    del ws
+    xh, lh = x.cpu(), logits.cpu()
+    for _ in range(args.warmup):
+        oracle_sample(spec, xh, lh, wh, tokens)
+    tot_p, tot_t, desc, threads = 0, 0.0, "", None
+    for _ in range(args.steps):
+        p, t, desc, threads = oracle_sample(spec, xh, lh, wh, tokens)
+        tot_p += p
+        tot_t += t
+    value = tot_p / tot_t
+    cores = threads if threads is not None else os.cpu_count()
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1e3 * tot_t / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": spec.name, "experts": spec.layer.num_experts, "top_k": spec.layer.top_k,
+                       "hidden": spec.layer.hidden, "inter": spec.layer.inter, "tokens": spec.tokens,
+                       "waves": spec.num_waves, "policy": policy_name(spec), "sample": desc},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "host_cores": os.cpu_count(),
+                             "kind": "oracle", "sample": desc},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
@@ -419,18 +656,10 @@ def main():
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         return run_reference(args, rank, world)
-    from workloads import get_config as _gc
-    if _gc(args.workload).num_layers > 1:
-        import __graft_entry__ as g
-        g.build()
-        import asynchronous_expert_execution_gb300 as pkg
-        torch.cuda.set_device(local)
-        return run_stream(args, pkg, torch.device("cuda", local))
-
+    assert args.warmup >= 3, "at least 3 warm-up steps"
     import __graft_entry__ as g
     g.build()
     import asynchronous_expert_execution_gb300 as pkg
-    from workloads import get_config
 
     assert torch.cuda.is_available(), "bench.py needs a CUDA device"
     torch.cuda.set_device(local)
@@ -439,130 +668,32 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
     spec = workload_spec(args)
-    L = spec.layer
-    assert args.warmup >= 3, "at least 3 warm-up steps"
-
-    x, logits, ws, waves = build_inputs(spec, args.seed + rank, dev)
-    weights = [{k: v for k, v in ws.items()}]
-    moe = pkg.MoEAsync(L.num_experts, L.top_k, L.hidden, L.inter, x.dtype, spec.tokens, weights=weights,
-                       has_shared=L.has_shared)
-    cpu_ws = None
-    if rank == 0 and not args.no_cpu_baseline:
-        cpu_ws = host_weights_for_sample(ws, waves, logits.cpu(), L.top_k, max_waves=len(waves))
-    del weights, ws
-    torch.cuda.empty_cache()
-    run = Pass(pkg, spec, moe, waves, dev)
-
-    def barrier():
-        torch.cuda.synchronize()
-        if world > 1:
-            torch.distributed.barrier()
-            torch.cuda.synchronize()
-
-    for _ in range(args.warmup):
-        run(x, logits)
-    assert moe.sync() == 0, "device error during warm-up"
-    assert int(run.n.item()) == spec.tokens
-    s0 = moe.stats()
-    stream = torch.cuda.current_stream()
-    clocks = ClockSampler(local)
-    barrier()
-    clocks.start()
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    ev0.record(stream)
-    for _ in range(args.steps):
-        run(x, logits)
-    ev1.record(stream)
-    barrier()
-    clk = clocks.stop()
-    routed_pairs_step = spec.tokens * L.top_k
-    ms, value = aggregate(ev0.elapsed_time(ev1), routed_pairs_step, args.steps, world, dev)
-    s1 = moe.stats()
-    assert s1["error"] == 0 and int(run.n.item()) == spec.tokens
-    pairs_step = (s1["pairs_executed"] - s0["pairs_executed"]) / args.steps
-    launches = (s1["kernel_launches"] - s0["kernel_launches"]) + args.steps   # + one route per step
-
-    # per-kernel durations: a second pass of K steps with every launch bracketed by events
-    moe.profile(True)
-    s2 = moe.stats()
-    for _ in range(args.steps):
-        run(x, logits)
-    prof = moe.profile_read()
-    moe.profile(False)
-    s3 = moe.stats()
-    runs = (s3["expert_runs"] - s2["expert_runs"]) / args.steps
-    pairs_p = (s3["pairs_executed"] - s2["pairs_executed"]) / args.steps
-    wbytes_step = (s3["weight_bytes"] - s2["weight_bytes"]) / args.steps
-    H, I = L.hidden, L.inter
-    es = 2 if L.dtype == "bf16" else 4
-    # algorithmic bytes per step of each FFN kernel (weights as scheduled + activations)
-    alg = {"ffn1": runs * 2 * H * I * es + pairs_p * (H + I) * es,
-           "ffn2": runs * H * I * es + pairs_p * I * es + spec.tokens * H * es}
-    kern_ms = {k: prof[k][0] / args.steps for k in prof}
-    dom = max(("ffn1", "ffn2"), key=lambda k: kern_ms[k])
-    hbm, tf_burst, tf_sust, src = peaks()
-    launches_dom = prof[dom][1] / args.steps
-    achieved = alg[dom] / (kern_ms[dom] / 1e3) / 1e9
-    roof = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm, "unit": "GB/s",
-            "frac": achieved / hbm, "peak_source": src,
-            "traffic": traffic_for(dom),
-            "bytes_per_launch": alg[dom] / launches_dom if launches_dom else None,
-            "ms_per_launch": kern_ms[dom] / launches_dom if launches_dom else None}
-    # whole FFN + combine path against its as-scheduled roofline
-    flops_step = pairs_p * 6 * H * I
-    bytes_step = wbytes_step + pairs_p * 2 * H * es + spec.tokens * H * es
-    t_roof = max(flops_step / (tf_sust * 1e12), bytes_step / (hbm * 1e9))
-    ffn_ms = kern_ms["ffn1"] + kern_ms["ffn2"]
-    path = {"t_roof_ms": 1e3 * t_roof, "ffn_combine_ms": ffn_ms, "frac": 1e3 * t_roof / ffn_ms,
-            "step_frac": 1e3 * t_roof / (ms / args.steps), "weight_bytes_per_step": wbytes_step,
-            "expert_runs_per_step": runs, "flops_per_step": flops_step,
-            "kernel_ms_per_step": {k: round(v, 4) for k, v in kern_ms.items()}}
-
-    # end to end through the C ABI from pinned host buffers (H2D inputs, D2H outputs per step)
-    xh = x.cpu().pin_memory()
-    lh = logits.cpu().pin_memory()
-    yh = torch.empty(run.y.shape, dtype=run.y.dtype).pin_memory()
-    sh = torch.empty(run.slots.shape, dtype=run.slots.dtype).pin_memory()
-    xd, ld = torch.empty_like(x), torch.empty_like(logits)
-    barrier()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(args.e2e_steps):
-        xd.copy_(xh, non_blocking=True)
-        ld.copy_(lh, non_blocking=True)
-        run(xd, ld)
-        yh.copy_(run.y, non_blocking=True)
-        sh.copy_(run.slots, non_blocking=True)
-    e1.record(stream)
-    barrier()
-    e2e_ms, e2e_value = aggregate(e0.elapsed_time(e1), routed_pairs_step, args.e2e_steps, world, dev)
-    h2d = xh.numel() * xh.element_size() + lh.numel() * lh.element_size()
-    d2h = yh.numel() * yh.element_size() + sh.numel() * sh.element_size()
-    e2e = {"value": e2e_value, "unit": UNIT,
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps}
-
-    cpu = None
-    if rank == 0 and cpu_ws is not None:
-        p, t, desc = oracle_sample(spec, x.cpu(), logits.cpu(), cpu_ws, waves, budget_s=10.0)
-        cpu = {"value": p / t, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle", "sample": desc,
-               "seconds": t}
-
+    if spec.num_layers > 1:
+        rec = measure_stream(args, pkg, spec, dev, args.steps, args.warmup, args.e2e_steps)
+    else:
+        rec = measure_layer(args, pkg, spec, dev, rank, world, args.steps, args.warmup, args.e2e_steps,
+                            with_cpu=rank == 0 and not args.no_cpu_baseline)
+    subs = {}
+    if world == 1 and args.subconfigs:
+        for name in [n for n in args.subconfigs.split(",") if n and n != args.workload]:
+            sp = workload_spec(args, name)
+            if sp.num_layers > 1:
+                subs[name] = measure_stream(args, pkg, sp, dev, max(1, args.sub_steps // 5), args.warmup,
+                                            max(1, args.e2e_steps // 10))
+            else:
+                subs[name] = measure_layer(args, pkg, sp, dev, rank, world, args.sub_steps, args.warmup,
+                                           args.e2e_steps, with_cpu=False)
     if rank == 0:
-        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-                "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
-                "scaling": "weak", "vs_baseline": None, "dtype": L.dtype, "data": "synthetic",
-                "config": {"workload": spec.name, "experts": L.num_experts, "top_k": L.top_k,
-                           "hidden": H, "inter": I, "tokens": spec.tokens, "waves": spec.num_waves,
-                           "ticks": run.last_tick, "policy": policy_name(spec),
-                           "routed_pairs_per_step": routed_pairs_step,
-                           "l2": "inputs larger than L2: every step streams the scheduled experts' "
-                                 f"weights ({wbytes_step / 1e9:.1f} GB) through HBM",
-                           "parallelism": f"replicas x{world}"},
-                "roofline": roof, "path_roofline": path, "cpu_baseline": cpu, "e2e": e2e,
-                "gpu_launches": int(launches), "clocks": clk}
+        line = {"metric": METRIC, "value": rec["value"], "unit": UNIT, "n_gpus": world, "steps": rec["steps"],
+                "warmup": rec["warmup"], "ms_per_step": rec["ms_per_step"], "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": rec["dtype"], "data": "synthetic",
+                "config": dict(rec["config"], parallelism=f"replicas x{world}")}
+        for k in ("roofline", "path_roofline", "cpu_baseline", "e2e", "gpu_launches", "clocks", "schedule"):
+            if k in rec:
+                line[k] = rec[k]
+        if subs:
+            line["subconfigs"] = subs
         print(json.dumps(line), flush=True)
-    moe.close()
     if world > 1:
         torch.distributed.destroy_process_group()
 

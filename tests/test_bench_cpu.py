@@ -25,18 +25,22 @@ def _args(*extra):
 
 
 def test_workload_spec_policy_options():
-    s = bench.workload_spec(_args())
+    s = bench.workload_spec(_args())                                  # the headline: DeepSeek-wide
+    assert s.name == "c4_deepseek_wide_shared" and s.policy == "threshold" and s.min_batch == 64
+    s = bench.workload_spec(_args("--workload", "c2"))
     assert (s.policy, s.max_groups) == ("mtfs", 0) and bench.policy_name(s) == "mtfs"
-    s = bench.workload_spec(_args("--ranks", "16"))
+    s = bench.workload_spec(_args("--workload", "c2", "--ranks", "16"))
     assert (s.policy, s.max_groups, s.fallback_groups) == ("ranks", 16, 1)
     assert bench.policy_name(s) == "ranks (R = 16, with stealing)"
-    s = bench.workload_spec(_args("--ranks", "8", "--no-steal"))
+    s = bench.workload_spec(_args("--workload", "c2", "--ranks", "8", "--no-steal"))
     assert (s.policy, s.max_groups, s.fallback_groups) == ("ranks", 8, 0)
     assert bench.policy_name(s) == "ranks (R = 8, no stealing)"
-    s = bench.workload_spec(_args("--max-groups", "4"))
+    s = bench.workload_spec(_args("--workload", "c2", "--max-groups", "4"))
     assert (s.policy, s.max_groups) == ("mtfs", 4) and bench.policy_name(s) == "mtfs (G = 4)"
-    s = bench.workload_spec(_args("--workload", "c4"))
-    assert s.policy == "threshold" and s.min_batch == 64
+    s = bench.workload_spec(_args(), "c5")                            # streaming: options left alone
+    assert s.num_layers == 4
+    a = _args()
+    assert a.subconfigs == "c2,c3,c5" and a.steps >= 50
 
 
 @pytest.fixture(scope="module")
@@ -46,19 +50,19 @@ def c1_inputs():
     return spec, x, logits, ws, waves
 
 
-def test_host_weights_cover_first_wave(c1_inputs):
+def test_oracle_sample_tokens_bounded_by_host_bytes(c1_inputs):
     from oracle import moe_oracle as om
     spec, x, logits, ws, waves = c1_inputs
     idx, _ = om.route(logits.numpy(), spec.layer.top_k)
-    first = sorted(waves, key=lambda w: w.tick)[0]
-    need = set(idx[np.asarray(first.tokens)].ravel().tolist())
-    wh = bench.host_weights_for_sample(ws, waves, logits, spec.layer.top_k)
-    assert set(wh["w1"]) == need
-    # a byte cap below one expert still keeps the first wave's experts, and nothing more
-    wh = bench.host_weights_for_sample(ws, waves, logits, spec.layer.top_k, max_waves=len(waves), max_bytes=1)
-    assert set(wh["w1"]) == need
-    wh = bench.host_weights_for_sample(ws, waves, logits, spec.layer.top_k, max_waves=len(waves))
-    assert set(wh["w1"]) == set(idx.ravel().tolist())
+    order = [int(t) for w in sorted(waves, key=lambda w: w.tick) for t in w.tokens]
+    tokens, need = bench.oracle_sample_tokens(spec, logits, waves)          # everything fits
+    assert tokens == order and need == set(idx.ravel().tolist())
+    per_expert = 3 * spec.layer.hidden * spec.layer.inter * 4
+    tokens, need = bench.oracle_sample_tokens(spec, logits, waves, max_bytes=3 * per_expert)
+    assert tokens == order[:len(tokens)] and len(need) <= 3 and len(tokens) >= 1
+    assert need == set(idx[tokens].ravel().tolist())
+    tokens, need = bench.oracle_sample_tokens(spec, logits, waves, max_bytes=1)   # at least one token
+    assert tokens == order[:1]
 
 
 @pytest.mark.parametrize("ranks", [0, 3])
@@ -66,14 +70,23 @@ def test_oracle_sample_bounded(c1_inputs, ranks):
     spec, x, logits, ws, waves = c1_inputs
     if ranks:
         spec = bench.workload_spec(_args("--workload", "c1", "--ranks", str(ranks)))
-    wh = bench.host_weights_for_sample(ws, waves, logits, spec.layer.top_k, max_waves=len(waves))
-    nonempty = [w for w in sorted(waves, key=lambda w: w.tick) if len(w.tokens)]
-    p, t, desc = bench.oracle_sample(spec, x, logits, wh, waves)             # no budget: one wave
-    assert p == len(nonempty[0].tokens) * spec.layer.top_k and t > 0
-    assert desc.startswith("first 1 arriving wave(s)")
-    p, t, desc = bench.oracle_sample(spec, x, logits, wh, waves, budget_s=1e9)   # every wave
-    assert p == spec.tokens * spec.layer.top_k
-    assert desc.startswith(f"first {len(nonempty)} arriving wave(s)")
+    tokens, need = bench.oracle_sample_tokens(spec, logits, waves, max_bytes=4 * 3 * 64 * 128 * 4)
+    wh = bench.host_weights(ws, need, spec.layer.has_shared)
+    p, t, desc, threads = bench.oracle_sample(spec, x, logits, wh, tokens)       # no budget: once
+    assert p == len(tokens) * spec.layer.top_k and t > 0
+    assert desc.startswith(f"the first {len(tokens)} arriving tokens") and "1 time(s)" in desc
+    assert "BLAS threads" in desc
+    p, t, desc, threads = bench.oracle_sample(spec, x, logits, wh, tokens, budget_s=t * 3)   # repeated
+    assert p % (len(tokens) * spec.layer.top_k) == 0 and p >= 2 * len(tokens) * spec.layer.top_k
+
+
+def test_schedule_independent_bytes(c1_inputs):
+    from oracle import moe_oracle as om
+    spec, x, logits, ws, waves = c1_inputs
+    touched, b = bench.schedule_independent_bytes(spec, logits)
+    idx, _ = om.route(logits.numpy(), spec.layer.top_k)
+    assert touched == len(set(idx.ravel().tolist()))
+    assert b == touched * 3 * spec.layer.hidden * spec.layer.inter * 4
 
 
 def test_reference_arm_json_line():

@@ -2,9 +2,9 @@
 
 A token's output must not depend on the width of the tile it ran in.  Checked on a two-expert
 top-2 layer (ragged M and K tails): all 256 tokens in one step (two items of 256 tokens: wide
-tiles in both GEMMs), steps of 40 tokens (wide GEMM1 tiles from 33 tokens, narrow GEMM2 tiles
-below 64) and steps of 32 (narrow tiles in both) give bitwise equal outputs, and they match
-the float64 oracle within the bf16 bound.
+tiles in both GEMMs), steps of 40 tokens (items of 33..63 tokens: one wide tile, its MMA only
+as wide as the item, in both GEMMs) and steps of 32 (narrow tiles in both) give bitwise equal
+outputs, and they match the float64 oracle within the bf16 bound.
 """
 import numpy as np
 import pytest
@@ -64,8 +64,8 @@ def test_wide_tiles_bitwise_equal_to_narrow_and_oracle(pkg):
     y_wide, tr_wide = _run(pkg, spec, wdev, x, idx, w, T)
     y_mixed, tr_mixed = _run(pkg, spec, wdev, x, idx, w, 40)
     y_narrow, tr_narrow = _run(pkg, spec, wdev, x, idx, w, 32)
-    # the premise: one step of two 256-token items; items of 33..63 tokens (wide GEMM1 tiles,
-    # narrow GEMM2 tiles); items of at most 32 tokens
+    # the premise: one step of two 256-token items; items of 33..63 tokens (one wide tile
+    # each, from the wide threshold of 33); items of at most 32 tokens
     assert sorted(c for _, _, _, c in tr_wide.tolist()) == [T, T]
     assert all(33 <= c < 64 for _, _, _, c in tr_mixed.tolist()[:-2])
     assert max(c for _, _, _, c in tr_narrow.tolist()) <= 32
