@@ -3,16 +3,19 @@ import ctypes
 import os
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libmoe_async.so")
+# MOE_DEBUG_BOUNDS=1 selects the bounds-checked build of the same library
+DEBUG_BOUNDS = os.environ.get("MOE_DEBUG_BOUNDS", "") == "1"
+LIB_PATH = os.path.join(_HERE, "libmoe_async_debug.so" if DEBUG_BOUNDS else "libmoe_async.so")
 
 MOE_OK, MOE_ERR_INVALID, MOE_ERR_CAPACITY, MOE_ERR_DUPLICATE, MOE_ERR_STALE, \
-    MOE_ERR_TIMEOUT, MOE_ERR_CUDA, MOE_ERR_UNSUPPORTED = range(8)
+    MOE_ERR_TIMEOUT, MOE_ERR_CUDA, MOE_ERR_UNSUPPORTED, MOE_ERR_BOUNDS = range(9)
 MOE_F32, MOE_BF16 = 0, 1
 MOE_POLICY_MTFS, MOE_POLICY_THRESHOLD, MOE_POLICY_RANKS = 0, 1, 2
 MOE_EXPERT_SWIGLU, MOE_EXPERT_IDENTITY = 0, 1
 
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID", 2: "MOE_ERR_CAPACITY", 3: "MOE_ERR_DUPLICATE",
-                4: "MOE_ERR_STALE", 5: "MOE_ERR_TIMEOUT", 6: "MOE_ERR_CUDA", 7: "MOE_ERR_UNSUPPORTED"}
+                4: "MOE_ERR_STALE", 5: "MOE_ERR_TIMEOUT", 6: "MOE_ERR_CUDA", 7: "MOE_ERR_UNSUPPORTED",
+                8: "MOE_ERR_BOUNDS"}
 
 # every symbol include/moe_async.h declares
 EXPORTS = ("moe_async_create", "moe_async_route", "moe_async_enqueue", "moe_async_schedule_step",
@@ -20,7 +23,7 @@ EXPORTS = ("moe_async_create", "moe_async_route", "moe_async_enqueue", "moe_asyn
            "moe_async_get_trace", "moe_async_snapshot", "moe_async_destroy",
            "moe_async_status_string", "moe_async_profile", "moe_async_profile_read",
            "moe_async_stream_setup", "moe_async_stream_run", "moe_async_stream_trace",
-           "moe_async_cancel")
+           "moe_async_cancel", "moe_async_debug_append_record")
 
 KERNEL_KINDS = ("enqueue", "schedule", "ffn1", "ffn2", "collect")
 
@@ -51,7 +54,7 @@ class StreamConfig(ctypes.Structure):
                [("defrag_decay", ctypes.c_double)]
 
 
-STREAM_POLICIES = {"mtfs": 0, "flfs": 1, "defrag": 2, "barrier": 3}
+STREAM_POLICIES = {"mtfs": 0, "flfs": 1, "defrag": 2, "barrier": 3, "defrag_src": 4}
 
 
 class MoEError(RuntimeError):
@@ -88,6 +91,7 @@ def load():
                                I32, ctypes.POINTER(ctypes.c_int32)],
         "moe_async_destroy": [P, P],
         "moe_async_cancel": [P, I32, I32, I32P, P],
+        "moe_async_debug_append_record": [P, I32, I32, I32, P],
         "moe_async_profile": [P, I32],
         "moe_async_profile_read": [P, P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64), I32],
         "moe_async_status_string": [ctypes.c_int],

@@ -1,8 +1,11 @@
-"""Build the in-tree shared library ``libmoe_async.so`` for sm_103a.
+"""Build the in-tree shared libraries for sm_103a.
 
-nvcc compiles each translation unit under ``csrc/`` in parallel and links them into
-one shared object next to this file.  A rebuild is skipped when the library is newer
-than every source and header.
+``libmoe_async.so`` is the release library; ``libmoe_async_debug.so`` is the same code
+compiled with MOE_DEBUG_BOUNDS, which checks every bucket, slot and k index the kernels read
+back from device state and latches MOE_ERR_BOUNDS instead of touching memory out of range
+(loaded when the environment sets MOE_DEBUG_BOUNDS=1).  nvcc compiles every translation unit
+of both under ``csrc/`` in parallel and links each set into one shared object next to this
+file.  A rebuild is skipped when a library is newer than every source and header.
 """
 import glob
 import os
@@ -15,7 +18,9 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libmoe_async.so")
+LIB_DEBUG = os.path.join(HERE, "libmoe_async_debug.so")
 BUILD_DIR = os.path.join(ROOT, "_build")
+VARIANTS = {"release": (LIB, []), "debug": (LIB_DEBUG, ["-DMOE_DEBUG_BOUNDS=1"])}
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
@@ -33,28 +38,33 @@ def sources():
     return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
 
 
-def _stale():
-    if not os.path.exists(LIB):
+def _stale(lib):
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     deps = sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(INCLUDE, "*.h"))
     return any(os.path.getmtime(p) > t for p in deps)
 
 
-def build(force=False, verbose=False):
-    """Compile and link libmoe_async.so; returns its path."""
-    if not force and not _stale():
+def build(force=False, verbose=False, variants=("release", "debug")):
+    """Compile and link the requested libraries (all translation units of all of them in
+    parallel); returns the release library's path."""
+    todo = [v for v in variants if force or _stale(VARIANTS[v][0])]
+    if not todo:
         return LIB
     nvcc = _nvcc()
-    os.makedirs(BUILD_DIR, exist_ok=True)
-    procs, objs = [], []
-    for src in sources():
-        obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
-        cmd = [nvcc, *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj]
-        if verbose:
-            print(" ".join(cmd), file=sys.stderr)
-        procs.append((src, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)))
-        objs.append(obj)
+    procs, objs = [], {}
+    for v in todo:
+        bdir = os.path.join(BUILD_DIR, v)
+        os.makedirs(bdir, exist_ok=True)
+        objs[v] = []
+        for src in sources():
+            obj = os.path.join(bdir, os.path.basename(src)[:-3] + ".o")
+            cmd = [nvcc, *ARCH, *NVCC_FLAGS, *VARIANTS[v][1], "-c", src, "-o", obj]
+            if verbose:
+                print(" ".join(cmd), file=sys.stderr)
+            procs.append((src, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)))
+            objs[v].append(obj)
     failed = []
     for src, p in procs:
         out, _ = p.communicate()
@@ -65,12 +75,14 @@ def build(force=False, verbose=False):
     if failed:
         msg = "\n".join(f"--- {s}\n{o}" for s, o in failed)
         raise RuntimeError(f"nvcc failed:\n{msg}")
-    tmp = LIB + ".tmp"
-    cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
-    r = subprocess.run(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)
-    if r.returncode != 0:
-        raise RuntimeError("link failed:\n" + r.stdout.decode(errors="replace"))
-    os.replace(tmp, LIB)
+    for v in todo:
+        lib = VARIANTS[v][0]
+        tmp = lib + ".tmp"
+        cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs[v]]
+        r = subprocess.run(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)
+        if r.returncode != 0:
+            raise RuntimeError("link failed:\n" + r.stdout.decode(errors="replace"))
+        os.replace(tmp, lib)
     return LIB
 
 

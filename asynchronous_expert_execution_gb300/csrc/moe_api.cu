@@ -194,6 +194,10 @@ __global__ void collect_kernel(LayerView L, Dims d, DevCounters* C, int max_out,
   const int chunks = d.H / V;
   for (int i = blockIdx.x; i < n; i += gridDim.x) {
     const int slot = L.ready[(rh + (uint32_t)i) % (uint32_t)d.S];
+    if (kDebugBounds && (slot < 0 || slot >= d.S)) {             // bounds-checked build
+      if (threadIdx.x == 0) set_error(C, MOE_ERR_BOUNDS);
+      continue;
+    }
     const int4* src = reinterpret_cast<const int4*>(static_cast<const T*>(L.y) + (size_t)slot * d.H);
     int4* dst = reinterpret_cast<int4*>(y_out + (size_t)(base + i) * d.H);
     for (int c = threadIdx.x; c < chunks; c += blockDim.x) dst[c] = __ldcg(src + c);
@@ -248,6 +252,19 @@ __global__ void cancel_kernel(LayerView L, Dims d, DevCounters* C, int n, const 
     atomicAdd(&C->cancelled, 1ull);
     if (retired_quiescent(old | kRetired, L.landed[slot], parts)) reclaim_slot(L, parts, slot);
   }
+}
+
+// Bounds-checked build only: append a raw record to bucket b (a test plants an out-of-range
+// record this way and checks that the kernels reject it).
+__global__ void debug_append_kernel(LayerView L, Dims d, DevCounters* C, int b, int32_t rec) {
+  const uint32_t pos = L.tail[b];
+  if (pos - L.head[b] >= (uint32_t)d.cap) {
+    set_error(C, MOE_ERR_CAPACITY);
+    return;
+  }
+  L.records[(size_t)b * d.cap + (pos % (uint32_t)d.cap)] = rec;
+  L.tail[b] = pos + 1u;
+  C->pending_pairs += 1;
 }
 
 // -------------------------------------------------------------- utilities
@@ -375,6 +392,7 @@ const char* moe_async_status_string(moe_status s) {
     case MOE_ERR_TIMEOUT: return "timeout: tokens still open";
     case MOE_ERR_CUDA: return "CUDA error";
     case MOE_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MOE_ERR_BOUNDS: return "index out of range (bounds-checked build)";
   }
   return "unknown status";
 }
@@ -775,6 +793,15 @@ moe_status moe_async_cancel(moe_async_t h, int32_t layer, int32_t n, const int32
   cancel_kernel<<<(n + 255) / 256, 256, 0, s>>>(h->layers[layer], h->dims, h->counters, n, d_slots,
                                                 h->parts_per_pair);
   prof_end(h, MOE_KERNEL_ENQUEUE, s);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status moe_async_debug_append_record(moe_async_t h, int32_t layer, int32_t bucket, int32_t record,
+                                        void* stream) {
+  if (!kDebugBounds) return MOE_ERR_UNSUPPORTED;          // release builds: no raw record writes
+  if (!valid_stream_layer(h, layer) || bucket < 0 || bucket >= h->dims.NB) return MOE_ERR_INVALID;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  debug_append_kernel<<<1, 1, 0, s>>>(h->layers[layer], h->dims, h->counters, (int)bucket, record);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

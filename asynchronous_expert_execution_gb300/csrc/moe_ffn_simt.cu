@@ -20,8 +20,8 @@ constexpr int kBH = 64;    // GEMM2 output features (of H) per tile
 // tile's 16 gathered tokens and 32 features.  Packed W13 row of gate feature f is
 // 32*(f/16) + f%16, its up row 16 further.
 template <typename T>
-__global__ void __launch_bounds__(256) ffn1_simt_kernel(LayerView L, Dims d, const StepPlan* __restrict__ P,
-                                                        T* __restrict__ hbuf) {
+__global__ void __launch_bounds__(256) ffn1_simt_kernel(LayerView L, Dims d, DevCounters* C,
+                                                        const StepPlan* __restrict__ P, T* __restrict__ hbuf) {
   __shared__ float xs[kBT][kKC + 1];
   __shared__ float gs[kBF][kKC + 1];
   __shared__ float us[kBF][kKC + 1];
@@ -39,7 +39,10 @@ __global__ void __launch_bounds__(256) ffn1_simt_kernel(LayerView L, Dims d, con
     (void)ftiles;
     const int f0 = fti * kBF, j0 = tti * kBT;
     const int nj = min(kBT, it.count - j0);
-    if (tid < kBT) slot_s[tid] = tid < nj ? (record_at(L, d, it.expert, it.head + j0 + tid) >> kKShift) : -1;
+    if (tid < kBT) {
+      const int rec = tid < nj ? record_checked(L, d, C, it.expert, it.head + j0 + tid) : -1;
+      slot_s[tid] = rec >= 0 ? rec >> kKShift : -1;
+    }
     __syncthreads();
     const int tx = tid & 31, ty = tid >> 5;
     float g0 = 0.f, g1 = 0.f, u0 = 0.f, u1 = 0.f;
@@ -107,10 +110,12 @@ __global__ void __launch_bounds__(256) ffn2_simt_kernel(LayerView L, Dims d, Dev
       int sl = -1, kk = 0;
       float wv = 0.f;
       if (tid < nj) {
-        const int rec = record_at(L, d, it.expert, it.head + j0 + tid);
-        sl = rec >> kKShift;
-        kk = rec & kKMask;
-        wv = L.wtab[(size_t)sl * d.KS + kk];
+        const int rec = record_checked(L, d, C, it.expert, it.head + j0 + tid);
+        if (rec >= 0) {
+          sl = rec >> kKShift;
+          kk = rec & kKMask;
+          wv = L.wtab[(size_t)sl * d.KS + kk];
+        }
       }
       slot_s[tid] = sl; k_s[tid] = kk; w_s[tid] = wv;
     }
@@ -142,7 +147,7 @@ __global__ void __launch_bounds__(256) ffn2_simt_kernel(LayerView L, Dims d, Dev
 #pragma unroll
       for (int m = 0; m < 4; ++m) {
         const int j = ty + 4 * m;
-        if (j < nj)
+        if (j < nj && (!kDebugBounds || slot_s[j] >= 0))
           L.slotbuf[((size_t)slot_s[j] * d.KS + k_s[j]) * d.H + f] = w_s[j] * acc[m];
       }
     }
@@ -167,15 +172,18 @@ __global__ void __launch_bounds__(256) identity_kernel(LayerView L, Dims d, DevC
       int sl = -1, kk = 0;
       float wv = 0.f;
       if (tid < nj) {
-        const int rec = record_at(L, d, it.expert, it.head + j0 + tid);
-        sl = rec >> kKShift;
-        kk = rec & kKMask;
-        wv = L.wtab[(size_t)sl * d.KS + kk];
+        const int rec = record_checked(L, d, C, it.expert, it.head + j0 + tid);
+        if (rec >= 0) {
+          sl = rec >> kKShift;
+          kk = rec & kKMask;
+          wv = L.wtab[(size_t)sl * d.KS + kk];
+        }
       }
       slot_s[tid] = sl; k_s[tid] = kk; w_s[tid] = wv;
     }
     __syncthreads();
     for (int j = 0; j < nj; ++j) {
+      if (kDebugBounds && slot_s[j] < 0) continue;
       const T* src = pool + (size_t)slot_s[j] * d.H;
       float* dst = L.slotbuf + ((size_t)slot_s[j] * d.KS + k_s[j]) * d.H;
       for (int f = tid; f < d.H; f += 256) dst[f] = w_s[j] * to_f(src[f]);
@@ -195,9 +203,9 @@ moe_status launch_ffn_simt(moe_async_s* h, int layer, cudaStream_t s) {
   const int parts = h->parts_per_pair;
   prof_begin(h, MOE_KERNEL_FFN1, s);
   if (d.dtype == MOE_BF16)
-    ffn1_simt_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(L, d, h->plan, static_cast<__nv_bfloat16*>(h->h));
+    ffn1_simt_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(L, d, h->counters, h->plan, static_cast<__nv_bfloat16*>(h->h));
   else
-    ffn1_simt_kernel<float><<<grid, 256, 0, s>>>(L, d, h->plan, static_cast<float*>(h->h));
+    ffn1_simt_kernel<float><<<grid, 256, 0, s>>>(L, d, h->counters, h->plan, static_cast<float*>(h->h));
   prof_end(h, MOE_KERNEL_FFN1, s);
   prof_begin(h, MOE_KERNEL_FFN2, s);
   if (d.dtype == MOE_BF16)

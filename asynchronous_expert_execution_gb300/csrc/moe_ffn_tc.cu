@@ -596,8 +596,8 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
           if (MODE == kModeAtt) {
             rp = static_cast<const __nv_bfloat16*>(p.sd.att_rowptr[tl.j0 + r]);
           } else {
-            const int rec = record_at(L, d, tl.expert, tl.head + tl.j0 + r);
-            rp = reinterpret_cast<const __nv_bfloat16*>(pool) + (size_t)(rec >> kKShift) * d.H;
+            const int rec = record_checked(L, d, C, tl.expert, tl.head + tl.j0 + r);
+            rp = rec >= 0 ? reinterpret_cast<const __nv_bfloat16*>(pool) + (size_t)(rec >> kKShift) * d.H : nullptr;
           }
         }
         rp_w[r] = rp;
@@ -683,11 +683,11 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
       const Tile tl = decode_tile<BN, BNW, MODE>(p, tb_s, un.t);
       if (MODE == kModeGemm2) {
         for (int j = et; j < tl.nj; j += 128) {
-          const int rec = record_at(L, d, tl.expert, tl.head + tl.j0 + j);
-          const int sl = rec >> kKShift, kk = rec & kKMask;
+          const int rec = record_checked(L, d, C, tl.expert, tl.head + tl.j0 + j);
+          const int sl = rec >= 0 ? rec >> kKShift : -1, kk = rec >= 0 ? rec & kKMask : 0;
           slot_s[j] = sl;
           k_s[j] = kk;
-          w_s[j] = L.wtab[(size_t)sl * d.KS + kk];
+          w_s[j] = rec >= 0 ? L.wtab[(size_t)sl * d.KS + kk] : 0.f;
         }
       } else if (MODE == kModeAtt) {
         for (int j = et; j < tl.nj; j += 128) {
@@ -783,7 +783,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
 #pragma unroll
               for (int j = 0; j < 16; ++j) {
                 const int col = c0 + j;
-                if (col < tl.nj)
+                if (col < tl.nj && (!kDebugBounds || slot_s[col] >= 0))
                   L.slotbuf[((size_t)slot_s[col] * d.KS + k_s[col]) * d.H + f] = w_s[col] * acc[col];
               }
             }

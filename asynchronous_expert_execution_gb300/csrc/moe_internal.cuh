@@ -110,6 +110,8 @@ struct StreamCtl {
   int32_t exp_tokens[kMaxLayers];   // tokens whose pairs wait in layer l's expert queue
   int32_t pad[4];
   int32_t drained[16][2 * kMaxLayers];   // tokens drained per queue, ring over the last ticks
+  int32_t snap[16][2 * kMaxLayers];      // depth of each queue at the decision, ring over the last ticks
+  int32_t snap_n;                        // snapshots recorded so far
 };
 
 constexpr int kMaxHistoryWindow = 16;
@@ -272,6 +274,33 @@ __device__ __forceinline__ int32_t record_at(const LayerView& L, const Dims& d, 
   return L.records[(size_t)e * d.cap + (pos % (uint32_t)d.cap)];
 }
 
+// Bounds-checked build (MOE_DEBUG_BOUNDS): every bucket, slot and k index read back from
+// device state is checked before it is used; an index out of range latches MOE_ERR_BOUNDS
+// and the access is skipped -- the stand-in for a memory checker.  Release builds compile
+// the checks out.
+#ifdef MOE_DEBUG_BOUNDS
+constexpr bool kDebugBounds = true;
+#else
+constexpr bool kDebugBounds = false;
+#endif
+
+// A queued record (slot << 5 | k) of bucket e.  In a bounds-checked build a bucket id outside
+// [0, NB), a slot outside [0, S) or a k outside [0, KS) latches MOE_ERR_BOUNDS and reads as
+// -1, which every consumer treats as an absent row: nothing gathered, nothing written.
+__device__ __forceinline__ int32_t record_checked(const LayerView& L, const Dims& d, DevCounters* C, int e,
+                                                  uint32_t pos) {
+  if (kDebugBounds && (e < 0 || e >= d.NB)) {
+    set_error(C, MOE_ERR_BOUNDS);
+    return -1;
+  }
+  const int32_t r = record_at(L, d, e, pos);
+  if (kDebugBounds && (r < 0 || (r >> kKShift) >= d.S || (r & kKMask) >= d.KS)) {
+    set_error(C, MOE_ERR_BOUNDS);
+    return -1;
+  }
+  return r;
+}
+
 // Streaming runtime: request r finished its step at `layer` (its merged output is already in
 // hist[r][n+1]).  Advance its step count, record the tick, reclaim its slot in this layer,
 // and queue it for the next layer's attention stage unless it reached its last step.
@@ -348,6 +377,10 @@ __device__ void land_and_merge(const LayerView& L, const Dims& d, DevCounters* C
   bar();
   for (int j = tid; j < nj; j += nthr) {
     const int slot = slots[j];
+    if (kDebugBounds && (slot < 0 || slot >= d.S)) {     // an absent row (bounds-checked build)
+      fin[j] = 0;
+      continue;
+    }
     const uint32_t mask = L.enq_mask[slot];              // stable during a step
     if (!sd) atomicMax(&L.emit_step[slot], (uint32_t)step);
     const uint32_t old = atomicAdd(&L.done_part[(size_t)slot * parts + part], 1u);

@@ -75,7 +75,7 @@ __device__ inline void plan_layer(const LayerView& L, const Dims& d, StepPlan* P
   // After an overflow or an out-of-range id the queues no longer describe valid pairs:
   // stop executing (the sticky error is reported to the host).
   const uint32_t err = *(volatile uint32_t*)&C->error;
-  const bool halted = err == MOE_ERR_CAPACITY || err == MOE_ERR_INVALID;
+  const bool halted = err == MOE_ERR_CAPACITY || err == MOE_ERR_INVALID || err == MOE_ERR_BOUNDS;
   // MTFS / THRESHOLD: the picks are a prefix of the deepest-first order of every non-empty
   // bucket; RANKS ranks the non-empty buckets too (its stealers take from that order)
   const bool ranks = pol.kind == MOE_POLICY_RANKS;
@@ -167,6 +167,11 @@ __device__ inline void plan_layer(const LayerView& L, const Dims& d, StepPlan* P
       row_run += __shfl_sync(0xffffffffu, s_cnt, 31);
       t1_run += __shfl_sync(0xffffffffu, s_t1, 31);
       t2_run += __shfl_sync(0xffffffffu, s_t2, 31);
+    }
+    if (kDebugBounds && lane == 0 && row_run > d.S * d.KS) {     // the step's rows overflow h
+      set_error(C, MOE_ERR_BOUNDS);
+      n = 0;
+      row_run = t1_run = t2_run = 0;
     }
     if (lane == 0) {
       P->layer = layer;

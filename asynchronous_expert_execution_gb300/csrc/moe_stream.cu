@@ -132,12 +132,41 @@ __global__ void __launch_bounds__(1024) stream_tick_kernel(const __grid_constant
           }
           if (pick < 0 || s > best_s) { pick = q; best_s = s; }
         }
+      } else if (sd.policy == MOE_STREAM_DEFRAG_SRC) {
+        // H(s) = mean of s's depth snapshots over the window of earlier ticks (those recorded);
+        // the lookahead wraps from the last expert queue to att_0.  IEEE round-to-nearest
+        // double ops without contraction, so scores equal a plain float64 evaluation.
+        const int hw = min(sd.hist_window, kMaxHistoryWindow);
+        const int nv = min(ctl->snap_n, hw);
+        double Hd[2 * kMaxLayers];
+        for (int q = 0; q < nq; ++q) {
+          int h = 0;
+          for (int i = 0; i < hw; ++i) h += ctl->snap[i][q];    // unrecorded rows are zero
+          Hd[q] = nv > 0 ? __ddiv_rn((double)h, (double)nv) : 0.0;
+        }
+        double best_s = 0.0;
+        for (int q = 0; q < nq; ++q) {
+          if (Q[q] <= 0) continue;
+          double s = (double)Q[q], dj = 1.0;
+          for (int j = 1; j <= sd.window; ++j) {
+            const int qj = (q + j) % nq;
+            dj = __dmul_rn(dj, sd.decay);
+            s = __dadd_rn(s, __dmul_rn(dj, __dadd_rn((double)Q[qj], Hd[qj])));
+          }
+          if (pick < 0 || s > best_s) { pick = q; best_s = s; }
+        }
       } else if (sd.policy == MOE_STREAM_MTFS) {
         int best = 0;
         for (int q = 0; q < nq; ++q)
           if (Q[q] > best) { best = Q[q]; pick = q; }
       }
       if (pick >= 0) { kind = 1 + (pick & 1); layer = pick >> 1; }
+      if (sd.hist_window > 0) {                       // this decision's depths, for H(s) later
+        const int hw = min(sd.hist_window, kMaxHistoryWindow);
+        int* row = ctl->snap[tick % hw];
+        for (int q = 0; q < 2 * kMaxLayers; ++q) row[q] = q < nq ? Q[q] : 0;
+        ctl->snap_n = min(ctl->snap_n + 1, hw);
+      }
     } else {
       ctl->done = 1;
     }
@@ -295,7 +324,7 @@ extern "C" moe_status moe_async_stream_setup(moe_async_t h, const moe_stream_con
     return MOE_ERR_INVALID;
   if (!h->use_tc || h->cfg.num_layers > kMaxLayers) return MOE_ERR_UNSUPPORTED;
   if (sc->num_requests < 1 || sc->num_requests > h->dims.S || sc->max_steps < 1 || sc->stop_combines < 0 ||
-      sc->policy < MOE_STREAM_MTFS || sc->policy > MOE_STREAM_BARRIER || sc->defrag_window < 0 ||
+      sc->policy < MOE_STREAM_MTFS || sc->policy > MOE_STREAM_DEFRAG_SRC || sc->defrag_window < 0 ||
       sc->history_window < 0 || sc->history_window > kMaxHistoryWindow || !(sc->defrag_decay == sc->defrag_decay))
     return MOE_ERR_INVALID;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -53,7 +53,7 @@ def parse(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
-    ap.add_argument("--policy", default="mtfs", choices=["mtfs", "flfs", "defrag", "barrier"],
+    ap.add_argument("--policy", default="mtfs", choices=["mtfs", "flfs", "defrag", "barrier", "defrag_src"],
                     help="layer-level policy of the streaming workloads (c5, s1)")
     ap.add_argument("--defrag-window", type=int, default=2)
     ap.add_argument("--defrag-decay", type=float, default=0.5)

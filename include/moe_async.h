@@ -58,7 +58,9 @@ typedef enum {
                             /* exceeded its 2 s bound -- the handle's state is then     */
                             /* undefined and it should be destroyed                     */
   MOE_ERR_CUDA = 6,         /* a CUDA runtime call failed                                */
-  MOE_ERR_UNSUPPORTED = 7   /* shape/dtype combination not supported by the kernels      */
+  MOE_ERR_UNSUPPORTED = 7,  /* shape/dtype combination not supported by the kernels      */
+  MOE_ERR_BOUNDS = 8        /* (bounds-checked build only) an index read back from device
+                               state was out of range; the access was skipped           */
 } moe_status;
 
 typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
@@ -268,7 +270,10 @@ typedef enum {
   MOE_STREAM_MTFS = 0,      /* most tokens first (StreamEP section 4)                             */
   MOE_STREAM_FLFS = 1,      /* first layer first: earliest non-empty queue of the chain           */
   MOE_STREAM_DEFRAG = 2,    /* S(s) = Q(s) + sum_{j=1..W} decay^j [Q(s_j) + H(s_j)] (section 4)   */
-  MOE_STREAM_BARRIER = 3    /* synchronous baseline: nothing served while a dispatch is in flight */
+  MOE_STREAM_BARRIER = 3,   /* synchronous baseline: nothing served while a dispatch is in flight */
+  MOE_STREAM_DEFRAG_SRC = 4 /* the same score as section 4 describes the source implementation:
+                               H(s) = average of s's depth snapshots over the last history_window
+                               ticks, lookahead continued cyclically along the chain              */
 } moe_stream_policy;
 
 typedef struct {
@@ -276,8 +281,9 @@ typedef struct {
   int32_t max_steps;        /* steps per request at most (history depth)                       */
   int32_t stop_combines;    /* attention queues are closed once this many merges are done      */
   int32_t policy;           /* moe_stream_policy                                               */
-  int32_t defrag_window;    /* DEFRAG: W, queues looked ahead along att_0, exp_0, att_1, ...  */
-  int32_t history_window;   /* DEFRAG: H(s) = tokens drained from s over the last N ticks, <=16 */
+  int32_t defrag_window;    /* DEFRAG(_SRC): W, queues looked ahead along att_0, exp_0, att_1, ... */
+  int32_t history_window;   /* DEFRAG: H(s) = tokens drained from s over the last N ticks, <=16;
+                               DEFRAG_SRC: the window of depth snapshots H(s) averages         */
   double defrag_decay;      /* DEFRAG: decay per lookahead step (scores in fp64)               */
 } moe_stream_config;
 
@@ -349,6 +355,15 @@ moe_status moe_async_forward_noalloc(int32_t T, int32_t E, int32_t K, int32_t H,
                                      int32_t dtype, const void* d_x, const int32_t* d_expert,
                                      const float* d_w, const void* d_w1, const void* d_w3,
                                      const void* d_w2, void* d_y, void* stream);
+
+/* Bounds-checked build (libmoe_async_debug.so, compiled with MOE_DEBUG_BOUNDS): every bucket,
+ * slot and k index the kernels read back from device state is checked before use, and an
+ * index out of range latches MOE_ERR_BOUNDS (the access is skipped, the scheduler halts).  This
+ * call appends the raw value `record` (slot << 5 | k, unchecked) to bucket `bucket` of `layer`,
+ * so a test can plant an out-of-range record and see it rejected without touching memory
+ * out of range.  Release builds return MOE_ERR_UNSUPPORTED and write nothing.  Asynchronous. */
+moe_status moe_async_debug_append_record(moe_async_t h, int32_t layer, int32_t bucket, int32_t record,
+                                        void* stream);
 
 /* Human-readable name of a status code (static string). */
 const char* moe_async_status_string(moe_status s);

@@ -409,7 +409,7 @@ def layer_pick(att_depth, exp_depth, allow_attention=True):
 
 
 def chain_pick(att_depth, exp_depth, policy, allow_attention=True, drained=None, window=2, decay=0.5,
-               in_transit=0):
+               in_transit=0, snap_avg=None):
     """Layer-level policies over the 2L micro-queues in chain order att_0, exp_0, att_1, ...
 
     mtfs    -- most tokens first (``layer_pick``), StreamEP section 4.
@@ -418,6 +418,11 @@ def chain_pick(att_depth, exp_depth, policy, allow_attention=True, drained=None,
                [Q(s_j) + H(s_j)], s_j the j-th queue after s along the chain (truncated at
                the last layer, the paper's version); H = tokens drained from a queue over the
                recent ticks (``drained``); highest score first, equal scores -> earlier queue.
+    defrag_src -- the same score as StreamEP section 4 describes the source implementation
+               (the paragraph after the formula): H(s_j) is the average of queue s_j's depth
+               snapshots over the recent window (``snap_avg``), and the lookahead continues
+               cyclically along the chain (the queue after the last layer's expert queue is
+               layer 0's attention queue) instead of stopping at the last layer.
     barrier -- the synchronous baseline: serve a queue only when nothing is in transit and it
                holds every token still being served (lockstep layers); if tokens are split
                with nothing in transit, serve the earliest queue so progress continues.
@@ -439,6 +444,14 @@ def chain_pick(att_depth, exp_depth, policy, allow_attention=True, drained=None,
         best, best_s = None, None
         for q in nonempty:
             look = [(Q[q + j], drained[q + j]) for j in range(1, window + 1) if q + j < 2 * L]
+            s = defrag_score(Q[q], look, decay)
+            if best is None or s > best_s:
+                best, best_s = q, s
+        return as_pick(best)
+    if policy == "defrag_src":
+        best, best_s = None, None
+        for q in nonempty:
+            look = [(Q[(q + j) % (2 * L)], snap_avg[(q + j) % (2 * L)]) for j in range(1, window + 1)]
             s = defrag_score(Q[q], look, decay)
             if best is None or s > best_s:
                 best, best_s = q, s
@@ -479,6 +492,7 @@ class StreamOracle:
         self.L, self.K = L, K
         self.policy, self.window, self.decay, self.hist_window = policy, window, decay, hist_window
         self.drain_log = []               # per tick: tokens drained from each of the 2L queues
+        self.snap_log = []                # per tick: depth of each of the 2L queues at its decision
         self.R = len(x0)
         self.x0 = np.asarray(x0, dtype=np.float64)
         self.proj, self.logits, self.delays = proj, logits, np.asarray(delays)
@@ -511,9 +525,14 @@ class StreamOracle:
             self.pending[int(self.n[r]) % self.L].add(r)
         recent = self.drain_log[-self.hist_window:] if self.hist_window > 0 else []
         drained = [sum(v[q] for v in recent) for q in range(2 * self.L)]
-        pick = chain_pick([len(a) for a in self.att], [len(p) for p in self.pending], self.policy,
-                          allow_attention=self.combined < self.stop, drained=drained,
-                          window=self.window, decay=self.decay, in_transit=len(self.transit))
+        snaps = self.snap_log[-self.hist_window:] if self.hist_window > 0 else []
+        snap_avg = [sum(v[q] for v in snaps) / len(snaps) if snaps else 0.0 for q in range(2 * self.L)]
+        allow = self.combined < self.stop
+        att_d, exp_d = [len(a) for a in self.att], [len(p) for p in self.pending]
+        pick = chain_pick(att_d, exp_d, self.policy, allow_attention=allow, drained=drained,
+                          window=self.window, decay=self.decay, in_transit=len(self.transit),
+                          snap_avg=snap_avg)
+        self.snap_log.append([v for l in range(self.L) for v in ((att_d[l] if allow else 0), exp_d[l])])
         tick_drain = [0] * (2 * self.L)
         self.drain_log.append(tick_drain)
         if pick is None:

@@ -139,7 +139,7 @@ def test_stream_c5_fullsize(pkg):
     assert max(errs) <= 2e-2, errs
 
 
-@pytest.mark.parametrize("policy", ["flfs", "defrag", "barrier"])
+@pytest.mark.parametrize("policy", ["flfs", "defrag", "barrier", "defrag_src"])
 def test_stream_small_policies(pkg, policy):
     """Each layer-level policy: exact bookkeeping against the oracle, and values bit-identical
     to the most-tokens-first run (the values do not depend on the schedule)."""
@@ -157,10 +157,11 @@ def test_stream_small_policies(pkg, policy):
             assert np.array_equal(base["hist"][r, n], res["hist"][r, n]), (r, n)
 
 
-def test_stream_c5_defrag_fullsize(pkg):
+@pytest.mark.parametrize("policy", ["defrag", "defrag_src"])
+def test_stream_c5_defrag_fullsize(pkg, policy):
     spec = get_config("c5")
     M = 64
-    res = _gpu_stream(pkg, spec, M, policy="defrag")
+    res = _gpu_stream(pkg, spec, M, policy=policy)
     assert res["status"] == 0
-    sim = _oracle_stream(spec, res["wl"], res["weights"], values=False, policy="defrag")
+    sim = _oracle_stream(spec, res["wl"], res["weights"], values=False, policy=policy)
     _check_bookkeeping(res, sim)

@@ -39,7 +39,7 @@ def test_every_declared_symbol_exported(lib):
 
 
 def test_status_strings(lib):
-    for code in range(8):
+    for code in range(9):
         assert lib.moe_async_status_string(code)
 
 
@@ -96,3 +96,23 @@ def test_product_path_has_no_oracle_import():
         if f.endswith(".py"):
             src = open(os.path.join(pkg, f)).read()
             assert not re.search(r"^\s*(from|import)\s+oracle\b", src, flags=re.M), f
+
+
+def test_release_build_refuses_raw_record_writes(lib):
+    """Only the bounds-checked build accepts raw records; the release library refuses before
+    looking at its arguments (no handle, no GPU needed)."""
+    from asynchronous_expert_execution_gb300 import _native as N
+    assert lib.moe_async_debug_append_record(None, 0, 0, 0, None) == N.MOE_ERR_UNSUPPORTED
+
+
+def test_bounds_checked_build_exports_every_symbol(lib):
+    from asynchronous_expert_execution_gb300 import build as b
+    assert os.path.exists(b.LIB_DEBUG), "build() makes the bounds-checked library too"
+    dbg = ctypes.CDLL(b.LIB_DEBUG)
+    for name in _declared():
+        assert hasattr(dbg, name), name
+    dbg.moe_async_debug_append_record.restype = ctypes.c_int
+    dbg.moe_async_debug_append_record.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int32,
+                                                  ctypes.c_int32, ctypes.c_void_p]
+    # the debug build checks its host arguments: no handle -> MOE_ERR_INVALID (not unsupported)
+    assert dbg.moe_async_debug_append_record(None, 0, 0, 0, None) == 1

@@ -166,6 +166,77 @@ def test_chain_policies():
     pin_chain_policies()
 
 
+def pin_defrag_source_variant():
+    """StreamEP section 4, the paragraph after the formula: the source averages the queue
+    snapshots over the history window and continues the lookahead cyclically along the chain.
+    Two layers: chain att_0, exp_0, att_1, exp_1; W = 2, delta = 0.5."""
+    # the wrap decides: Q = (8, 1, 2, 6), no history.  Cyclic: S(att_0) = 8 + .5*1 + .25*2 =
+    # 9; S(exp_1) = 6 + .5*8 (att_0, wrapped) + .25*1 (exp_0) = 10.25 -> exp_1.  Truncated at
+    # the chain end (the paper's version): S(exp_1) = 6 -> att_0.
+    att, exp = [8, 2], [1, 6]
+    assert om.chain_pick(att, exp, "defrag_src", snap_avg=[0.0] * 4, window=2, decay=0.5) == ("exp", 1)
+    assert om.chain_pick(att, exp, "defrag", drained=[0] * 4, window=2, decay=0.5) == ("att", 0)
+    # the average decides: Q = (0, 6, 4, 1) and exp_1's snapshots over the window are 20 and 0.
+    # Average H = 10: S(exp_0) = 6 + .5*4 + .25*(1 + 10) = 10.75 > S(att_1) = 4 + .5*(1 + 10)
+    # = 9.5 -> exp_0.  Summed (H = 20) it would be 13.25 < 14.5 -> att_1.
+    att, exp = [0, 4], [6, 1]
+    assert om.chain_pick(att, exp, "defrag_src", snap_avg=[0.0, 0.0, 0.0, 10.0], window=2, decay=0.5) == ("exp", 0)
+    assert om.chain_pick(att, exp, "defrag_src", snap_avg=[0.0, 0.0, 0.0, 20.0], window=2, decay=0.5) == ("att", 1)
+
+
+def test_defrag_source_variant():
+    pin_defrag_source_variant()
+
+
+def test_defrag_source_snapshots_are_window_averages():
+    """The stream oracle under defrag_src: tick t's decision sees, as H, the average of the
+    depth snapshots of the (at most hist_window) ticks before it -- zero before any."""
+    R, L, E, K, H, M = 12, 3, 4, 2, 5, 8
+    d = np.random.default_rng(5).integers(1, 5, size=(R, M))
+    s = _mk(R, L, E, K, H, d, stop=60, max_steps=M, values=False)
+    s.policy, s.hist_window = "defrag_src", 3
+    seen = []
+    real = om.chain_pick
+
+    def spy(*a, **kw):
+        seen.append(list(kw["snap_avg"]))
+        return real(*a, **kw)
+    om.chain_pick = spy
+    try:
+        s.run()
+    finally:
+        om.chain_pick = real
+    assert len(seen) == len(s.snap_log) == s.tick and seen[0] == [0.0] * (2 * L)
+    for t in range(1, s.tick):
+        win = s.snap_log[max(0, t - 3):t]
+        assert seen[t] == [sum(v[q] for v in win) / len(win) for q in range(2 * L)]
+    assert s.combined >= 60 and not s.transit and not any(s.pending)
+
+
+def test_defrag_source_pins_catch_planted_mistakes(monkeypatch):
+    real = om.chain_pick
+
+    def truncated(att, exp, policy, **kw):            # the lookahead stops at the chain end
+        if policy != "defrag_src":
+            return real(att, exp, policy, **kw)
+        Lq = len(att)
+        Q = [v for l in range(Lq) for v in (att[l], exp[l])]
+        best, best_s = None, None
+        for q in [q for q in range(2 * Lq) if Q[q] > 0]:
+            look = [(Q[q + j], kw["snap_avg"][q + j]) for j in range(1, kw["window"] + 1) if q + j < 2 * Lq]
+            sc = om.defrag_score(Q[q], look, kw["decay"])
+            if best is None or sc > best_s:
+                best, best_s = q, sc
+        return ("att" if best % 2 == 0 else "exp", best // 2)
+    monkeypatch.setattr(om, "chain_pick", truncated)
+    try:
+        pin_defrag_source_variant()
+        caught = False
+    except AssertionError:
+        caught = True
+    assert caught
+
+
 def test_barrier_trace_hand():
     delays = np.ones((2, 8), dtype=np.int64)
     delays[1, 0] = 3
@@ -182,7 +253,7 @@ def test_policies_same_values_and_conservation():
     R, L, E, K, H, M = 10, 3, 4, 2, 5, 8
     d = np.random.default_rng(11).integers(1, 5, size=(R, M))
     runs = {}
-    for pol in ("mtfs", "flfs", "defrag", "barrier"):
+    for pol in ("mtfs", "flfs", "defrag", "barrier", "defrag_src"):
         s = _mk(R, L, E, K, H, d, stop=40, max_steps=M)
         s.policy = pol
         s.run()
