@@ -22,7 +22,7 @@ EXPORTS = ("moe_async_create", "moe_async_route", "moe_async_enqueue", "moe_asyn
            "moe_async_schedule_steps", "moe_async_collect", "moe_async_wait", "moe_async_sync", "moe_async_get_stats",
            "moe_async_get_trace", "moe_async_snapshot", "moe_async_destroy",
            "moe_async_status_string", "moe_async_profile", "moe_async_profile_read",
-           "moe_async_stream_setup", "moe_async_stream_run", "moe_async_stream_trace",
+           "moe_async_stream_setup", "moe_async_stream_run", "moe_async_stream_trace", "moe_async_stream_stats",
            "moe_async_cancel", "moe_async_debug_append_record")
 
 KERNEL_KINDS = ("enqueue", "schedule", "ffn1", "ffn2", "collect")
@@ -55,6 +55,11 @@ class StreamConfig(ctypes.Structure):
 
 
 STREAM_POLICIES = {"mtfs": 0, "flfs": 1, "defrag": 2, "barrier": 3, "defrag_src": 4}
+
+
+class StreamStats(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("ticks", "combined", "peak_transit", "peak_bucket", "num_queues")] + \
+               [("peak_queue", ctypes.c_int32 * 16), ("occupancy_sum", ctypes.c_int64 * 16)]
 
 
 class MoEError(RuntimeError):
@@ -95,7 +100,8 @@ def load():
         "moe_async_profile": [P, I32],
         "moe_async_profile_read": [P, P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64), I32],
         "moe_async_status_string": [ctypes.c_int],
-        "moe_async_stream_setup": [P, ctypes.POINTER(StreamConfig), VPP, P, P, P, P, P, P],
+        "moe_async_stream_setup": [P, ctypes.POINTER(StreamConfig), VPP, P, P, P, P, P, P, P],
+        "moe_async_stream_stats": [P, P, ctypes.POINTER(StreamStats)],
         "moe_async_stream_run": [P, I32, I32, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32), P],
         "moe_async_stream_trace": [P, P, ctypes.POINTER(ctypes.c_int32), I32, ctypes.POINTER(ctypes.c_int32)],
     }

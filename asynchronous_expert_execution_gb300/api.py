@@ -156,18 +156,28 @@ class MoEAsync:
 
     # -- streaming multi-layer decode (2L micro-queues) --------------------------
     def stream_setup(self, proj, x0, logits, delays, max_steps, stop, history, done_tick, policy="mtfs",
-                     window=2, decay=0.5, hist_window=8, stream=None):
+                     window=2, decay=0.5, hist_window=8, admit=None, stream=None):
         """proj: list of L [H, H] device tensors; x0 [R, H]; logits [R, M, E] fp32; delays
-        [R, M] int32; history [R, M+1, H] and done_tick [R, M+1] int32 are outputs.
-        policy: "mtfs" | "flfs" | "defrag" | "barrier" (layer-level queue choice)."""
+        [R, M] int32; admit [R] int32 admission ticks (None: all at the start); history
+        [R, M+1, H] and done_tick [R, M+1] int32 are outputs.
+        policy: "mtfs" | "flfs" | "defrag" | "barrier" | "defrag_src" (layer-level queue choice)."""
         R = x0.shape[0]
         arr = ctypes.c_void_p * len(proj)
-        self._stream_keep = (logits, delays, history, done_tick)
+        self._stream_keep = (logits, delays, admit, history, done_tick)
         cfg = N.StreamConfig(R, max_steps, stop, N.STREAM_POLICIES[policy], window, hist_window, decay)
         st = self.lib.moe_async_stream_setup(self.h, ctypes.byref(cfg), arr(*[p.data_ptr() for p in proj]),
-                                             _ptr(x0), _ptr(logits), _ptr(delays), _ptr(history),
+                                             _ptr(x0), _ptr(logits), _ptr(delays), _ptr(admit), _ptr(history),
                                              _ptr(done_tick), _stream(stream))
         N.check(st, "moe_async_stream_setup")
+
+    def stream_stats(self, stream=None):
+        """Occupancy of the streaming runtime: ticks, merges, peaks and per-queue sums."""
+        out = N.StreamStats()
+        N.check(self.lib.moe_async_stream_stats(self.h, _stream(stream), ctypes.byref(out)), "stream_stats")
+        nq = out.num_queues
+        return {"ticks": out.ticks, "combined": out.combined, "peak_transit": out.peak_transit,
+                "peak_bucket": out.peak_bucket, "peak_queue": list(out.peak_queue[:nq]),
+                "occupancy_sum": list(out.occupancy_sum[:nq])}
 
     def stream_run(self, max_ticks=100000, check_every=16, stream=None):
         """Run ticks until the stream is drained; returns (status, ticks, merges)."""

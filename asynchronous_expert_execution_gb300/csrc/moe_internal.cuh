@@ -112,6 +112,11 @@ struct StreamCtl {
   int32_t drained[16][2 * kMaxLayers];   // tokens drained per queue, ring over the last ticks
   int32_t snap[16][2 * kMaxLayers];      // depth of each queue at the decision, ring over the last ticks
   int32_t snap_n;                        // snapshots recorded so far
+  int32_t to_admit;                      // requests whose admission tick has not come yet
+  int32_t peak_transit;                  // most requests in transit at a decision
+  int32_t peak_bucket;                   // deepest expert bucket when its layer was served
+  int32_t peak_q[2 * kMaxLayers];        // deepest each queue was at a decision
+  long long occ_sum[2 * kMaxLayers];     // sum over ticks of each queue's depth at the decision
 };
 
 constexpr int kMaxHistoryWindow = 16;
@@ -138,6 +143,7 @@ struct StreamDev {
   float* route_w;
   const float* logits;
   const int32_t* delay;
+  const int32_t* admit;                  // [R] admission tick of each request (null: all at 0)
   void* hist;
   int32_t* done_tick;
   int32_t* att_batch;

@@ -69,6 +69,7 @@ __global__ void __launch_bounds__(1024) stream_tick_kernel(const __grid_constant
       if (ctl->exp_tokens[l] > 0) busy = 1;
       if (allow_att && sd.att_ht[2 * l + 1] != sd.att_ht[2 * l]) busy = 1;
     }
+    if (allow_att && ctl->to_admit > 0) busy = 1;
     if (ctl->done) busy = 0;
     s_busy = busy;
     s_tick = ctl->tick + (busy ? 1 : 0);
@@ -94,6 +95,15 @@ __global__ void __launch_bounds__(1024) stream_tick_kernel(const __grid_constant
       atomicAdd(&a.C->open_tokens, 1);
       atomicAdd(&a.C->pending_pairs, a.d.K);
     }
+    // requests whose admission tick it is join layer 0's attention queue
+    if (sd.admit) {
+      for (int r = tid; r < sd.R; r += blockDim.x) {
+        if (sd.admit[r] != tick) continue;
+        const uint32_t pos = atomicAdd(&sd.att_ht[1], 1u);
+        sd.att_ring[pos % (uint32_t)sd.R] = r;
+        atomicSub(&ctl->to_admit, 1);
+      }
+    }
   }
   __threadfence();
   __syncthreads();
@@ -109,6 +119,11 @@ __global__ void __launch_bounds__(1024) stream_tick_kernel(const __grid_constant
         Q[2 * l + 1] = ctl->exp_tokens[l];
       }
       const int nq = 2 * Lc;
+      for (int q = 0; q < nq; ++q) {                  // occupancy seen at this decision
+        ctl->peak_q[q] = max(ctl->peak_q[q], Q[q]);
+        ctl->occ_sum[q] += Q[q];
+      }
+      ctl->peak_transit = max(ctl->peak_transit, ctl->in_transit);
       int pick = -1;
       if (sd.policy == MOE_STREAM_FLFS ||
           (sd.policy == MOE_STREAM_BARRIER && ctl->in_transit == 0)) {
@@ -178,6 +193,11 @@ __global__ void __launch_bounds__(1024) stream_tick_kernel(const __grid_constant
   moe_async_policy all{MOE_POLICY_MTFS, 0, 0, 1};
   plan_layer(a.views[kind == 2 ? layer : 0], a.d, a.P, a.C, all, a.g, kind == 2 ? layer : 0, 0, nullptr,
              a.wbytes, tick, kind == 2, sc);
+  if (tid == 0 && kind == 2) {                        // the deepest bucket of the served queue
+    int mb = 0;
+    for (int b = 0; b < a.d.NB; ++b) mb = max(mb, sc.depth[b]);
+    ctl->peak_bucket = max(ctl->peak_bucket, mb);
+  }
   int cnt = 0;
   if (kind == 1) {
     const uint32_t hd = sd.att_ht[2 * layer], tl = sd.att_ht[2 * layer + 1];
@@ -262,12 +282,22 @@ __global__ void stream_init_kernel(StreamDev sd) {
   for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < sd.R; r += gridDim.x * blockDim.x) {
     sd.req_n[r] = 0;
     sd.arr_tick[r] = -1;
-    sd.att_ring[r] = r;                     // every request starts in layer 0's attention queue
+    if (!sd.admit) sd.att_ring[r] = r;      // every request starts in layer 0's attention queue
   }
   if (blockIdx.x == 0 && threadIdx.x == 0) {
+    uint32_t n0 = (uint32_t)sd.R;
+    if (sd.admit) {                         // those admitted at tick 0, in request order
+      n0 = 0u;
+      int later = 0;
+      for (int r = 0; r < sd.R; ++r) {
+        if (sd.admit[r] <= 0) sd.att_ring[n0++] = r;
+        else ++later;
+      }
+      sd.ctl->to_admit = later;
+    }
     for (int l = 0; l < sd.L; ++l) {
       sd.att_ht[2 * l] = 0u;
-      sd.att_ht[2 * l + 1] = l == 0 ? (uint32_t)sd.R : 0u;
+      sd.att_ht[2 * l + 1] = l == 0 ? n0 : 0u;
     }
   }
 }
@@ -319,7 +349,8 @@ using namespace moe;
 extern "C" moe_status moe_async_stream_setup(moe_async_t h, const moe_stream_config* sc,
                                              const void* const* d_proj, const void* d_x0,
                                              const float* d_logits, const int32_t* d_delay,
-                                             void* d_history, int32_t* d_done_tick, void* stream) {
+                                             const int32_t* d_admit, void* d_history,
+                                             int32_t* d_done_tick, void* stream) {
   if (!h || !sc || !d_proj || !d_x0 || !d_logits || !d_delay || !d_history || !d_done_tick)
     return MOE_ERR_INVALID;
   if (!h->use_tc || h->cfg.num_layers > kMaxLayers) return MOE_ERR_UNSUPPORTED;
@@ -346,6 +377,7 @@ extern "C" moe_status moe_async_stream_setup(moe_async_t h, const moe_stream_con
   sd.decay = sc->defrag_decay;
   sd.logits = d_logits;
   sd.delay = d_delay;
+  sd.admit = d_admit;
   sd.hist = d_history;
   sd.done_tick = d_done_tick;
   bool ok = salloc(&sd.ctl, sizeof(StreamCtl)) == cudaSuccess &&
@@ -427,6 +459,27 @@ extern "C" moe_status moe_async_stream_run(moe_async_t h, int32_t max_ticks, int
   }
   moe_status dev = moe_async_sync(h, stream);
   return dev;
+}
+
+extern "C" moe_status moe_async_stream_stats(moe_async_t h, void* stream, moe_stream_stats* out) {
+  if (!h || !out) return MOE_ERR_INVALID;
+  StreamState* st = static_cast<StreamState*>(h->stream_state);
+  if (!st) return MOE_ERR_INVALID;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  MOE_CUDA_TRY(cudaMemcpyAsync(st->host_ctl, st->sd.ctl, sizeof(StreamCtl), cudaMemcpyDeviceToHost, s));
+  MOE_CUDA_TRY(cudaStreamSynchronize(s));
+  const StreamCtl& c = *st->host_ctl;
+  std::memset(static_cast<void*>(out), 0, sizeof(*out));
+  out->ticks = c.tick;
+  out->combined = c.combined;
+  out->peak_transit = c.peak_transit;
+  out->peak_bucket = c.peak_bucket;
+  out->num_queues = 2 * st->sd.L;
+  for (int q = 0; q < 2 * st->sd.L; ++q) {
+    out->peak_queue[q] = c.peak_q[q];
+    out->occupancy_sum[q] = c.occ_sum[q];
+  }
+  return MOE_OK;
 }
 
 extern "C" moe_status moe_async_stream_trace(moe_async_t h, void* stream, int32_t* h_buf, int32_t cap,

@@ -521,10 +521,11 @@ def measure_stream(args, pkg, spec, dev, steps, warmup, e2e_steps):
     proj = [p.to(dev) for p in wl.proj]
     x0, logits = wl.x0.to(dev), wl.logits.to(dev)
     delays = torch.as_tensor(wl.delays, dtype=torch.int32).to(dev)
+    admit = torch.as_tensor(wl.admit, dtype=torch.int32).to(dev) if wl.admit.any() else None
     hist = torch.zeros((R, M + 1, H), dtype=torch.bfloat16, device=dev)
     done = torch.empty((R, M + 1), dtype=torch.int32, device=dev)
     pol = dict(policy=args.policy, window=args.defrag_window, decay=args.defrag_decay,
-               hist_window=args.history_window)
+               hist_window=args.history_window, admit=admit)
     stream = torch.cuda.current_stream()
     times, out = [], None
     clk = None
@@ -548,6 +549,7 @@ def measure_stream(args, pkg, spec, dev, steps, warmup, e2e_steps):
                    s1["kernel_launches"] - s0["kernel_launches"])
     clk = clocks.stop()
     tr = moe.stream_trace()
+    occ = moe.stream_stats()
     dn = done.cpu().numpy()
     # end to end: inputs from pinned host memory, setup + run, outputs back to pinned memory
     x0h, lh, dh = x0.cpu().pin_memory(), logits.cpu().pin_memory(), delays.cpu().pin_memory()
@@ -570,10 +572,13 @@ def measure_stream(args, pkg, spec, dev, steps, warmup, e2e_steps):
     e2e_s = time.perf_counter() - t0
     moe.close()
     ticks, comb, runs, wbytes, launches = out
-    lat = []
+    lat, req_mean, req_steps = [], [], []
     for r in range(R):
-        ts = [0] + [int(t) for t in dn[r, 1:] if t >= 0]
-        lat += list(np.diff(ts))
+        ts = [int(wl.admit[r])] + [int(t) for t in dn[r, 1:] if t >= 0]
+        d = np.diff(ts)
+        lat += list(d)
+        req_steps.append(len(d))
+        req_mean.append(float(np.mean(d)) if len(d) else None)
     ms = float(np.median(times))
     pairs = comb * lay.top_k
     hbm, tf_burst, tf_sust, src = peaks()
@@ -607,7 +612,41 @@ def measure_stream(args, pkg, spec, dev, steps, warmup, e2e_steps):
                     "h2d_bytes_per_step": x0h.numel() * 2 + lh.numel() * 4 + dh.numel() * 4,
                     "d2h_bytes_per_step": hh.numel() * 2 + doh.numel() * 4, "steps": e2e_steps,
                     "includes": "stream setup (projection packing, graph capture) and run, host copies"},
+            "study": stream_study(spec, lay, ticks, comb, lat, req_mean, req_steps, tr, occ, ms, pairs,
+                                  1e3 * t_roof / ms),
             "gpu_launches": int(launches), "clocks": clk}
+
+
+SLO_TICKS = 8      # per-step latency target of the study's goodput (ticks, mean over a request)
+
+
+def stream_study(spec, lay, ticks, comb, lat, req_mean, req_steps, tr, occ, ms, pairs, roof_frac):
+    """The latency study's figures for one streaming run ("asynchronous MoE serving" notes,
+    second research candidate): accepted load, goodput under a per-step latency target, tail
+    step latency, request completion, queue and bucket occupancy, and how busy the GPU was."""
+    R = spec.tokens
+    ms_tick = ms / max(1, ticks)
+    ok = [r for r in range(R) if req_mean[r] is not None and req_mean[r] <= SLO_TICKS]
+    busy_ticks = int((tr[:, 1] != 0).sum()) if len(tr) else 0
+    nq = len(occ["peak_queue"])
+    return {
+        "accepted_load": {"merges_per_tick": comb / max(1, ticks), "pairs_per_s": pairs / (ms / 1e3)},
+        "step_latency_ticks": {"mean": float(np.mean(lat)), "p50": float(np.percentile(lat, 50)),
+                               "p99": float(np.percentile(lat, 99)), "max": int(np.max(lat))},
+        "step_latency_ms_gpu": {"p50": float(np.percentile(lat, 50)) * ms_tick,
+                                "p99": float(np.percentile(lat, 99)) * ms_tick},
+        "goodput": {"slo_mean_step_ticks": SLO_TICKS, "requests_meeting_frac": len(ok) / R,
+                    "pairs_per_s": sum(req_steps[r] for r in ok) * lay.top_k / (ms / 1e3),
+                    "merges_per_tick": sum(req_steps[r] for r in ok) / max(1, ticks)},
+        "completion": {"steps_min": int(min(req_steps)), "steps_median": float(np.median(req_steps)),
+                       "steps_max": int(max(req_steps)), "requests_served_frac": sum(1 for n in req_steps if n) / R},
+        "occupancy": {"peak_queue": occ["peak_queue"],
+                      "mean_queue": [round(v / max(1, occ["ticks"]), 2) for v in occ["occupancy_sum"]],
+                      "peak_in_transit": occ["peak_transit"], "peak_bucket": occ["peak_bucket"],
+                      "queues": [f"{'att' if q % 2 == 0 else 'exp'}_{q // 2}" for q in range(nq)]},
+        "busy_ticks_frac": busy_ticks / max(1, ticks),
+        "gpu_roofline_frac": roof_frac,
+        "ms_per_tick": ms_tick}
 
 
 # -------------------------------------------------------------------- main
@@ -688,9 +727,9 @@ def main():
                 "warmup": rec["warmup"], "ms_per_step": rec["ms_per_step"], "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": rec["dtype"], "data": "synthetic",
                 "config": dict(rec["config"], parallelism=f"replicas x{world}")}
-        for k in ("roofline", "path_roofline", "cpu_baseline", "e2e", "gpu_launches", "clocks", "schedule"):
-            if k in rec:
-                line[k] = rec[k]
+        for k, v in rec.items():                     # roofline, e2e, cpu_baseline, clocks, schedule, study ...
+            if k not in line and k not in ("workload",):
+                line[k] = v
         if subs:
             line["subconfigs"] = subs
         print(json.dumps(line), flush=True)

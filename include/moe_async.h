@@ -293,14 +293,35 @@ typedef struct {
  *   d_x0        : [R, H] bf16 initial states (copied into the history)
  *   d_logits    : [R, max_steps, E] fp32 router logits of (request, step)   (borrowed)
  *   d_delay     : [R, max_steps] int32 dispatch delay in ticks, >= 1       (borrowed)
+ *   d_admit     : [R] int32 tick at which each request enters layer 0's attention queue
+ *                 (<= 0: at the start); NULL = every request at the start   (borrowed)
  *   d_history   : [R, max_steps + 1, H] bf16 out: x^(n) of every request, x^(0) at n = 0
  *   d_done_tick : [R, max_steps + 1] int32 out: tick at which step n completed (-1 = not)
- * Every request starts in layer 0's attention queue.  MOE_ERR_UNSUPPORTED for fp32 or
- * identity handles or more than 8 layers. */
+ * Requests admitted later join the attention queue at the start of their tick, after that
+ * tick's dispatches are delivered; while attention is open, requests still to be admitted
+ * keep the stream running (idle ticks).  MOE_ERR_UNSUPPORTED for fp32 or identity handles or
+ * more than 8 layers. */
 moe_status moe_async_stream_setup(moe_async_t h, const moe_stream_config* sc,
                                   const void* const* d_proj, const void* d_x0,
                                   const float* d_logits, const int32_t* d_delay,
-                                  void* d_history, int32_t* d_done_tick, void* stream);
+                                  const int32_t* d_admit, void* d_history, int32_t* d_done_tick,
+                                  void* stream);
+
+/* Queue occupancy of the streaming runtime so far (for latency studies; StreamEP section 4:
+ * queue depths are what the scheduler acts on).  Depths are in tokens (requests), seen at
+ * each tick's decision after that tick's arrivals and admissions. */
+typedef struct {
+  int32_t ticks;                 /* ticks run                                                    */
+  int32_t combined;              /* merges completed (token-layer steps)                         */
+  int32_t peak_transit;          /* most requests in transit (dispatched, not yet arrived)       */
+  int32_t peak_bucket;           /* deepest expert bucket at the moment its layer was served     */
+  int32_t num_queues;            /* 2L: the queues below in chain order att_0, exp_0, att_1, ... */
+  int32_t peak_queue[16];        /* deepest each queue was at a decision (closed attention: 0)   */
+  int64_t occupancy_sum[16];     /* each queue's depth summed over the ticks (mean = / ticks)    */
+} moe_stream_stats;
+
+/* Synchronise `stream` and read the streaming runtime's occupancy figures. */
+moe_status moe_async_stream_stats(moe_async_t h, void* stream, moe_stream_stats* out);
 
 /* Run ticks until nothing is left (no dispatch in transit, expert queues empty, attention
  * queues closed or empty), reading the control block every `check_every` ticks; at most

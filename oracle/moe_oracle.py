@@ -483,12 +483,19 @@ class StreamOracle:
     once `stop` merges have completed (checked at the start of a tick) attention queues are
     no longer served, in-flight work still finishes.
 
-    Per tick: deliver the arrivals due, pick a queue, serve it.  ``values`` = False keeps only
-    the integer bookkeeping; ``compute`` restricts the float chain to some requests.
+    Per tick: deliver the arrivals due, admit the requests whose admission tick it is into
+    layer 0's attention queue (``admit``: per-request tick, None = every request at the start),
+    pick a queue, serve it.  ``values`` = False keeps only the integer bookkeeping; ``compute``
+    restricts the float chain to some requests.
+
+    Occupancy, for the latency study (StreamEP section 4: queue depths drive the scheduler):
+    per queue in chain order the largest depth the scheduler saw at a decision and the sum of
+    those depths over the ticks; the largest number of requests in transit; the deepest
+    expert bucket at the moment its layer's expert queue was served.
     """
 
     def __init__(self, L, K, x0, proj, logits, delays, experts, stop, max_steps,
-                 values=True, compute=None, policy="mtfs", window=2, decay=0.5, hist_window=8):
+                 values=True, compute=None, policy="mtfs", window=2, decay=0.5, hist_window=8, admit=None):
         self.L, self.K = L, K
         self.policy, self.window, self.decay, self.hist_window = policy, window, decay, hist_window
         self.drain_log = []               # per tick: tokens drained from each of the 2L queues
@@ -501,8 +508,14 @@ class StreamOracle:
         self.values = values
         self.compute = set(range(self.R)) if compute is None else set(int(r) for r in compute)
         self.n = np.zeros(self.R, dtype=np.int64)
+        self.admit = np.zeros(self.R, dtype=np.int64) if admit is None else np.asarray(admit, dtype=np.int64)
         self.att = [set() for _ in range(L)]
-        self.att[0] = set(range(self.R))
+        self.att[0] = set(int(r) for r in range(self.R) if self.admit[r] <= 0)
+        self.to_admit = int((self.admit > 0).sum())
+        self.peak_q = [0] * (2 * L)
+        self.occ_sum = [0] * (2 * L)
+        self.peak_transit = 0
+        self.peak_bucket = 0
         self.transit = {}                 # r -> arrival tick
         self.pending = [set() for _ in range(L)]   # requests whose pairs sit in layer l's queue
         self.a = {}                       # r -> attention output for its current step
@@ -515,7 +528,7 @@ class StreamOracle:
         self.trace = []
 
     def busy(self):
-        open_att = self.combined < self.stop and any(self.att)
+        open_att = self.combined < self.stop and (any(self.att) or self.to_admit > 0)
         return bool(self.transit) or any(self.pending) or open_att
 
     def step(self):
@@ -523,6 +536,9 @@ class StreamOracle:
         for r in sorted(r for r, t in self.transit.items() if t == self.tick):
             del self.transit[r]
             self.pending[int(self.n[r]) % self.L].add(r)
+        for r in np.nonzero(self.admit == self.tick)[0]:
+            self.att[0].add(int(r))
+            self.to_admit -= 1
         recent = self.drain_log[-self.hist_window:] if self.hist_window > 0 else []
         drained = [sum(v[q] for v in recent) for q in range(2 * self.L)]
         snaps = self.snap_log[-self.hist_window:] if self.hist_window > 0 else []
@@ -532,7 +548,12 @@ class StreamOracle:
         pick = chain_pick(att_d, exp_d, self.policy, allow_attention=allow, drained=drained,
                           window=self.window, decay=self.decay, in_transit=len(self.transit),
                           snap_avg=snap_avg)
-        self.snap_log.append([v for l in range(self.L) for v in ((att_d[l] if allow else 0), exp_d[l])])
+        snap = [v for l in range(self.L) for v in ((att_d[l] if allow else 0), exp_d[l])]
+        self.snap_log.append(snap)
+        for q in range(2 * self.L):
+            self.peak_q[q] = max(self.peak_q[q], snap[q])
+            self.occ_sum[q] += snap[q]
+        self.peak_transit = max(self.peak_transit, len(self.transit))
         tick_drain = [0] * (2 * self.L)
         self.drain_log.append(tick_drain)
         if pick is None:
@@ -552,6 +573,11 @@ class StreamOracle:
         else:
             batch = sorted(self.pending[l])
             self.pending[l] = set()
+            per_expert = {}
+            for r in batch:
+                for e in self.route[r][0]:
+                    per_expert[int(e)] = per_expert.get(int(e), 0) + 1
+            self.peak_bucket = max([self.peak_bucket] + list(per_expert.values()))
             for r in batch:
                 n = int(self.n[r])
                 if self.values and r in self.compute:

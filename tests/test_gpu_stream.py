@@ -41,14 +41,16 @@ def _gpu_stream(pkg, spec, M, seed=0, delay_seed=None, weights=None, policy="mtf
     hist = torch.zeros((R, M + 1, H), dtype=torch.bfloat16, device="cuda")
     done = torch.empty((R, M + 1), dtype=torch.int32, device="cuda")
     delays = torch.as_tensor(wl.delays, dtype=torch.int32).cuda()
+    admit = torch.as_tensor(wl.admit, dtype=torch.int32).cuda() if wl.admit is not None and wl.admit.any() else None
     moe.stream_setup(proj, wl.x0.cuda(), wl.logits.cuda(), delays, M, spec.stream_steps, hist, done,
-                     policy=policy, window=2, decay=0.5, hist_window=8)
+                     policy=policy, window=2, decay=0.5, hist_window=8, admit=admit)
     st, ticks, comb = moe.stream_run(max_ticks=100000, check_every=16)
     trace = moe.stream_trace()
     stats = moe.stats()
+    occ = moe.stream_stats()
     moe.close()
     return dict(wl=wl, weights=weights, status=st, ticks=ticks, combined=comb, trace=trace, stats=stats,
-                hist=hist.float().cpu().numpy().astype(np.float64), done=done.cpu().numpy())
+                occupancy=occ, hist=hist.float().cpu().numpy().astype(np.float64), done=done.cpu().numpy())
 
 
 def _oracle_stream(spec, wl, weights, values, compute=None, policy="mtfs"):
@@ -64,7 +66,7 @@ def _oracle_stream(spec, wl, weights, values, compute=None, policy="mtfs"):
     return om.StreamOracle(spec.num_layers, lay.top_k, wl.x0.double().numpy(), lambda l: proj[l],
                            lambda r, n: lg[r, n], wl.delays, experts, spec.stream_steps, wl.max_steps,
                            values=values, compute=compute, policy=policy, window=2, decay=0.5,
-                           hist_window=8).run()
+                           hist_window=8, admit=wl.admit).run()
 
 
 def _check_bookkeeping(res, sim):
@@ -77,6 +79,10 @@ def _check_bookkeeping(res, sim):
     for r in range(R):
         for n in range(1, M1):
             assert res["done"][r, n] == sim.done_tick.get((r, n), -1), (r, n)
+    occ = res["occupancy"]                          # occupancy seen at the decisions
+    assert occ["ticks"] == sim.tick and occ["combined"] == sim.combined
+    assert occ["peak_queue"] == sim.peak_q and occ["occupancy_sum"] == sim.occ_sum
+    assert occ["peak_transit"] == sim.peak_transit and occ["peak_bucket"] == sim.peak_bucket
 
 
 def test_stream_small_parity(pkg):
@@ -165,3 +171,23 @@ def test_stream_c5_defrag_fullsize(pkg, policy):
     assert res["status"] == 0
     sim = _oracle_stream(spec, res["wl"], res["weights"], values=False, policy=policy)
     _check_bookkeeping(res, sim)
+
+
+@pytest.mark.parametrize("policy", ["mtfs", "flfs", "defrag", "barrier", "defrag_src"])
+def test_stream_regimes_small(pkg, policy):
+    """The small stream under all three delay regimes at once (bursts of requests admitted
+    over time, Zipf expert popularity, three slow simulated ranks): exact bookkeeping and
+    occupancy against the oracle, values elementwise for the first step of every request."""
+    spec = get_config("s1x")
+    M = 16
+    res = _gpu_stream(pkg, spec, M, policy=policy)
+    assert res["status"] == 0
+    sim = _oracle_stream(spec, res["wl"], res["weights"], values=True, policy=policy,
+                         compute=range(spec.tokens))
+    _check_bookkeeping(res, sim)
+    assert int(res["wl"].admit.max()) > 0 and sim.to_admit == 0
+    served = [r for r in range(spec.tokens) if sim.n[r] >= 1]
+    assert len(served) >= spec.tokens // 2
+    got = np.stack([res["hist"][r, 1] for r in served])
+    want = np.stack([sim.history[r][1] for r in served])
+    assert np.abs(got - want).max() / np.abs(want).max() <= 2e-2

@@ -8,7 +8,8 @@ import numpy as np
 from oracle import moe_oracle as om
 
 
-def _mk(R, L, E, K, H, delays, stop, max_steps, logits=None, experts=None, proj=None, x0=None, values=True):
+def _mk(R, L, E, K, H, delays, stop, max_steps, logits=None, experts=None, proj=None, x0=None, values=True,
+        admit=None):
     rng = np.random.default_rng(0)
     if logits is None:
         tab = rng.uniform(size=(R, max_steps, E))
@@ -22,7 +23,7 @@ def _mk(R, L, E, K, H, delays, stop, max_steps, logits=None, experts=None, proj=
         Ws = {(l, e): (rng.standard_normal((H, H)) / math.sqrt(H), rng.standard_normal((H, H)) / math.sqrt(H),
                        rng.standard_normal((H, H)) / math.sqrt(H)) for l in range(L) for e in range(E)}
         experts = lambda l, e: Ws[(l, e)]
-    return om.StreamOracle(L, K, x0, proj, logits, delays, experts, stop, max_steps, values=values)
+    return om.StreamOracle(L, K, x0, proj, logits, delays, experts, stop, max_steps, values=values, admit=admit)
 
 
 def pin_layer_pick():
@@ -265,3 +266,55 @@ def test_policies_same_values_and_conservation():
         for r in range(R):
             for n in range(min(len(s.history[r]), len(ref.history[r]))):
                 assert np.array_equal(s.history[r][n], ref.history[r][n]), (pol, r, n)
+
+
+def pin_admission_and_occupancy_hand():
+    """Requests 0 and 1 start in layer 0's attention queue, request 2 is admitted at tick 2;
+    every dispatch takes one tick, two layers, one expert (E = K = 1), MTFS.
+      t1: att_0 {0, 1} (depths att_0 2)            -> 0, 1 in transit to exp_0 (arrive t2)
+      t2: admit 2; exp_0 {0, 1} (2) vs att_0 {2} (1) -> exp_0; 0, 1 join att_1
+      t3: att_1 {0, 1} (2) vs att_0 {2} (1)          -> att_1; 0, 1 in transit (arrive t4)
+      t4: exp_1 {0, 1} (2) vs att_0 {2} (1)          -> exp_1 (stop = 4 merges reached)
+      t5: attention closed, nothing in flight: the stream ends with request 2 never served.
+    Occupancy seen at the decisions, chain att_0, exp_0, att_1, exp_1 -- t1: (2, 0, 0, 0),
+    t2: (1, 2, 0, 0), t3: (1, 0, 2, 0), t4: (1, 0, 0, 2); in transit at a decision: 0 every
+    time (arrivals are delivered first); the deepest bucket at service: 2."""
+    delays = np.ones((3, 8), dtype=np.int64)
+    s = _mk(R=3, L=2, E=1, K=1, H=3, delays=delays, stop=4, max_steps=8, values=False, admit=[0, 0, 2]).run()
+    got = [(t.tick, t.kind, t.layer, t.count) for t in s.trace]
+    assert got == [(1, "att", 0, 2), (2, "exp", 0, 2), (3, "att", 1, 2), (4, "exp", 1, 2)]
+    assert s.n.tolist() == [2, 2, 0] and s.combined == 4
+    assert s.peak_q == [2, 2, 2, 2] and s.occ_sum == [5, 2, 2, 2]
+    assert s.peak_transit == 0 and s.peak_bucket == 2 and s.to_admit == 0
+
+
+def test_admission_and_occupancy_hand():
+    pin_admission_and_occupancy_hand()
+
+
+def test_admission_pin_catches_planted_early_admission(monkeypatch):
+    """Admitting every request at the start (ignoring the admission ticks) must fail the pin."""
+    real = om.StreamOracle.__init__
+
+    def early(self, *a, **kw):
+        kw["admit"] = None
+        real(self, *a, **kw)
+    monkeypatch.setattr(om.StreamOracle, "__init__", early)
+    try:
+        pin_admission_and_occupancy_hand()
+        caught = False
+    except AssertionError:
+        caught = True
+    assert caught
+
+
+def test_admission_bursts_conserve_and_serve_all():
+    """Bursts with no stop: every request is admitted and runs all its steps, each merge is
+    counted once, and no request finishes a step before its admission tick."""
+    R, L, E, K, H, M = 24, 2, 4, 2, 5, 12
+    d = np.random.default_rng(3).integers(1, 4, size=(R, M))
+    admit = (np.arange(R) // 6) * 4                     # 6 requests every 4 ticks
+    s = _mk(R, L, E, K, H, d, stop=10 ** 6, max_steps=M, values=False, admit=admit).run()
+    assert s.to_admit == 0 and s.combined == int(s.n.sum()) == R * M
+    first = {r: s.done_tick[(r, 1)] for r in range(R)}
+    assert all(first[r] > admit[r] for r in range(R))  # a request's first step ends after it is admitted

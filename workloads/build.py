@@ -184,8 +184,13 @@ class StreamWorkload:
     x0      [R, H]        initial request states, N(0, 1)
     proj    [L] x [H, H]  attention-stub projections, N(0, sd 1/sqrt(H))
     weights [L] x dict    routed experts of every layer (as make_layer_weights)
-    logits  [R, M, E]     router logits of (request r, step n), U(0, 1) like c2
-    delays  [R, M]        dispatch delay in ticks: ceil(LogNormal(0, sigma)), at least 1
+    logits  [R, M, E]     router logits of (request r, step n): U(0, 1) like c2, or with the
+                          "zipf" stream router log p + N(0, 1), p the Zipf popularity of the
+                          step's layer (n mod L), one seeded expert order per layer
+    delays  [R, M]        dispatch delay in ticks: ceil(LogNormal(0, sigma)), at least 1;
+                          x slow_factor for requests homed (r mod stream_ranks) on a slow rank
+    admit   [R]           tick at which request r enters layer 0's attention queue (0 = at
+                          start; bursts of admit_burst requests every admit_gap ticks)
     """
     spec: WorkloadSpec
     seed: int
@@ -195,6 +200,7 @@ class StreamWorkload:
     weights: list
     logits: torch.Tensor
     delays: np.ndarray
+    admit: np.ndarray = None
 
 
 def make_stream_inputs(spec, seed, max_steps, device="cpu", weights=True, requests=None, delay_seed=None):
@@ -207,12 +213,28 @@ def make_stream_inputs(spec, seed, max_steps, device="cpu", weights=True, reques
         v = counter_normal(seed, _stream(l, _S_PROJ), H * H, device=device) / math.sqrt(H)
         proj.append(to_dtype_exact(v, lay.dtype).view(H, H))
     ws = [make_layer_weights(lay, seed, l, device) for l in range(L)] if weights else []
-    logits = counter_uniform(seed, _stream(0, _S_LOGIT) + 7, R * max_steps * E, device=device)
-    logits = logits.to(torch.float32).view(R, max_steps, E)
+    if spec.stream_router == "zipf":
+        noise = counter_normal(seed, _stream(0, _S_LOGIT) + 7, R * max_steps * E, device=device).view(R, max_steps, E)
+        logp = torch.empty((L, E), dtype=torch.float64, device=device)
+        for l in range(L):
+            ranks = np.random.default_rng([seed, 101, l]).permutation(E) + 1
+            p = ranks.astype(np.float64) ** (-spec.zipf_s)
+            logp[l] = torch.tensor(np.log(p / p.sum()), dtype=torch.float64, device=device)
+        layer_of_step = torch.arange(max_steps, device=device) % L
+        logits = (noise + logp[layer_of_step][None, :, :]).to(torch.float32)
+    else:
+        logits = counter_uniform(seed, _stream(0, _S_LOGIT) + 7, R * max_steps * E, device=device)
+        logits = logits.to(torch.float32).view(R, max_steps, E)
     z = counter_normal(seed if delay_seed is None else delay_seed, _stream(0, _S_DELAY), R * max_steps).numpy()
     delays = np.maximum(1, np.ceil(np.exp(spec.stream_sigma * z))).astype(np.int32).reshape(R, max_steps)
+    if spec.slow_ranks > 0:
+        slow = (np.arange(R) % spec.stream_ranks) < spec.slow_ranks
+        delays[slow] *= np.int32(spec.slow_factor)
+    admit = np.zeros(R, dtype=np.int32)
+    if spec.admit_burst > 0:
+        admit = ((np.arange(R) // spec.admit_burst) * spec.admit_gap).astype(np.int32)
     return StreamWorkload(spec=spec, seed=seed, max_steps=max_steps, x0=x0, proj=proj, weights=ws,
-                          logits=logits, delays=delays)
+                          logits=logits, delays=delays, admit=admit)
 
 
 def shuffled_waves(waves, seed):

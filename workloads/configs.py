@@ -43,6 +43,16 @@ class WorkloadSpec:
     stream_steps: int = 0             # stop after this many combined token-layer steps
     stream_ranks: int = 16
     stream_sigma: float = 1.0
+    # delay regimes of the streaming decode: burst admission of requests (admit_burst requests
+    # every admit_gap ticks; 0 = all at tick 0), skewed expert load (router "zipf": logits =
+    # log-popularity + N(0, 1), one popularity order per layer), and delayed simulated ranks
+    # (the requests homed on the first slow_ranks of stream_ranks ranks get slow_factor x
+    # their dispatch delays)
+    stream_router: str = "uniform"
+    admit_burst: int = 0
+    admit_gap: int = 0
+    slow_ranks: int = 0
+    slow_factor: int = 1
     notes: str = ""
 
 
@@ -73,6 +83,22 @@ CONFIGS = {
         waves="stream", num_waves=16, arrival="lognormal", policy="mtfs", num_layers=4,
         stream_steps=10000, stream_ranks=16, stream_sigma=1.0,
         notes="4 layers of the c2 shape, 512 requests, RMSNorm+projection attention stub"),
+    # the streaming decode under three delay regimes (its policy and latency study)
+    "c5b": WorkloadSpec(
+        name="c5b_streaming_burst", layer=GPT_OSS_LAYER, tokens=512, router="uniform",
+        waves="stream", num_waves=16, arrival="lognormal", policy="mtfs", num_layers=4,
+        stream_steps=10000, stream_ranks=16, stream_sigma=1.0, admit_burst=128, admit_gap=8,
+        notes="c5 with requests admitted in bursts of 128 every 8 ticks"),
+    "c5s": WorkloadSpec(
+        name="c5s_streaming_skewed", layer=GPT_OSS_LAYER, tokens=512, router="uniform",
+        waves="stream", num_waves=16, arrival="lognormal", policy="mtfs", num_layers=4,
+        stream_steps=10000, stream_ranks=16, stream_sigma=1.0, stream_router="zipf",
+        notes="c5 with Zipf(1.2) expert popularity per layer"),
+    "c5d": WorkloadSpec(
+        name="c5d_streaming_delayed_ranks", layer=GPT_OSS_LAYER, tokens=512, router="uniform",
+        waves="stream", num_waves=16, arrival="lognormal", policy="mtfs", num_layers=4,
+        stream_steps=10000, stream_ranks=16, stream_sigma=1.0, slow_ranks=2, slow_factor=4,
+        notes="c5 with 2 of 16 simulated ranks delivering 4x later"),
 }
 
 # Smaller cases for element-by-element parity (several tiles + ragged tails).
@@ -107,6 +133,13 @@ TEST_CONFIGS = {
         name="s1_stream_small", layer=LayerSpec(16, 4, 320, 192, "bf16"), tokens=48, router="uniform",
         waves="stream", num_waves=16, arrival="lognormal", policy="mtfs", num_layers=4,
         stream_steps=150, stream_ranks=16, stream_sigma=1.0),
+    # the small stream with all three regimes at once: bursts of 12 requests every 5 ticks,
+    # Zipf routing, ranks 0-2 of 8 four times slower
+    "s1x": WorkloadSpec(
+        name="s1x_stream_small_regimes", layer=LayerSpec(16, 4, 320, 192, "bf16"), tokens=48,
+        router="uniform", waves="stream", num_waves=16, arrival="lognormal", policy="mtfs", num_layers=4,
+        stream_steps=150, stream_ranks=8, stream_sigma=1.0, stream_router="zipf", admit_burst=12,
+        admit_gap=5, slow_ranks=3, slow_factor=4),
     # deep K, split over K chunks when a step has few tiles: H = 6136 (96 k-blocks, the last
     # 56 wide -> 4 chunks of 24), I = 3088 (49 k-blocks, the last 16 wide -> 2 chunks of
     # 24/25), 2I = 6176 (48 tiles + 32 rows), H = 47 tiles + 120 rows.
