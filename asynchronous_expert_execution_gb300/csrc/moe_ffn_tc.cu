@@ -392,8 +392,7 @@ struct SmemLayout {
   static constexpr int kNumBars = 2 * STAGES + 4;
   static constexpr int kOffTmem = kOffBar + kNumBars * 8;
   static constexpr int kOffAbort = kOffTmem + 4;
-  static constexpr int kOffRowPtr = (kOffAbort + 4 + 15) & ~15;
-  static constexpr int kOffSlot = kOffRowPtr + 2 * BNW * 8;   // row pointers of both B warps
+  static constexpr int kOffSlot = (kOffAbort + 4 + 15) & ~15;
   static constexpr int kOffK = kOffSlot + BNW * 4;
   static constexpr int kOffFin = kOffK + BNW * 4;
   static constexpr int kOffW = kOffFin + BNW * 4;
@@ -418,7 +417,6 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
   uint64_t* tempty = bars + 2 * STAGES + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SL::kOffTmem);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SL::kOffAbort);
-  const __nv_bfloat16** rowptr = reinterpret_cast<const __nv_bfloat16**>(smem + SL::kOffRowPtr);
   int* slot_s = reinterpret_cast<int*>(smem + SL::kOffSlot);
   int* k_s = reinterpret_cast<int*>(smem + SL::kOffK);
   int* fin = reinterpret_cast<int*>(smem + SL::kOffFin);
@@ -581,28 +579,36 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
     }
   } else if ((warp == 1 || warp == 3) && MODE != kModeGemm2) {
     // ------------------------------- B producer (two warps): gathered rows via cp.async
+    // Lane l of B warp wi copies the 16-byte chunk c = l % 8 of rows 4 wi + l / 8 + 8 i of every
+    // k-block (i < BNW / 8): its rows, its chunk and its swizzled destination offset are fixed
+    // for a tile, so each lane looks its rows' source addresses up once per tile and a k-block
+    // is just its copies (measured: the copy issue loop, not DRAM, had set the pace of wide tiles).
     const int wi = warp == 1 ? 0 : 1;               // each warp copies half of every stage
-    const __nv_bfloat16** rp_w = rowptr + wi * BNW;
+    constexpr int kRowsPerLane = BNW / 8;
+    const int c8 = lane & 7;
+    const int rbase = (lane >> 3) + 4 * wi;
+    const uint32_t dst_off = (uint32_t)(rbase * 128 + ((c8 ^ (rbase & 7)) << 4));
     const char* pool = static_cast<const char*>(L.pool);
     uint32_t it = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
       const Unit un = unit_of(u, n_whole, nchunk);
       const Tile tl = decode_tile<BN, BNW, MODE>(p, tb_s, un.t);
-      __syncwarp();
-      for (int r = lane; r < tl.nmma; r += 32) {
-        const __nv_bfloat16* rp = nullptr;
+      const char* srow[kRowsPerLane];
+#pragma unroll
+      for (int i = 0; i < kRowsPerLane; ++i) {
+        const int r = rbase + 8 * i;
+        const char* rp = nullptr;
         if (r < tl.nj) {
           if (MODE == kModeAtt) {
-            rp = static_cast<const __nv_bfloat16*>(p.sd.att_rowptr[tl.j0 + r]);
+            rp = static_cast<const char*>(p.sd.att_rowptr[tl.j0 + r]);
           } else {
             const int rec = record_checked(L, d, C, tl.expert, tl.head + tl.j0 + r);
-            rp = rec >= 0 ? reinterpret_cast<const __nv_bfloat16*>(pool) + (size_t)(rec >> kKShift) * d.H : nullptr;
+            rp = rec >= 0 ? pool + (size_t)(rec >> kKShift) * d.H * 2 : nullptr;
           }
         }
-        rp_w[r] = rp;
+        srow[i] = rp;
       }
-      __syncwarp();
       for (int ch = un.c0; ch < un.c1 && ok; ++ch) {
         const int kb1 = chunk_kb(ch + 1, nk, nchunk);
         for (int kbs = chunk_kb(ch, nk, nchunk); kbs < kb1; kbs += tl.kps, ++it) {
@@ -613,15 +619,17 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
           if (!(ok = __all_sync(0xffffffffu, w_ok))) break;
           const uint32_t b_s = smem_u32(smem + s * SL::kStage) + tl.kps * SL::kA1;
           for (int j = 0; j < nv; ++j) {
-            const uint32_t bs = b_s + j * tl.bn * kBK * 2;
-            const int col0 = (kbs + j) * kBK;
-            for (int q = wi * 32 + lane; q < tl.nmma * 8; q += 64) {
-              const int r = q >> 3, c = q & 7;
-              const __nv_bfloat16* rp = rp_w[r];
-              const int col = col0 + c * 8;
-              const bool valid = rp != nullptr && col < Kdim;
-              const void* src = valid ? static_cast<const void*>(rp + col) : static_cast<const void*>(pool);
-              cp_async16(bs + r * 128 + ((c ^ (r & 7)) << 4), src, valid ? 16u : 0u);
+            const uint32_t bs = b_s + j * tl.bn * kBK * 2 + dst_off;
+            const int col = (kbs + j) * kBK + c8 * 8;
+            const bool colok = col < Kdim;
+#pragma unroll
+            for (int i = 0; i < kRowsPerLane; ++i) {
+              if (rbase + 8 * i < tl.nmma) {
+                const bool valid = srow[i] != nullptr && colok;
+                cp_async16(bs + i * 1024, valid ? static_cast<const void*>(srow[i] + (size_t)col * 2)
+                                                : static_cast<const void*>(pool),
+                           valid ? 16u : 0u);
+              }
             }
           }
           // each lane's copies arrive on the stage barrier when they complete -- no waiting
