@@ -190,17 +190,14 @@ __global__ void collect_kernel(LayerView L, Dims d, DevCounters* C, int max_out,
   const uint32_t rh = L.ready_ht[0], rt = L.ready_ht[1];
   const int base = append ? *n_io : 0;
   const int n = max(0, min((int)(rt - rh), max_out - base));
-  constexpr int V = 16 / sizeof(T);
-  const int chunks = d.H / V;
   for (int i = blockIdx.x; i < n; i += gridDim.x) {
     const int slot = L.ready[(rh + (uint32_t)i) % (uint32_t)d.S];
     if (kDebugBounds && (slot < 0 || slot >= d.S)) {             // bounds-checked build
       if (threadIdx.x == 0) set_error(C, MOE_ERR_BOUNDS);
       continue;
     }
-    const int4* src = reinterpret_cast<const int4*>(static_cast<const T*>(L.y) + (size_t)slot * d.H);
-    int4* dst = reinterpret_cast<int4*>(y_out + (size_t)(base + i) * d.H);
-    for (int c = threadIdx.x; c < chunks; c += blockDim.x) dst[c] = __ldcg(src + c);
+    // the top-k merge of the ready token: y = sum of its KS weighted results, ascending k
+    merge_row<T>(L, d, slot, y_out + (size_t)(base + i) * d.H, threadIdx.x, blockDim.x);
     for (int p = threadIdx.x; p < parts; p += blockDim.x) L.done_part[(size_t)slot * parts + p] = 0u;
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -607,15 +604,15 @@ moe_status moe_async_collect(moe_async_t h, int32_t layer, int32_t max_out, void
   if (reinterpret_cast<uintptr_t>(d_y_out) % 16) return MOE_ERR_INVALID;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const Dims& d = h->dims;
-  const int grid = std::max(1, std::min(max_out, h->num_sms * 4));
+  const int grid = std::max(1, std::min(max_out, h->num_sms * 8));
   prof_begin(h, MOE_KERNEL_COLLECT, s);
   cudaError_t e;
   if (d.dtype == MOE_BF16)
-    e = launch_dependent(collect_kernel<__nv_bfloat16>, dim3(grid), dim3(128), s, h->layers[layer], d, h->counters,
+    e = launch_dependent(collect_kernel<__nv_bfloat16>, dim3(grid), dim3(256), s, h->layers[layer], d, h->counters,
                      (int)max_out, static_cast<__nv_bfloat16*>(d_y_out), d_slot_out, d_gen_out, d_step_out,
                      d_n_out, (int)append, h->parts_per_pair);
   else
-    e = launch_dependent(collect_kernel<float>, dim3(grid), dim3(128), s, h->layers[layer], d, h->counters,
+    e = launch_dependent(collect_kernel<float>, dim3(grid), dim3(256), s, h->layers[layer], d, h->counters,
                      (int)max_out, static_cast<float*>(d_y_out), d_slot_out, d_gen_out, d_step_out, d_n_out,
                      (int)append, h->parts_per_pair);
   prof_end(h, MOE_KERNEL_COLLECT, s);

@@ -151,7 +151,7 @@ __global__ void __launch_bounds__(256) ffn2_simt_kernel(LayerView L, Dims d, Dev
           L.slotbuf[((size_t)slot_s[j] * d.KS + k_s[j]) * d.H + f] = w_s[j] * acc[m];
       }
     }
-    land_and_merge<T>(L, d, C, slot_s, nj, fti, parts, f0, kBH, tid, 256, fin, CtaBarrier{}, it.step);
+    land_only(L, d, C, slot_s, nj, parts, tid, 256, CtaBarrier{}, it.step);
   }
 }
 
@@ -188,7 +188,7 @@ __global__ void __launch_bounds__(256) identity_kernel(LayerView L, Dims d, DevC
       float* dst = L.slotbuf + ((size_t)slot_s[j] * d.KS + k_s[j]) * d.H;
       for (int f = tid; f < d.H; f += 256) dst[f] = w_s[j] * to_f(src[f]);
     }
-    land_and_merge<T>(L, d, C, slot_s, nj, 0, 1, 0, d.H, tid, 256, fin, CtaBarrier{}, it.step);
+    land_only(L, d, C, slot_s, nj, 1, tid, 256, CtaBarrier{}, it.step);
   }
 }
 

@@ -19,7 +19,7 @@
 //   warp 0  lane 0: TMA producer for A (and for GEMM2's B)
 //   warps 1, 3: cp.async producers for the gathered B (GEMM1, attention projection)
 //   warp 2  lane 0: MMA issuer; warp 2 allocates / frees TMEM
-//   warps 4-7: epilogue (TMEM lanes 32*(warp-4) ..), double-buffered accumulators
+//   warps 4-7: epilogue (TMEM lanes 32*(warp-4) ..), kAccBufs accumulator buffers
 // Every wait is bounded in time; a timeout latches MOE_ERR_TIMEOUT, stops all roles, and the
 // CTA still frees its TMEM before exiting.
 #include <cuda.h>
@@ -64,6 +64,12 @@ constexpr int kKps = MOE_TC_KPS;      // narrow tiles
 #define MOE_TC_WIDE_MIN2 33
 #endif
 constexpr int kKpsW = MOE_TC_KPSW;
+// TMEM accumulator buffers (each BNW columns): the MMA may run this many units' chunks ahead of
+// the epilogue, which absorbs epilogues made slow by the merges some tiles complete.
+#ifndef MOE_TC_ACC
+#define MOE_TC_ACC 4
+#endif
+constexpr int kAccBufs = MOE_TC_ACC;
 constexpr int kWideMin1 = MOE_TC_WIDE_MIN1, kWideMin2 = MOE_TC_WIDE_MIN2;
 constexpr int kThreads = 256;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // 2 s per wait
@@ -389,7 +395,7 @@ struct SmemLayout {
   static constexpr int kStageW = BNW > BN ? kKpsW * (kA1 + BNW * kBK * 2) : 0;
   static constexpr int kStage = ((kStageN > kStageW ? kStageN : kStageW) + 1023) & ~1023;
   static constexpr int kOffBar = STAGES * kStage;
-  static constexpr int kNumBars = 2 * STAGES + 4;
+  static constexpr int kNumBars = 2 * STAGES + 2 * kAccBufs;
   static constexpr int kOffTmem = kOffBar + kNumBars * 8;
   static constexpr int kOffAbort = kOffTmem + 4;
   static constexpr int kOffSlot = (kOffAbort + 4 + 15) & ~15;
@@ -407,14 +413,15 @@ struct SmemLayout {
 template <int BN, int BNW, int STAGES, int MODE>
 __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_constant__ TcParams p) {
   using SL = SmemLayout<BN, BNW, STAGES>;
-  constexpr uint32_t kTmemCols = 2 * BNW;     // two accumulator buffers (the wider width)
+  constexpr uint32_t kTmemCols = kAccBufs * BNW;   // accumulator buffers of the wider width
+  static_assert(kTmemCols <= 512 && (kTmemCols & (kTmemCols - 1)) == 0, "TMEM columns: a power of 2, at most 512");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SL::kOffBar);
   uint64_t* full = bars;
   uint64_t* empty = bars + STAGES;
   uint64_t* tfull = bars + 2 * STAGES;
-  uint64_t* tempty = bars + 2 * STAGES + 2;
+  uint64_t* tempty = bars + 2 * STAGES + kAccBufs;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SL::kOffTmem);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SL::kOffAbort);
   int* slot_s = reinterpret_cast<int*>(smem + SL::kOffSlot);
@@ -484,7 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
       mbar_init(&full[s], MODE == kModeGemm2 ? 1 : 1 + 64);
       mbar_init(&empty[s], 1);        // tcgen05.commit
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kAccBufs; ++b) {
       mbar_init(&tfull[b], 1);        // tcgen05.commit after the tile's last MMA
       mbar_init(&tempty[b], 4);       // one arrive per epilogue warp
     }
@@ -649,11 +656,11 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
         const Unit un = unit_of(u, n_whole, nchunk);
         const Tile tl = decode_tile<BN, BNW, MODE>(p, tb_s, un.t);
         const uint32_t idesc = idesc_bf16(kBM, tl.nmma);
-        // one accumulator buffer per chunk, alternating, so the epilogue drains chunk c
-        // while chunk c + 1 accumulates
+        // one accumulator buffer per chunk, in rotation, so the epilogue drains earlier chunks
+        // while later ones accumulate
         for (int c = un.c0; c < un.c1 && ok; ++c, ++acc_i) {
-          const int buf = acc_i & 1;
-          const uint32_t tph = (acc_i >> 1) & 1u;
+          const int buf = acc_i % kAccBufs;
+          const uint32_t tph = (acc_i / kAccBufs) & 1u;
           if (!(ok = mbar_wait(&tempty[buf], tph ^ 1u, abort_flag, C))) break;
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BNW);
@@ -707,8 +714,8 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
       float acc[BNW];
       bool ok = true;
       for (int c = un.c0; c < un.c1; ++c, ++acc_i) {
-        const int buf = acc_i & 1;
-        const uint32_t tph = (acc_i >> 1) & 1u;
+        const int buf = acc_i % kAccBufs;
+        const uint32_t tph = (acc_i / kAccBufs) & 1u;
         const bool w_ok = mbar_wait(&tfull[buf], tph, abort_flag, C);
         if (!(ok = epi_bar_and(w_ok))) break;
         tc_fence_after();
@@ -814,9 +821,11 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
           }
         }
       }
-      if (MODE == kModeGemm2)
-        land_and_merge<__nv_bfloat16>(L, d, C, slot_s, tl.nj, tl.fti, p.parts, tl.fti * kBM, kBM, et, 128, fin, EpiBarrier{},
-                                      tl.step, p.stream_on ? &p.sd : nullptr, layer);
+      if (MODE == kModeGemm2 && p.stream_on)        // streaming runtime: merge in place (its
+        land_and_merge<__nv_bfloat16>(L, d, C, slot_s, tl.nj, tl.fti, p.parts, tl.fti * kBM, kBM, et, 128, fin,
+                                      EpiBarrier{}, tl.step, &p.sd, layer);   // next tick reads it)
+      else if (MODE == kModeGemm2)                   // per-layer path: collect merges ready tokens
+        land_only(L, d, C, slot_s, tl.nj, p.parts, et, 128, EpiBarrier{}, tl.step);
       else
         asm volatile("bar.sync 1, 128;" ::: "memory");   // slot_s / w_s / last_flag reused by the next unit
     }

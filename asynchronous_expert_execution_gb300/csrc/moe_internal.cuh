@@ -459,6 +459,73 @@ __device__ void land_and_merge(const LayerView& L, const Dims& d, DevCounters* C
   bar();
 }
 
+// Landing of one tile's results when the merge is left to the collect kernel (the per-layer
+// path).  Called by the `nthr` threads of the tile's epilogue after its slotbuf writes.  Each
+// token's landing count is bumped once per (tile, token); the tile that brings it to KS x parts
+// results (every feature slice of every pair) publishes the token on the ready ring.  No fence
+// orders the slotbuf writes before the count: collect, which reads them, runs after this kernel
+// has finished.  A retired (cancelled) slot is never published and is freed at its last landing.
+template <typename Bar>
+__device__ void land_only(const LayerView& L, const Dims& d, DevCounters* C, const int* slots, int nj,
+                          int parts, int tid, int nthr, Bar bar, int step) {
+  const uint32_t target = (uint32_t)d.KS * (uint32_t)parts;
+  for (int j = tid; j < nj; j += nthr) {
+    const int slot = slots[j];
+    if (kDebugBounds && (slot < 0 || slot >= d.S)) continue;     // an absent row (bounds-checked build)
+    const uint32_t mask = L.enq_mask[slot];                      // stable during a step
+    atomicMax(&L.emit_step[slot], (uint32_t)step);
+    const uint32_t landed = atomicAdd(&L.landed[slot], 1u) + 1u;
+    if (mask & kRetired) {
+      if (retired_quiescent(mask, landed, parts)) reclaim_slot(L, parts, slot);   // last landing
+    } else if (landed == target) {
+      L.done[slot] = (uint32_t)parts;                            // complete: too late to cancel
+      publish_ready(L, d, C, slot);
+    } else if (landed > target) {
+      set_error(C, MOE_ERR_DUPLICATE);
+    }
+  }
+  bar();
+}
+
+// The merge of one ready token, y = sum_k slotbuf[slot][k] in ascending k (fp32, stored in the
+// output dtype with round-to-nearest), by `nthr` threads: 4 features per thread at a time.
+template <typename T>
+__device__ __forceinline__ void merge_row(const LayerView& L, const Dims& d, int slot, T* __restrict__ y,
+                                          int tid, int nthr) {
+  const float* src = L.slotbuf + (size_t)slot * d.KS * d.H;
+  for (int f = 4 * tid; f < d.H; f += 4 * nthr) {
+    float4 a = __ldcg(reinterpret_cast<const float4*>(src + f));
+    int k = 1;
+    for (; k + 8 <= d.KS; k += 8) {          // eight loads in flight, then the adds in k order
+      float4 b[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) b[u] = __ldcg(reinterpret_cast<const float4*>(src + (size_t)(k + u) * d.H + f));
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        a.x += b[u].x;
+        a.y += b[u].y;
+        a.z += b[u].z;
+        a.w += b[u].w;
+      }
+    }
+    float4 b[7];
+    const int rest = d.KS - k;               // < 8
+#pragma unroll
+    for (int u = 0; u < 7; ++u)
+      if (u < rest) b[u] = __ldcg(reinterpret_cast<const float4*>(src + (size_t)(k + u) * d.H + f));
+#pragma unroll
+    for (int u = 0; u < 7; ++u) {
+      if (u < rest) {
+        a.x += b[u].x;
+        a.y += b[u].y;
+        a.z += b[u].z;
+        a.w += b[u].w;
+      }
+    }
+    store4<T>(y + f, a);
+  }
+}
+
 // ------------------------------------------------------------ host helpers
 
 #define MOE_CUDA_TRY(expr)                                  \
