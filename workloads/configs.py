@@ -128,6 +128,14 @@ TEST_CONFIGS = {
     "p3": WorkloadSpec(
         name="p3_gptoss_prefill_slice", layer=GPT_OSS_LAYER.__class__(32, 4, 2880, 2880, "bf16"), tokens=2048,
         router="zipf", zipf_s=1.2, waves="even", num_waves=4, arrival="index", policy="mtfs"),
+    # profiling-sized slice of the DeepSeek-wide layer: 32 of its experts + the shared expert
+    # (2.9 GB of weights, well above L2), 320 tokens so each routed expert gets ~80, one wave,
+    # threshold 64 -- the shapes of that layer's big step in one launch pair.
+    "p4": WorkloadSpec(
+        name="p4_deepseek_wide_slice",
+        layer=LayerSpec(32, 8, 7168, 2048, "bf16", has_shared=True, shared_inter=2048), tokens=320,
+        router="normal", waves="even", num_waves=1, arrival="index", policy="threshold", min_batch=64,
+        fallback_groups=1),
     # streaming multi-layer decode, small: 4 layers, ragged H (2.5 tiles of 128), 48 requests.
     "s1": WorkloadSpec(
         name="s1_stream_small", layer=LayerSpec(16, 4, 320, 192, "bf16"), tokens=48, router="uniform",
