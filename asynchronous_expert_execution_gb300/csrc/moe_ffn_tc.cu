@@ -11,13 +11,15 @@
 //          tokens in the expert's bucket (the gather of StreamEP section 3, step 4, fused into
 //          the operand load); epilogue: h = silu(gate) * up, stored bf16.
 //   GEMM2: A = W2^T, K = I, B = the expert's h rows; epilogue: slotbuf[slot][k] = w * o
-//          (fp32), then readiness counting and the top-k merge y = sum_k (ascending k).
+//          (fp32), then readiness counting; the top-k merge y = sum_k (ascending k) runs in
+//          the collect kernel (or, in the streaming runtime, in this epilogue).
 // K may be cut into fixed chunks whose partials are added in chunk order; a launch with few
 // tiles spreads a tile's chunks over CTAs (see Unit).
 //
 // Warp roles (256 threads, one persistent CTA per SM):
-//   warp 0  lane 0: TMA producer for A (and for GEMM2's B)
-//   warps 1, 3: cp.async producers for the gathered B (GEMM1, attention projection)
+//   warp 0  lane 0: TMA producer for A (the weights)
+//   warps 1, 3: cp.async producers for B: the gathered pool rows (GEMM1, attention projection)
+//               or the item's contiguous h rows (GEMM2, after GEMM1 has finished)
 //   warp 2  lane 0: MMA issuer; warp 2 allocates / frees TMEM
 //   warps 4-7: epilogue (TMEM lanes 32*(warp-4) ..), kAccBufs accumulator buffers
 // Every wait is bounded in time; a timeout latches MOE_ERR_TIMEOUT, stops all roles, and the
@@ -135,14 +137,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
       " [%0], [%1, {%3, %4, %5}], [%2], %6;" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
-      : "memory");
-}
-
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%3, %4}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
       : "memory");
 }
 
@@ -274,7 +268,6 @@ enum : int { kModeGemm1 = 0, kModeGemm2 = 1, kModeAtt = 2 };
 // device (the step plan, or the streaming runtime's pick), so one launch serves any layer.
 struct TcParams {
   CUtensorMap mapA[kMaxLayers];     // GEMM1: packed W13, GEMM2: packed W2^T, ATT: packed P^T
-  CUtensorMap mapB16, mapBn, mapBw; // GEMM2: the step's h rows [S*KS, I], boxes of 16 / narrow / wide rows
   LayerView views[kMaxLayers];
   Dims d;
   DevCounters* C;
@@ -323,13 +316,6 @@ __device__ __forceinline__ int chunk_kb(int c, int nk, int nchunk) {
   if (c >= nchunk) return nk;
   const int e = (int)(((long long)c * nk) / nchunk);
   return min(nk, (e + 3) / 6 * 6);
-}
-
-// A chunk's k-blocks move kps at a time (kps: the tile's k-blocks per stage): stage st of
-// chunk c starts at chunk_kb(c) + st kps and holds min(kps, chunk end - start) k-blocks (a
-// stage never spans two chunks).
-__device__ __forceinline__ int chunk_nstages(int c, int nk, int nchunk, int kps) {
-  return (chunk_kb(c + 1, nk, nchunk) - chunk_kb(c, nk, nchunk) + kps - 1) / kps;
 }
 
 struct Tile {
@@ -481,14 +467,8 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
 
   if (threadIdx.x == 0) {
     prefetch_tmap(tmA);                        // descriptors load while the CTA sets up
-    if (MODE == kModeGemm2) {
-      prefetch_tmap(&p.mapB16);
-      prefetch_tmap(&p.mapBn);
-      prefetch_tmap(&p.mapBw);
-    }
     for (int s = 0; s < STAGES; ++s) {
-      // GEMM2: one expect_tx arrive (A and B both by TMA); else + 64 cp.async B-producer lanes
-      mbar_init(&full[s], MODE == kModeGemm2 ? 1 : 1 + 64);
+      mbar_init(&full[s], 1 + 64);    // the A producer's expect_tx arrive + 64 cp.async B lanes
       mbar_init(&empty[s], 1);        // tcgen05.commit
     }
     for (int b = 0; b < kAccBufs; ++b) {
@@ -522,25 +502,12 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
       const uint64_t pol_reuse = policy_evict_normal();
       uint32_t it = 0;
       bool ok = true;
-      // GEMM2 runs as a programmatic dependent of GEMM1: the weights do not depend on GEMM1,
-      // so the first ring of W2 stages is requested at once; the h rows (GEMM1's output) only
-      // after griddepcontrol.wait.
-      const Unit u0 = unit_of(blockIdx.x, n_whole, nchunk);
-      const Tile t0 = decode_tile<BN, BNW, MODE>(p, tb_s, u0.t);
-      int deferred = 0;
-      if (MODE == kModeGemm2) {
-        for (int c = u0.c0; c < u0.c1; ++c) deferred += chunk_nstages(c, nk, nchunk, t0.kps);
-        deferred = min(STAGES, deferred);
-      }
-      int def_n = 0;
+      // GEMM2 runs as a programmatic dependent of GEMM1: its weights do not depend on GEMM1,
+      // so this producer streams W2 at once; the B warps wait for GEMM1 before the h rows.
       for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
         const Unit un = unit_of(u, n_whole, nchunk);
         const Tile tl = decode_tile<BN, BNW, MODE>(p, tb_s, un.t);
         const uint64_t pol = tl.single ? pol_stream : pol_reuse;
-        // GEMM2's B = the item's contiguous h rows: a 16-row or tile-wide box (rows past the
-        // item feed MMA columns the epilogue ignores; rows past the buffer are zero-filled)
-        const int brows = tl.nmma <= 16 ? 16 : tl.bn;
-        const CUtensorMap* mapB = tl.nmma <= 16 ? &p.mapB16 : (tl.bn == BN ? &p.mapBn : &p.mapBw);
         for (int c = un.c0; c < un.c1 && ok; ++c) {
           const int kb1 = chunk_kb(c + 1, nk, nchunk);
           for (int kbs = chunk_kb(c, nk, nchunk); kbs < kb1; kbs += tl.kps, ++it) {
@@ -549,42 +516,14 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
             const uint32_t ph = (it / STAGES) & 1u;
             if (!(ok = mbar_wait(&empty[s], ph ^ 1u, abort_flag, C))) break;
             const uint32_t a_s = smem_u32(smem + s * SL::kStage);
-            const uint32_t b_s = a_s + tl.kps * SL::kA1;
-            if (MODE == kModeGemm2) {
-              mbar_arrive_expect_tx(&full[s], nv * (SL::kA1 + brows * kBK * 2));
-              for (int j = 0; j < nv; ++j)
-                tma_load_3d(a_s + j * SL::kA1, tmA, &full[s], (kbs + j) * kBK, tl.fti * kBM, tl.expert, pol);
-              if (deferred > 0) {                       // first ring of the first unit: A only
-                if (++def_n == deferred) {              // then wait for GEMM1, and fetch its B
-                  griddep_wait();
-                  const CUtensorMap* mapB0 = t0.nmma <= 16 ? &p.mapB16 : (t0.bn == BN ? &p.mapBn : &p.mapBw);
-                  const int row0 = t0.row_base + t0.j0;
-                  int idx = 0;
-                  for (int c2 = u0.c0; c2 < u0.c1 && idx < deferred; ++c2) {
-                    const int e2 = chunk_kb(c2 + 1, nk, nchunk);
-                    for (int k2 = chunk_kb(c2, nk, nchunk); k2 < e2 && idx < deferred; k2 += t0.kps, ++idx) {
-                      const int n2 = min(t0.kps, e2 - k2);
-                      const uint32_t b0s = smem_u32(smem + idx * SL::kStage) + t0.kps * SL::kA1;
-                      for (int j = 0; j < n2; ++j)
-                        tma_load_2d(b0s + j * t0.bn * kBK * 2, mapB0, &full[idx], (k2 + j) * kBK, row0);
-                    }
-                  }
-                  deferred = 0;
-                }
-                continue;
-              }
-              for (int j = 0; j < nv; ++j)
-                tma_load_2d(b_s + j * tl.bn * kBK * 2, mapB, &full[s], (kbs + j) * kBK, tl.row_base + tl.j0);
-            } else {
-              mbar_arrive_expect_tx(&full[s], nv * SL::kA1);
-              for (int j = 0; j < nv; ++j)
-                tma_load_3d(a_s + j * SL::kA1, tmA, &full[s], (kbs + j) * kBK, tl.fti * kBM, tl.expert, pol);
-            }
+            mbar_arrive_expect_tx(&full[s], nv * SL::kA1);
+            for (int j = 0; j < nv; ++j)
+              tma_load_3d(a_s + j * SL::kA1, tmA, &full[s], (kbs + j) * kBK, tl.fti * kBM, tl.expert, pol);
           }
         }
       }
     }
-  } else if ((warp == 1 || warp == 3) && MODE != kModeGemm2) {
+  } else if (warp == 1 || warp == 3) {
     // ------------------------------- B producer (two warps): gathered rows via cp.async
     // Lane l of B warp wi copies the 16-byte chunk c = l % 8 of rows 4 wi + l / 8 + 8 i of every
     // k-block (i < BNW / 8): its rows, its chunk and its swizzled destination offset are fixed
@@ -596,6 +535,8 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
     const int rbase = (lane >> 3) + 4 * wi;
     const uint32_t dst_off = (uint32_t)(rbase * 128 + ((c8 ^ (rbase & 7)) << 4));
     const char* pool = static_cast<const char*>(L.pool);
+    // GEMM2: the h rows are GEMM1's output -- wait for it (the weight producer does not)
+    if (MODE == kModeGemm2) griddep_wait();
     uint32_t it = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
@@ -609,6 +550,8 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
         if (r < tl.nj) {
           if (MODE == kModeAtt) {
             rp = static_cast<const char*>(p.sd.att_rowptr[tl.j0 + r]);
+          } else if (MODE == kModeGemm2) {
+            rp = reinterpret_cast<const char*>(p.hbuf) + (size_t)(tl.row_base + tl.j0 + r) * d.I * 2;
           } else {
             const int rec = record_checked(L, d, C, tl.expert, tl.head + tl.j0 + r);
             rp = rec >= 0 ? pool + (size_t)(rec >> kKShift) * d.H * 2 : nullptr;
@@ -671,7 +614,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
             const uint32_t ph = (it / STAGES) & 1u;
             if (!(ok = mbar_wait(&full[s], ph, abort_flag, C))) break;
             tc_fence_after();
-            if (MODE != kModeGemm2) fence_proxy_async();   // B came through cp.async (generic proxy)
+            fence_proxy_async();                      // B came through cp.async (generic proxy)
             const uint32_t a_s = smem_u32(smem + s * SL::kStage);
             for (int j = 0; j < nv; ++j) {
               const uint32_t a0 = a_s + j * SL::kA1;
@@ -893,20 +836,6 @@ bool encode_weights(CUtensorMap* m, const void* base, int K, int rows, int nb) {
   return r == CUDA_SUCCESS;
 }
 
-// 2-D map over row-major bf16 rows [rows][K], box 64 x box_rows, 128B swizzle, zero fill.
-bool encode_rows(CUtensorMap* m, const void* base, int K, int rows, int box_rows) {
-  auto fn = get_encode();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)K * 2};
-  cuuint32_t box[2] = {kBK, (cuuint32_t)box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
 template <int BN, int BNW, int STAGES, int MODE>
 cudaError_t set_attrs() {
   using SL = SmemLayout<BN, BNW, STAGES>;
@@ -991,12 +920,6 @@ moe_status tc_setup(moe_async_s* h) {
   const Dims& d = h->dims;
   fill_common(h, st->gemm1);
   fill_common(h, st->gemm2);
-  const int hrows = h->dims.S * h->dims.KS;
-  if (!encode_rows(&st->gemm2.mapB16, h->h, d.I, hrows, 16) || !encode_rows(&st->gemm2.mapBn, h->h, d.I, hrows, kBN) ||
-      !encode_rows(&st->gemm2.mapBw, h->h, d.I, hrows, kBNW)) {
-    delete st;
-    return MOE_ERR_CUDA;
-  }
   for (int l = 0; l < h->cfg.num_layers; ++l) {
     if (!encode_weights(&st->gemm1.mapA[l], h->layers[l].w13, d.H, 2 * d.I, d.NB) ||
         !encode_weights(&st->gemm2.mapA[l], h->layers[l].w2, d.I, d.H, d.NB)) {
