@@ -70,14 +70,17 @@ __global__ void route_kernel(const float* __restrict__ logits, int T, int E, int
 }
 
 // --------------------------------------------------------------- Receptor
+constexpr int kCopyDepth = 16;         // 16-byte loads in flight per lane in the pool copy
+
 // One warp takes `tpw` whole tokens at a time (tpw * KS <= 32): lane l handles pair k = l % KS
-// of token l / KS (k == K is the shared expert).  Appends use warp-aggregated atomics: lanes
-// bound for the same bucket elect a leader that reserves all of their positions with one
-// atomicAdd on the bucket tail.  Then the same warp copies into pool[slot] (16-byte vectors)
-// the row of each of its tokens that had at least one pair accepted by this call: a stale,
-// retired or duplicate delivery leaves the pool row of the slot's current request untouched
-// ("asynchronous MoE serving" notes, inferred obligations: accept exactly the selected
-// contributions).
+// of token l / KS (k == K is the shared expert).  Once a pair's acceptance is known, the warp
+// copies into pool[slot] (16-byte vectors) the row of each of its tokens that had at least
+// one pair accepted by this call: a stale, retired or duplicate delivery leaves the pool row
+// of the slot's current request untouched ("asynchronous MoE serving" notes, inferred
+// obligations: accept exactly the selected contributions).  Then the appends, with
+// warp-aggregated atomics: lanes bound for the same bucket elect a leader that reserves all
+// of their positions with one atomicAdd on the bucket tail.
+
 template <typename T>
 __global__ void enqueue_kernel(LayerView L, Dims d, DevCounters* C, int n, int tpw,
                                const int32_t* __restrict__ rows, const int32_t* __restrict__ slots,
@@ -131,6 +134,25 @@ __global__ void enqueue_kernel(LayerView L, Dims d, DevCounters* C, int n, int t
         }
       }
     }
+    // token rows -> pool, only for tokens with a pair accepted here (warp-uniform loop); the
+    // copies are issued before the bucket appends so their loads overlap the atomics' trips
+    const uint32_t acc = __ballot_sync(0xffffffffu, accepted);
+    for (int j = 0; j < tpw; ++j) {
+      if (!((acc >> (j * d.KS)) & kbits)) continue;
+      const int row_j = __shfl_sync(0xffffffffu, row, j * d.KS);
+      const int slot_j = __shfl_sync(0xffffffffu, slot, j * d.KS);
+      const int4* src = reinterpret_cast<const int4*>(x + (size_t)row_j * d.H);
+      int4* dst = reinterpret_cast<int4*>(static_cast<T*>(L.pool) + (size_t)slot_j * d.H);
+      for (int c = lane; c < chunks; c += 32 * kCopyDepth) {   // kCopyDepth loads in flight
+        int4 v[kCopyDepth];
+#pragma unroll
+        for (int u = 0; u < kCopyDepth; ++u)
+          if (c + 32 * u < chunks) v[u] = __ldg(src + c + 32 * u);
+#pragma unroll
+        for (int u = 0; u < kCopyDepth; ++u)
+          if (c + 32 * u < chunks) dst[c + 32 * u] = v[u];
+      }
+    }
     const uint32_t peers = __match_any_sync(0xffffffffu, key);
     if (key >= 0) {
       const int leader = __ffs(peers) - 1;
@@ -147,17 +169,6 @@ __global__ void enqueue_kernel(LayerView L, Dims d, DevCounters* C, int n, int t
       } else {
         L.records[(size_t)key * d.cap + (pos % (uint32_t)d.cap)] = (slot << kKShift) | k;
       }
-    }
-    // token rows -> pool, only for tokens with a pair accepted here (warp-uniform loop)
-    const uint32_t acc = __ballot_sync(0xffffffffu, accepted);
-    for (int j = 0; j < tpw; ++j) {
-      if (!((acc >> (j * d.KS)) & kbits)) continue;
-      const int row_j = __shfl_sync(0xffffffffu, row, j * d.KS);
-      const int slot_j = __shfl_sync(0xffffffffu, slot, j * d.KS);
-      const int4* src = reinterpret_cast<const int4*>(x + (size_t)row_j * d.H);
-      int4* dst = reinterpret_cast<int4*>(static_cast<T*>(L.pool) + (size_t)slot_j * d.H);
-#pragma unroll 4
-      for (int c = lane; c < chunks; c += 32) dst[c] = __ldg(src + c);
     }
   }
 }
@@ -548,16 +559,17 @@ moe_status moe_async_enqueue(moe_async_t h, int32_t layer, int32_t n, const int3
   const int tpw_max = 32 / d.KS;
   const long long warps_one_round = (long long)h->num_sms * 16;
   const int tpw = (int)std::min<long long>(tpw_max, std::max<long long>(1, (n + warps_one_round - 1) / warps_one_round));
+  // two warps a block, so a wave of a few hundred tokens spreads over every SM
   const long long warps = (n + tpw - 1) / tpw;
-  const int grid = (int)std::max<long long>(1, std::min<long long>((warps + 7) / 8, (long long)h->num_sms * 8));
+  const int grid = (int)std::max<long long>(1, std::min<long long>((warps + 1) / 2, (long long)h->num_sms * 32));
   prof_begin(h, MOE_KERNEL_ENQUEUE, s);
   cudaError_t e;
   if (d.dtype == MOE_BF16)
-    e = launch_dependent(enqueue_kernel<__nv_bfloat16>, dim3(grid), dim3(256), s, h->layers[layer], d, h->counters,
+    e = launch_dependent(enqueue_kernel<__nv_bfloat16>, dim3(grid), dim3(64), s, h->layers[layer], d, h->counters,
                          (int)n, tpw, d_rows, d_slot, static_cast<const __nv_bfloat16*>(d_x), d_expert, d_w, d_kmask,
                          d_gen);
   else
-    e = launch_dependent(enqueue_kernel<float>, dim3(grid), dim3(256), s, h->layers[layer], d, h->counters, (int)n,
+    e = launch_dependent(enqueue_kernel<float>, dim3(grid), dim3(64), s, h->layers[layer], d, h->counters, (int)n,
                          tpw, d_rows, d_slot, static_cast<const float*>(d_x), d_expert, d_w, d_kmask, d_gen);
   prof_end(h, MOE_KERNEL_ENQUEUE, s);
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;

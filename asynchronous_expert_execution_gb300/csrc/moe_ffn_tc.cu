@@ -14,10 +14,13 @@
 //          (fp32), then readiness counting; the top-k merge y = sum_k (ascending k) runs in
 //          the collect kernel (or, in the streaming runtime, in this epilogue).
 // K may be cut into fixed chunks whose partials are added in chunk order; a launch with few
-// tiles spreads a tile's chunks over CTAs (see Unit).
+// tiles spreads a tile's chunks over CTAs (see Unit).  Units are handed out dynamically: a
+// CTA claims its next unit from a per-launch counter as it finishes issuing the previous
+// one, so SMs that stream faster take more of the launch.
 //
 // Warp roles (256 threads, one persistent CTA per SM):
-//   warp 0  lane 0: TMA producer for A (the weights)
+//   warp 0  lane 0: TMA producer for A (the weights); claims the units and passes their
+//                   indices to the other roles through a ring in shared memory
 //   warps 1, 3: cp.async producers for B: the gathered pool rows (GEMM1, attention projection)
 //               or the item's contiguous h rows (GEMM2, after GEMM1 has finished)
 //   warp 2  lane 0: MMA issuer; warp 2 allocates / frees TMEM
@@ -74,6 +77,7 @@ constexpr int kKpsW = MOE_TC_KPSW;
 constexpr int kAccBufs = MOE_TC_ACC;
 constexpr int kWideMin1 = MOE_TC_WIDE_MIN1, kWideMin2 = MOE_TC_WIDE_MIN2;
 constexpr int kThreads = 256;
+constexpr int kMaxChunks = 4;          // most K chunks of a contraction
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;   // 2 s per wait
 
 // ------------------------------------------------------------------ PTX wrappers
@@ -281,8 +285,11 @@ struct TcParams {
   // whether a tile's chunks ran on one CTA or on several (split steps).
   int nchunk;
   int split_cap;                    // most tiles a launch may split (workspace capacity)
-  float* ws;                        // [split_cap][nchunk][BNW][128] fp32 chunk partials
+  float* ws;                        // [split_cap][nchunk][BNW / 4][128] float4 chunk partials
   int* cnt;                         // [split_cap] arrivals per split tile (zero between launches)
+  // dynamic unit assignment: [0] units claimed beyond the first round, [1] CTAs that have
+  // finished; both zero between launches (the last CTA to finish resets them)
+  int* unit_ctr;
 };
 
 // A unit of work: one tile and a range of its K chunks [c0, c1).  The first n_whole tiles of a
@@ -308,6 +315,65 @@ __device__ __forceinline__ Unit unit_of(int u, int n_whole, int nchunk) {
     x.split = true;
   }
   return x;
+}
+
+// Dynamic unit assignment.  A CTA's first unit is its own index; each later one is claimed
+// from the launch's counter when the weight producer has issued the previous unit's last
+// stage, so a CTA that streams faster takes more units and the launch ends evenly.  The
+// producer hands the indices, in order, to the other roles through a ring in shared memory:
+// -1 ends a CTA's sequence.
+constexpr int kUnitQ = 16;                // ring depth: above the most units a reader can lag
+constexpr uint32_t kUnitReaders = 7;      // the two B warps, the MMA thread, four epilogue warps
+
+struct UnitRing {
+  int* q;
+  uint64_t* full;
+  uint64_t* empty;
+};
+
+__device__ __forceinline__ bool ring_put(const UnitRing& r, uint32_t& i, int u, volatile int* abort_flag,
+                                         DevCounters* C) {
+  const int s = (int)(i % kUnitQ);
+  const uint32_t ph = (i / kUnitQ) & 1u;
+  ++i;
+  if (!mbar_wait(&r.empty[s], ph ^ 1u, abort_flag, C)) return false;
+  r.q[s] = u;
+  mbar_arrive(&r.full[s]);                  // release: the index is visible to the readers
+  return true;
+}
+
+// The next unit for one thread (the MMA issuer); -1 at the end or after an abort.
+__device__ __forceinline__ int ring_get(const UnitRing& r, uint32_t& i, volatile int* abort_flag, DevCounters* C) {
+  const int s = (int)(i % kUnitQ);
+  const uint32_t ph = (i / kUnitQ) & 1u;
+  ++i;
+  if (!mbar_wait(&r.full[s], ph, abort_flag, C)) return -1;
+  const int u = *reinterpret_cast<volatile int*>(&r.q[s]);
+  mbar_arrive(&r.empty[s]);
+  return u;
+}
+
+// The next unit for every lane of a warp (one arrival per warp, after all lanes have read).
+__device__ __forceinline__ int ring_get_warp(const UnitRing& r, uint32_t& i, int lane, volatile int* abort_flag,
+                                             DevCounters* C) {
+  const int s = (int)(i % kUnitQ);
+  const uint32_t ph = (i / kUnitQ) & 1u;
+  ++i;
+  const bool ok = mbar_wait(&r.full[s], ph, abort_flag, C);
+  const int u = ok ? *reinterpret_cast<volatile int*>(&r.q[s]) : -1;
+  const bool all_ok = __all_sync(0xffffffffu, ok);
+  if (all_ok && lane == 0) mbar_arrive(&r.empty[s]);
+  return all_ok ? u : -1;
+}
+
+// Called once per CTA by one thread after every role has stopped: the last CTA of the launch
+// puts the counters back to zero for the next launch of these parameters.
+__device__ __forceinline__ void unit_ctr_exit(int* ctr) {
+  __threadfence();
+  if (atomicAdd(&ctr[1], 1) == (int)gridDim.x - 1) {
+    ctr[0] = 0;
+    ctr[1] = 0;
+  }
 }
 
 // first k-block of chunk c (chunk c covers [chunk_kb(c), chunk_kb(c + 1))): the even cut,
@@ -389,7 +455,9 @@ struct SmemLayout {
   static constexpr int kOffFin = kOffK + BNW * 4;
   static constexpr int kOffW = kOffFin + BNW * 4;
   static constexpr int kOffFlag = kOffW + BNW * 4;
-  static constexpr int kOffTb = kOffFlag + 16;
+  static constexpr int kOffRingBar = (kOffFlag + 16 + 7) & ~7;
+  static constexpr int kOffRing = kOffRingBar + 2 * kUnitQ * 8;
+  static constexpr int kOffTb = kOffRing + kUnitQ * 4;
   static constexpr int kBytes = kOffTb + kMaxBuckets * 4;
   static constexpr int kAlloc = kBytes + 1024;               // room to align the base to 1024
 };
@@ -416,6 +484,8 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
   float* w_s = reinterpret_cast<float*>(smem + SL::kOffW);
   volatile int* last_flag = reinterpret_cast<volatile int*>(smem + SL::kOffFlag);
   int* tb_s = reinterpret_cast<int*>(smem + SL::kOffTb);
+  uint64_t* ring_bars = reinterpret_cast<uint64_t*>(smem + SL::kOffRingBar);
+  const UnitRing ring{reinterpret_cast<int*>(smem + SL::kOffRing), ring_bars, ring_bars + kUnitQ};
 
   const Dims& d = p.d;
   DevCounters* C = p.C;
@@ -462,6 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
     // every CTA of a programmatic dependent waits for its predecessor before it ends, so this
     // launch's completion implies GEMM1's even when it has no work
     if (MODE == kModeGemm2) griddep_wait();
+    if (threadIdx.x == 0) unit_ctr_exit(p.unit_ctr);
     return;
   }
 
@@ -474,6 +545,10 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
     for (int b = 0; b < kAccBufs; ++b) {
       mbar_init(&tfull[b], 1);        // tcgen05.commit after the tile's last MMA
       mbar_init(&tempty[b], 4);       // one arrive per epilogue warp
+    }
+    for (int i = 0; i < kUnitQ; ++i) {
+      mbar_init(&ring.full[i], 1);              // the weight producer
+      mbar_init(&ring.empty[i], kUnitReaders);  // every reader role
     }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -504,7 +579,9 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
       bool ok = true;
       // GEMM2 runs as a programmatic dependent of GEMM1: its weights do not depend on GEMM1,
       // so this producer streams W2 at once; the B warps wait for GEMM1 before the h rows.
-      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+      uint32_t qi = 0;
+      for (int u = blockIdx.x; ok;) {
+        if (!(ok = ring_put(ring, qi, u, abort_flag, C)) || u < 0) break;
         const Unit un = unit_of(u, n_whole, nchunk);
         const Tile tl = decode_tile<BN, BNW, MODE>(p, tb_s, un.t);
         const uint64_t pol = tl.single ? pol_stream : pol_reuse;
@@ -521,6 +598,9 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
               tma_load_3d(a_s + j * SL::kA1, tmA, &full[s], (kbs + j) * kBK, tl.fti * kBM, tl.expert, pol);
           }
         }
+        if (!ok) break;
+        const int nxt = (int)gridDim.x + atomicAdd(&p.unit_ctr[0], 1);   // claimed now, streamed next
+        u = nxt < n_units ? nxt : -1;
       }
     }
   } else if (warp == 1 || warp == 3) {
@@ -537,9 +617,10 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
     const char* pool = static_cast<const char*>(L.pool);
     // GEMM2: the h rows are GEMM1's output -- wait for it (the weight producer does not)
     if (MODE == kModeGemm2) griddep_wait();
-    uint32_t it = 0;
+    uint32_t it = 0, qi = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+    for (int u = ring_get_warp(ring, qi, lane, abort_flag, C); u >= 0 && ok;
+         u = ring_get_warp(ring, qi, lane, abort_flag, C)) {
       const Unit un = unit_of(u, n_whole, nchunk);
       const Tile tl = decode_tile<BN, BNW, MODE>(p, tb_s, un.t);
       const char* srow[kRowsPerLane];
@@ -593,9 +674,9 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
   } else if (warp == 2) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
-      uint32_t it = 0, acc_i = 0;
+      uint32_t it = 0, acc_i = 0, qi = 0;
       bool ok = true;
-      for (int u = blockIdx.x; u < n_units && ok; u += gridDim.x) {
+      for (int u = ring_get(ring, qi, abort_flag, C); u >= 0 && ok; u = ring_get(ring, qi, abort_flag, C)) {
         const Unit un = unit_of(u, n_whole, nchunk);
         const Tile tl = decode_tile<BN, BNW, MODE>(p, tb_s, un.t);
         const uint32_t idesc = idesc_bf16(kBM, tl.nmma);
@@ -635,8 +716,8 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
     const int q = warp - 4;                       // TMEM lane quarter
     const int et = threadIdx.x - 128;             // 0..127
     const int row = 32 * q + lane;                // accumulator row (A row of the tile)
-    uint32_t acc_i = 0;
-    for (int u = blockIdx.x; u < n_units; u += gridDim.x) {
+    uint32_t acc_i = 0, qi = 0;
+    for (int u = ring_get_warp(ring, qi, lane, abort_flag, C); u >= 0; u = ring_get_warp(ring, qi, lane, abort_flag, C)) {
       const Unit un = unit_of(u, n_whole, nchunk);
       const Tile tl = decode_tile<BN, BNW, MODE>(p, tb_s, un.t);
       if (MODE == kModeGemm2) {
@@ -680,14 +761,17 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
       if (un.split) {
         // this unit holds one chunk of the tile: publish its partial; the unit that arrives
         // last adds all partials of the tile in chunk order and runs the epilogue
+        // partials as [chunk][column / 4][row] float4 groups: a warp's 32 rows store (and the
+        // fold later loads) 512 contiguous bytes per instruction
         const int st = un.t - n_whole;              // split tiles: [0, split_cap)
-        float* wt = p.ws + (size_t)st * nchunk * BNW * kBM;
+        float4* wt = reinterpret_cast<float4*>(p.ws + (size_t)st * nchunk * BNW * kBM);
 #pragma unroll
         for (int c0 = 0; c0 < BNW; c0 += 16) {
           if (c0 < tl.nj) {
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-              if (c0 + j < tl.nj) __stcg(wt + ((size_t)un.c0 * BNW + c0 + j) * kBM + row, acc[c0 + j]);
+            for (int j = 0; j < 16; j += 4)
+              __stcg(wt + ((size_t)un.c0 * (BNW / 4) + (c0 + j) / 4) * kBM + row,
+                     make_float4(acc[c0 + j], acc[c0 + j + 1], acc[c0 + j + 2], acc[c0 + j + 3]));
           }
         }
         __threadfence();
@@ -701,15 +785,34 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
         EpiBarrier{}();
         if (!*last_flag) continue;
         __threadfence();
-        for (int c = 0; c < nchunk; ++c) {
+        // 8 columns of every chunk in flight at once, then the adds in ascending chunk order
 #pragma unroll
-          for (int c0 = 0; c0 < BNW; c0 += 16) {
-            if (c0 < tl.nj) {
+        for (int c0 = 0; c0 < BNW; c0 += 8) {
+          if (c0 < tl.nj) {
+            float4 v[kMaxChunks][2];
 #pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                const float v = c0 + j < tl.nj ? __ldcg(wt + ((size_t)c * BNW + c0 + j) * kBM + row) : 0.f;
-                acc[c0 + j] = c == 0 ? v : acc[c0 + j] + v;
+            for (int c = 0; c < kMaxChunks; ++c) {
+              if (c < nchunk) {
+#pragma unroll
+                for (int j = 0; j < 2; ++j) v[c][j] = __ldcg(wt + ((size_t)c * (BNW / 4) + c0 / 4 + j) * kBM + row);
               }
+            }
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              float4 a = v[0][j];
+#pragma unroll
+              for (int c = 1; c < kMaxChunks; ++c) {
+                if (c < nchunk) {
+                  a.x += v[c][j].x;
+                  a.y += v[c][j].y;
+                  a.z += v[c][j].z;
+                  a.w += v[c][j].w;
+                }
+              }
+              acc[c0 + 4 * j] = a.x;
+              acc[c0 + 4 * j + 1] = a.y;
+              acc[c0 + 4 * j + 2] = a.z;
+              acc[c0 + 4 * j + 3] = a.w;
             }
           }
         }
@@ -777,6 +880,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (threadIdx.x == 0) unit_ctr_exit(p.unit_ctr);
   if (warp == 2) {
     __syncwarp();
     tmem_dealloc(tmem_base, kTmemCols);
@@ -788,6 +892,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
 struct TcState {
   TcParams gemm1, gemm2, att;       // parameter blocks (tensor maps of every layer)
   bool att_ready;
+  int* unit_ctr;                    // two counters per parameter block, zeroed once
   void* split_buf[2];               // GEMM1 / GEMM2 chunk-partial workspace + arrival counters
 };
 
@@ -873,6 +978,7 @@ void fill_common(moe_async_s* h, TcParams& p) {
   p.split_cap = 0;
   p.ws = nullptr;
   p.cnt = nullptr;
+  p.unit_ctr = nullptr;
 }
 
 // K chunks for a contraction of nk k-blocks: 1, 2 or 4 chunks of at least MOE_SPLIT_MIN_KB
@@ -885,7 +991,7 @@ void fill_common(moe_async_s* h, TcParams& p) {
 #endif
 int chunks_for(int nk) {
   const int q = nk / MOE_SPLIT_MIN_KB;
-  return q >= 4 ? 4 : q >= 2 ? 2 : 1;
+  return q >= kMaxChunks ? kMaxChunks : q >= 2 ? 2 : 1;
 }
 
 // Workspace for launches that split tiles over their K chunks: up to two tiles per SM.
@@ -928,7 +1034,15 @@ moe_status tc_setup(moe_async_s* h) {
     }
   }
   h->tc_state = st;
-  if (setup_split(h, st->gemm1, d.H, &st->split_buf[0]) != cudaSuccess ||
+  if (cudaMalloc(&st->unit_ctr, 6 * sizeof(int)) != cudaSuccess) {
+    st->unit_ctr = nullptr;
+    tc_teardown(h);
+    return MOE_ERR_CUDA;
+  }
+  st->gemm1.unit_ctr = st->unit_ctr;
+  st->gemm2.unit_ctr = st->unit_ctr + 2;
+  if (cudaMemset(st->unit_ctr, 0, 6 * sizeof(int)) != cudaSuccess ||
+      setup_split(h, st->gemm1, d.H, &st->split_buf[0]) != cudaSuccess ||
       setup_split(h, st->gemm2, d.I, &st->split_buf[1]) != cudaSuccess) {
     tc_teardown(h);
     return MOE_ERR_CUDA;
@@ -941,6 +1055,7 @@ void tc_teardown(moe_async_s* h) {
   if (st) {
     for (void* b : st->split_buf)
       if (b) cudaFree(b);
+    if (st->unit_ctr) cudaFree(st->unit_ctr);
   }
   delete st;
   h->tc_state = nullptr;
@@ -966,6 +1081,7 @@ moe_status tc_stream_setup(moe_async_s* h, const void* const* proj_packed, const
   TcState* st = static_cast<TcState*>(h->tc_state);
   if (!st) return MOE_ERR_UNSUPPORTED;
   fill_common(h, st->att);
+  st->att.unit_ctr = st->unit_ctr + 4;
   for (int l = 0; l < h->cfg.num_layers; ++l)
     if (!encode_weights(&st->att.mapA[l], proj_packed[l], h->dims.H, h->dims.H, 1)) return MOE_ERR_CUDA;
   st->att.sd = sd;

@@ -24,6 +24,7 @@ namespace moe {
 // the last non-empty one (at most max_steps), and only those are counted.
 struct PlanScratch {
   int depth[kMaxBuckets];
+  uint32_t head[kMaxBuckets];     // queue heads read with the depths
   int order[kMaxBuckets];
   int pick[kMaxBuckets];          // RANKS: each rank's bucket (-1: none)
   unsigned char taken[kMaxBuckets];
@@ -64,17 +65,19 @@ __device__ inline void plan_layer(const LayerView& L, const Dims& d, StepPlan* P
   const int tid = threadIdx.x, nt = blockDim.x;
   if (tid == 0) { sc.n_elig = 0; sc.n_nonempty = 0; }
   __syncthreads();
+  // After an overflow or an out-of-range id the queues no longer describe valid pairs:
+  // stop executing (the sticky error is reported to the host).  Read with the depths.
+  const uint32_t err = *(volatile uint32_t*)&C->error;
   for (int b = tid; b < d.NB; b += nt) {
-    const int dep = enabled ? min((int)(L.tail[b] - L.head[b]), d.cap) : 0;
+    const uint32_t hd = L.head[b];
+    const int dep = enabled ? min((int)(L.tail[b] - hd), d.cap) : 0;
+    sc.head[b] = hd;
     depth[b] = dep;
     if (dep > 0) atomicAdd(&sc.n_nonempty, 1);
     if (dep > 0 && (pol.kind != MOE_POLICY_THRESHOLD || dep >= pol.min_batch)) atomicAdd(&sc.n_elig, 1);
   }
   __syncthreads();
   const int n_elig = sc.n_elig, n_nonempty = sc.n_nonempty;
-  // After an overflow or an out-of-range id the queues no longer describe valid pairs:
-  // stop executing (the sticky error is reported to the host).
-  const uint32_t err = *(volatile uint32_t*)&C->error;
   const bool halted = err == MOE_ERR_CAPACITY || err == MOE_ERR_INVALID || err == MOE_ERR_BOUNDS;
   // MTFS / THRESHOLD: the picks are a prefix of the deepest-first order of every non-empty
   // bucket; RANKS ranks the non-empty buckets too (its stealers take from that order)
@@ -131,6 +134,12 @@ __device__ inline void plan_layer(const LayerView& L, const Dims& d, StepPlan* P
     int row_run = 0, t1_run = 0, t2_run = 0;
     const int ft1 = (2 * d.I + g.bm1 - 1) / g.bm1;
     const int ft2 = (d.H + g.bm2 - 1) / g.bm2;
+    // trace entries of the n picks, in pick order, reserved at once
+    int ti0 = 0;
+    if (trace && trace_cap > 0 && n > 0) {
+      if (lane == 0) ti0 = atomicAdd(&C->trace_n, n);
+      ti0 = __shfl_sync(0xffffffffu, ti0, 0);
+    }
     for (int c0 = 0; c0 < n; c0 += 32) {
       const int r = c0 + lane;
       int b = 0, cnt = 0, t1 = 0, t2 = 0;
@@ -151,7 +160,7 @@ __device__ inline void plan_layer(const LayerView& L, const Dims& d, StepPlan* P
       if (r < n) {
         WorkItem it;
         it.expert = b;
-        it.head = L.head[b];
+        it.head = sc.head[b];
         it.count = cnt;
         it.row_base = row_run + s_cnt - cnt;
         it.t1_base = t1_run + s_t1 - t1;
@@ -159,10 +168,7 @@ __device__ inline void plan_layer(const LayerView& L, const Dims& d, StepPlan* P
         it.step = trace_step + (ranks ? 0 : pick_step(pol, n_elig, r));
         P->items[r] = it;
         L.head[b] = it.head + (uint32_t)cnt;
-        if (trace && trace_cap > 0) {
-          const int ti = atomicAdd(&C->trace_n, 1);
-          if (ti < trace_cap) trace[ti] = make_int4(it.step, layer, b, cnt);
-        }
+        if (trace && trace_cap > 0 && ti0 + r < trace_cap) trace[ti0 + r] = make_int4(it.step, layer, b, cnt);
       }
       row_run += __shfl_sync(0xffffffffu, s_cnt, 31);
       t1_run += __shfl_sync(0xffffffffu, s_t1, 31);
