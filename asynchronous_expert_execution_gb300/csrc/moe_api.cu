@@ -466,7 +466,7 @@ moe_status moe_async_create(const moe_async_config* cfg, const void* const* w1,
     ok = ok && dalloc(&L.landed, S * 4) == cudaSuccess;
     ok = ok && dalloc(&L.gen, S * 4) == cudaSuccess;
     ok = ok && dalloc(&L.emit_step, S * 4) == cudaSuccess;
-    ok = ok && dalloc(&L.slotbuf, S * KS * H * 4) == cudaSuccess;
+    ok = ok && dalloc(&L.slotbuf, S * KS * H * es) == cudaSuccess;   // result rows in the layer dtype
     ok = ok && dalloc(&L.y, S * H * es) == cudaSuccess;
     ok = ok && dalloc(&L.records, (size_t)d.NB * d.cap * 4) == cudaSuccess;
     ok = ok && dalloc(&L.head, (size_t)d.NB * 4) == cudaSuccess;
@@ -493,7 +493,7 @@ moe_status moe_async_create(const moe_async_config* cfg, const void* const* w1,
            cudaMemsetAsync(L.tail, 0, (size_t)d.NB * 4, s) == cudaSuccess &&
            cudaMemsetAsync(L.ready_ht, 0, 16, s) == cudaSuccess &&
            cudaMemsetAsync(L.records, 0, (size_t)d.NB * d.cap * 4, s) == cudaSuccess &&
-           cudaMemsetAsync(L.slotbuf, 0, S * KS * H * 4, s) == cudaSuccess;
+           cudaMemsetAsync(L.slotbuf, 0, S * KS * H * es, s) == cudaSuccess;
     }
     if (ok && swiglu) {
       // W1 [E,H,I] -> packed rows 32*(i/16) + i%16 ; W3 -> same + 16 ; W2 [E,I,H] -> [E,H,I]

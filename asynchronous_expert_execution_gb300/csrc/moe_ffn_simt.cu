@@ -86,19 +86,19 @@ __global__ void __launch_bounds__(256) ffn1_simt_kernel(LayerView L, Dims d, Dev
   }
 }
 
-// GEMM2 + weighted scatter + merge: o[f] = sum_i h[i] W2[i, f] for 64 features of H and
-// 16 tokens; slotbuf[slot][k][f] = w * o[f]; then landing and merges.
+// GEMM2 + scatter + landing: o[f] = sum_i h[i] W2[i, f] for 64 features of H and 16 tokens;
+// slotbuf[slot][k][f] = o[f] (the layer dtype); the merge applies the top-k weights.
 template <typename T>
 __global__ void __launch_bounds__(256) ffn2_simt_kernel(LayerView L, Dims d, DevCounters* C,
                                                         const StepPlan* __restrict__ P,
                                                         const T* __restrict__ hbuf, int parts) {
   __shared__ float hs[kBT][kKC + 1];
   __shared__ float ws[kBH][kKC + 1];
-  __shared__ int slot_s[kBT], k_s[kBT], fin[kBT];
-  __shared__ float w_s[kBT];
+  __shared__ int slot_s[kBT], k_s[kBT];
   const int tid = threadIdx.x;
   const int n_tiles = P->n_tiles2;
   const T* w2 = static_cast<const T*>(L.w2);
+  T* rows = static_cast<T*>(L.slotbuf);
   for (int t = blockIdx.x; t < n_tiles; t += gridDim.x) {
     const WorkItem it = P->items[find_item(P, t, true)];
     const int local = t - it.t2_base;
@@ -108,16 +108,14 @@ __global__ void __launch_bounds__(256) ffn2_simt_kernel(LayerView L, Dims d, Dev
     const int nj = min(kBT, it.count - j0);
     if (tid < kBT) {
       int sl = -1, kk = 0;
-      float wv = 0.f;
       if (tid < nj) {
         const int rec = record_checked(L, d, C, it.expert, it.head + j0 + tid);
         if (rec >= 0) {
           sl = rec >> kKShift;
           kk = rec & kKMask;
-          wv = L.wtab[(size_t)sl * d.KS + kk];
         }
       }
-      slot_s[tid] = sl; k_s[tid] = kk; w_s[tid] = wv;
+      slot_s[tid] = sl; k_s[tid] = kk;
     }
     __syncthreads();
     const int tx = tid & 63, ty = tid >> 6;
@@ -148,19 +146,18 @@ __global__ void __launch_bounds__(256) ffn2_simt_kernel(LayerView L, Dims d, Dev
       for (int m = 0; m < 4; ++m) {
         const int j = ty + 4 * m;
         if (j < nj && (!kDebugBounds || slot_s[j] >= 0))
-          L.slotbuf[((size_t)slot_s[j] * d.KS + k_s[j]) * d.H + f] = w_s[j] * acc[m];
+          rows[((size_t)slot_s[j] * d.KS + k_s[j]) * d.H + f] = from_f<T>(acc[m]);
       }
     }
     land_only(L, d, C, slot_s, nj, parts, tid, 256, CtaBarrier{}, it.step);
   }
 }
 
-// Identity experts: slotbuf[slot][k] = w * x (one part per pair), then landing and merges.
+// Identity experts: slotbuf[slot][k] = x (one part per pair), then landing.
 template <typename T>
 __global__ void __launch_bounds__(256) identity_kernel(LayerView L, Dims d, DevCounters* C,
                                                        const StepPlan* __restrict__ P) {
-  __shared__ int slot_s[kBT], k_s[kBT], fin[kBT];
-  __shared__ float w_s[kBT];
+  __shared__ int slot_s[kBT], k_s[kBT];
   const int tid = threadIdx.x;
   const int n_tiles = P->n_tiles2;
   const T* pool = static_cast<const T*>(L.pool);
@@ -170,23 +167,21 @@ __global__ void __launch_bounds__(256) identity_kernel(LayerView L, Dims d, DevC
     const int nj = min(kBT, it.count - j0);
     if (tid < kBT) {
       int sl = -1, kk = 0;
-      float wv = 0.f;
       if (tid < nj) {
         const int rec = record_checked(L, d, C, it.expert, it.head + j0 + tid);
         if (rec >= 0) {
           sl = rec >> kKShift;
           kk = rec & kKMask;
-          wv = L.wtab[(size_t)sl * d.KS + kk];
         }
       }
-      slot_s[tid] = sl; k_s[tid] = kk; w_s[tid] = wv;
+      slot_s[tid] = sl; k_s[tid] = kk;
     }
     __syncthreads();
     for (int j = 0; j < nj; ++j) {
       if (kDebugBounds && slot_s[j] < 0) continue;
       const T* src = pool + (size_t)slot_s[j] * d.H;
-      float* dst = L.slotbuf + ((size_t)slot_s[j] * d.KS + k_s[j]) * d.H;
-      for (int f = tid; f < d.H; f += 256) dst[f] = w_s[j] * to_f(src[f]);
+      T* dst = static_cast<T*>(L.slotbuf) + ((size_t)slot_s[j] * d.KS + k_s[j]) * d.H;
+      for (int f = tid; f < d.H; f += 256) dst[f] = src[f];
     }
     land_only(L, d, C, slot_s, nj, 1, tid, 256, CtaBarrier{}, it.step);
   }

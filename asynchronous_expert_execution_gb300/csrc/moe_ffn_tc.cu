@@ -10,9 +10,10 @@
 //   GEMM1: A = W13 (gate/up rows interleaved in blocks of 16), K = H, B = pool rows of the
 //          tokens in the expert's bucket (the gather of StreamEP section 3, step 4, fused into
 //          the operand load); epilogue: h = silu(gate) * up, stored bf16.
-//   GEMM2: A = W2^T, K = I, B = the expert's h rows; epilogue: slotbuf[slot][k] = w * o
-//          (fp32), then readiness counting; the top-k merge y = sum_k (ascending k) runs in
-//          the collect kernel (or, in the streaming runtime, in this epilogue).
+//   GEMM2: A = W2^T, K = I, B = the expert's h rows; epilogue: slotbuf[slot][k] = o (bf16,
+//          the activation dtype), then readiness counting; the top-k merge
+//          y = sum_k w_k o_k (fp32, ascending k) runs in the collect kernel (or, in the
+//          streaming runtime, in this epilogue).
 // K may be cut into fixed chunks whose partials are added in chunk order; a launch with few
 // tiles spreads a tile's chunks over CTAs (see Unit).  Units are handed out dynamically: a
 // CTA claims its next unit from a per-launch counter as it finishes issuing the previous
@@ -723,10 +724,8 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
       if (MODE == kModeGemm2) {
         for (int j = et; j < tl.nj; j += 128) {
           const int rec = record_checked(L, d, C, tl.expert, tl.head + tl.j0 + j);
-          const int sl = rec >= 0 ? rec >> kKShift : -1, kk = rec >= 0 ? rec & kKMask : 0;
-          slot_s[j] = sl;
-          k_s[j] = kk;
-          w_s[j] = rec >= 0 ? L.wtab[(size_t)sl * d.KS + kk] : 0.f;
+          slot_s[j] = rec >= 0 ? rec >> kKShift : -1;
+          k_s[j] = rec >= 0 ? rec & kKMask : 0;
         }
       } else if (MODE == kModeAtt) {
         for (int j = et; j < tl.nj; j += 128) {
@@ -836,7 +835,9 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
           }
         }
       } else if (MODE == kModeGemm2) {
+        // E_k(x) rounded to bf16 (the activation dtype); the merge applies the top-k weight
         const int f = tl.fti * kBM + row;                               // output feature of H
+        __nv_bfloat16* rows = static_cast<__nv_bfloat16*>(L.slotbuf);
         if (f < d.H) {
 #pragma unroll
           for (int c0 = 0; c0 < BNW; c0 += 16) {
@@ -845,7 +846,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
               for (int j = 0; j < 16; ++j) {
                 const int col = c0 + j;
                 if (col < tl.nj && (!kDebugBounds || slot_s[col] >= 0))
-                  L.slotbuf[((size_t)slot_s[col] * d.KS + k_s[col]) * d.H + f] = w_s[col] * acc[col];
+                  rows[((size_t)slot_s[col] * d.KS + k_s[col]) * d.H + f] = __float2bfloat16_rn(acc[col]);
               }
             }
           }

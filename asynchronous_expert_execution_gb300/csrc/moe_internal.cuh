@@ -10,8 +10,10 @@
 //     done     [S]             result parts landed (target = KS * parts_per_pair)
 //     gen      [S]             slot generation (advanced when the output is collected)
 //     emit_step[S]             scheduling step in which the slot's last result landed
-//     slotbuf  [S, KS, H] f32  weighted expert results w_k * E_k(x), one row per (slot, k)
-//     y        [S, H]          merged output sum_k slotbuf[slot][k] (ascending k)
+//     slotbuf  [S, KS, H]      expert results E_k(x) in the layer's activation dtype, one row
+//                              per (slot, k), as a result row returns to the token's home
+//     y        [S, H]          merged output sum_k wtab[slot][k] * slotbuf[slot][k] (fp32,
+//                              ascending k)
 //     records  [NB, cap] i32   per-expert micro-queue (ring) of (slot << 5 | k); NB = E + has_shared
 //     head/tail [NB] u32       monotonic ring counters; depth = tail - head
 //     ready    [S] + ready_ht  ring of combined slots awaiting collection
@@ -76,7 +78,7 @@ struct LayerView {
   uint32_t* landed;     // [S] results landed over all slices (for retirement)
   uint32_t* gen;
   uint32_t* emit_step;  // [S] largest step among the slot's landed results (its emission step)
-  float* slotbuf;
+  void* slotbuf;        // [S][KS][H] in the layer dtype: E_k(x), unweighted
   void* y;
   int32_t* records;
   uint32_t* head;
@@ -210,15 +212,65 @@ template <typename T> __device__ __forceinline__ T from_f(float v);
 template <> __device__ __forceinline__ float from_f<float>(float v) { return v; }
 template <> __device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
 
-// four consecutive outputs (16-byte aligned for fp32, 8-byte aligned for bf16)
-template <typename T> __device__ __forceinline__ void store4(T* p, float4 v);
-template <> __device__ __forceinline__ void store4<float>(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
-template <> __device__ __forceinline__ void store4<__nv_bfloat16>(__nv_bfloat16* p, float4 v) {
-  __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
-  uint2 u;
-  u.x = *reinterpret_cast<uint32_t*>(&lo);
-  u.y = *reinterpret_cast<uint32_t*>(&hi);
-  *reinterpret_cast<uint2*>(p) = u;
+// One 16-byte vector of slot-row elements (8 bf16 or 4 fp32), widened to fp32 and back.
+template <typename T> struct Vec {
+  static constexpr int N = 16 / (int)sizeof(T);
+};
+template <typename T> __device__ __forceinline__ void unpack16(const uint4& u, float (&v)[Vec<T>::N]);
+template <> __device__ __forceinline__ void unpack16<float>(const uint4& u, float (&v)[4]) {
+  v[0] = __uint_as_float(u.x);
+  v[1] = __uint_as_float(u.y);
+  v[2] = __uint_as_float(u.z);
+  v[3] = __uint_as_float(u.w);
+}
+template <> __device__ __forceinline__ void unpack16<__nv_bfloat16>(const uint4& u, float (&v)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {                     // a bf16 is the top half of an fp32
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+template <typename T> __device__ __forceinline__ uint4 pack16(const float (&v)[Vec<T>::N]);
+template <> __device__ __forceinline__ uint4 pack16<float>(const float (&v)[4]) {
+  return make_uint4(__float_as_uint(v[0]), __float_as_uint(v[1]), __float_as_uint(v[2]), __float_as_uint(v[3]));
+}
+template <> __device__ __forceinline__ uint4 pack16<__nv_bfloat16>(const float (&v)[8]) {
+  uint32_t w[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const __nv_bfloat162 b = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+    w[i] = *reinterpret_cast<const uint32_t*>(&b);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// The top-k merge of one 16-byte vector of features: a = sum_k w_k * E_k over the slot's KS
+// result rows `src` (row stride H) in ascending k, each product and sum rounded in fp32 (no
+// fused multiply-add), so the value depends only on the results and weights.  Eight rows'
+// loads are in flight at a time.
+template <typename T>
+__device__ __forceinline__ void merge_vec(const T* src, const float* wk, int KS, int H, float (&a)[Vec<T>::N]) {
+  constexpr int N = Vec<T>::N;
+  for (int k0 = 0; k0 < KS; k0 += 8) {
+    uint4 b[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      if (k0 + u < KS) b[u] = __ldcg(reinterpret_cast<const uint4*>(src + (size_t)(k0 + u) * H));
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (k0 + u < KS) {
+        const float w = __ldg(wk + k0 + u);
+        float v[N];
+        unpack16<T>(b[u], v);
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+          const float p = __fmul_rn(w, v[i]);
+          a[i] = k0 + u == 0 ? p : __fadd_rn(a[i], p);
+        }
+      }
+    }
+  }
 }
 
 // Locate the work item owning global tile `t` (items' bases are ascending).
@@ -397,49 +449,24 @@ __device__ void land_and_merge(const LayerView& L, const Dims& d, DevCounters* C
   }
   __threadfence();
   bar();
-  // the merge of every finished token's slice: (token, 4 features) items spread over the
-  // group, four items per thread at a time, so the loads of different tokens are in flight
-  // together (H % 8 == 0 and f0 a multiple of 8 make every item 16-byte aligned)
+  // the merge of every finished token's slice: (token, one 16-byte vector of features) items
+  // spread over the group (H % 8 == 0 and f0 a multiple of 8 keep every item aligned)
+  constexpr int N = Vec<T>::N;
   const int fend = min(f0 + fcount, d.H);
-  const int nvec = (fend - f0) >> 2;
+  const int nvec = (fend - f0) / N;
   const int total = nj * nvec;
-  constexpr int kU = 4;
-  for (int w0 = tid; w0 < total; w0 += kU * nthr) {
-    const float* src[kU];
-    int slot[kU], f[kU];
-    bool act[kU];
-    float4 a[kU];
-#pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      const int w = w0 + u * nthr;
-      const int j = w < total ? w / nvec : 0;
-      act[u] = w < total && fin[j];
-      slot[u] = act[u] ? slots[j] : 0;
-      f[u] = f0 + 4 * (w - j * nvec);
-      src[u] = L.slotbuf + (size_t)slot[u] * d.KS * d.H + f[u];
-      if (act[u]) a[u] = __ldcg(reinterpret_cast<const float4*>(src[u]));
-    }
-#pragma unroll 4
-    for (int k = 1; k < d.KS; ++k) {
-#pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        if (act[u]) {
-          const float4 b = __ldcg(reinterpret_cast<const float4*>(src[u] + (size_t)k * d.H));
-          a[u].x += b.x;
-          a[u].y += b.y;
-          a[u].z += b.z;
-          a[u].w += b.w;
-        }
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < kU; ++u) {
-      if (!act[u]) continue;
-      store4<T>(reinterpret_cast<T*>(L.y) + (size_t)slot[u] * d.H + f[u], a[u]);
-      if (sd)                                        // req_n is stable until the last slice
-        store4<T>(static_cast<T*>(sd->hist) + ((size_t)slot[u] * (sd->n_max + 1) + sd->req_n[slot[u]] + 1) * d.H + f[u],
-                  a[u]);
-    }
+  const T* rows = static_cast<const T*>(L.slotbuf);
+  for (int w = tid; w < total; w += nthr) {
+    const int j = w / nvec;
+    if (!fin[j]) continue;
+    const int slot = slots[j];
+    const int f = f0 + N * (w - j * nvec);
+    float a[N];
+    merge_vec<T>(rows + (size_t)slot * d.KS * d.H + f, L.wtab + (size_t)slot * d.KS, d.KS, d.H, a);
+    const uint4 o = pack16<T>(a);
+    *reinterpret_cast<uint4*>(static_cast<T*>(L.y) + (size_t)slot * d.H + f) = o;
+    if (sd)                                          // req_n is stable until the last slice
+      *reinterpret_cast<uint4*>(static_cast<T*>(sd->hist) + ((size_t)slot * (sd->n_max + 1) + sd->req_n[slot] + 1) * d.H + f) = o;
   }
   __threadfence();
   bar();
@@ -487,42 +514,18 @@ __device__ void land_only(const LayerView& L, const Dims& d, DevCounters* C, con
   bar();
 }
 
-// The merge of one ready token, y = sum_k slotbuf[slot][k] in ascending k (fp32, stored in the
-// output dtype with round-to-nearest), by `nthr` threads: 4 features per thread at a time.
+// The merge of one ready token, y = sum_k w_k * slotbuf[slot][k] in ascending k (fp32, stored
+// in the output dtype with round-to-nearest), by `nthr` threads: one 16-byte vector each at a time.
 template <typename T>
 __device__ __forceinline__ void merge_row(const LayerView& L, const Dims& d, int slot, T* __restrict__ y,
                                           int tid, int nthr) {
-  const float* src = L.slotbuf + (size_t)slot * d.KS * d.H;
-  for (int f = 4 * tid; f < d.H; f += 4 * nthr) {
-    float4 a = __ldcg(reinterpret_cast<const float4*>(src + f));
-    int k = 1;
-    for (; k + 8 <= d.KS; k += 8) {          // eight loads in flight, then the adds in k order
-      float4 b[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) b[u] = __ldcg(reinterpret_cast<const float4*>(src + (size_t)(k + u) * d.H + f));
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        a.x += b[u].x;
-        a.y += b[u].y;
-        a.z += b[u].z;
-        a.w += b[u].w;
-      }
-    }
-    float4 b[7];
-    const int rest = d.KS - k;               // < 8
-#pragma unroll
-    for (int u = 0; u < 7; ++u)
-      if (u < rest) b[u] = __ldcg(reinterpret_cast<const float4*>(src + (size_t)(k + u) * d.H + f));
-#pragma unroll
-    for (int u = 0; u < 7; ++u) {
-      if (u < rest) {
-        a.x += b[u].x;
-        a.y += b[u].y;
-        a.z += b[u].z;
-        a.w += b[u].w;
-      }
-    }
-    store4<T>(y + f, a);
+  constexpr int N = Vec<T>::N;
+  const T* src = static_cast<const T*>(L.slotbuf) + (size_t)slot * d.KS * d.H;
+  const float* wk = L.wtab + (size_t)slot * d.KS;
+  for (int f = N * tid; f < d.H; f += N * nthr) {
+    float a[N];
+    merge_vec<T>(src + f, wk, d.KS, d.H, a);
+    *reinterpret_cast<uint4*>(y + f) = pack16<T>(a);
   }
 }
 

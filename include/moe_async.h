@@ -125,9 +125,9 @@ typedef struct {
 typedef enum {
   MOE_KERNEL_ENQUEUE = 0,    /* Receptor: pairs into buckets, token rows into the pool          */
   MOE_KERNEL_SCHEDULE = 1,   /* device-side policy + work list                                  */
-  MOE_KERNEL_FFN1 = 2,       /* gather + GEMM1 (gate/up) + SwiGLU   (identity: scatter + merge) */
-  MOE_KERNEL_FFN2 = 3,       /* GEMM2 (down) + weighted scatter + readiness + merge             */
-  MOE_KERNEL_COLLECT = 4,    /* ready rows to the caller + slot reclaim                         */
+  MOE_KERNEL_FFN1 = 2,       /* gather + GEMM1 (gate/up) + SwiGLU   (identity: scatter)         */
+  MOE_KERNEL_FFN2 = 3,       /* GEMM2 (down) + scatter of the results + readiness               */
+  MOE_KERNEL_COLLECT = 4,    /* top-k merge of ready tokens, rows to the caller, slot reclaim   */
   MOE_KERNEL_KINDS = 5
 } moe_kernel_kind;
 
@@ -178,9 +178,10 @@ moe_status moe_async_enqueue(moe_async_t h, int32_t layer, int32_t n,
 /* One scheduling step of layer `layer`, decided on the device from the bucket depths
  * (no host synchronisation): the policy picks buckets, each picked bucket is drained whole,
  * its tokens are gathered and run through the expert (grouped GEMM over all picks), the
- * weighted results are written to their combine slots, and every token whose K (+shared)
- * results are now complete is combined (y = sum in ascending k) and appended to the ready
- * list.  A step with nothing to pick launches kernels that exit at once. */
+ * results E_k(x) are written to their combine slots in the activation dtype, and every
+ * token whose K (+shared) results are now complete is appended to the ready list (its
+ * merge runs in moe_async_collect).  A step with nothing to pick launches kernels that exit
+ * at once. */
 moe_status moe_async_schedule_step(moe_async_t h, int32_t layer, const moe_async_policy* policy,
                                    void* stream);
 
@@ -200,7 +201,9 @@ moe_status moe_async_schedule_step(moe_async_t h, int32_t layer, const moe_async
 moe_status moe_async_schedule_steps(moe_async_t h, int32_t layer, const moe_async_policy* policy,
                                     int32_t max_steps, void* stream);
 
-/* Collect ready tokens of layer `layer` in completion order:
+/* Collect ready tokens of layer `layer` in completion order, each merged on the way out:
+ * y = sum_k w_k E_k(x) in fp32, ascending k (k = K is the shared expert, weight 1), each
+ * product and sum rounded (no fused multiply-add), stored in the cfg dtype:
  *   d_y_out    : [max_out, H] cfg dtype     d_slot_out : [max_out] int32
  *   d_gen_out  : [max_out] uint32 (generation the result belongs to; may be NULL)
  *   d_step_out : [max_out] uint32 (emission step: the scheduling step, counted from 1 over
