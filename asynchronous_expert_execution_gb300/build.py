@@ -25,6 +25,9 @@ VARIANTS = {"release": (LIB, []), "debug": (LIB_DEBUG, ["-DMOE_DEBUG_BOUNDS=1"])
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
               "--expt-relaxed-constexpr", "-I", INCLUDE]
+# The tcgen05 kernel must not spill: it holds an SM's whole register file, and a build of a
+# variant that spilled faulted on the GPU.  ptxas turns a spill into a build error.
+FILE_FLAGS = {"moe_ffn_tc.cu": ["-Xptxas", "--warn-on-spills,--warning-as-error"]}
 
 
 def _nvcc():
@@ -60,7 +63,8 @@ def build(force=False, verbose=False, variants=("release", "debug")):
         objs[v] = []
         for src in sources():
             obj = os.path.join(bdir, os.path.basename(src)[:-3] + ".o")
-            cmd = [nvcc, *ARCH, *NVCC_FLAGS, *VARIANTS[v][1], "-c", src, "-o", obj]
+            cmd = [nvcc, *ARCH, *NVCC_FLAGS, *FILE_FLAGS.get(os.path.basename(src), []), *VARIANTS[v][1],
+                   "-c", src, "-o", obj]
             if verbose:
                 print(" ".join(cmd), file=sys.stderr)
             procs.append((src, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)))
