@@ -18,14 +18,14 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID", 2: "MOE_ERR_CAPACITY", 3: "MO
                 8: "MOE_ERR_BOUNDS"}
 
 # every symbol include/moe_async.h declares
-EXPORTS = ("moe_async_create", "moe_async_route", "moe_async_enqueue", "moe_async_schedule_step",
+EXPORTS = ("moe_async_create", "moe_async_route", "moe_async_enqueue", "moe_async_schedule_step", "moe_async_tick",
            "moe_async_schedule_steps", "moe_async_collect", "moe_async_wait", "moe_async_sync", "moe_async_get_stats",
            "moe_async_get_trace", "moe_async_snapshot", "moe_async_destroy",
            "moe_async_status_string", "moe_async_profile", "moe_async_profile_read",
            "moe_async_stream_setup", "moe_async_stream_run", "moe_async_stream_trace", "moe_async_stream_stats",
            "moe_async_cancel", "moe_async_debug_append_record")
 
-KERNEL_KINDS = ("enqueue", "schedule", "ffn1", "ffn2", "collect")
+KERNEL_KINDS = ("enqueue", "schedule", "ffn1", "ffn2", "collect", "tick")
 
 
 class Config(ctypes.Structure):
@@ -88,6 +88,8 @@ def load():
         "moe_async_schedule_step": [P, I32, ctypes.POINTER(Policy), P],
         "moe_async_schedule_steps": [P, I32, ctypes.POINTER(Policy), I32, P],
         "moe_async_collect": [P, I32, I32, P, I32P, U32P, U32P, I32P, I32, P],
+        "moe_async_tick": [P, I32, I32, I32P, I32P, P, I32P, F32P, U32P, U32P, ctypes.POINTER(Policy), I32, P, I32P,
+                           U32P, U32P, I32P, I32, P],
         "moe_async_wait": [P, I32, ctypes.POINTER(Policy), I32, I32, P],
         "moe_async_sync": [P, P],
         "moe_async_get_stats": [P, P, ctypes.POINTER(Stats)],

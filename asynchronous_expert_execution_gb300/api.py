@@ -114,6 +114,26 @@ class MoEAsync:
                                         _ptr(step_out), _ptr(n_out), int(append), _stream(stream))
         N.check(st, "moe_async_collect")
 
+    def tick(self, layer, policy, x=None, expert=None, w=None, n=None, rows=None, slots=None, kmask=None, gen=None,
+             y_out=None, slot_out=None, n_out=None, gen_out=None, step_out=None, append=False, max_out=None,
+             stream=None):
+        """One serving tick in one control launch: collect what was ready (into y_out ..
+        n_out, as `collect`; no outputs collects nothing), enqueue a wave (as `enqueue`; no x
+        enqueues nothing), then one scheduling step under `policy`."""
+        if x is None:
+            n = 0
+        else:
+            n = (rows.shape[0] if rows is not None else x.shape[0]) if n is None else n
+        if y_out is None:
+            max_out = 0
+        else:
+            max_out = y_out.shape[0] if max_out is None else max_out
+        p = policy.c()
+        st = self.lib.moe_async_tick(self.h, layer, n, _ptr(rows), _ptr(slots), _ptr(x), _ptr(expert), _ptr(w),
+                                     _ptr(kmask), _ptr(gen), ctypes.byref(p), max_out, _ptr(y_out), _ptr(slot_out),
+                                     _ptr(gen_out), _ptr(step_out), _ptr(n_out), int(append), _stream(stream))
+        N.check(st, "moe_async_tick")
+
     def cancel(self, layer, slots, stream=None):
         """Retire the current request of each slot (int32 device tensor of slot ids)."""
         N.check(self.lib.moe_async_cancel(self.h, layer, slots.numel(), _ptr(slots), _stream(stream)),

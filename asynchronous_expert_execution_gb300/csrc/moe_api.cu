@@ -81,19 +81,14 @@ constexpr int kCopyDepth = 16;         // 16-byte loads in flight per lane in th
 // warp-aggregated atomics: lanes bound for the same bucket elect a leader that reserves all
 // of their positions with one atomicAdd on the bucket tail.
 
+// The Receptor's work for warp `gw` of `nwarps` (whole tokens, `tpw` a warp at a time).
 template <typename T>
-__global__ void enqueue_kernel(LayerView L, Dims d, DevCounters* C, int n, int tpw,
-                               const int32_t* __restrict__ rows, const int32_t* __restrict__ slots,
-                               const T* __restrict__ x, const int32_t* __restrict__ expert,
-                               const float* __restrict__ w, const uint32_t* __restrict__ kmask,
-                               const uint32_t* __restrict__ gens) {
+__device__ __forceinline__ void enqueue_warps(const LayerView& L, const Dims& d, DevCounters* C, int n, int tpw,
+                                              const int32_t* __restrict__ rows, const int32_t* __restrict__ slots,
+                                              const T* __restrict__ x, const int32_t* __restrict__ expert,
+                                              const float* __restrict__ w, const uint32_t* __restrict__ kmask,
+                                              const uint32_t* __restrict__ gens, long long gw, long long nwarps) {
   const int lane = threadIdx.x & 31;
-  // launched as a programmatic dependent of the kernel before it (e.g. the previous collect):
-  // wait for it, then let the scheduler start; the scheduler waits for this kernel
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const long long nwarps = (long long)gridDim.x * (blockDim.x >> 5);
-  const long long gw = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int jl = lane / d.KS;              // this lane's token within the warp's group
   const int k = lane % d.KS;
   const uint32_t kbits = (1u << d.KS) - 1u;  // KS <= 31
@@ -173,6 +168,21 @@ __global__ void enqueue_kernel(LayerView L, Dims d, DevCounters* C, int n, int t
   }
 }
 
+template <typename T>
+__global__ void enqueue_kernel(LayerView L, Dims d, DevCounters* C, int n, int tpw,
+                               const int32_t* __restrict__ rows, const int32_t* __restrict__ slots,
+                               const T* __restrict__ x, const int32_t* __restrict__ expert,
+                               const float* __restrict__ w, const uint32_t* __restrict__ kmask,
+                               const uint32_t* __restrict__ gens) {
+  // launched as a programmatic dependent of the kernel before it (e.g. the previous collect):
+  // wait for it, then let the scheduler start; the scheduler waits for this kernel
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const long long nwarps = (long long)gridDim.x * (blockDim.x >> 5);
+  const long long gw = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  enqueue_warps<T>(L, d, C, n, tpw, rows, slots, x, expert, w, kmask, gens, gw, nwarps);
+}
+
 // -------------------------------------------------------------- scheduler
 __global__ void __launch_bounds__(1024) schedule_kernel(LayerView L, Dims d, StepPlan* P,
                                                         DevCounters* C, moe_async_policy pol,
@@ -236,6 +246,86 @@ __global__ void collect_kernel(LayerView L, Dims d, DevCounters* C, int max_out,
   }
 }
 
+// ------------------------------------------------------------------ tick
+// One scheduling tick of a layer in one launch (moe_async_tick).  Blocks [0, n_enq) run the
+// Receptor on the arriving wave; the others merge and copy out the tokens that were ready
+// when the call was made (as collect_kernel does, with the same outputs).  The block that
+// finishes last -- once every pair of the wave is accepted or rejected and every collected
+// row has been read -- reclaims the collected slots, advances the ready ring and plans the
+// step (plan_layer), so the FFN kernels launched after it run that step.
+// Threads a block (the planner runs on one block of these).  Measured on GB300 against the
+// same ticks as three calls (pairs/s, DeepSeek-wide layer / Zipf prefill): 128 -- 3.62 M /
+// 4.69 M; 256 -- 3.67 M / 4.71 M; 512 -- 3.70 M / 4.71 M; three calls 3.71 M / 4.76 M.  The
+// control work of a tick is the same; what the single launch saves is host-side launches.
+#ifndef MOE_TICK_THREADS
+#define MOE_TICK_THREADS 512
+#endif
+constexpr int kTickThreads = MOE_TICK_THREADS;
+
+template <typename T>
+__global__ void __launch_bounds__(kTickThreads) tick_kernel(
+    LayerView L, Dims d, DevCounters* C, StepPlan* P, moe_async_policy pol, TileGeom g, int layer,
+    int trace_cap, int4* trace, long long weight_bytes_per_run,
+    int n, int tpw, int n_enq, const int32_t* __restrict__ rows, const int32_t* __restrict__ slots,
+    const T* __restrict__ x, const int32_t* __restrict__ expert, const float* __restrict__ w,
+    const uint32_t* __restrict__ kmask, const uint32_t* __restrict__ gens,
+    int max_out, T* __restrict__ y_out, int32_t* __restrict__ slot_out, uint32_t* __restrict__ gen_out,
+    uint32_t* __restrict__ step_out, int32_t* __restrict__ n_io, int append, int parts) {
+  __shared__ PlanScratch sc;
+  __shared__ int last;
+  // a programmatic dependent of the previous step's GEMM2: wait for it, then let GEMM1 start
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const uint32_t rh = L.ready_ht[0], rt = L.ready_ht[1];
+  const int base = (max_out > 0 && append) ? *n_io : 0;
+  const int nc = max_out > 0 ? max(0, min((int)(rt - rh), max_out - base)) : 0;
+  if ((int)blockIdx.x < n_enq) {
+    const long long nwarps = (long long)n_enq * (blockDim.x >> 5);
+    const long long gw = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    enqueue_warps<T>(L, d, C, n, tpw, rows, slots, x, expert, w, kmask, gens, gw, nwarps);
+  } else {
+    const int cb = (int)blockIdx.x - n_enq, ncb = (int)gridDim.x - n_enq;
+    for (int i = cb; i < nc; i += ncb) {
+      const int slot = L.ready[(rh + (uint32_t)i) % (uint32_t)d.S];
+      if (kDebugBounds && (slot < 0 || slot >= d.S)) {           // bounds-checked build
+        if (threadIdx.x == 0) set_error(C, MOE_ERR_BOUNDS);
+        continue;
+      }
+      merge_row<T>(L, d, slot, y_out + (size_t)(base + i) * d.H, threadIdx.x, blockDim.x);
+      if (threadIdx.x == 0) {
+        slot_out[base + i] = slot;
+        if (gen_out) gen_out[base + i] = L.gen[slot];
+        if (step_out) step_out[base + i] = L.emit_step[slot];
+      }
+    }
+  }
+  // every thread's appends and reads are ordered before the block's arrival
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) last = atomicAdd(&L.ready_ht[2], 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  for (int i = threadIdx.x; i < nc; i += blockDim.x) {             // reclaim the collected slots
+    const int slot = L.ready[(rh + (uint32_t)i) % (uint32_t)d.S];
+    if (kDebugBounds && (slot < 0 || slot >= d.S)) continue;
+    for (int q = 0; q < parts; ++q) L.done_part[(size_t)slot * parts + q] = 0u;
+    L.enq_mask[slot] = 0u;
+    L.done[slot] = 0u;
+    L.landed[slot] = 0u;
+    L.emit_step[slot] = 0u;
+    L.gen[slot] = L.gen[slot] + 1u;
+  }
+  if (threadIdx.x == 0) {
+    L.ready_ht[2] = 0u;
+    L.ready_ht[0] = rh + (uint32_t)nc;
+    C->ready -= nc;
+    if (max_out > 0) *n_io = base + nc;
+  }
+  __syncthreads();
+  plan_layer(L, d, P, C, pol, g, layer, trace_cap, trace, weight_bytes_per_run, (int)C->steps + 1, true, sc, 1);
+}
+
 // ----------------------------------------------------------- cancellation
 // Retire the current request of each listed slot ("asynchronous MoE serving" notes: an
 // abandoned operation retires its buffer until a quiescent point; CascadeEP: readiness is
@@ -292,6 +382,32 @@ cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, cu
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+// Collect CTAs per SM (each merges whole tokens, 256 threads): fewer blocks end sooner (each
+// takes part in the last-block count); measured (collect ms per pass, Zipf prefill /
+// DeepSeek-wide layer): 8 -- 0.160 / 0.197, 4 -- 0.148 / 0.196, 2 -- 0.139 / 0.196, 1 --
+// 0.169 / 0.271.
+#ifndef MOE_COLLECT_CTAS_PER_SM
+#define MOE_COLLECT_CTAS_PER_SM 2
+#endif
+constexpr int kCollectCtasPerSm = MOE_COLLECT_CTAS_PER_SM;
+
+// Receptor tokens per warp: one while the wave fits in one round of 16 warps per SM (each warp
+// then copies one row), more for large waves; whole tokens per warp, tpw * KS <= 32.
+int enqueue_tpw(const moe_async_s* h, long long n) {
+  const int tpw_max = 32 / h->dims.KS;
+  const long long warps_one_round = (long long)h->num_sms * 16;
+  return (int)std::min<long long>(tpw_max, std::max<long long>(1, (n + warps_one_round - 1) / warps_one_round));
+}
+
+bool valid_policy(const moe_async_policy* policy, int max_steps) {
+  if (!policy || max_steps < 1) return false;
+  if (policy->kind != MOE_POLICY_MTFS && policy->kind != MOE_POLICY_THRESHOLD && policy->kind != MOE_POLICY_RANKS)
+    return false;
+  if (policy->max_groups < 0 || policy->min_batch < 0 || policy->fallback_groups < 0) return false;
+  if (policy->kind == MOE_POLICY_RANKS && policy->max_groups < 1) return false;
+  return true;
 }
 
 bool valid_stream_layer(moe_async_t h, int layer) {
@@ -554,11 +670,7 @@ moe_status moe_async_enqueue(moe_async_t h, int32_t layer, int32_t n, const int3
   if (reinterpret_cast<uintptr_t>(d_x) % 16) return MOE_ERR_INVALID;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const Dims& d = h->dims;
-  // tokens per warp: one while the wave fits in one round of 16 warps per SM (each warp then
-  // copies one row), more for large waves; whole tokens per warp, tpw * KS <= 32
-  const int tpw_max = 32 / d.KS;
-  const long long warps_one_round = (long long)h->num_sms * 16;
-  const int tpw = (int)std::min<long long>(tpw_max, std::max<long long>(1, (n + warps_one_round - 1) / warps_one_round));
+  const int tpw = enqueue_tpw(h, n);
   // two warps a block, so a wave of a few hundred tokens spreads over every SM
   const long long warps = (n + tpw - 1) / tpw;
   const int grid = (int)std::max<long long>(1, std::min<long long>((warps + 1) / 2, (long long)h->num_sms * 32));
@@ -575,13 +687,15 @@ moe_status moe_async_enqueue(moe_async_t h, int32_t layer, int32_t n, const int3
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
+static moe_status launch_ffn(moe_async_t h, int32_t layer, cudaStream_t s) {
+  if (h->cfg.expert_kind == MOE_EXPERT_IDENTITY) return launch_identity(h, layer, s);
+  if (h->use_tc) return launch_ffn_tc(h, layer, s);
+  return launch_ffn_simt(h, layer, s);
+}
+
 moe_status schedule_impl(moe_async_t h, int32_t layer, const moe_async_policy* policy, int32_t max_steps,
                          void* stream) {
-  if (!valid_stream_layer(h, layer) || !policy || max_steps < 1) return MOE_ERR_INVALID;
-  if (policy->kind != MOE_POLICY_MTFS && policy->kind != MOE_POLICY_THRESHOLD && policy->kind != MOE_POLICY_RANKS)
-    return MOE_ERR_INVALID;
-  if (policy->max_groups < 0 || policy->min_batch < 0 || policy->fallback_groups < 0) return MOE_ERR_INVALID;
-  if (policy->kind == MOE_POLICY_RANKS && policy->max_groups < 1) return MOE_ERR_INVALID;
+  if (!valid_stream_layer(h, layer) || !valid_policy(policy, max_steps)) return MOE_ERR_INVALID;
   if (policy->kind == MOE_POLICY_RANKS && max_steps > 1) return MOE_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const Dims& d = h->dims;
@@ -593,9 +707,7 @@ moe_status schedule_impl(moe_async_t h, int32_t layer, const moe_async_policy* p
                                          h->trace, wbytes, (int)max_steps);
   prof_end(h, MOE_KERNEL_SCHEDULE, s);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
-  if (h->cfg.expert_kind == MOE_EXPERT_IDENTITY) return launch_identity(h, layer, s);
-  if (h->use_tc) return launch_ffn_tc(h, layer, s);
-  return launch_ffn_simt(h, layer, s);
+  return launch_ffn(h, layer, s);
 }
 
 moe_status moe_async_schedule_step(moe_async_t h, int32_t layer, const moe_async_policy* policy,
@@ -608,6 +720,47 @@ moe_status moe_async_schedule_steps(moe_async_t h, int32_t layer, const moe_asyn
   return schedule_impl(h, layer, policy, max_steps, stream);
 }
 
+moe_status moe_async_tick(moe_async_t h, int32_t layer, int32_t n, const int32_t* d_rows, const int32_t* d_slot,
+                          const void* d_x, const int32_t* d_expert, const float* d_w, const uint32_t* d_kmask,
+                          const uint32_t* d_gen, const moe_async_policy* policy, int32_t max_out, void* d_y_out,
+                          int32_t* d_slot_out, uint32_t* d_gen_out, uint32_t* d_step_out, int32_t* d_n_out,
+                          int32_t append, void* stream) {
+  if (!valid_stream_layer(h, layer) || n < 0 || max_out < 0 || !valid_policy(policy, 1)) return MOE_ERR_INVALID;
+  if (n > 0 && (!d_x || !d_expert || !d_w || reinterpret_cast<uintptr_t>(d_x) % 16)) return MOE_ERR_INVALID;
+  if (max_out > 0 && (!d_y_out || !d_slot_out || !d_n_out || reinterpret_cast<uintptr_t>(d_y_out) % 16))
+    return MOE_ERR_INVALID;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const Dims& d = h->dims;
+  const int tpw = n > 0 ? enqueue_tpw(h, n) : 1;
+  const long long warps = n > 0 ? ((long long)n + tpw - 1) / tpw : 0;
+  const int per_block = kTickThreads / 32;
+  const int n_enq = (int)std::min<long long>((warps + per_block - 1) / per_block, (long long)h->num_sms * 8);
+  // every block resident at once (512 threads an SM): the last one to finish plans the step,
+  // so a second round of blocks would delay it
+  const int resident = h->num_sms * (512 / kTickThreads);
+  const int n_col = max_out > 0 ? std::max(1, std::min(max_out, resident - n_enq)) : 0;
+  const int grid = std::max(1, n_enq + n_col);
+  const long long wbytes = h->cfg.expert_kind == MOE_EXPERT_SWIGLU
+                               ? 3ll * d.H * d.I * (long long)elem_size(d.dtype) : 0ll;
+  prof_begin(h, MOE_KERNEL_TICK, s);
+  cudaError_t e;
+  if (d.dtype == MOE_BF16)
+    e = launch_dependent(tick_kernel<__nv_bfloat16>, dim3(grid), dim3(kTickThreads), s, h->layers[layer], d,
+                         h->counters, h->plan, *policy, h->geom, (int)layer, (int)h->cfg.trace_capacity, h->trace,
+                         wbytes, (int)n, tpw, n_enq, d_rows, d_slot, static_cast<const __nv_bfloat16*>(d_x), d_expert,
+                         d_w, d_kmask, d_gen, (int)max_out, static_cast<__nv_bfloat16*>(d_y_out), d_slot_out, d_gen_out,
+                         d_step_out, d_n_out, (int)append, h->parts_per_pair);
+  else
+    e = launch_dependent(tick_kernel<float>, dim3(grid), dim3(kTickThreads), s, h->layers[layer], d, h->counters,
+                         h->plan, *policy, h->geom, (int)layer, (int)h->cfg.trace_capacity, h->trace, wbytes, (int)n,
+                         tpw, n_enq, d_rows, d_slot, static_cast<const float*>(d_x), d_expert, d_w, d_kmask, d_gen,
+                         (int)max_out, static_cast<float*>(d_y_out), d_slot_out, d_gen_out, d_step_out, d_n_out,
+                         (int)append, h->parts_per_pair);
+  prof_end(h, MOE_KERNEL_TICK, s);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  return launch_ffn(h, layer, s);
+}
+
 moe_status moe_async_collect(moe_async_t h, int32_t layer, int32_t max_out, void* d_y_out,
                              int32_t* d_slot_out, uint32_t* d_gen_out, uint32_t* d_step_out,
                              int32_t* d_n_out, int32_t append, void* stream) {
@@ -616,13 +769,7 @@ moe_status moe_async_collect(moe_async_t h, int32_t layer, int32_t max_out, void
   if (reinterpret_cast<uintptr_t>(d_y_out) % 16) return MOE_ERR_INVALID;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const Dims& d = h->dims;
-  // CTAs per SM (each merges whole tokens, 256 threads): fewer blocks end sooner (each takes
-  // part in the last-block count); measured (collect ms per pass, Zipf prefill / DeepSeek-wide
-  // layer): 8 -- 0.160 / 0.197, 4 -- 0.148 / 0.196, 2 -- 0.139 / 0.196, 1 -- 0.169 / 0.271
-#ifndef MOE_COLLECT_CTAS_PER_SM
-#define MOE_COLLECT_CTAS_PER_SM 2
-#endif
-  const int grid = std::max(1, std::min(max_out, h->num_sms * MOE_COLLECT_CTAS_PER_SM));
+  const int grid = std::max(1, std::min(max_out, h->num_sms * kCollectCtasPerSm));
   prof_begin(h, MOE_KERNEL_COLLECT, s);
   cudaError_t e;
   if (d.dtype == MOE_BF16)

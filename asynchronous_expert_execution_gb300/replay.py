@@ -41,24 +41,42 @@ class LayerReplay:
         self.n_out = torch.zeros(1, dtype=torch.int32, device=device)
         self.tick_counts = torch.zeros(4096, dtype=torch.int32, device=device)
 
-    def run_ticks(self, x, idx, w, policy, stream=None, collect_each_step=True):
+    def run_ticks(self, x, idx, w, policy, stream=None, collect_each_step=True, fused=False):
         """Deliver every wave on its tick and run one scheduling step per tick, up to the
-        last arrival tick.  No host synchronisation."""
+        last arrival tick.  No host synchronisation.
+
+        fused: one ``moe_async_tick`` a tick (collect of what the previous steps made ready,
+        the tick's last wave, the step); earlier waves of the same tick are enqueued first, and
+        a collect after the last tick takes that step's tokens."""
         moe, L = self.moe, self.layer
         self.n_out.zero_()
         nxt = 0
         for tick in range(1, self.last_tick + 1):
+            due = []
             while nxt < len(self.waves) and self.waves[nxt].tick <= tick:
-                moe.enqueue(L, x, idx, w, rows=self.rows[nxt], kmask=self.kmask[nxt], stream=stream)
+                due.append(nxt)
                 nxt += 1
+            if fused:
+                for i in due[:-1]:
+                    moe.enqueue(L, x, idx, w, rows=self.rows[i], kmask=self.kmask[i], stream=stream)
+                wave = dict(x=x, expert=idx, w=w, rows=self.rows[due[-1]], kmask=self.kmask[due[-1]]) if due else {}
+                moe.tick(L, policy, y_out=self.y_out, slot_out=self.slot_out, n_out=self.n_out, append=True,
+                         step_out=self.step_out, stream=stream, **wave)
+                if tick >= 2:                    # the tokens of steps up to tick - 1
+                    self.tick_counts[tick - 2:tick - 1].copy_(self.n_out)
+                continue
+            for i in due:
+                moe.enqueue(L, x, idx, w, rows=self.rows[i], kmask=self.kmask[i], stream=stream)
             moe.schedule_step(L, policy, stream=stream)
             if collect_each_step:
                 moe.collect(L, self.y_out, self.slot_out, self.n_out, append=True, stream=stream,
                             step_out=self.step_out)
                 self.tick_counts[tick - 1:tick].copy_(self.n_out)
-        if not collect_each_step:
+        if fused or not collect_each_step:
             moe.collect(L, self.y_out, self.slot_out, self.n_out, append=True, stream=stream,
                         step_out=self.step_out)
+            if self.last_tick >= 1:
+                self.tick_counts[self.last_tick - 1:self.last_tick].copy_(self.n_out)
         self.ticks_run = self.last_tick
 
     def drain(self, policy, max_steps=10000, check_every=8, stream=None):

@@ -53,6 +53,8 @@ def parse(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--fused-tick", action="store_true",
+                    help="drive each tick with one moe_async_tick instead of enqueue, schedule_step and collect")
     ap.add_argument("--policy", default="mtfs", choices=["mtfs", "flfs", "defrag", "barrier", "defrag_src"],
                     help="layer-level policy of the streaming workloads (c5, s1)")
     ap.add_argument("--defrag-window", type=int, default=2)
@@ -247,10 +249,15 @@ def build_inputs(spec, seed, dev):
 
 
 class Pass:
-    """One full pass of the hot path over the batch (route, waves, steps, drain, collect)."""
+    """One full pass of the hot path over the batch (route, waves, steps, drain, collect).
 
-    def __init__(self, pkg, spec, moe, waves, dev):
+    Each tick: enqueue the tick's waves, one scheduling step, collect what is ready.  fused:
+    one ``moe_async_tick`` a tick instead -- the collect of what earlier steps made ready, the
+    tick's wave and the step in one control launch, then the step's FFN launches."""
+
+    def __init__(self, pkg, spec, moe, waves, dev, fused=False):
         self.pkg, self.spec, self.moe = pkg, spec, moe
+        self.fused = fused
         self.waves = sorted(waves, key=lambda w: w.tick)
         self.rows = [torch.as_tensor(np.asarray(w.tokens, dtype=np.int32), device=dev) for w in self.waves]
         T, L = spec.tokens, spec.layer
@@ -269,9 +276,18 @@ class Pass:
         self.n.zero_()
         nxt = 0
         for tick in range(1, self.last_tick + 1):
+            due = []
             while nxt < len(self.waves) and self.waves[nxt].tick <= tick:
-                moe.enqueue(0, x, self.idx, self.w, rows=self.rows[nxt])
+                due.append(nxt)
                 nxt += 1
+            if self.fused:
+                for i in due[:-1]:
+                    moe.enqueue(0, x, self.idx, self.w, rows=self.rows[i])
+                wave = dict(x=x, expert=self.idx, w=self.w, rows=self.rows[due[-1]]) if due else {}
+                moe.tick(0, self.policy, y_out=self.y, slot_out=self.slots, n_out=self.n, append=True, **wave)
+                continue
+            for i in due:
+                moe.enqueue(0, x, self.idx, self.w, rows=self.rows[i])
             moe.schedule_step(0, self.policy)
             moe.collect(0, self.y, self.slots, self.n, append=True)
         if self.drains:
@@ -279,6 +295,7 @@ class Pass:
             # moe_async_wait runs the remaining steps as one device plan (MTFS / threshold)
             st = moe.wait(0, self.policy, max_steps=100000, check_every=32)
             assert st == 0, st
+        if self.drains or self.fused:
             moe.collect(0, self.y, self.slots, self.n, append=True)
 
 
@@ -377,7 +394,7 @@ def measure_layer(args, pkg, spec, dev, rank, world, steps, warmup, e2e_steps, w
         cpu_in = (tokens, host_weights(ws, need, L.has_shared))
     del ws
     torch.cuda.empty_cache()
-    run = Pass(pkg, spec, moe, waves, dev)
+    run = Pass(pkg, spec, moe, waves, dev, fused=args.fused_tick)
 
     def barrier():
         torch.cuda.synchronize()
@@ -492,6 +509,8 @@ def measure_layer(args, pkg, spec, dev, rank, world, steps, warmup, e2e_steps, w
                        "top_k": L.top_k, "hidden": H, "inter": I, "tokens": spec.tokens,
                        "waves": spec.num_waves, "ticks": run_ticks(waves), "policy": policy_name(spec),
                        "routed_pairs_per_step": routed_pairs_step,
+                       "ticks_driven_by": "moe_async_tick" if args.fused_tick
+                       else "moe_async_enqueue + moe_async_schedule_step + moe_async_collect",
                        "l2": "inputs larger than L2: every step streams the scheduled experts' "
                              f"weights ({wbytes_step / 1e9:.1f} GB) through HBM"},
             "roofline": roof, "path_roofline": path, "cpu_baseline": cpu, "e2e": e2e,

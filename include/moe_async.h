@@ -128,7 +128,8 @@ typedef enum {
   MOE_KERNEL_FFN1 = 2,       /* gather + GEMM1 (gate/up) + SwiGLU   (identity: scatter)         */
   MOE_KERNEL_FFN2 = 3,       /* GEMM2 (down) + scatter of the results + readiness               */
   MOE_KERNEL_COLLECT = 4,    /* top-k merge of ready tokens, rows to the caller, slot reclaim   */
-  MOE_KERNEL_KINDS = 5
+  MOE_KERNEL_TICK = 5,       /* moe_async_tick's control kernel: collect + Receptor + plan      */
+  MOE_KERNEL_KINDS = 6
 } moe_kernel_kind;
 
 /* Create a handle.  Weights are given per layer as arrays of L device pointers:
@@ -200,6 +201,27 @@ moe_status moe_async_schedule_step(moe_async_t h, int32_t layer, const moe_async
  * synchronisation. */
 moe_status moe_async_schedule_steps(moe_async_t h, int32_t layer, const moe_async_policy* policy,
                                     int32_t max_steps, void* stream);
+
+/* One tick of a serving loop in one control launch plus the step's FFN launches: the
+ * collect of the tokens that were ready when the call was made (outputs as moe_async_collect,
+ * with max_out, d_y_out .. d_n_out and append meaning the same; max_out = 0 collects nothing and
+ * d_n_out may then be NULL), the Receptor for a wave of n arriving tokens (arguments as
+ * moe_async_enqueue; n = 0 for none), then one scheduling step under `policy` (as
+ * moe_async_schedule_step).  StreamEP section 3 (the Receptor feeds the per-expert queues,
+ * ready tokens leave after their K results) and section 4 (the scheduler then picks).
+ *   Equivalent to moe_async_collect, moe_async_enqueue and moe_async_schedule_step in that
+ * order, with one difference: the collected slots are reclaimed after the wave's pairs have
+ * been judged, so a pair of this wave for a slot collected by this call is judged against the
+ * request it completed (a duplicate) rather than against the slot's next generation.  A
+ * caller learns which slots are free only from a collect's outputs, so it never assigns a new
+ * request to a slot collected by the same call.
+ *   Asynchronous, no host synchronisation.  Errors as the three calls; MOE_ERR_INVALID for a
+ * bad argument of any of them. */
+moe_status moe_async_tick(moe_async_t h, int32_t layer, int32_t n, const int32_t* d_rows, const int32_t* d_slot,
+                          const void* d_x, const int32_t* d_expert, const float* d_w, const uint32_t* d_kmask,
+                          const uint32_t* d_gen, const moe_async_policy* policy, int32_t max_out, void* d_y_out,
+                          int32_t* d_slot_out, uint32_t* d_gen_out, uint32_t* d_step_out, int32_t* d_n_out,
+                          int32_t append, void* stream);
 
 /* Collect ready tokens of layer `layer` in completion order, each merged on the way out:
  * y = sum_k w_k E_k(x) in fp32, ascending k (k = K is the shared expert, weight 1), each

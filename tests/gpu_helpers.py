@@ -37,13 +37,14 @@ def oracle_policy(spec):
 
 
 def gpu_layer(pkg, spec, wl, waves=None, dev="cuda", expert_kind="swiglu", x=None, idx=None, w=None,
-              trace_capacity=65536, max_drain=20000, weights_dev=None, drain="steps"):
+              trace_capacity=65536, max_drain=20000, weights_dev=None, drain="steps", fused=False):
     """Run one layer of `wl` through the library; returns a dict of host results.
 
     drain = "steps": after the last arrival, single steps each followed by a collect (the
     emission step of every token is also derived on the host from the per-step counts and
     must equal the device's); "wait": ``moe_async_wait`` then one collect, as the benchmark
-    drains (one device plan of the remaining steps under MTFS / THRESHOLD)."""
+    drains (one device plan of the remaining steps under MTFS / THRESHOLD).  fused: one
+    ``moe_async_tick`` a tick instead of enqueue, schedule_step and collect."""
     L = spec.layer
     waves = wl.waves if waves is None else waves
     dt = wl.x.dtype
@@ -59,7 +60,7 @@ def gpu_layer(pkg, spec, wl, waves=None, dev="cuda", expert_kind="swiglu", x=Non
         idx, w = idx.to(dev).contiguous(), w.to(dev).contiguous()
     rep = pkg.LayerReplay(moe, waves, spec.tokens, device=dev, idx_host=idx.cpu().numpy())
     pol = pkg.Policy.from_spec(spec)
-    rep.run_ticks(xd, idx, w, pol)
+    rep.run_ticks(xd, idx, w, pol, fused=fused)
     if drain == "wait":
         drained = 0 if rep.finish(pol, max_steps=max_drain) == 0 else -1
         slots, y, _ = rep.results()
