@@ -26,9 +26,10 @@ def pkg():
     return p
 
 
-@pytest.mark.parametrize("dtype,kind,shared", [("bf16", "swiglu", False), ("bf16", "swiglu", True),
-                                               ("f32", "swiglu", False), ("f32", "identity", False)])
-def test_planted_out_of_range_records_are_rejected(pkg, dtype, kind, shared):
+@pytest.mark.parametrize("dtype,kind,shared,via", [("bf16", "swiglu", False, "step"), ("bf16", "swiglu", True, "step"),
+                                                   ("f32", "swiglu", False, "step"), ("f32", "identity", False, "step"),
+                                                   ("bf16", "swiglu", True, "tick")])
+def test_planted_out_of_range_records_are_rejected(pkg, dtype, kind, shared, via):
     from asynchronous_expert_execution_gb300 import _native as N
     T, E, K, H, I = 48, 8, 2, 136, 80
     spec = WorkloadSpec(name="bounds", layer=LayerSpec(E, K, H, I, dtype, has_shared=shared, shared_inter=I),
@@ -46,7 +47,10 @@ def test_planted_out_of_range_records_are_rejected(pkg, dtype, kind, shared):
            ((1 << 25) << 5) | 1]          # slot far beyond (still a positive int32)
     for b, rec in zip((0, 3, E - 1), bad):
         N.check(moe.lib.moe_async_debug_append_record(moe.h, 0, b, rec, None), "append")
-    moe.schedule_step(0, pkg.Policy())
+    if via == "tick":                                              # the step from moe_async_tick
+        moe.tick(0, pkg.Policy())
+    else:
+        moe.schedule_step(0, pkg.Policy())
     y = torch.empty((T, H), dtype=x.dtype, device="cuda")
     slots = torch.empty(T, dtype=torch.int32, device="cuda")
     n = torch.zeros(1, dtype=torch.int32, device="cuda")

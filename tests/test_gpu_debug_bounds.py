@@ -27,6 +27,8 @@ def test_bounds_checked_build_parity_and_rejection():
            "tests/test_gpu_parity.py::test_duplicate_wave_does_not_overwrite_pool",
            "tests/test_gpu_parity.py::test_cancel_withheld_request_then_reuse",
            "tests/test_gpu_split.py", "tests/test_gpu_wide.py",
+           "tests/test_gpu_tick.py::test_tick_equals_separate_calls",
+           "tests/test_gpu_tick.py::test_tick_duplicate_of_a_token_it_collects",
            "tests/test_gpu_stream.py::test_stream_small_parity"]
     out = subprocess.run(cmd, cwd=ROOT, env=env, capture_output=True, text=True, timeout=1200)
     assert out.returncode == 0, out.stdout[-4000:] + out.stderr[-2000:]
