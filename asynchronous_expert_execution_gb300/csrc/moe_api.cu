@@ -217,7 +217,7 @@ __global__ void collect_kernel(LayerView L, Dims d, DevCounters* C, int max_out,
       if (threadIdx.x == 0) set_error(C, MOE_ERR_BOUNDS);
       continue;
     }
-    // the top-k merge of the ready token: y = sum of its KS weighted results, ascending k
+    // the top-k merge of the ready token: y = sum_k w_k E_k(x) over its KS results, ascending k
     merge_row<T>(L, d, slot, y_out + (size_t)(base + i) * d.H, threadIdx.x, blockDim.x);
     for (int p = threadIdx.x; p < parts; p += blockDim.x) L.done_part[(size_t)slot * parts + p] = 0u;
     __syncthreads();

@@ -5,7 +5,8 @@
 // each drained whole, whose tokens form one contiguous batch (StreamEP section 3, step 4:
 // scattered inputs are reorganised into a contiguous batch before expert compute).  The
 // gather is fused into GEMM1's operand load (token rows read from the pool by the slot
-// stored in each queue record) and the weighted top-k merge into GEMM2's epilogue.
+// stored in each queue record); GEMM2's epilogue writes each result row E_k(x) and counts
+// the token's landings, and the top-k merge y = sum_k w_k E_k(x) runs in collect.
 #include "moe_internal.cuh"
 
 namespace moe {
