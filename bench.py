@@ -505,8 +505,10 @@ def measure_layer(args, pkg, spec, dev, rank, world, steps, warmup, e2e_steps, w
     H, I = L.hidden, L.inter
     es = 2 if L.dtype == "bf16" else 4
     # algorithmic bytes per step of each FFN kernel (weights as scheduled + activations)
+    # GEMM2: weights and h in; its bf16 result rows are an implementation cost, and y is
+    # written by collect's merge
     alg = {"ffn1": runs * 2 * H * I * es + pairs_p * (H + I) * es,
-           "ffn2": runs * H * I * es + pairs_p * I * es + spec.tokens * H * es}
+           "ffn2": runs * H * I * es + pairs_p * I * es}
     kern_ms = {k: prof[k][0] / steps for k in prof}
     dom = max(("ffn1", "ffn2"), key=lambda k: kern_ms[k])
     hbm, tf_burst, tf_sust, src = peaks()
