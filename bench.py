@@ -547,6 +547,10 @@ def measure_layer(args, pkg, spec, dev, rank, world, steps, warmup, e2e_steps, w
     barrier()
     assert moe.sync() == 0 and int(arr.n.item()) == spec.tokens
     assert sorted(arr.sh.tolist()) == list(range(spec.tokens))
+    # token by token (the completion order may differ), the host copies equal the outputs of
+    # the resident pass: the same picks and values
+    oa, ob = torch.argsort(arr.sh.long()), torch.argsort(run.slots.cpu().long())
+    assert torch.equal(arr.yh[oa], run.y.cpu()[ob]), "end-to-end pass differs from the resident pass"
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
