@@ -301,10 +301,11 @@ class Pass:
 
 class ArrivalPass:
     """One pass fed from host memory as the waves arrive (the end-to-end measurement): each
-    wave's token rows and router logits sit packed in pinned host buffers, as a transport
-    delivers them; a side stream copies every wave to the device ahead of need, and the tick
-    that delivers a wave waits for its copy, routes it and enqueues it (slot = token id).
-    The outputs are copied back after the last collect."""
+    wave's token rows sit packed in pinned host buffers, as a transport delivers them, and a
+    side stream copies every wave to the device ahead of need; the router logits of the batch
+    are copied and routed first (one launch, as in the resident pass); the tick that delivers
+    a wave waits for its rows and enqueues them (slot = token id).  The outputs are copied
+    back after the last collect."""
 
     def __init__(self, pkg, spec, moe, waves, x_host, logits_host, dev):
         self.pkg, self.spec, self.moe = pkg, spec, moe
@@ -312,7 +313,8 @@ class ArrivalPass:
         T, L = spec.tokens, spec.layer
         tok = [np.asarray(w.tokens, dtype=np.int64) for w in self.waves]
         self.xh = [x_host[torch.as_tensor(t)].contiguous().pin_memory() for t in tok]
-        self.lh = [logits_host[torch.as_tensor(t)].contiguous().pin_memory() for t in tok]
+        order = torch.as_tensor(np.concatenate(tok))
+        self.lh = logits_host[order].contiguous().pin_memory()      # arrival order, like xd
         self.off = np.concatenate([[0], np.cumsum([len(t) for t in tok])]).astype(np.int64)
         self.slot_w = [torch.as_tensor(t.astype(np.int32), device=dev) for t in tok]
         self.xd = torch.empty((T, L.hidden), dtype=x_host.dtype, device=dev)
@@ -331,7 +333,7 @@ class ArrivalPass:
         self.ready = [torch.cuda.Event() for _ in self.waves]
 
     def h2d_bytes(self):
-        return sum(t.numel() * t.element_size() for t in self.xh + self.lh)
+        return sum(t.numel() * t.element_size() for t in self.xh) + self.lh.numel() * self.lh.element_size()
 
     def d2h_bytes(self):
         return self.yh.numel() * self.yh.element_size() + self.sh.numel() * self.sh.element_size()
@@ -345,15 +347,15 @@ class ArrivalPass:
             for i in range(len(self.waves)):
                 a, b = int(self.off[i]), int(self.off[i + 1])
                 self.xd[a:b].copy_(self.xh[i], non_blocking=True)
-                self.ld[a:b].copy_(self.lh[i], non_blocking=True)
                 self.ready[i].record(cs)
+        self.ld.copy_(self.lh, non_blocking=True)
+        pkg.route(self.ld, K, self.idx, self.w)
         self.n.zero_()
         nxt = 0
         for tick in range(1, self.last_tick + 1):
             while nxt < len(self.waves) and self.waves[nxt].tick <= tick:
                 a, b = int(self.off[nxt]), int(self.off[nxt + 1])
                 main.wait_event(self.ready[nxt])
-                pkg.route(self.ld[a:b], K, self.idx[a:b], self.w[a:b])
                 moe.enqueue(0, self.xd[a:b], self.idx[a:b], self.w[a:b], slots=self.slot_w[nxt])
                 nxt += 1
             moe.schedule_step(0, self.policy)
@@ -562,8 +564,8 @@ def measure_layer(args, pkg, spec, dev, rank, world, steps, warmup, e2e_steps, w
     e2e_ms, e2e_value = aggregate(e0.elapsed_time(e1), routed_pairs_step, e2e_steps, world, dev)
     e2e = {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": arr.h2d_bytes(),
            "d2h_bytes_per_step": arr.d2h_bytes(), "steps": e2e_steps,
-           "copies": "each wave's rows and logits host to device on a side stream as it arrives; "
-                     "outputs device to host after the last collect"}
+           "copies": "router logits host to device first; each wave's token rows host to device on a "
+                     "side stream as it arrives; outputs device to host after the last collect"}
 
     cpu = None
     if cpu_in is not None:
