@@ -9,5 +9,5 @@ abstract's streamFFN).  The compute lives in ``libmoe_async.so`` (C ABI in
 ``include/moe_async.h``); this package is its thin binding.
 """
 from ._native import MoEError, load  # noqa: F401
-from .api import MoEAsync, Policy, route  # noqa: F401
+from .api import MoEAsync, Policy, host_writable, route  # noqa: F401
 from .replay import LayerReplay  # noqa: F401

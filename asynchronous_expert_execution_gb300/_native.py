@@ -21,7 +21,7 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID", 2: "MOE_ERR_CAPACITY", 3: "MO
 EXPORTS = ("moe_async_create", "moe_async_route", "moe_async_enqueue", "moe_async_schedule_step", "moe_async_tick",
            "moe_async_schedule_steps", "moe_async_collect", "moe_async_wait", "moe_async_sync", "moe_async_get_stats",
            "moe_async_get_trace", "moe_async_snapshot", "moe_async_destroy",
-           "moe_async_status_string", "moe_async_profile", "moe_async_profile_read",
+           "moe_async_status_string", "moe_async_host_writable", "moe_async_profile", "moe_async_profile_read",
            "moe_async_stream_setup", "moe_async_stream_run", "moe_async_stream_trace", "moe_async_stream_stats",
            "moe_async_cancel", "moe_async_debug_append_record")
 
@@ -102,6 +102,7 @@ def load():
         "moe_async_profile": [P, I32],
         "moe_async_profile_read": [P, P, ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int64), I32],
         "moe_async_status_string": [ctypes.c_int],
+        "moe_async_host_writable": [P, ctypes.c_int64],
         "moe_async_stream_setup": [P, ctypes.POINTER(StreamConfig), VPP, P, P, P, P, P, P, P],
         "moe_async_stream_stats": [P, P, ctypes.POINTER(StreamStats)],
         "moe_async_stream_run": [P, I32, I32, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32), P],

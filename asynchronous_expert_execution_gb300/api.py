@@ -42,6 +42,14 @@ class Policy:
         return Policy(spec.policy, spec.max_groups, spec.min_batch, spec.fallback_groups)
 
 
+def host_writable(t):
+    """True if the kernels can write the host tensor `t` directly (pinned host memory mapped
+    at the same address), so it can be a collect output."""
+    if t.is_cuda:
+        return False
+    return bool(N.load().moe_async_host_writable(ctypes.c_void_p(t.data_ptr()), t.numel() * t.element_size()))
+
+
 def route(logits, top_k, idx=None, w=None, stream=None):
     """Top-K router on the device: returns (idx int32 [T,K], w fp32 [T,K])."""
     lib = N.load()

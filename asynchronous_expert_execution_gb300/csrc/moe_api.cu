@@ -506,6 +506,23 @@ void prof_end(moe_async_s* h, int kind, cudaStream_t s) {
 
 extern "C" {
 
+int32_t moe_async_host_writable(const void* p, int64_t n) {
+  if (!p || n < 0) return 0;
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();                          // an unregistered pointer: clear, answer no
+    return 0;
+  }
+  if (a.type != cudaMemoryTypeHost || a.devicePointer != p) return 0;
+  cudaPointerAttributes b;                       // the last byte lies in the same allocation
+  if (n > 0 && (cudaPointerGetAttributes(&b, static_cast<const char*>(p) + (n - 1)) != cudaSuccess ||
+                b.type != cudaMemoryTypeHost)) {
+    cudaGetLastError();
+    return 0;
+  }
+  return 1;
+}
+
 const char* moe_async_status_string(moe_status s) {
   switch (s) {
     case MOE_OK: return "ok";

@@ -304,8 +304,9 @@ class ArrivalPass:
     wave's token rows sit packed in pinned host buffers, as a transport delivers them, and a
     side stream copies every wave to the device ahead of need; the router logits of the batch
     are copied and routed first (one launch, as in the resident pass); the tick that delivers
-    a wave waits for its rows and enqueues them (slot = token id).  The outputs are copied
-    back after the last collect."""
+    a wave waits for its rows and enqueues them (slot = token id).  The outputs go to pinned
+    host buffers: written there by collect itself when the kernels can address them (each
+    merged row crosses the link as it is produced), else copied back after the last collect."""
 
     def __init__(self, pkg, spec, moe, waves, x_host, logits_host, dev):
         self.pkg, self.spec, self.moe = pkg, spec, moe
@@ -331,6 +332,7 @@ class ArrivalPass:
         self.drains = self.policy.kind != "mtfs" or self.policy.max_groups > 0
         self.copy_stream = torch.cuda.Stream(device=dev)
         self.ready = [torch.cuda.Event() for _ in self.waves]
+        self.direct = pkg.host_writable(self.yh) and pkg.host_writable(self.sh)
 
     def h2d_bytes(self):
         return sum(t.numel() * t.element_size() for t in self.xh) + self.lh.numel() * self.lh.element_size()
@@ -351,6 +353,7 @@ class ArrivalPass:
         self.ld.copy_(self.lh, non_blocking=True)
         pkg.route(self.ld, K, self.idx, self.w)
         self.n.zero_()
+        y_out, s_out = (self.yh, self.sh) if self.direct else (self.y, self.slots)
         nxt = 0
         for tick in range(1, self.last_tick + 1):
             while nxt < len(self.waves) and self.waves[nxt].tick <= tick:
@@ -359,13 +362,14 @@ class ArrivalPass:
                 moe.enqueue(0, self.xd[a:b], self.idx[a:b], self.w[a:b], slots=self.slot_w[nxt])
                 nxt += 1
             moe.schedule_step(0, self.policy)
-            moe.collect(0, self.y, self.slots, self.n, append=True)
+            moe.collect(0, y_out, s_out, self.n, append=True)
         if self.drains:
             st = moe.wait(0, self.policy, max_steps=100000, check_every=32)
             assert st == 0, st
-            moe.collect(0, self.y, self.slots, self.n, append=True)
-        self.yh.copy_(self.y, non_blocking=True)
-        self.sh.copy_(self.slots, non_blocking=True)
+            moe.collect(0, y_out, s_out, self.n, append=True)
+        if not self.direct:
+            self.yh.copy_(self.y, non_blocking=True)
+            self.sh.copy_(self.slots, non_blocking=True)
 
 
 def schedule_independent_bytes(spec, logits):
@@ -565,7 +569,8 @@ def measure_layer(args, pkg, spec, dev, rank, world, steps, warmup, e2e_steps, w
     e2e = {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": arr.h2d_bytes(),
            "d2h_bytes_per_step": arr.d2h_bytes(), "steps": e2e_steps,
            "copies": "router logits host to device first; each wave's token rows host to device on a "
-                     "side stream as it arrives; outputs device to host after the last collect"}
+                     "side stream as it arrives; outputs " + ("written to pinned host memory by collect as "
+                     "each token completes" if arr.direct else "device to host after the last collect")}
 
     cpu = None
     if cpu_in is not None:

@@ -411,6 +411,13 @@ moe_status moe_async_forward_noalloc(int32_t T, int32_t E, int32_t K, int32_t H,
 moe_status moe_async_debug_append_record(moe_async_t h, int32_t layer, int32_t bucket, int32_t record,
                                         void* stream);
 
+/* 1 if the kernels can write `n` bytes at host address `p` directly (pinned host memory
+ * mapped into the device's address space at the same address), else 0.  A caller may then
+ * pass such a buffer as a collect output (d_y_out, d_slot_out, ...), so each merged row goes
+ * to host memory as it is produced instead of by a copy after the step.  Host-side query, no
+ * device work. */
+int32_t moe_async_host_writable(const void* p, int64_t n);
+
 /* Human-readable name of a status code (static string). */
 const char* moe_async_status_string(moe_status s);
 

@@ -536,3 +536,31 @@ def test_duplicate_wave_does_not_overwrite_pool(pkg):
     assert rel_err(got, want) <= TOL["f32"], rel_err(got, want)
     assert moe.stats()["duplicates"] == 2 * L.top_k
     moe.close()
+
+
+def test_collect_into_pinned_host_memory(pkg):
+    """Collect outputs written by the kernels straight into pinned host buffers (when
+    moe_async_host_writable says the kernels can address them) equal those written to device
+    buffers, token by token; pageable host memory is reported as not writable."""
+    spec, wl, moe, x, idx, w = _small(pkg, shared=True)
+    T, H = spec.tokens, spec.layer.hidden
+    yh = torch.empty((T, H), dtype=x.dtype).pin_memory()
+    sh = torch.empty(T, dtype=torch.int32).pin_memory()
+    assert not pkg.host_writable(torch.empty((T, H), dtype=x.dtype))      # pageable
+    if not (pkg.host_writable(yh) and pkg.host_writable(sh)):
+        pytest.skip("pinned host memory is not mapped into the device's address space here")
+    n = torch.zeros(1, dtype=torch.int32, device="cuda")
+    moe.enqueue(0, x, idx, w, rows=torch.arange(0, T // 2, dtype=torch.int32, device="cuda"))
+    moe.schedule_step(0, pkg.Policy())
+    moe.collect(0, yh, sh, n, append=True)
+    moe.enqueue(0, x, idx, w, rows=torch.arange(T // 2, T, dtype=torch.int32, device="cuda"))
+    moe.schedule_step(0, pkg.Policy())
+    moe.collect(0, yh, sh, n, append=True)
+    assert moe.sync() == 0 and int(n.item()) == T
+    L = spec.layer
+    ii, ww = om.route(wl.logits.numpy(), L.top_k)
+    ref = om.dense_moe(wl.x.double().numpy(), ii, ww, expert_getter(wl.weights[0], L.num_experts),
+                       shared=expert_getter(wl.weights[0], L.num_experts)(L.num_experts))
+    got = by_token(sh.numpy(), yh.float().numpy().astype(np.float64), T, H)
+    assert rel_err(got, ref) <= TOL["bf16"]
+    moe.close()
