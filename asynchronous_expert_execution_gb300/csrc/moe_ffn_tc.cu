@@ -70,6 +70,13 @@ constexpr int kKps = MOE_TC_KPS;      // narrow tiles
 #define MOE_TC_WIDE_MIN2 33
 #endif
 constexpr int kKpsW = MOE_TC_KPSW;
+// A wide tile of at most MOE_TC_MID tokens (MMA N) moves 3 k-blocks a stage: its token rows
+// take 3 x N x 128 B beside 3 x 16 KB of weights, so the stage carries half again as many
+// weight bytes as a 2-k-block one (0 turns this off).
+#ifndef MOE_TC_MID
+#define MOE_TC_MID 64
+#endif
+constexpr int kMidMax = MOE_TC_MID;
 // TMEM accumulator buffers (each BNW columns): the MMA may run this many units' chunks ahead of
 // the epilogue, which absorbs epilogues made slow by the merges some tiles complete.
 #ifndef MOE_TC_ACC
@@ -396,6 +403,7 @@ struct Tile {
   int nmma;     // MMA N (multiple of 16, >= nj)
   int bn;       // tile width: narrow or wide
   int kps;      // k-blocks per pipeline stage for this tile width
+  int bstride;  // bytes between the B sub-blocks of a stage (nmma rows of 128 B)
   bool single;  // the item has one token tile: its A rows are read once
 };
 
@@ -429,13 +437,14 @@ __device__ __forceinline__ Tile decode_tile(const TcParams& p, const int* tb, in
   // the planner applies the same rule
   const bool wide = BNW > BN && count >= (MODE == kModeGemm2 ? kWideMin2 : kWideMin1);
   tl.bn = wide ? BNW : BN;
-  tl.kps = wide ? kKpsW : kKps;
   const int ntt = (count + tl.bn - 1) / tl.bn;
   tl.single = ntt <= 1;
   tl.fti = local / ntt;
   tl.j0 = (local % ntt) * tl.bn;
   tl.nj = min(tl.bn, count - tl.j0);
   tl.nmma = min(tl.bn, max(16, (tl.nj + 15) & ~15));
+  tl.kps = wide ? (tl.nmma <= kMidMax ? 3 : kKpsW) : kKps;
+  tl.bstride = tl.nmma * kBK * 2;
   return tl;
 }
 
@@ -446,7 +455,9 @@ struct SmemLayout {
   static constexpr int kA1 = kBM * kBK * 2;                  // 16 KB: one k-block of A
   static constexpr int kStageN = kKps * (kA1 + BN * kBK * 2);
   static constexpr int kStageW = BNW > BN ? kKpsW * (kA1 + BNW * kBK * 2) : 0;
-  static constexpr int kStage = ((kStageN > kStageW ? kStageN : kStageW) + 1023) & ~1023;
+  static constexpr int kStageM = BNW > BN && kMidMax > 0 ? 3 * (kA1 + kMidMax * kBK * 2) : 0;
+  static constexpr int kStageNW = kStageN > kStageW ? kStageN : kStageW;
+  static constexpr int kStage = ((kStageNW > kStageM ? kStageNW : kStageM) + 1023) & ~1023;
   static constexpr int kOffBar = STAGES * kStage;
   static constexpr int kNumBars = 2 * STAGES + 2 * kAccBufs;
   static constexpr int kOffTmem = kOffBar + kNumBars * 8;
@@ -461,6 +472,7 @@ struct SmemLayout {
   static constexpr int kOffTb = kOffRing + kUnitQ * 4;
   static constexpr int kBytes = kOffTb + kMaxBuckets * 4;
   static constexpr int kAlloc = kBytes + 1024;               // room to align the base to 1024
+  static_assert(kAlloc <= 227 * 1024, "dynamic shared memory of a CTA: at most 227 KB");
 };
 
 // ------------------------------------------------------------------ the kernel
@@ -651,7 +663,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
           if (!(ok = __all_sync(0xffffffffu, w_ok))) break;
           const uint32_t b_s = smem_u32(smem + s * SL::kStage) + tl.kps * SL::kA1;
           for (int j = 0; j < nv; ++j) {
-            const uint32_t bs = b_s + j * tl.bn * kBK * 2 + dst_off;
+            const uint32_t bs = b_s + j * tl.bstride + dst_off;
             const int col = (kbs + j) * kBK + c8 * 8;
             const bool colok = col < Kdim;
 #pragma unroll
@@ -700,7 +712,7 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
             const uint32_t a_s = smem_u32(smem + s * SL::kStage);
             for (int j = 0; j < nv; ++j) {
               const uint32_t a0 = a_s + j * SL::kA1;
-              const uint32_t b0 = a_s + tl.kps * SL::kA1 + j * tl.bn * kBK * 2;
+              const uint32_t b0 = a_s + tl.kps * SL::kA1 + j * tl.bstride;
 #pragma unroll
               for (int k = 0; k < kBK / 16; ++k)
                 mma_bf16(d_tmem, sw128_desc(a0 + k * 32), sw128_desc(b0 + k * 32), idesc,
