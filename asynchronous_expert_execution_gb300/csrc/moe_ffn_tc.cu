@@ -77,6 +77,12 @@ constexpr int kKpsW = MOE_TC_KPSW;
 #define MOE_TC_MID 64
 #endif
 constexpr int kMidMax = MOE_TC_MID;
+// Most k-blocks a stage: a tile whose k-blocks are small enough (few tokens) fills the stage
+// with up to this many (a 16-token decode tile: 4 x 18 KB in a 72 KB stage).
+#ifndef MOE_TC_KPS_MAX
+#define MOE_TC_KPS_MAX 4
+#endif
+constexpr int kKpsMax = MOE_TC_KPS_MAX;
 // TMEM accumulator buffers (each BNW columns): the MMA may run this many units' chunks ahead of
 // the epilogue, which absorbs epilogues made slow by the merges some tiles complete.
 #ifndef MOE_TC_ACC
@@ -392,6 +398,33 @@ __device__ __forceinline__ int chunk_kb(int c, int nk, int nchunk) {
   return min(nk, (e + 3) / 6 * 6);
 }
 
+// A stage holds kps k-blocks of a tile: A sub-blocks (16 KB each) from the stage base, then
+// B sub-blocks (nmma x 128 B each).  Its size fits every tile width with its k-blocks a stage.
+template <int BN, int BNW, int STAGES>
+struct SmemLayout {
+  static constexpr int kA1 = kBM * kBK * 2;                  // 16 KB: one k-block of A
+  static constexpr int kStageN = kKps * (kA1 + BN * kBK * 2);
+  static constexpr int kStageW = BNW > BN ? kKpsW * (kA1 + BNW * kBK * 2) : 0;
+  static constexpr int kStageM = BNW > BN && kMidMax > 0 ? 3 * (kA1 + kMidMax * kBK * 2) : 0;
+  static constexpr int kStageNW = kStageN > kStageW ? kStageN : kStageW;
+  static constexpr int kStage = ((kStageNW > kStageM ? kStageNW : kStageM) + 1023) & ~1023;
+  static constexpr int kOffBar = STAGES * kStage;
+  static constexpr int kNumBars = 2 * STAGES + 2 * kAccBufs;
+  static constexpr int kOffTmem = kOffBar + kNumBars * 8;
+  static constexpr int kOffAbort = kOffTmem + 4;
+  static constexpr int kOffSlot = (kOffAbort + 4 + 15) & ~15;
+  static constexpr int kOffK = kOffSlot + BNW * 4;
+  static constexpr int kOffFin = kOffK + BNW * 4;
+  static constexpr int kOffW = kOffFin + BNW * 4;
+  static constexpr int kOffFlag = kOffW + BNW * 4;
+  static constexpr int kOffRingBar = (kOffFlag + 16 + 7) & ~7;
+  static constexpr int kOffRing = kOffRingBar + 2 * kUnitQ * 8;
+  static constexpr int kOffTb = kOffRing + kUnitQ * 4;
+  static constexpr int kBytes = kOffTb + kMaxBuckets * 4;
+  static constexpr int kAlloc = kBytes + 1024;               // room to align the base to 1024
+  static_assert(kAlloc <= 227 * 1024, "dynamic shared memory of a CTA: at most 227 KB");
+};
+
 struct Tile {
   int expert;
   int step;     // scheduling step of the work item
@@ -445,35 +478,12 @@ __device__ __forceinline__ Tile decode_tile(const TcParams& p, const int* tb, in
   tl.nmma = min(tl.bn, max(16, (tl.nj + 15) & ~15));
   tl.kps = wide ? (tl.nmma <= kMidMax ? 3 : kKpsW) : kKps;
   tl.bstride = tl.nmma * kBK * 2;
+  // as many k-blocks as the stage holds, up to kKpsMax (never fewer than the rule above)
+  const int fit = SmemLayout<BN, BNW, 1>::kStage / (SmemLayout<BN, BNW, 1>::kA1 + tl.bstride);
+  tl.kps = max(tl.kps, min(fit, kKpsMax));
   return tl;
 }
 
-// A stage holds kps k-blocks of a tile: A sub-blocks (16 KB each) from the stage base, then
-// B sub-blocks (bn x 128 B each).  Its size fits either tile width.
-template <int BN, int BNW, int STAGES>
-struct SmemLayout {
-  static constexpr int kA1 = kBM * kBK * 2;                  // 16 KB: one k-block of A
-  static constexpr int kStageN = kKps * (kA1 + BN * kBK * 2);
-  static constexpr int kStageW = BNW > BN ? kKpsW * (kA1 + BNW * kBK * 2) : 0;
-  static constexpr int kStageM = BNW > BN && kMidMax > 0 ? 3 * (kA1 + kMidMax * kBK * 2) : 0;
-  static constexpr int kStageNW = kStageN > kStageW ? kStageN : kStageW;
-  static constexpr int kStage = ((kStageNW > kStageM ? kStageNW : kStageM) + 1023) & ~1023;
-  static constexpr int kOffBar = STAGES * kStage;
-  static constexpr int kNumBars = 2 * STAGES + 2 * kAccBufs;
-  static constexpr int kOffTmem = kOffBar + kNumBars * 8;
-  static constexpr int kOffAbort = kOffTmem + 4;
-  static constexpr int kOffSlot = (kOffAbort + 4 + 15) & ~15;
-  static constexpr int kOffK = kOffSlot + BNW * 4;
-  static constexpr int kOffFin = kOffK + BNW * 4;
-  static constexpr int kOffW = kOffFin + BNW * 4;
-  static constexpr int kOffFlag = kOffW + BNW * 4;
-  static constexpr int kOffRingBar = (kOffFlag + 16 + 7) & ~7;
-  static constexpr int kOffRing = kOffRingBar + 2 * kUnitQ * 8;
-  static constexpr int kOffTb = kOffRing + kUnitQ * 4;
-  static constexpr int kBytes = kOffTb + kMaxBuckets * 4;
-  static constexpr int kAlloc = kBytes + 1024;               // room to align the base to 1024
-  static_assert(kAlloc <= 227 * 1024, "dynamic shared memory of a CTA: at most 227 KB");
-};
 
 // ------------------------------------------------------------------ the kernel
 
