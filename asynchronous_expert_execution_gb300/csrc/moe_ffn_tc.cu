@@ -39,14 +39,21 @@ namespace {
 
 constexpr int kBM = 128;              // MMA M (weight rows per tile)
 constexpr int kBK = 64;               // K per k-block (one 128-byte swizzle atom)
-// k-blocks moved per pipeline stage: a stage's fixed cost (barrier round trip, TMA issue,
-// MMA commit) is paid once per kKps k-blocks.  Measured on GB300 with an MMA consumer: a
-// lone SM streams 36 / 53 / 69 GB/s with 16 / 32 / 64 KB weight stages, and 152 SMs
-// 5.3 / 6.1 TB/s with 16 / 32 KB stages.
-#ifndef MOE_TC_KPS
-#define MOE_TC_KPS 3
+// Pipeline stages fill the shared memory left over (kStage bytes each) and a tile moves as
+// many k-blocks a stage as fit (at most MOE_TC_KPS_MAX): a stage's fixed cost (barrier round
+// trip, TMA issue, MMA commit) is paid once per stage.  Measured on GB300 with an MMA
+// consumer: a lone SM streams 36 / 53 / 69 GB/s with 16 / 32 / 64 KB weight stages, and 152
+// SMs 5.3 / 6.1 TB/s with 16 / 32 KB stages.  With 3 stages of 72 KB a 32-token tile moves 3
+// k-blocks, a 16-token one 4, a wide tile of up to 64 tokens 3 and a wider one 2 (against 2
+// for every wide tile in 64 KB stages: DeepSeek-wide layer +1.7%, Zipf prefill +1.9%).
+#ifndef MOE_TC_KPS_MAX
+#define MOE_TC_KPS_MAX 8
 #endif
-constexpr int kKps = MOE_TC_KPS;      // narrow tiles
+constexpr int kKpsMax = MOE_TC_KPS_MAX;
+#ifndef MOE_TC_STAGES
+#define MOE_TC_STAGES 3
+#endif
+constexpr int kStagesCfg = MOE_TC_STAGES;   // pipeline stages of the shared-memory ring
 // Wide tiles: an item with at least MOE_TC_WIDE_MIN1 (GEMM1, attention stub) or
 // MOE_TC_WIDE_MIN2 (GEMM2) tokens is cut into MOE_TC_BNW-token tiles, so its weight rows are
 // read once per BNW tokens and each MMA is wide enough for the tensor pipe (measured: 46
@@ -60,29 +67,12 @@ constexpr int kKps = MOE_TC_KPS;      // narrow tiles
 #ifndef MOE_TC_BNW
 #define MOE_TC_BNW 128
 #endif
-#ifndef MOE_TC_KPSW
-#define MOE_TC_KPSW 2
-#endif
 #ifndef MOE_TC_WIDE_MIN1
 #define MOE_TC_WIDE_MIN1 33
 #endif
 #ifndef MOE_TC_WIDE_MIN2
 #define MOE_TC_WIDE_MIN2 33
 #endif
-constexpr int kKpsW = MOE_TC_KPSW;
-// A wide tile of at most MOE_TC_MID tokens (MMA N) moves 3 k-blocks a stage: its token rows
-// take 3 x N x 128 B beside 3 x 16 KB of weights, so the stage carries half again as many
-// weight bytes as a 2-k-block one (0 turns this off).
-#ifndef MOE_TC_MID
-#define MOE_TC_MID 64
-#endif
-constexpr int kMidMax = MOE_TC_MID;
-// Most k-blocks a stage: a tile whose k-blocks are small enough (few tokens) fills the stage
-// with up to this many (a 16-token decode tile: 4 x 18 KB in a 72 KB stage).
-#ifndef MOE_TC_KPS_MAX
-#define MOE_TC_KPS_MAX 4
-#endif
-constexpr int kKpsMax = MOE_TC_KPS_MAX;
 // TMEM accumulator buffers (each BNW columns): the MMA may run this many units' chunks ahead of
 // the epilogue, which absorbs epilogues made slow by the merges some tiles complete.
 #ifndef MOE_TC_ACC
@@ -399,17 +389,18 @@ __device__ __forceinline__ int chunk_kb(int c, int nk, int nchunk) {
 }
 
 // A stage holds kps k-blocks of a tile: A sub-blocks (16 KB each) from the stage base, then
-// B sub-blocks (nmma x 128 B each).  Its size fits every tile width with its k-blocks a stage.
+// B sub-blocks (nmma x 128 B each).  The stages take the dynamic shared memory that the
+// barriers, the per-unit arrays and the item table leave (227 KB a CTA, 1 KB of alignment
+// slack), in whole KB.
 template <int BN, int BNW, int STAGES>
 struct SmemLayout {
   static constexpr int kA1 = kBM * kBK * 2;                  // 16 KB: one k-block of A
-  static constexpr int kStageN = kKps * (kA1 + BN * kBK * 2);
-  static constexpr int kStageW = BNW > BN ? kKpsW * (kA1 + BNW * kBK * 2) : 0;
-  static constexpr int kStageM = BNW > BN && kMidMax > 0 ? 3 * (kA1 + kMidMax * kBK * 2) : 0;
-  static constexpr int kStageNW = kStageN > kStageW ? kStageN : kStageW;
-  static constexpr int kStage = ((kStageNW > kStageM ? kStageNW : kStageM) + 1023) & ~1023;
-  static constexpr int kOffBar = STAGES * kStage;
   static constexpr int kNumBars = 2 * STAGES + 2 * kAccBufs;
+  static constexpr int kTail = kNumBars * 8 + 8 + 15 + 4 * BNW * 4 + 16 + 7 + 2 * kUnitQ * 8 + kUnitQ * 4 +
+                               kMaxBuckets * 4;              // everything after the stages (upper bound)
+  static constexpr int kStage = ((227 * 1024 - 1024 - kTail) / STAGES) & ~1023;
+  static_assert(kStage >= kA1 + BNW * kBK * 2, "a stage must hold one k-block of the widest tile");
+  static constexpr int kOffBar = STAGES * kStage;
   static constexpr int kOffTmem = kOffBar + kNumBars * 8;
   static constexpr int kOffAbort = kOffTmem + 4;
   static constexpr int kOffSlot = (kOffAbort + 4 + 15) & ~15;
@@ -476,11 +467,10 @@ __device__ __forceinline__ Tile decode_tile(const TcParams& p, const int* tb, in
   tl.j0 = (local % ntt) * tl.bn;
   tl.nj = min(tl.bn, count - tl.j0);
   tl.nmma = min(tl.bn, max(16, (tl.nj + 15) & ~15));
-  tl.kps = wide ? (tl.nmma <= kMidMax ? 3 : kKpsW) : kKps;
   tl.bstride = tl.nmma * kBK * 2;
-  // as many k-blocks as the stage holds, up to kKpsMax (never fewer than the rule above)
-  const int fit = SmemLayout<BN, BNW, 1>::kStage / (SmemLayout<BN, BNW, 1>::kA1 + tl.bstride);
-  tl.kps = max(tl.kps, min(fit, kKpsMax));
+  // as many k-blocks as a stage holds, up to kKpsMax
+  using SL = SmemLayout<BN, BNW, kStagesCfg>;
+  tl.kps = max(1, min(kKpsMax, SL::kStage / (SL::kA1 + tl.bstride)));
   return tl;
 }
 
@@ -919,22 +909,17 @@ struct TcState {
   void* split_buf[2];               // GEMM1 / GEMM2 chunk-partial workspace + arrival counters
 };
 
-// Token-tile width and pipeline depth (smem ring = kStages x kKps x (16 KB A + kBN*128 B B)).
-// Measured on GB300 (bench c2/c3/c4, pairs/s): 32-token tiles suit decode and steps with few
-// experts (more CTAs per expert); prefill with very popular experts prefers wider tiles
-// (64: c3 +9%, c2 -1.7%, c4 -22%).  Stages of kKps k-blocks x kStages, same tile:
-// 1 x 10 -- c2 176.5 K, c3 2.61 M, c4 1.08 M; 2 x 5 -- 179.1 K, 2.79 M, 1.15 M;
-// 3 x 3 -- 181.8 K, 2.92 M, 1.19 M; 4 x 2 -- 175.3 K, 2.91 M, 1.18 M; 5 x 2 -- 181.4 K,
-// 2.98 M, 1.20 M.
+// Token-tile width and pipeline depth.  Measured on GB300 (bench c2/c3/c4, pairs/s): 32-token
+// tiles suit decode and steps with few experts (more CTAs per expert); prefill with very
+// popular experts prefers wider tiles (64: c3 +9%, c2 -1.7%, c4 -22%).  Earlier stage sweeps
+// (k-blocks x stages, same tile): 1 x 10 -- c2 176.5 K, c3 2.61 M, c4 1.08 M; 2 x 5 -- 179.1 K,
+// 2.79 M, 1.15 M; 3 x 3 -- 181.8 K, 2.92 M, 1.19 M; 4 x 2 -- 175.3 K, 2.91 M, 1.18 M.
 #ifndef MOE_TC_BN
 #define MOE_TC_BN 32
 #endif
-#ifndef MOE_TC_STAGES
-#define MOE_TC_STAGES 3
-#endif
 constexpr int kBN = MOE_TC_BN;
 constexpr int kBNW = kWideMin1 > 0 && kWideMin2 > 0 && MOE_TC_BNW > MOE_TC_BN ? MOE_TC_BNW : MOE_TC_BN;
-constexpr int kStages = MOE_TC_STAGES;
+constexpr int kStages = kStagesCfg;
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
