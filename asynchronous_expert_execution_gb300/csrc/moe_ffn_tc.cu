@@ -43,7 +43,7 @@ constexpr int kBK = 64;               // K per k-block (one 128-byte swizzle ato
 // many k-blocks a stage as fit (at most MOE_TC_KPS_MAX): a stage's fixed cost (barrier round
 // trip, TMA issue, MMA commit) is paid once per stage.  Measured on GB300 with an MMA
 // consumer: a lone SM streams 36 / 53 / 69 GB/s with 16 / 32 / 64 KB weight stages, and 152
-// SMs 5.3 / 6.1 TB/s with 16 / 32 KB stages.  With 3 stages of 72 KB a 32-token tile moves 3
+// SMs 5.3 / 6.1 TB/s with 16 / 32 KB stages.  With 3 stages of 73 KB a 32-token tile moves 3
 // k-blocks, a 16-token one 4, a wide tile of up to 64 tokens 3 and a wider one 2 (against 2
 // for every wide tile in 64 KB stages: DeepSeek-wide layer +1.7%, Zipf prefill +1.9%).
 #ifndef MOE_TC_KPS_MAX
