@@ -97,6 +97,7 @@ __device__ __forceinline__ void enqueue_warps(const LayerView& L, const Dims& d,
   for (long long g0 = gw * tpw; g0 < n; g0 += nwarps * tpw) {
     int key = -1 - lane;          // unique key for lanes with nothing to append
     int slot = -1, row = -1;
+    uint32_t head_e = 0;
     bool accepted = false;
     if (jl < tpw && g0 + jl < n) {
       const int i = (int)(g0 + jl);
@@ -110,10 +111,15 @@ __device__ __forceinline__ void enqueue_warps(const LayerView& L, const Dims& d,
       }
       if (ok && k < d.K && kmask && !((kmask[i] >> k) & 1u)) ok = false;
       int e = d.E;
+      float wk = 1.0f;                       // the shared expert's weight
       if (ok && k < d.K) {
         e = expert[(size_t)row * d.K + k];
+        wk = w[(size_t)row * d.K + k];
         if (e < 0 || e >= d.E) { set_error(C, MOE_ERR_INVALID); ok = false; }
       }
+      // the bucket's head, read with the mask (its loads overlap the atomics below); the
+      // scheduler, the only writer of heads, is ordered after this kernel in the stream
+      if (ok) head_e = L.head[e];
       if (ok && (L.enq_mask[slot] & kRetired)) ok = false;   // late pair of a cancelled request
       if (ok) {
         const uint32_t bit = 1u << k;
@@ -123,7 +129,7 @@ __device__ __forceinline__ void enqueue_warps(const LayerView& L, const Dims& d,
           ok = false;            // shared expert: already enqueued by an earlier wave
         } else {
           if (old == 0u) atomicAdd(&C->open_tokens, 1);
-          L.wtab[(size_t)slot * d.KS + k] = (k < d.K) ? w[(size_t)row * d.K + k] : 1.0f;
+          L.wtab[(size_t)slot * d.KS + k] = wk;
           key = e;
           accepted = true;
         }
@@ -159,7 +165,7 @@ __device__ __forceinline__ void enqueue_warps(const LayerView& L, const Dims& d,
       }
       pos0 = __shfl_sync(peers, pos0, leader);
       const uint32_t pos = pos0 + __popc(peers & ((1u << lane) - 1u));
-      if (pos - L.head[key] >= (uint32_t)d.cap) {
+      if (pos - head_e >= (uint32_t)d.cap) {
         set_error(C, MOE_ERR_CAPACITY);
       } else {
         L.records[(size_t)key * d.cap + (pos % (uint32_t)d.cap)] = (slot << kKShift) | k;

@@ -506,7 +506,31 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
   // Programmatic dependent launch: GEMM1 may start while the scheduling kernel runs and waits
   // here for its plan; it then lets GEMM2 start on SMs as they free up.  (A no-op when the
   // kernel was launched without a programmatic dependency.)
+  // barriers and TMEM do not depend on the plan: GEMM1 sets them up before it waits for it
+  auto setup = [&]() {
+    if (threadIdx.x == 0) {
+      for (int s = 0; s < STAGES; ++s) {
+        mbar_init(&full[s], 1 + 64);    // the A producer's expect_tx arrive + 64 cp.async B lanes
+        mbar_init(&empty[s], 1);        // tcgen05.commit
+      }
+      for (int b = 0; b < kAccBufs; ++b) {
+        mbar_init(&tfull[b], 1);        // tcgen05.commit after the tile's last MMA
+        mbar_init(&tempty[b], 4);       // one arrive per epilogue warp
+      }
+      for (int i = 0; i < kUnitQ; ++i) {
+        mbar_init(&ring.full[i], 1);              // the weight producer
+        mbar_init(&ring.empty[i], kUnitReaders);  // every reader role
+      }
+      *abort_flag = 0;
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 2) {
+      tmem_alloc(tmem_slot, kTmemCols);
+      tmem_relinquish();
+    }
+  };
   if (MODE == kModeGemm1) {
+    setup();
     griddep_wait();
     griddep_launch_dependents();
   }
@@ -541,35 +565,25 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
     if (split < whole) n_whole = 0;
   }
   const int n_units = n_whole + (n_tiles - n_whole) * nchunk;
-  if ((int)blockIdx.x >= n_units) {              // no work for this CTA: skip all set-up
+  if ((int)blockIdx.x >= n_units) {              // no work for this CTA: skip the rest of the set-up
     // every CTA of a programmatic dependent waits for its predecessor before it ends, so this
     // launch's completion implies GEMM1's even when it has no work
     if (MODE == kModeGemm2) griddep_wait();
+    if (MODE == kModeGemm1) {                   // give back the TMEM taken before the plan
+      tc_fence_before();
+      __syncthreads();
+      tc_fence_after();
+      if (warp == 2) {
+        __syncwarp();
+        tmem_dealloc(*tmem_slot, kTmemCols);
+      }
+    }
     if (threadIdx.x == 0) unit_ctr_exit(p.unit_ctr);
     return;
   }
 
-  if (threadIdx.x == 0) {
-    prefetch_tmap(tmA);                        // descriptors load while the CTA sets up
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1 + 64);    // the A producer's expect_tx arrive + 64 cp.async B lanes
-      mbar_init(&empty[s], 1);        // tcgen05.commit
-    }
-    for (int b = 0; b < kAccBufs; ++b) {
-      mbar_init(&tfull[b], 1);        // tcgen05.commit after the tile's last MMA
-      mbar_init(&tempty[b], 4);       // one arrive per epilogue warp
-    }
-    for (int i = 0; i < kUnitQ; ++i) {
-      mbar_init(&ring.full[i], 1);              // the weight producer
-      mbar_init(&ring.empty[i], kUnitReaders);  // every reader role
-    }
-    *abort_flag = 0;
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  if (warp == 2) {
-    tmem_alloc(tmem_slot, kTmemCols);
-    tmem_relinquish();
-  }
+  if (threadIdx.x == 0) prefetch_tmap(tmA);     // descriptors load while the CTA sets up
+  if (MODE != kModeGemm1) setup();
   if (MODE != kModeAtt) {                       // item lookups then search shared memory
     const int nw = min(p.P->n_work, kMaxBuckets);
     for (int i = threadIdx.x; i < nw; i += blockDim.x)

@@ -23,13 +23,44 @@ namespace moe {
 // fallback_groups a step.  Each work item carries its step; the plan holds the steps up to
 // the last non-empty one (at most max_steps), and only those are counted.
 struct PlanScratch {
+  // deepest-first sort keys: depth in the high word, the complement of the bucket id in the
+  // low word (equal depth -> lower id first), 0 for an empty bucket; padded to whole pairs
+  alignas(16) unsigned long long key[kMaxBuckets + 1];
   int depth[kMaxBuckets];
   uint32_t head[kMaxBuckets];     // queue heads read with the depths
   int order[kMaxBuckets];
   int pick[kMaxBuckets];          // RANKS: each rank's bucket (-1: none)
   unsigned char taken[kMaxBuckets];
-  int n_elig, n_nonempty, n_picks;
+  unsigned long long wmax[32];     // per-warp maxima (few picks)
+  int n_elig, n_nonempty, n_picks, trace0;
 };
+
+// Plans with at most this many picks (MTFS / THRESHOLD) take them by rounds of a block-wide
+// maximum over the keys instead of ranking every bucket.
+constexpr int kFewPicks = 4;
+
+__device__ __forceinline__ unsigned long long warp_max_u64(unsigned long long v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const unsigned long long o = __shfl_xor_sync(0xffffffffu, v, off);
+    v = o > v ? o : v;
+  }
+  return v;
+}
+
+// Threads that rank one bucket together (a power of 2 dividing the warp): each scans an
+// interleaved share of the key pairs and the group adds its counts.  Chosen to minimise
+// rounds x (pairs a thread scans + the shuffle levels) for nb buckets and nt threads.
+__device__ __forceinline__ int rank_group(int nb, int nt) {
+  const int pairs = (nb + 1) >> 1;       // nb <= kMaxBuckets, nt <= 1024: int arithmetic
+  int best = 1, best_cost = -1;
+  for (int per = 1, lv = 0; per <= 32; per <<= 1, ++lv) {
+    const int rounds = (nb * per + nt - 1) / nt;
+    const int cost = rounds * (((pairs + per - 1) >> lv) + 2 * lv);
+    if (best_cost < 0 || cost < best_cost) { best_cost = cost; best = per; }
+  }
+  return best;
+}
 
 // Step (0-based, within this plan) of the r-th bucket in the deepest-first order.
 __device__ __forceinline__ int pick_step(const moe_async_policy& pol, int n_elig, int r) {
@@ -68,13 +99,28 @@ __device__ inline void plan_layer(const LayerView& L, const Dims& d, StepPlan* P
   // After an overflow or an out-of-range id the queues no longer describe valid pairs:
   // stop executing (the sticky error is reported to the host).  Read with the depths.
   const uint32_t err = *(volatile uint32_t*)&C->error;
-  for (int b = tid; b < d.NB; b += nt) {
-    const uint32_t hd = L.head[b];
-    const int dep = enabled ? min((int)(L.tail[b] - hd), d.cap) : 0;
-    sc.head[b] = hd;
-    depth[b] = dep;
-    if (dep > 0) atomicAdd(&sc.n_nonempty, 1);
-    if (dep > 0 && (pol.kind != MOE_POLICY_THRESHOLD || dep >= pol.min_batch)) atomicAdd(&sc.n_elig, 1);
+  const int nkey = (d.NB + 1) & ~1;
+  int my_nonempty = 0, my_elig = 0;
+  for (int b = tid; b < nkey; b += nt) {
+    unsigned long long key = 0ull;
+    if (b < d.NB) {
+      const uint32_t hd = L.head[b];
+      const int dep = enabled ? min((int)(L.tail[b] - hd), d.cap) : 0;
+      sc.head[b] = hd;
+      depth[b] = dep;
+      if (dep > 0) {
+        key = ((unsigned long long)(uint32_t)dep << 32) | (0xffffffffu - (uint32_t)b);
+        ++my_nonempty;
+        if (pol.kind != MOE_POLICY_THRESHOLD || dep >= pol.min_batch) ++my_elig;
+      }
+    }
+    sc.key[b] = key;
+  }
+  my_nonempty = __reduce_add_sync(0xffffffffu, my_nonempty);
+  my_elig = __reduce_add_sync(0xffffffffu, my_elig);
+  if ((tid & 31) == 0) {
+    if (my_nonempty) atomicAdd(&sc.n_nonempty, my_nonempty);
+    if (my_elig) atomicAdd(&sc.n_elig, my_elig);
   }
   __syncthreads();
   const int n_elig = sc.n_elig, n_nonempty = sc.n_nonempty;
@@ -83,17 +129,49 @@ __device__ inline void plan_layer(const LayerView& L, const Dims& d, StepPlan* P
   // bucket; RANKS ranks the non-empty buckets too (its stealers take from that order)
   const bool ranks = pol.kind == MOE_POLICY_RANKS;
   int n = halted ? 0 : (ranks ? n_nonempty : picks_within(pol, n_nonempty, n_elig, max(max_steps, 1)));
-  for (int b = tid; b < d.NB; b += nt) {
-    const int db = depth[b];
-    if (db >= 1) {
-      int r = 0;
-      for (int c = 0; c < d.NB; ++c) {
-        const int dc = depth[c];
-        r += (dc >= 1) && (dc > db || (dc == db && c < b));
+  // the trace entries of the picks are reserved while the buckets are ranked (RANKS knows
+  // its pick count only after the ranking)
+  const bool want_trace = trace && trace_cap > 0;
+  int trace0 = 0;                       // its value is first used after the ranking
+  if (tid == 0 && want_trace && !ranks && n > 0) trace0 = atomicAdd(&C->trace_n, n);
+  if (!ranks && n <= kFewPicks) {
+    // pick r is the largest key left: a block-wide maximum, then that bucket leaves the keys
+    const int lane = tid & 31, warp = tid >> 5;
+    for (int r = 0; r < n; ++r) {
+      unsigned long long m = 0ull;
+      for (int b = tid; b < nkey; b += nt) m = sc.key[b] > m ? sc.key[b] : m;
+      m = warp_max_u64(m);
+      if (lane == 0) sc.wmax[warp] = m;
+      __syncthreads();
+      if (warp == 0) {
+        m = warp_max_u64(lane < (nt >> 5) ? sc.wmax[lane] : 0ull);
+        if (lane == 0 && m != 0ull) {
+          const int b = (int)(0xffffffffu - (uint32_t)m);
+          order[r] = b;
+          sc.key[b] = 0ull;
+        }
       }
-      if (r < n) order[r] = b;
+      __syncthreads();
+    }
+  } else {
+    // rank of every non-empty bucket in the deepest-first order = the keys above its own
+    const int per = rank_group(d.NB, nt);
+    const ulonglong2* k2 = reinterpret_cast<const ulonglong2*>(sc.key);
+    const int pairs = nkey >> 1;
+    for (int base = 0; base < d.NB * per; base += nt) {     // the same trips for every thread
+      const int idx = base + tid, b = idx / per, part = idx - b * per;
+      const unsigned long long kb = b < d.NB ? sc.key[b] : 0ull;
+      int r = 0;
+      if (kb != 0ull)
+        for (int c = part; c < pairs; c += per) {
+          const ulonglong2 v = k2[c];
+          r += (int)(v.x > kb) + (int)(v.y > kb);
+        }
+      for (int off = per >> 1; off > 0; off >>= 1) r += __shfl_down_sync(0xffffffffu, r, off, per);
+      if (part == 0 && kb != 0ull && r < n) order[r] = b;
     }
   }
+  if (tid == 0) sc.trace0 = trace0;
   __syncthreads();
   if (pol.kind == MOE_POLICY_RANKS) {
     // simulated expert-parallel ranks: bucket b belongs to rank b mod R; each rank runs its
@@ -136,9 +214,13 @@ __device__ inline void plan_layer(const LayerView& L, const Dims& d, StepPlan* P
     const int ft2 = (d.H + g.bm2 - 1) / g.bm2;
     // trace entries of the n picks, in pick order, reserved at once
     int ti0 = 0;
-    if (trace && trace_cap > 0 && n > 0) {
-      if (lane == 0) ti0 = atomicAdd(&C->trace_n, n);
-      ti0 = __shfl_sync(0xffffffffu, ti0, 0);
+    if (want_trace && n > 0) {
+      if (ranks) {
+        if (lane == 0) ti0 = atomicAdd(&C->trace_n, n);
+        ti0 = __shfl_sync(0xffffffffu, ti0, 0);
+      } else {
+        ti0 = sc.trace0;
+      }
     }
     for (int c0 = 0; c0 < n; c0 += 32) {
       const int r = c0 + lane;
@@ -192,11 +274,12 @@ __device__ inline void plan_layer(const LayerView& L, const Dims& d, StepPlan* P
       // one step is always counted (an empty step too); a plan of several steps counts the
       // steps up to its last non-empty one
       const int steps_run = max_steps <= 1 ? 1 : (n > 0 ? pick_step(pol, n_elig, n - 1) + 1 : 0);
-      C->steps += (unsigned long long)steps_run;
-      C->pairs_executed += (unsigned long long)row_run;
-      C->expert_runs += (unsigned long long)n;
-      C->weight_bytes += (unsigned long long)n * (unsigned long long)weight_bytes_per_run;
-      C->pending_pairs -= row_run;
+      // reductions without a returned value: no round trip on the planner's path
+      atomicAdd(&C->steps, (unsigned long long)steps_run);
+      atomicAdd(&C->pairs_executed, (unsigned long long)row_run);
+      atomicAdd(&C->expert_runs, (unsigned long long)n);
+      atomicAdd(&C->weight_bytes, (unsigned long long)n * (unsigned long long)weight_bytes_per_run);
+      atomicSub(&C->pending_pairs, row_run);
     }
   }
 }
