@@ -125,9 +125,9 @@ class MoEAsync:
     def tick(self, layer, policy, x=None, expert=None, w=None, n=None, rows=None, slots=None, kmask=None, gen=None,
              y_out=None, slot_out=None, n_out=None, gen_out=None, step_out=None, append=False, max_out=None,
              stream=None):
-        """One serving tick in one control launch: collect what was ready (into y_out ..
-        n_out, as `collect`; no outputs collects nothing), enqueue a wave (as `enqueue`; no x
-        enqueues nothing), then one scheduling step under `policy`."""
+        """One serving tick: collect what was ready (into y_out .. n_out, as `collect`; no
+        outputs collects nothing) and enqueue a wave (as `enqueue`; no x enqueues nothing) in
+        one control launch, then one scheduling step under `policy`."""
         if x is None:
             n = 0
         else:

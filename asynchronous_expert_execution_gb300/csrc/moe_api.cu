@@ -253,16 +253,19 @@ __global__ void collect_kernel(LayerView L, Dims d, DevCounters* C, int max_out,
 }
 
 // ------------------------------------------------------------------ tick
-// One scheduling tick of a layer in one launch (moe_async_tick).  Blocks [0, n_enq) run the
-// Receptor on the arriving wave; the others merge and copy out the tokens that were ready
-// when the call was made (as collect_kernel does, with the same outputs).  The block that
-// finishes last -- once every pair of the wave is accepted or rejected and every collected
-// row has been read -- reclaims the collected slots, advances the ready ring and plans the
-// step (plan_layer), so the FFN kernels launched after it run that step.
-// Threads a block (the planner runs on one block of these).  Measured on GB300 against the
-// same ticks as three calls (pairs/s, DeepSeek-wide layer / Zipf prefill): 128 -- 3.62 M /
-// 4.69 M; 256 -- 3.67 M / 4.71 M; 512 -- 3.70 M / 4.71 M; three calls 3.71 M / 4.76 M.  The
-// control work of a tick is the same; what the single launch saves is host-side launches.
+// The control launch of a scheduling tick (moe_async_tick).  Blocks [0, n_enq) run the
+// Receptor on the arriving wave while the others merge and copy out the tokens that were
+// ready when the call was made (as collect_kernel does, with the same outputs).  The block
+// that finishes last -- once every pair of the wave is accepted or rejected and every
+// collected row has been read -- reclaims the collected slots and advances the ready ring;
+// the scheduling kernel launched next plans the step.  Measured on GB300 against the three
+// separate calls (pairs/s, same box): DeepSeek-wide layer 3.870 M vs 3.869 M, decode 194.5 K
+// vs 194.2 K, Zipf prefill 4.86 M vs 4.90 M.  Planning in that last block instead was 0.5%
+// slower on the DeepSeek-wide layer: it kept the step's GEMM1 CTAs, which each need an SM's
+// whole shared memory, off the SMs until the whole launch had ended.
+// Threads a block.  Measured on GB300 with the planner in the last block (pairs/s,
+// DeepSeek-wide layer / Zipf prefill): 128 -- 3.62 M / 4.69 M; 256 -- 3.67 M / 4.71 M; 512 --
+// 3.70 M / 4.71 M.
 #ifndef MOE_TICK_THREADS
 #define MOE_TICK_THREADS 512
 #endif
@@ -270,16 +273,15 @@ constexpr int kTickThreads = MOE_TICK_THREADS;
 
 template <typename T>
 __global__ void __launch_bounds__(kTickThreads) tick_kernel(
-    LayerView L, Dims d, DevCounters* C, StepPlan* P, moe_async_policy pol, TileGeom g, int layer,
-    int trace_cap, int4* trace, long long weight_bytes_per_run,
-    int n, int tpw, int n_enq, const int32_t* __restrict__ rows, const int32_t* __restrict__ slots,
+    LayerView L, Dims d, DevCounters* C, int n, int tpw, int n_enq, const int32_t* __restrict__ rows,
+    const int32_t* __restrict__ slots,
     const T* __restrict__ x, const int32_t* __restrict__ expert, const float* __restrict__ w,
     const uint32_t* __restrict__ kmask, const uint32_t* __restrict__ gens,
     int max_out, T* __restrict__ y_out, int32_t* __restrict__ slot_out, uint32_t* __restrict__ gen_out,
     uint32_t* __restrict__ step_out, int32_t* __restrict__ n_io, int append, int parts) {
-  __shared__ PlanScratch sc;
   __shared__ int last;
-  // a programmatic dependent of the previous step's GEMM2: wait for it, then let GEMM1 start
+  // a programmatic dependent of the previous step's GEMM2: wait for it, then let the
+  // scheduling kernel start
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const uint32_t rh = L.ready_ht[0], rt = L.ready_ht[1];
@@ -328,8 +330,6 @@ __global__ void __launch_bounds__(kTickThreads) tick_kernel(
     C->ready -= nc;
     if (max_out > 0) *n_io = base + nc;
   }
-  __syncthreads();
-  plan_layer(L, d, P, C, pol, g, layer, trace_cap, trace, weight_bytes_per_run, (int)C->steps + 1, true, sc, 1);
 }
 
 // ----------------------------------------------------------- cancellation
@@ -758,30 +758,26 @@ moe_status moe_async_tick(moe_async_t h, int32_t layer, int32_t n, const int32_t
   const long long warps = n > 0 ? ((long long)n + tpw - 1) / tpw : 0;
   const int per_block = kTickThreads / 32;
   const int n_enq = (int)std::min<long long>((warps + per_block - 1) / per_block, (long long)h->num_sms * 8);
-  // every block resident at once (512 threads an SM): the last one to finish plans the step,
-  // so a second round of blocks would delay it
+  // every block resident at once (512 threads an SM): the last one to finish reclaims the
+  // collected slots, so a second round of blocks would delay it
   const int resident = h->num_sms * (512 / kTickThreads);
   const int n_col = max_out > 0 ? std::max(1, std::min(max_out, resident - n_enq)) : 0;
   const int grid = std::max(1, n_enq + n_col);
-  const long long wbytes = h->cfg.expert_kind == MOE_EXPERT_SWIGLU
-                               ? 3ll * d.H * d.I * (long long)elem_size(d.dtype) : 0ll;
   prof_begin(h, MOE_KERNEL_TICK, s);
   cudaError_t e;
   if (d.dtype == MOE_BF16)
     e = launch_dependent(tick_kernel<__nv_bfloat16>, dim3(grid), dim3(kTickThreads), s, h->layers[layer], d,
-                         h->counters, h->plan, *policy, h->geom, (int)layer, (int)h->cfg.trace_capacity, h->trace,
-                         wbytes, (int)n, tpw, n_enq, d_rows, d_slot, static_cast<const __nv_bfloat16*>(d_x), d_expert,
-                         d_w, d_kmask, d_gen, (int)max_out, static_cast<__nv_bfloat16*>(d_y_out), d_slot_out, d_gen_out,
-                         d_step_out, d_n_out, (int)append, h->parts_per_pair);
+                         h->counters, (int)n, tpw, n_enq, d_rows, d_slot, static_cast<const __nv_bfloat16*>(d_x),
+                         d_expert, d_w, d_kmask, d_gen, (int)max_out, static_cast<__nv_bfloat16*>(d_y_out), d_slot_out,
+                         d_gen_out, d_step_out, d_n_out, (int)append, h->parts_per_pair);
   else
     e = launch_dependent(tick_kernel<float>, dim3(grid), dim3(kTickThreads), s, h->layers[layer], d, h->counters,
-                         h->plan, *policy, h->geom, (int)layer, (int)h->cfg.trace_capacity, h->trace, wbytes, (int)n,
-                         tpw, n_enq, d_rows, d_slot, static_cast<const float*>(d_x), d_expert, d_w, d_kmask, d_gen,
-                         (int)max_out, static_cast<float*>(d_y_out), d_slot_out, d_gen_out, d_step_out, d_n_out,
+                         (int)n, tpw, n_enq, d_rows, d_slot, static_cast<const float*>(d_x), d_expert, d_w, d_kmask,
+                         d_gen, (int)max_out, static_cast<float*>(d_y_out), d_slot_out, d_gen_out, d_step_out, d_n_out,
                          (int)append, h->parts_per_pair);
   prof_end(h, MOE_KERNEL_TICK, s);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
-  return launch_ffn(h, layer, s);
+  return schedule_impl(h, layer, policy, 1, stream);   // the step: plan, GEMM1, GEMM2
 }
 
 moe_status moe_async_collect(moe_async_t h, int32_t layer, int32_t max_out, void* d_y_out,

@@ -128,7 +128,7 @@ typedef enum {
   MOE_KERNEL_FFN1 = 2,       /* gather + GEMM1 (gate/up) + SwiGLU   (identity: scatter)         */
   MOE_KERNEL_FFN2 = 3,       /* GEMM2 (down) + scatter of the results + readiness               */
   MOE_KERNEL_COLLECT = 4,    /* top-k merge of ready tokens, rows to the caller, slot reclaim   */
-  MOE_KERNEL_TICK = 5,       /* moe_async_tick's control kernel: collect + Receptor + plan      */
+  MOE_KERNEL_TICK = 5,       /* moe_async_tick's control kernel: collect + Receptor + reclaim   */
   MOE_KERNEL_KINDS = 6
 } moe_kernel_kind;
 
@@ -202,8 +202,9 @@ moe_status moe_async_schedule_step(moe_async_t h, int32_t layer, const moe_async
 moe_status moe_async_schedule_steps(moe_async_t h, int32_t layer, const moe_async_policy* policy,
                                     int32_t max_steps, void* stream);
 
-/* One tick of a serving loop in one control launch plus the step's FFN launches: the
- * collect of the tokens that were ready when the call was made (outputs as moe_async_collect,
+/* One tick of a serving loop in one control launch plus the step's launches (plan, GEMM1,
+ * GEMM2): the control launch runs, side by side, the collect of the tokens that were ready
+ * when the call was made (outputs as moe_async_collect,
  * with max_out, d_y_out .. d_n_out and append meaning the same; max_out = 0 collects nothing and
  * d_n_out may then be NULL), the Receptor for a wave of n arriving tokens (arguments as
  * moe_async_enqueue; n = 0 for none), then one scheduling step under `policy` (as

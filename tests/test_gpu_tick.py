@@ -1,5 +1,5 @@
-"""GPU: the one-launch serving tick (``moe_async_tick``: collect of what was ready, the wave's
-Receptor and the scheduling step in one control kernel) against the separate calls and the
+"""GPU: the serving tick (``moe_async_tick``: collect of what was ready and the wave's
+Receptor in one control kernel, then the scheduling step) against the separate calls and the
 oracle.
 
 The tick changes when tokens are handed back (a call returns the tokens that earlier steps
