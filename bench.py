@@ -248,6 +248,23 @@ def build_inputs(spec, seed, dev):
     return x, logits, ws, make_waves(spec, seed)
 
 
+# Steps of the drain plan: with nothing arriving, every step takes at least one bucket, so this
+# bound never cuts a drain short.
+DRAIN_STEPS = 1 << 20
+
+
+def drain(moe, policy):
+    """After the last arrival, the buckets a policy may leave behind run as one device plan of
+    consecutive steps (moe_async_schedule_steps, MTFS / threshold), asynchronously like every
+    other call of the pass; RANKS steps one at a time through moe_async_wait.  The pass checks
+    afterwards that every token was collected."""
+    if policy.kind in ("mtfs", "threshold"):
+        moe.schedule_steps(0, policy, DRAIN_STEPS)
+    else:
+        st = moe.wait(0, policy, max_steps=100000, check_every=32)
+        assert st == 0, st
+
+
 class Pass:
     """One full pass of the hot path over the batch (route, waves, steps, drain, collect).
 
@@ -291,10 +308,7 @@ class Pass:
             moe.schedule_step(0, self.policy)
             moe.collect(0, self.y, self.slots, self.n, append=True)
         if self.drains:
-            # a policy that may leave buckets behind after the last arrival drains them:
-            # moe_async_wait runs the remaining steps as one device plan (MTFS / threshold)
-            st = moe.wait(0, self.policy, max_steps=100000, check_every=32)
-            assert st == 0, st
+            drain(moe, self.policy)
         if self.drains or self.fused:
             moe.collect(0, self.y, self.slots, self.n, append=True)
 
@@ -364,8 +378,7 @@ class ArrivalPass:
             moe.schedule_step(0, self.policy)
             moe.collect(0, y_out, s_out, self.n, append=True)
         if self.drains:
-            st = moe.wait(0, self.policy, max_steps=100000, check_every=32)
-            assert st == 0, st
+            drain(moe, self.policy)
             moe.collect(0, y_out, s_out, self.n, append=True)
         if not self.direct:
             self.yh.copy_(self.y, non_blocking=True)
@@ -468,6 +481,8 @@ def measure_layer(args, pkg, spec, dev, rank, world, steps, warmup, e2e_steps, w
     del ws
     torch.cuda.empty_cache()
     run = Pass(pkg, spec, moe, waves, dev, fused=args.fused_tick)
+    drain_by = (None if not run.drains else "moe_async_schedule_steps (one device plan)"
+                if run.policy.kind in ("mtfs", "threshold") else "moe_async_wait")
 
     def barrier():
         torch.cuda.synchronize()
@@ -589,6 +604,7 @@ def measure_layer(args, pkg, spec, dev, rank, world, steps, warmup, e2e_steps, w
                        "routed_pairs_per_step": routed_pairs_step,
                        "ticks_driven_by": "moe_async_tick" if args.fused_tick
                        else "moe_async_enqueue + moe_async_schedule_step + moe_async_collect",
+                       "drain": drain_by,
                        "l2": "inputs larger than L2: every step streams the scheduled experts' "
                              f"weights ({wbytes_step / 1e9:.1f} GB) through HBM"},
             "roofline": roof, "path_roofline": path, "cpu_baseline": cpu, "e2e": e2e,
