@@ -206,8 +206,12 @@ __global__ void __launch_bounds__(1024) schedule_kernel(LayerView L, Dims d, Ste
 
 // ---------------------------------------------------------------- collect
 // Copy ready rows (in completion order) to the caller, then reclaim each slot: clear its
-// accepted mask and landing count and advance its generation, after the row was read.
-template <typename T>
+// accepted mask and landing count and advance its generation, after the row was read.  G result
+// rows' loads in flight per merged vector: 16 when a token has more than 8 results (one round
+// trip for top-8 + the shared expert), else 8 (half the registers).  Measured on GB300 (pairs/s,
+// same box): DeepSeek-wide layer 3.823 M -> 3.851 M with 16 (collect 0.140 -> 0.132 ms a pass);
+// top-4 Zipf prefill 4.88 M -> 4.84 M with 16 (collect 0.138 -> 0.152 ms), hence 8 there.
+template <typename T, int G>
 __global__ void collect_kernel(LayerView L, Dims d, DevCounters* C, int max_out, T* __restrict__ y_out,
                                int32_t* __restrict__ slot_out, uint32_t* __restrict__ gen_out,
                                uint32_t* __restrict__ step_out, int32_t* __restrict__ n_io, int append,
@@ -224,7 +228,7 @@ __global__ void collect_kernel(LayerView L, Dims d, DevCounters* C, int max_out,
       continue;
     }
     // the top-k merge of the ready token: y = sum_k w_k E_k(x) over its KS results, ascending k
-    merge_row<T>(L, d, slot, y_out + (size_t)(base + i) * d.H, threadIdx.x, blockDim.x);
+    merge_row<T, G>(L, d, slot, y_out + (size_t)(base + i) * d.H, threadIdx.x, blockDim.x);
     for (int p = threadIdx.x; p < parts; p += blockDim.x) L.done_part[(size_t)slot * parts + p] = 0u;
     __syncthreads();
     if (threadIdx.x == 0) {
@@ -299,7 +303,7 @@ __global__ void __launch_bounds__(kTickThreads) tick_kernel(
         if (threadIdx.x == 0) set_error(C, MOE_ERR_BOUNDS);
         continue;
       }
-      merge_row<T>(L, d, slot, y_out + (size_t)(base + i) * d.H, threadIdx.x, blockDim.x);
+      merge_row<T, 8>(L, d, slot, y_out + (size_t)(base + i) * d.H, threadIdx.x, blockDim.x);
       if (threadIdx.x == 0) {
         slot_out[base + i] = slot;
         if (gen_out) gen_out[base + i] = L.gen[slot];
@@ -791,14 +795,16 @@ moe_status moe_async_collect(moe_async_t h, int32_t layer, int32_t max_out, void
   const int grid = std::max(1, std::min(max_out, h->num_sms * kCollectCtasPerSm));
   prof_begin(h, MOE_KERNEL_COLLECT, s);
   cudaError_t e;
+  const bool wide = d.KS > 8;
   if (d.dtype == MOE_BF16)
-    e = launch_dependent(collect_kernel<__nv_bfloat16>, dim3(grid), dim3(256), s, h->layers[layer], d, h->counters,
-                     (int)max_out, static_cast<__nv_bfloat16*>(d_y_out), d_slot_out, d_gen_out, d_step_out,
-                     d_n_out, (int)append, h->parts_per_pair);
+    e = launch_dependent(wide ? collect_kernel<__nv_bfloat16, 16> : collect_kernel<__nv_bfloat16, 8>, dim3(grid),
+                         dim3(256), s, h->layers[layer], d, h->counters, (int)max_out,
+                         static_cast<__nv_bfloat16*>(d_y_out), d_slot_out, d_gen_out, d_step_out, d_n_out,
+                         (int)append, h->parts_per_pair);
   else
-    e = launch_dependent(collect_kernel<float>, dim3(grid), dim3(256), s, h->layers[layer], d, h->counters,
-                     (int)max_out, static_cast<float*>(d_y_out), d_slot_out, d_gen_out, d_step_out, d_n_out,
-                     (int)append, h->parts_per_pair);
+    e = launch_dependent(wide ? collect_kernel<float, 16> : collect_kernel<float, 8>, dim3(grid), dim3(256), s,
+                         h->layers[layer], d, h->counters, (int)max_out, static_cast<float*>(d_y_out), d_slot_out,
+                         d_gen_out, d_step_out, d_n_out, (int)append, h->parts_per_pair);
   prof_end(h, MOE_KERNEL_COLLECT, s);
   return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -247,18 +247,18 @@ template <> __device__ __forceinline__ uint4 pack16<__nv_bfloat16>(const float (
 
 // The top-k merge of one 16-byte vector of features: a = sum_k w_k * E_k over the slot's KS
 // result rows `src` (row stride H) in ascending k, each product and sum rounded in fp32 (no
-// fused multiply-add), so the value depends only on the results and weights.  Eight rows'
-// loads are in flight at a time.
-template <typename T>
+// fused multiply-add), so the value depends only on the results and weights.  G rows' loads
+// are in flight at a time.
+template <typename T, int G = 8>
 __device__ __forceinline__ void merge_vec(const T* src, const float* wk, int KS, int H, float (&a)[Vec<T>::N]) {
   constexpr int N = Vec<T>::N;
-  for (int k0 = 0; k0 < KS; k0 += 8) {
-    uint4 b[8];
+  for (int k0 = 0; k0 < KS; k0 += G) {
+    uint4 b[G];
 #pragma unroll
-    for (int u = 0; u < 8; ++u)
+    for (int u = 0; u < G; ++u)
       if (k0 + u < KS) b[u] = __ldcg(reinterpret_cast<const uint4*>(src + (size_t)(k0 + u) * H));
 #pragma unroll
-    for (int u = 0; u < 8; ++u) {
+    for (int u = 0; u < G; ++u) {
       if (k0 + u < KS) {
         const float w = __ldg(wk + k0 + u);
         float v[N];
@@ -515,8 +515,10 @@ __device__ void land_only(const LayerView& L, const Dims& d, DevCounters* C, con
 }
 
 // The merge of one ready token, y = sum_k w_k * slotbuf[slot][k] in ascending k (fp32, stored
-// in the output dtype with round-to-nearest), by `nthr` threads: one 16-byte vector each at a time.
-template <typename T>
+// in the output dtype with round-to-nearest), by `nthr` threads: one 16-byte vector each at a
+// time, the loads of up to G result rows in flight at once (G = 16: one round trip for top-8 +
+// the shared expert).
+template <typename T, int G = 16>
 __device__ __forceinline__ void merge_row(const LayerView& L, const Dims& d, int slot, T* __restrict__ y,
                                           int tid, int nthr) {
   constexpr int N = Vec<T>::N;
@@ -524,7 +526,7 @@ __device__ __forceinline__ void merge_row(const LayerView& L, const Dims& d, int
   const float* wk = L.wtab + (size_t)slot * d.KS;
   for (int f = N * tid; f < d.H; f += N * nthr) {
     float a[N];
-    merge_vec<T>(src + f, wk, d.KS, d.H, a);
+    merge_vec<T, G>(src + f, wk, d.KS, d.H, a);
     *reinterpret_cast<uint4*>(y + f) = pack16<T>(a);
   }
 }
