@@ -202,13 +202,12 @@ moe_status moe_async_schedule_step(moe_async_t h, int32_t layer, const moe_async
 moe_status moe_async_schedule_steps(moe_async_t h, int32_t layer, const moe_async_policy* policy,
                                     int32_t max_steps, void* stream);
 
-/* One tick of a serving loop in one control launch plus the step's launches (plan, GEMM1,
- * GEMM2): the control launch runs, side by side, the collect of the tokens that were ready
- * when the call was made (outputs as moe_async_collect,
- * with max_out, d_y_out .. d_n_out and append meaning the same; max_out = 0 collects nothing and
- * d_n_out may then be NULL), the Receptor for a wave of n arriving tokens (arguments as
- * moe_async_enqueue; n = 0 for none), then one scheduling step under `policy` (as
- * moe_async_schedule_step).  StreamEP section 3 (the Receptor feeds the per-expert queues,
+/* One tick of a serving loop: one control launch, then the step's launches (plan, GEMM1,
+ * GEMM2).  The control launch runs, side by side, the collect of the tokens that were ready
+ * when the call was made (outputs as moe_async_collect, with max_out, d_y_out .. d_n_out and
+ * append meaning the same; max_out = 0 collects nothing and d_n_out may then be NULL) and the
+ * Receptor for a wave of n arriving tokens (arguments as moe_async_enqueue; n = 0 for none);
+ * then one scheduling step runs under `policy` (as moe_async_schedule_step).  StreamEP section 3 (the Receptor feeds the per-expert queues,
  * ready tokens leave after their K results) and section 4 (the scheduler then picks).
  *   Equivalent to moe_async_collect, moe_async_enqueue and moe_async_schedule_step in that
  * order, with one difference: the collected slots are reclaimed after the wave's pairs have
