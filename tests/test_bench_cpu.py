@@ -101,3 +101,32 @@ def test_reference_arm_json_line():
     assert line["e2e"] == {"value": line["value"], "unit": "pairs/s", "h2d_bytes_per_step": 0,
                            "d2h_bytes_per_step": 0}
     assert line["config"]["workload"] == "c1_tiny_fp32"
+
+
+def test_drain_is_one_asynchronous_plan_except_for_ranks():
+    """After the last wave the pass drains MTFS / threshold buckets with one device plan
+    (moe_async_schedule_steps, no host read in the timed pass) and RANKS through
+    moe_async_wait, whose status must be 0."""
+    from asynchronous_expert_execution_gb300.api import Policy
+
+    class Fake:
+        def __init__(self, status=0):
+            self.calls, self.status = [], status
+
+        def schedule_steps(self, layer, policy, max_steps):
+            self.calls.append(("plan", layer, policy.kind, max_steps))
+
+        def wait(self, layer, policy, max_steps=0, check_every=0):
+            self.calls.append(("wait", layer, policy.kind))
+            return self.status
+
+    for pol in (Policy("threshold", min_batch=64, fallback_groups=1), Policy("mtfs", max_groups=4)):
+        m = Fake()
+        bench.drain(m, pol)
+        assert m.calls == [("plan", 0, pol.kind, bench.DRAIN_STEPS)]
+    assert bench.DRAIN_STEPS >= 1025                 # one bucket a step at least: never cut short
+    m = Fake()
+    bench.drain(m, Policy("ranks", max_groups=16, fallback_groups=1))
+    assert m.calls == [("wait", 0, "ranks")]
+    with pytest.raises(AssertionError):
+        bench.drain(Fake(status=5), Policy("ranks", max_groups=4))
