@@ -810,20 +810,24 @@ __global__ void __launch_bounds__(kThreads, 1) ffn_tc_kernel(const __grid_consta
         EpiBarrier{}();
         if (!*last_flag) continue;
         __threadfence();
-        // 8 columns of every chunk in flight at once, then the adds in ascending chunk order
+        // 12 columns of every chunk in flight at once (a group may read workspace columns past
+        // nj that no unit wrote this launch: in bounds, and their sums are never stored), then
+        // the adds in ascending chunk order
 #pragma unroll
-        for (int c0 = 0; c0 < BNW; c0 += 8) {
+        for (int c0 = 0; c0 < BNW; c0 += 12) {
           if (c0 < tl.nj) {
-            float4 v[kMaxChunks][2];
+            float4 v[kMaxChunks][3];
 #pragma unroll
             for (int c = 0; c < kMaxChunks; ++c) {
               if (c < nchunk) {
 #pragma unroll
-                for (int j = 0; j < 2; ++j) v[c][j] = __ldcg(wt + ((size_t)c * (BNW / 4) + c0 / 4 + j) * kBM + row);
+                for (int j = 0; j < 3; ++j)
+                  if (c0 + 4 * j < BNW) v[c][j] = __ldcg(wt + ((size_t)c * (BNW / 4) + c0 / 4 + j) * kBM + row);
               }
             }
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
+            for (int j = 0; j < 3; ++j) {
+              if (c0 + 4 * j >= BNW) continue;
               float4 a = v[0][j];
 #pragma unroll
               for (int c = 1; c < kMaxChunks; ++c) {
